@@ -1,0 +1,497 @@
+"""Benchmark of the fused row-parallel GEMM + partial channel-reduce hot path.
+
+One step = one pass of the whole path over one synthetic batch of the chosen
+workload (default: the 130M-shaped layers, h = 768, FFN 3072, t = 8 emulated
+tensor-parallel ranks, N = 8 x 1024 tokens, p = 0.5): for each row-parallel layer
+(attention out-projection K = 768, MLP down-projection K = 3072) the fused
+forward (GEMM + partial channel-reduce into t rank outputs) and the backward
+(partial reduce of the upstream gradient, dX, dW).  Metric: algorithmic TFLOP/s
+(2NKh forward + 4NKh backward per layer, independent of p).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl caat|reference]
+                  [--workload 130m|1.1b|7b_prefill] [--no-extras]
+
+Under torchrun each rank runs its own replica on its own GPU (no collective on
+the data path; weak scaling); rank 0 prints one JSON line.  ``--impl reference``
+times the CPU oracle on the host cores instead.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import caat_inputs as ci  # noqa: E402
+
+METRIC = "fused rowpar-GEMM+partial-reduce TFLOP/s & reduce GB/s (% of GB300 peak), 1 GPU"
+L2_BYTES = 129 * 2**20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sus=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- GPU arm
+
+class LayerData:
+    def __init__(self, torch, w, li, device):
+        L = w.layers[li]
+        X, Wl, G = ci.layer_tensors(w, li)
+        self.K = L.K
+        self.name = L.name
+        self.S = None
+        bf = torch.bfloat16
+
+        def dev(a):
+            return torch.from_numpy(ci.bf16_words(a).view(np.int16)).to(device).view(bf)
+
+        self.X_host = ci.bf16_words(X)
+        self.X = dev(X)
+        self.Wstore = dev(np.ascontiguousarray(Wl.T))     # nn.Linear layout [h, K]
+        self.W = self.Wstore.t()
+        self.G_host = [ci.bf16_words(G[r]) for r in range(w.t)] if G is not None else None
+        self.G = [dev(G[r]) for r in range(w.t)] if G is not None else None
+        self.Y = [torch.empty((w.N, w.h), dtype=bf, device=device) for _ in range(w.t)]
+        self.dX = torch.empty((w.N, L.K), dtype=bf, device=device)
+        self.dWstore = torch.empty((w.h, L.K), dtype=bf, device=device)
+        self.dW = self.dWstore.t()
+        self.flops_fwd = 2.0 * w.N * L.K * w.h
+        self.flops_bwd = 4.0 * w.N * L.K * w.h if w.backward else 0.0
+        self.bytes_fwd = 2.0 * (w.N * L.K + L.K * w.h + w.t * w.N * w.h)
+
+
+def run_gpu(args, w):
+    import torch
+    import partial_activation_sync_gb300 as caat
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    peaks = _peaks()
+
+    S = caat.select_channels(w.h, w.p, w.layout, w.seeds()["perm"])
+    sel = torch.from_numpy(S).to(device)
+    layers = [LayerData(torch, w, i, device) for i in range(len(w.layers))]
+    ws_bytes = max(caat.rowpar_linear_bwd_workspace(w.t, w.N, w.h, 1, 0), 256)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        k = 0
+        for L in layers:
+            if evs is not None:
+                evs[k].record(stream); k += 1
+            caat.rowpar_linear_fwd(L.X, L.W, w.t, sel, outs=L.Y)
+            if w.backward:
+                if evs is not None:
+                    evs[k].record(stream); k += 1
+                caat.rowpar_linear_bwd(L.X, L.W, L.G, w.t, sel, caat.CAAT_BWD_REDUCE_DOUT,
+                                       dX=L.dX, dW=L.dW, workspace=ws)
+        if evs is not None:
+            evs[k].record(stream)
+
+    n_calls = len(layers) * (2 if w.backward else 1)
+    for _ in range(args.warmup):
+        step()
+        flush.fill_(1.0)
+    torch.cuda.synchronize()
+    assert caat.device_status() == 0
+
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = caat.launch_count()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    all_evs = []
+    for _ in range(args.steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 1)]
+        step(evs)
+        all_evs.append(evs)
+        flush.fill_(float(len(all_evs)))      # L2 flush between timed steps (not timed)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    launches = caat.launch_count() - launches0
+    clk = clocks.stop()
+    assert caat.device_status() == 0
+
+    per_call = np.zeros(n_calls)
+    for evs in all_evs:
+        for i in range(n_calls):
+            per_call[i] += evs[i].elapsed_time(evs[i + 1])
+    total_ms = float(per_call.sum())
+    if dist is not None:
+        tt = torch.tensor([total_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    flops_step = sum(L.flops_fwd + L.flops_bwd for L in layers)
+    ms_step = total_ms / args.steps
+    tflops = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
+
+    # per-call breakdown (ms per step) and the dominant kernel's roofline
+    names = []
+    for L in layers:
+        names.append("fwd_" + L.name)
+        if w.backward:
+            names.append("bwd_" + L.name)
+    breakdown = {n: round(float(v) / args.steps, 4) for n, v in zip(names, per_call)}
+    fwd_idx = [i for i, n in enumerate(names) if n.startswith("fwd_")]
+    dom = max(fwd_idx, key=lambda i: per_call[i])
+    Ld = layers[fwd_idx.index(dom)]
+    t_dom = per_call[dom] / args.steps * 1e-3
+    ai = Ld.flops_fwd / Ld.bytes_fwd
+    ridge = peaks["bf16"] * 1e12 / (peaks["hbm"] * 1e9)
+    if ai >= ridge:
+        ach = Ld.flops_fwd / t_dom / 1e12
+        roof = {"kernel": "rowpar_fwd (%s, %s)" % (Ld.name, caat.last_kernel()), "bound": "tensor",
+                "achieved": round(ach, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": round(ach / peaks["bf16"], 4)}
+    else:
+        ach = Ld.bytes_fwd / t_dom / 1e9
+        roof = {"kernel": "rowpar_fwd (%s)" % Ld.name, "bound": "hbm",
+                "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": round(ach / peaks["hbm"], 4)}
+    roof["peak_source"] = peaks["source"] + " (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback"
+    roof["traffic"] = None
+    roof["algorithmic_per_launch"] = {"flops": Ld.flops_fwd, "bytes": Ld.bytes_fwd}
+
+    result = {
+        "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations/gradients, N(0,0.02) weights)",
+        "config": {"workload": w.name, "t": w.t, "N": w.N, "h": w.h,
+                   "layers": {L.name: L.K for L in layers}, "p": w.p,
+                   "S": "contiguous" if w.layout == 0 else "random",
+                   "fwd_and_bwd": bool(w.backward),
+                   "l2": "flushed between timed steps (2x L2 write, untimed)",
+                   "parallelism": "replicas" if world > 1 else "1 GPU, t ranks emulated"},
+        "breakdown_ms": breakdown,
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "roofline": roof,
+    }
+
+    # end to end through the public API with host buffers (pinned), per step:
+    # H2D of the step's activations X and upstream gradients dOut, D2H of dX, dW
+    e2e = run_e2e(torch, caat, w, layers, sel, ws, args, device, dist)
+    result["e2e"] = e2e
+
+    if rank == 0 and not args.no_extras:
+        result["extras"] = run_extras(torch, caat, device, peaks)
+    if rank == 0:
+        result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    if dist is not None:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
+    stream = torch.cuda.current_stream()
+    hostX = [torch.from_numpy(L.X_host.view(np.int16)).pin_memory() for L in layers]
+    hostG = [[torch.from_numpy(g.view(np.int16)).pin_memory() for g in L.G_host]
+             if w.backward else [] for L in layers]
+    outdX = [torch.empty(L.dX.shape, dtype=torch.int16).pin_memory() for L in layers]
+    outdW = [torch.empty(L.dWstore.shape, dtype=torch.int16).pin_memory() for L in layers]
+    outY0 = [torch.empty(L.Y[0].shape, dtype=torch.int16).pin_memory() for L in layers]
+    h2d = sum(x.numel() * 2 for x in hostX) + sum(g.numel() * 2 for gs in hostG for g in gs)
+    if w.backward:
+        d2h = sum(x.numel() * 2 for x in outdX) + sum(x.numel() * 2 for x in outdW)
+    else:
+        d2h = sum(x.numel() * 2 for x in outY0)
+
+    def step():
+        for li, L in enumerate(layers):
+            L.X.view(torch.int16).copy_(hostX[li], non_blocking=True)
+            if w.backward:
+                for r in range(w.t):
+                    L.G[r].view(torch.int16).copy_(hostG[li][r], non_blocking=True)
+            caat.rowpar_linear_fwd(L.X, L.W, w.t, sel, outs=L.Y)
+            if w.backward:
+                caat.rowpar_linear_bwd(L.X, L.W, L.G, w.t, sel, caat.CAAT_BWD_REDUCE_DOUT,
+                                       dX=L.dX, dW=L.dW, workspace=ws)
+                outdX[li].copy_(L.dX.view(torch.int16), non_blocking=True)
+                outdW[li].copy_(L.dWstore.view(torch.int16), non_blocking=True)
+            else:
+                outY0[li].copy_(L.Y[0].view(torch.int16), non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist is not None:
+        tt = torch.tensor([ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    world = dist.get_world_size() if dist is not None else 1
+    flops = sum(L.flops_fwd + L.flops_bwd for L in layers)
+    return {"value": round(flops * args.steps * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms / args.steps, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def _time_call(torch, fn, reps, flush=None):
+    stream = torch.cuda.current_stream()
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.fill_(0.5)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ts) * 1e-3
+
+
+def run_extras(torch, caat, device, peaks):
+    """Short side measurements for the two targets named with the metric: the
+    fused forward at Llama2-7B prefill shapes (tensor-bound) and the standalone
+    reduce on a working set far above L2 (HBM-bound)."""
+    out = {}
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    # standalone PCR, bf16 and fp32, t=8, [4096, 4096], p=0.5, out of place
+    for dt_name, dt, es in (("bf16", torch.bfloat16, 2), ("f32", torch.float32, 4)):
+        t, N, h = 8, 4096, 4096
+        ins = [torch.randn((N, h), device=device).to(dt) for _ in range(t)]
+        outs = [torch.empty_like(x) for x in ins]
+        sel = torch.from_numpy(caat.select_channels(h, 0.5)).to(device)
+        fn = lambda: caat.partial_channel_reduce(ins, sel, outs=outs)  # noqa: E731
+        fn()
+        sec = _time_call(torch, fn, 20, flush)
+        gbs = 2.0 * t * N * h * es / sec / 1e9
+        out["pcr_%s_t8_4096x4096" % dt_name] = {
+            "GB/s": round(gbs, 1), "frac_hbm": round(gbs / peaks["hbm"], 4),
+            "us": round(sec * 1e6, 2), "kernel": caat.last_kernel()}
+        del ins, outs
+    # config-1 PCR (fp32, t=2, [256, 768]), L2-resident, launch-latency bound
+    Y = ci.normal(1001, (2, 256, 768))
+    ins = [torch.from_numpy(Y[r]).to(device) for r in range(2)]
+    outs = [torch.empty_like(x) for x in ins]
+    sel = torch.from_numpy(caat.select_channels(768, 0.5)).to(device)
+    fn = lambda: caat.partial_channel_reduce(ins, sel, outs=outs)  # noqa: E731
+    fn()
+    sec = _time_call(torch, fn, 50)
+    out["pcr_f32_t2_256x768"] = {"GB/s": round(2.0 * 2 * 256 * 768 * 4 / sec / 1e9, 1),
+                                 "us": round(sec * 1e6, 2)}
+    # 7B prefill forward (out-proj K=4096, down-proj K=11008), p = 0.5
+    w = ci.WORKLOADS["7b_prefill"]
+    S = caat.select_channels(w.h, w.p, 0)
+    sel = torch.from_numpy(S).to(device)
+    for li, L in enumerate(w.layers):
+        X = torch.randn((w.N, L.K), device=device).to(torch.bfloat16)
+        Wst = (torch.randn((w.h, L.K), device=device) * 0.02).to(torch.bfloat16)
+        Ys = [torch.empty((w.N, w.h), dtype=torch.bfloat16, device=device) for _ in range(w.t)]
+        fn = lambda: caat.rowpar_linear_fwd(X, Wst.t(), w.t, sel, outs=Ys)  # noqa: E731
+        fn()
+        sec = _time_call(torch, fn, 10, flush)
+        tf = 2.0 * w.N * L.K * w.h / sec / 1e12
+        out["7b_prefill_fwd_" + L.name] = {
+            "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4),
+            "us": round(sec * 1e6, 1), "kernel": caat.last_kernel()}
+        del X, Wst, Ys
+    torch.cuda.synchronize()
+    return out
+
+
+# ----------------------------------------------------------- CPU oracle arm
+
+def _oracle_sample(w, rows, threads):
+    """The oracle on `rows` token rows of every layer of the workload, fwd and
+    (for training workloads) bwd.  Returns (algorithmic FLOPs, seconds)."""
+    from oracle import oracle as orc
+    orc.set_threads(threads)
+    S = orc.select_channels(w.h, w.p, w.layout, w.seeds()["perm"])
+    flops, sec = 0.0, 0.0
+    for li, L in enumerate(w.layers):
+        X, Wl, G = ci.layer_tensors(w, li, N=rows)
+        Xd = ci.words_to_f32(ci.bf16_words(X)).astype(np.float64)
+        Wd = ci.words_to_f32(ci.bf16_words(Wl)).astype(np.float64)
+        t0 = time.perf_counter()
+        orc.rowpar_fwd(Xd, Wd, w.t, S)
+        flops += 2.0 * rows * L.K * w.h
+        if w.backward:
+            Gd = ci.words_to_f32(ci.bf16_words(G)).astype(np.float64)
+            orc.rowpar_bwd(Xd, Wd, Gd, w.t, S, 0)
+            flops += 4.0 * rows * L.K * w.h
+        sec += time.perf_counter() - t0
+    return flops, sec
+
+
+def _calibrate_rows(w, threads, budget_s):
+    """Rows of the workload the oracle processes in about budget_s seconds."""
+    rows = 4 * max(threads, 4)
+    while True:      # grow until a sample costs a quarter of the budget (cost is not linear)
+        _, s = _oracle_sample(w, rows, threads)
+        if s >= budget_s / 4 or rows >= w.N:
+            break
+        rows = int(min(w.N, rows * min(8.0, max(2.0, budget_s / 4 / max(s, 1e-3)))))
+    rows = int(min(w.N, max(threads, rows * budget_s / max(s, 1e-3))))
+    return max(threads, rows // threads * threads)
+
+
+def cpu_baseline(w, budget_s=12.0):
+    from oracle import oracle as orc
+    threads = os.cpu_count() or 1
+    orc.set_threads(threads)
+    rows2 = _calibrate_rows(w, threads, budget_s)
+    f, s = _oracle_sample(w, rows2, threads)
+    return {"value": round(f / s / 1e12, 6), "unit": "TFLOP/s", "cores": orc.get_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d token rows of every layer (%s), fwd%s, float64 naive loops, %.1f s"
+                      % (rows2, w.N, ",".join(L.name for L in w.layers),
+                         "+bwd" if w.backward else "", s)}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    from oracle import oracle as orc
+    threads = os.cpu_count() or 1
+    orc.set_threads(threads)
+    # a bounded sample per step so the K timed steps stay within about two minutes
+    per_step_s = max(1.0, min(10.0, 120.0 / max(1, args.steps)))
+    rows = _calibrate_rows(w, threads, per_step_s)
+    for _ in range(args.warmup):
+        _oracle_sample(w, min(rows, threads), threads)
+    tot_f, tot_s = 0.0, 0.0
+    for _ in range(args.steps):
+        f, s = _oracle_sample(w, rows, threads)
+        tot_f += f
+        tot_s += s
+    v = tot_f / tot_s / 1e12
+    sample = "%d of %d token rows of every layer per step, float64 naive loops" % (rows, w.N)
+    return {"metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(tot_s / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "t": w.t, "N": w.N, "h": w.h, "p": w.p,
+                       "layers": {L.name: L.K for L in w.layers},
+                       "fwd_and_bwd": bool(w.backward)},
+            "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": orc.get_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["caat", "reference"], default="caat")
+    ap.add_argument("--workload", default="130m", choices=["130m", "1.1b", "7b_prefill"])
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = ci.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        res = run_reference(args, w)
+    else:
+        res = run_gpu(args, w)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * caat.h -- C ABI of the GB300 (sm_103a) partial channel-reduce library.
+ *
+ * The operation comes from "Tensor-Parallelism with Partially Synchronized
+ * Activations" (Lamprecht et al., NeurIPS 2025), Introduction, the paragraph that
+ * defines the partial channel-reduce (PCR): after a tensor-parallel (row-parallel)
+ * layer, only a subset S of the hidden channels is summed over the t ranks; on the
+ * other channels each rank keeps the partial result it computed, so activations
+ * differ across ranks.  S empty is the "ensemble" limit, S = all channels is the
+ * vanilla all-reduce.  The same paragraph requires the backward pass to match the
+ * forward.  The experimental setup fixes the size of S by the fraction p
+ * (p = 0.5 with tensor-parallel dimension 8 for the 7B model).
+ *
+ * On one GPU the t ranks are emulated as t shards resident in the same memory.
+ *
+ * Conventions shared by every call
+ *  - Every compute call is asynchronous on the stream `stream` (a cudaStream_t;
+ *    NULL = the legacy default stream) and keeps no state between calls.
+ *  - "device pointer" = memory the caller allocated on the current CUDA device;
+ *    the library never allocates or frees device memory and never keeps a pointer
+ *    after the call returns.  Arrays "of t device pointers" are HOST arrays whose
+ *    entries are device pointers; the library copies them before returning.
+ *  - Matrices are dense in their last dimension unless a stride says otherwise;
+ *    strides and leading dimensions are in ELEMENTS, not bytes.
+ *  - Arguments are validated before anything is launched.  On any error nothing
+ *    is written and nothing is launched.
+ *  - bf16 data is stored as 16-bit words; all arithmetic accumulates in fp32.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef CAAT_H
+#define CAAT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *caat_stream_t;
+
+typedef enum {
+    CAAT_OK = 0,
+    CAAT_ERR_INVALID_ARG = 1,  /* a null pointer, a size or stride out of range       */
+    CAAT_ERR_UNSUPPORTED = 2,  /* valid, but no kernel of this build takes it         */
+    CAAT_ERR_CUDA = 3,         /* a CUDA runtime call or a launch failed              */
+    CAAT_ERR_TIMEOUT = 4       /* a bounded device-side wait gave up (see below)      */
+} caat_status;
+
+typedef enum { CAAT_F32 = 0, CAAT_BF16 = 1 } caat_dtype;
+
+/* Which channels make up S.  The paper fixes only its size. */
+typedef enum {
+    CAAT_S_CONTIGUOUS = 0,     /* S = {0, ..., s-1}                                   */
+    CAAT_S_RANDOM = 1          /* first s entries of a seeded Fisher-Yates shuffle    */
+} caat_layout;
+
+/* Where the backward reduce sits (the paper requires only that it match the forward). */
+typedef enum {
+    CAAT_BWD_REDUCE_DOUT = 0,  /* dY = PCR(dOut): exact gradient of sum_r <dOut_r, Out_r> */
+    CAAT_BWD_NO_REDUCE = 1     /* dY_r = dOut_r: the reduce is done by the matching       */
+                               /* column-parallel layer's input gradient                   */
+} caat_bwd_mode;
+
+/*
+ * caat_select_channels -- the synchronized channel set S (host only, no GPU).
+ *
+ * Paper: Introduction (PCR reduces "a subset of the channels"); experimental
+ * setup (hyper-parameter p, the reduced fraction; p = 0.5).
+ * s = floor(p*h + 1/2), clamped to [0, h].
+ *   CAAT_S_CONTIGUOUS: S = {0..s-1}.
+ *   CAAT_S_RANDOM:     permutation pi of {0..h-1} by Fisher-Yates, i = h-1 down to
+ *                      1, j = splitmix64_next() mod (i+1), swap pi[i], pi[j]; the
+ *                      splitmix64 state starts at `seed`.  S = sort(pi[0..s)).
+ *                      Sets are nested: S(p1) is a subset of S(p2) when p1 <= p2.
+ * idx:   host int32[h] written with S in ascending order (caller allocates h entries).
+ * n_sel: host, receives s.
+ * Errors: INVALID_ARG for h < 0 or h > 2^31-1, p outside [0,1] or NaN, an unknown
+ * layout, or a null pointer (idx may be null when h == 0).
+ */
+caat_status caat_select_channels(int64_t h, double p, caat_layout layout, uint64_t seed,
+                                 int32_t *idx, int64_t *n_sel);
+
+/*
+ * caat_partial_channel_reduce -- standalone PCR over t partial tensors.
+ *
+ * Paper: Introduction, definition of the partial channel-reduce.
+ *   out_r[n, c] = in_0[n, c] + in_1[n, c] + ... + in_{t-1}[n, c]   if c in S
+ *   out_r[n, c] = in_r[n, c]                                       otherwise
+ * The sum is a left fold in rank order in fp32 (bit-reproducible); bf16 data is
+ * widened exactly and rounded once (nearest-even) to bf16 at the end.
+ * t:      1 .. 64 ranks.      N: rows (tokens), >= 0.    h: channels, 0 .. 2^24.
+ * in:     host array of t device pointers, each [N, h] with row stride ld_in.
+ * out:    host array of t device pointers, each [N, h] with row stride ld_out.
+ *         out may equal in (in place: then only the channels of S are written).
+ *         Otherwise the t outputs must not overlap any input.
+ * sel:    device int32[n_sel], ascending, unique, each in [0, h)  (S).
+ *         May be null when n_sel == 0.
+ * Errors: INVALID_ARG for t out of range, negative sizes, ld < h, null pointers,
+ *         or in/out arrays that are in place for some ranks and not for others.
+ *         Unsorted or out-of-range entries of sel are not checked on the device;
+ *         out-of-range entries are ignored by the kernel, duplicates are harmless.
+ */
+caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, caat_dtype dt,
+                                        const void *const *in, int64_t ld_in,
+                                        void *const *out, int64_t ld_out,
+                                        const int32_t *sel, int64_t n_sel,
+                                        caat_stream_t stream);
+
+/*
+ * caat_rowpar_linear_fwd -- row-parallel linear layer fused with the PCR.
+ *
+ * Paper: Introduction (the PCR replaces the all-reduce that follows the
+ * tensor-parallel block: attention out-projection, MLP down-projection).
+ * K splits into t equal shards k_t = K/t; rank r owns X[:, r*k_t .. (r+1)*k_t)
+ * and rows r*k_t .. (r+1)*k_t of W.  With Y_r = X_r W_r:
+ *   Y[r][n, c] = Y_0[n, c] + ... + Y_{t-1}[n, c]  (= (X W)[n, c], full K)  if c in S
+ *   Y[r][n, c] = Y_r[n, c]                                              otherwise
+ * X:   device [N, K], row stride ldx.
+ * W:   device, logical [K, h]: element (k, c) at W[k*w_rs + c*w_cs].
+ *      (w_rs, w_cs) = (1, K) is torch's nn.Linear weight [h, K] (K contiguous),
+ *      the layout the tensor-core path takes; (h, 1) is a row-major [K, h].
+ * Y:   host array of t device pointers, each [N, h] with row stride ldy; they
+ *      must not overlap each other or X, W.
+ * sel: device int32[n_sel], ascending and unique (S); may be null if n_sel == 0.
+ * Precision: bf16 in, fp32 accumulate, one rounding to bf16; or fp32 throughout
+ * (fp32 FMA, no TF32).
+ * Errors: INVALID_ARG for t outside 1..64, K % t != 0, negative sizes, a stride
+ *         or leading dimension smaller than the row it spans, null pointers.
+ *         UNSUPPORTED when no kernel takes the layout and alignment given.
+ */
+caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                   const void *X, int64_t ldx,
+                                   const void *W, int64_t w_rs, int64_t w_cs,
+                                   void *const *Y, int64_t ldy,
+                                   const int32_t *sel, int64_t n_sel,
+                                   caat_stream_t stream);
+
+/*
+ * caat_rowpar_linear_bwd -- gradients of the fused row-parallel layer.
+ *
+ * Paper: Introduction (forward and backward must agree; a mismatch diverges).
+ * dOut: host array of t device pointers, each [N, h] with row stride ld_dout:
+ *       the gradient arriving at each rank's output Y[r].
+ * mode CAAT_BWD_REDUCE_DOUT: dY = PCR(dOut) with the same S (PCR is symmetric,
+ *       so this is the exact gradient of sum_r <dOut_r, Y[r]>);
+ * mode CAAT_BWD_NO_REDUCE:   dY_r = dOut_r.
+ * Writes dX [N, K] (row stride lddx; shard r = columns r*k_t..) with
+ *   dX[:, shard r] = dY_r W_r^T,
+ * and dW, logical [K, h] with element (k, c) at dW[k*dw_rs + c*dw_cs], with
+ *   dW[shard r, :] = X_r^T dY_r.
+ * workspace: device scratch of at least caat_rowpar_linear_bwd_workspace() bytes,
+ *       256-byte aligned, owned by the caller and untouched after the stream reaches
+ *       the end of this call; may be null when that size is 0.
+ * Errors: as caat_rowpar_linear_fwd; INVALID_ARG also when ws_bytes is too small.
+ */
+size_t caat_rowpar_linear_bwd_workspace(int t, int64_t N, int64_t h, caat_dtype dt,
+                                        caat_bwd_mode mode);
+
+caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                   const void *X, int64_t ldx,
+                                   const void *W, int64_t w_rs, int64_t w_cs,
+                                   const void *const *dOut, int64_t ld_dout,
+                                   void *dX, int64_t lddx,
+                                   void *dW, int64_t dw_rs, int64_t dw_cs,
+                                   const int32_t *sel, int64_t n_sel, caat_bwd_mode mode,
+                                   void *workspace, size_t ws_bytes,
+                                   caat_stream_t stream);
+
+/* Human-readable name of a status code (static string, never null). */
+const char *caat_status_string(caat_status st);
+
+/*
+ * caat_get_device_status -- synchronizes `stream`, then reports and clears the
+ * library's device-side error word of the current device.  Every wait inside the
+ * tensor-core kernels is bounded; a wait that gives up records CAAT_ERR_TIMEOUT
+ * there and the kernel exits (its outputs are then undefined) instead of hanging.
+ * Returns CAAT_ERR_CUDA when the synchronization itself fails.
+ */
+caat_status caat_get_device_status(caat_stream_t stream);
+
+/*
+ * caat_last_kernel -- which kernel the last successful launch on this host
+ * thread used (static string, e.g. "pcr_vec", "rowpar_fwd_tc", "rowpar_fwd_simt").
+ * For tests and benchmarks.
+ */
+const char *caat_last_kernel(void);
+
+/* Number of kernels this host thread has launched through the library so far. */
+uint64_t caat_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CAAT_H */

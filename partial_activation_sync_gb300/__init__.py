@@ -1,0 +1,214 @@
+"""GB300 (sm_103a) partial channel-reduce for tensor-parallel layers (CAAT-Net).
+
+Thin PyTorch binding over the C ABI of ``include/caat.h``: every function below
+only marshals tensors (device pointers, sizes, strides, the current CUDA stream)
+into one library call; all arithmetic runs in the library's CUDA kernels.
+
+"Tensor-Parallelism with Partially Synchronized Activations" (NeurIPS 2025),
+Introduction: the partial channel-reduce sums only a subset S of the hidden
+channels over the t tensor-parallel ranks after a row-parallel layer.
+"""
+import ctypes
+
+import numpy as np
+
+from . import _lib
+
+CAAT_F32, CAAT_BF16 = 0, 1
+CAAT_S_CONTIGUOUS, CAAT_S_RANDOM = 0, 1
+CAAT_BWD_REDUCE_DOUT, CAAT_BWD_NO_REDUCE = 0, 1
+
+__all__ = [
+    "select_channels", "partial_channel_reduce", "rowpar_linear_fwd", "rowpar_linear_bwd",
+    "rowpar_linear_bwd_workspace", "device_status", "last_kernel", "launch_count",
+    "CaatError", "CAAT_S_CONTIGUOUS", "CAAT_S_RANDOM", "CAAT_BWD_REDUCE_DOUT",
+    "CAAT_BWD_NO_REDUCE",
+]
+
+
+class CaatError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib.load().caat_status_string(status).decode()
+        super().__init__("%s: %s" % (where, msg))
+
+
+def _check(st: int, where: str):
+    if st != 0:
+        raise CaatError(st, where)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return CAAT_F32
+    if t.dtype == torch.bfloat16:
+        return CAAT_BF16
+    raise TypeError("caat: dtype must be float32 or bfloat16, got %s" % t.dtype)
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _rowmajor(t, name):
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError("caat: %s must be 2-D with unit column stride" % name)
+    if not t.is_cuda:
+        raise ValueError("caat: %s must be a CUDA tensor" % name)
+    return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def _sel_ptr(sel):
+    if sel is None:
+        return None, 0
+    if not sel.is_cuda or sel.dtype != _torch().int32 or sel.dim() != 1 or not sel.is_contiguous():
+        raise ValueError("caat: sel must be a contiguous 1-D int32 CUDA tensor")
+    return ctypes.c_void_p(sel.data_ptr() if sel.numel() else 0), sel.numel()
+
+
+# --------------------------------------------------------------- channels
+
+def select_channels(h: int, p: float, layout: int = CAAT_S_CONTIGUOUS, seed: int = 0) -> np.ndarray:
+    """Sorted int32 indices of S, |S| = floor(p*h + 1/2) (host call)."""
+    idx = np.zeros(max(int(h), 1), dtype=np.int32)
+    n = ctypes.c_int64(0)
+    st = _lib.load().caat_select_channels(int(h), float(p), int(layout),
+                                           ctypes.c_uint64(int(seed) & (2**64 - 1)),
+                                           idx.ctypes.data_as(ctypes.c_void_p), ctypes.byref(n))
+    _check(st, "caat_select_channels")
+    return idx[: n.value].copy()
+
+
+# ------------------------------------------------- partial channel-reduce
+
+def partial_channel_reduce(ins, sel, outs=None, stream=None):
+    """PCR over the t tensors ``ins`` (each [N, h], same shape/stride/dtype).
+
+    Returns ``outs`` (allocated when None).  ``outs is ins`` (the same tensors)
+    runs in place.
+    """
+    torch = _torch()
+    t = len(ins)
+    if t == 0:
+        raise ValueError("caat: need at least one input")
+    N, h = ins[0].shape
+    ld_in = _rowmajor(ins[0], "ins[0]")
+    for x in ins:
+        if x.shape != ins[0].shape or x.dtype != ins[0].dtype or _rowmajor(x, "ins") != ld_in:
+            raise ValueError("caat: all inputs need one shape, dtype and row stride")
+    if outs is None:
+        outs = [torch.empty_like(x) for x in ins]
+    ld_out = _rowmajor(outs[0], "outs[0]")
+    for y in outs:
+        if y.shape != ins[0].shape or y.dtype != ins[0].dtype or _rowmajor(y, "outs") != ld_out:
+            raise ValueError("caat: all outputs need the inputs' shape and dtype, one row stride")
+    sp, ns = _sel_ptr(sel)
+    st = _lib.load().caat_partial_channel_reduce(
+        t, N, h, _dtype_code(ins[0]), _lib.ptr_array([x.data_ptr() for x in ins]), ld_in,
+        _lib.ptr_array([y.data_ptr() for y in outs]), ld_out, sp, ns, _stream_ptr(stream))
+    _check(st, "caat_partial_channel_reduce")
+    return outs
+
+
+# ---------------------------------------------------- row-parallel layer
+
+def _weight_strides(W, K, h):
+    if W.dim() != 2 or tuple(W.shape) != (K, h) or not W.is_cuda:
+        raise ValueError("caat: W must be a CUDA tensor of logical shape [K, h] = [%d, %d]" % (K, h))
+    return W.stride(0), W.stride(1)
+
+
+def rowpar_linear_fwd(X, W, t: int, sel, outs=None, stream=None):
+    """Row-parallel linear layer + PCR.  X [N, K]; W logical [K, h] (any strides,
+    e.g. ``linear.weight.t()``).  Returns t tensors [N, h]."""
+    torch = _torch()
+    N, K = X.shape
+    h = W.shape[1]
+    ldx = _rowmajor(X, "X")
+    w_rs, w_cs = _weight_strides(W, K, h)
+    if W.dtype != X.dtype:
+        raise TypeError("caat: X and W must share a dtype")
+    if outs is None:
+        outs = [torch.empty((N, h), dtype=X.dtype, device=X.device) for _ in range(t)]
+    if len(outs) != t:
+        raise ValueError("caat: need t output tensors")
+    ldy = _rowmajor(outs[0], "outs[0]")
+    for y in outs:
+        if tuple(y.shape) != (N, h) or y.dtype != X.dtype or _rowmajor(y, "outs") != ldy:
+            raise ValueError("caat: outputs must be [N, h] of X's dtype with one row stride")
+    sp, ns = _sel_ptr(sel)
+    st = _lib.load().caat_rowpar_linear_fwd(
+        int(t), N, K, h, _dtype_code(X), ctypes.c_void_p(X.data_ptr()), ldx,
+        ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
+        _lib.ptr_array([y.data_ptr() for y in outs]), ldy, sp, ns, _stream_ptr(stream))
+    _check(st, "caat_rowpar_linear_fwd")
+    return outs
+
+
+def rowpar_linear_bwd_workspace(t: int, N: int, h: int, dtype_code: int, mode: int) -> int:
+    return int(_lib.load().caat_rowpar_linear_bwd_workspace(int(t), int(N), int(h),
+                                                            int(dtype_code), int(mode)))
+
+
+def rowpar_linear_bwd(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
+                      dX=None, dW=None, workspace=None, stream=None):
+    """Gradients of ``rowpar_linear_fwd``.  dOut: t tensors [N, h].
+    Returns (dX [N, K], dW logical [K, h] with W's strides when allocated here)."""
+    torch = _torch()
+    N, K = X.shape
+    h = W.shape[1]
+    ldx = _rowmajor(X, "X")
+    w_rs, w_cs = _weight_strides(W, K, h)
+    if len(dOut) != t:
+        raise ValueError("caat: need t upstream gradients")
+    ldd = _rowmajor(dOut[0], "dOut[0]")
+    for g in dOut:
+        if tuple(g.shape) != (N, h) or g.dtype != X.dtype or _rowmajor(g, "dOut") != ldd:
+            raise ValueError("caat: dOut tensors must be [N, h] of X's dtype with one row stride")
+    if dX is None:
+        dX = torch.empty((N, K), dtype=X.dtype, device=X.device)
+    lddx = _rowmajor(dX, "dX")
+    if dW is None:
+        if w_rs == 1:    # same layout as an nn.Linear weight: [h, K] storage
+            dW = torch.empty((h, K), dtype=X.dtype, device=X.device).t()
+        else:
+            dW = torch.empty((K, h), dtype=X.dtype, device=X.device)
+    dw_rs, dw_cs = _weight_strides(dW, K, h)
+    dt = _dtype_code(X)
+    need = rowpar_linear_bwd_workspace(t, N, h, dt, mode)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    wp = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    wb = workspace.numel() if workspace is not None else 0
+    sp, ns = _sel_ptr(sel)
+    st = _lib.load().caat_rowpar_linear_bwd(
+        int(t), N, K, h, dt, ctypes.c_void_p(X.data_ptr()), ldx,
+        ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
+        _lib.ptr_array([g.data_ptr() for g in dOut]), ldd,
+        ctypes.c_void_p(dX.data_ptr()), lddx, ctypes.c_void_p(dW.data_ptr()), dw_rs, dw_cs,
+        sp, ns, int(mode), wp, wb, _stream_ptr(stream))
+    _check(st, "caat_rowpar_linear_bwd")
+    return dX, dW
+
+
+# ------------------------------------------------------------ diagnostics
+
+def device_status(stream=None) -> int:
+    """Synchronize and return (and clear) the device-side error word."""
+    return int(_lib.load().caat_get_device_status(_stream_ptr(stream)))
+
+
+def last_kernel() -> str:
+    return _lib.load().caat_last_kernel().decode()
+
+
+def launch_count() -> int:
+    return int(_lib.load().caat_launch_count())

@@ -1,0 +1,265 @@
+// C-ABI entry points: argument validation, kernel choice, launch bookkeeping.
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "caat_internal.h"
+
+namespace caat {
+
+namespace {
+thread_local const char *t_last_kernel = "none";
+thread_local uint64_t t_launches = 0;
+int g_sms[128];
+std::mutex g_mu;
+}  // namespace
+
+void note_launch(const char *kernel_name, int launches)
+{
+    t_last_kernel = kernel_name;
+    t_launches += (uint64_t)launches;
+}
+
+int num_sms()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_sms[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 148;
+        g_sms[dev] = v;
+    }
+    return g_sms[dev];
+}
+
+// defined next to the kernels that own the device error word
+caat_status read_and_clear_device_error();
+
+namespace {
+
+inline int64_t elem_size(caat_dtype dt) { return dt == CAAT_BF16 ? 2 : 4; }
+
+inline bool valid_dtype(caat_dtype dt) { return dt == CAAT_F32 || dt == CAAT_BF16; }
+
+// [lo, hi) byte range of a row-strided [rows, cols] matrix
+struct Span { uintptr_t lo, hi; };
+inline Span span_of(const void *p, int64_t rows, int64_t cols, int64_t ld, int64_t es)
+{
+    const uintptr_t lo = (uintptr_t)p;
+    const int64_t n = rows > 0 && cols > 0 ? ((rows - 1) * ld + cols) * es : 0;
+    return {lo, lo + (uintptr_t)n};
+}
+inline bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+}  // namespace
+}  // namespace caat
+
+using namespace caat;
+
+extern "C" const char *caat_status_string(caat_status st)
+{
+    switch (st) {
+    case CAAT_OK: return "CAAT_OK";
+    case CAAT_ERR_INVALID_ARG: return "CAAT_ERR_INVALID_ARG: invalid argument";
+    case CAAT_ERR_UNSUPPORTED: return "CAAT_ERR_UNSUPPORTED: no kernel takes this layout or size";
+    case CAAT_ERR_CUDA: return "CAAT_ERR_CUDA: a CUDA call or kernel launch failed";
+    case CAAT_ERR_TIMEOUT: return "CAAT_ERR_TIMEOUT: a bounded device-side wait gave up";
+    }
+    return "CAAT: unknown status";
+}
+
+extern "C" const char *caat_last_kernel(void) { return t_last_kernel; }
+
+extern "C" uint64_t caat_launch_count(void) { return t_launches; }
+
+extern "C" caat_status caat_get_device_status(caat_stream_t stream)
+{
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return CAAT_ERR_CUDA;
+    return read_and_clear_device_error();
+}
+
+extern "C" caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, caat_dtype dt,
+                                                   const void *const *in, int64_t ld_in,
+                                                   void *const *out, int64_t ld_out,
+                                                   const int32_t *sel, int64_t n_sel,
+                                                   caat_stream_t stream)
+{
+    if (t < 1 || t > CAAT_MAX_T || N < 0 || h < 0 || !valid_dtype(dt)) return CAAT_ERR_INVALID_ARG;
+    if (in == nullptr || out == nullptr) return CAAT_ERR_INVALID_ARG;
+    if (ld_in < h || ld_out < h || n_sel < 0 || n_sel > h) return CAAT_ERR_INVALID_ARG;
+    if (n_sel > 0 && sel == nullptr) return CAAT_ERR_INVALID_ARG;
+    const int64_t es = elem_size(dt);
+    ConstPtrs pin{};
+    MutPtrs pout{};
+    int same = 0;
+    for (int r = 0; r < t; ++r) {
+        if ((N > 0 && h > 0) && (in[r] == nullptr || out[r] == nullptr)) return CAAT_ERR_INVALID_ARG;
+        pin.p[r] = in[r];
+        pout.p[r] = out[r];
+        same += (in[r] == out[r]);
+    }
+    if (same != 0 && same != t) return CAAT_ERR_INVALID_ARG;
+    const bool in_place = same == t;
+    if (in_place && ld_in != ld_out) return CAAT_ERR_INVALID_ARG;
+    for (int r = 0; r < t; ++r) {
+        const Span so = span_of(out[r], N, h, ld_out, es);
+        for (int q = 0; q < t; ++q) {
+            if (q != r && overlap(so, span_of(out[q], N, h, ld_out, es))) return CAAT_ERR_INVALID_ARG;
+            if (!in_place && overlap(so, span_of(in[q], N, h, ld_in, es))) return CAAT_ERR_INVALID_ARG;
+        }
+    }
+    return launch_pcr(t, N, h, dt, pin, ld_in, pout, ld_out, in_place, sel, n_sel,
+                      (cudaStream_t)stream);
+}
+
+namespace {
+
+caat_status check_layer_args(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                             const void *X, int64_t ldx, const void *W, int64_t w_rs,
+                             int64_t w_cs, const int32_t *sel, int64_t n_sel)
+{
+    if (t < 1 || t > CAAT_MAX_T || N < 0 || K < 0 || h < 0 || !valid_dtype(dt))
+        return CAAT_ERR_INVALID_ARG;
+    if (K % t != 0) return CAAT_ERR_INVALID_ARG;
+    if (ldx < K || n_sel < 0 || n_sel > h) return CAAT_ERR_INVALID_ARG;
+    if (n_sel > 0 && sel == nullptr) return CAAT_ERR_INVALID_ARG;
+    if (N > 0 && K > 0 && X == nullptr) return CAAT_ERR_INVALID_ARG;
+    if (K > 0 && h > 0) {
+        if (W == nullptr || w_rs < 1 || w_cs < 1) return CAAT_ERR_INVALID_ARG;
+        // the two strides must not make distinct elements coincide
+        const bool row_major = w_cs == 1 && w_rs >= h;
+        const bool col_major = w_rs == 1 && w_cs >= K;
+        const bool general = (w_rs >= h * w_cs) || (w_cs >= K * w_rs);
+        if (!(row_major || col_major || general)) return CAAT_ERR_INVALID_ARG;
+    }
+    return CAAT_OK;
+}
+
+}  // namespace
+
+extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64_t h,
+                                              caat_dtype dt, const void *X, int64_t ldx,
+                                              const void *W, int64_t w_rs, int64_t w_cs,
+                                              void *const *Y, int64_t ldy,
+                                              const int32_t *sel, int64_t n_sel,
+                                              caat_stream_t stream)
+{
+    caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, sel, n_sel);
+    if (st != CAAT_OK) return st;
+    if (Y == nullptr || ldy < h) return CAAT_ERR_INVALID_ARG;
+    const int64_t es = elem_size(dt);
+    MutPtrs py{};
+    for (int r = 0; r < t; ++r) {
+        if (N > 0 && h > 0 && Y[r] == nullptr) return CAAT_ERR_INVALID_ARG;
+        py.p[r] = Y[r];
+    }
+    for (int r = 0; r < t; ++r) {
+        const Span so = span_of(Y[r], N, h, ldy, es);
+        for (int q = r + 1; q < t; ++q)
+            if (overlap(so, span_of(Y[q], N, h, ldy, es))) return CAAT_ERR_INVALID_ARG;
+        if (overlap(so, span_of(X, N, K, ldx, es))) return CAAT_ERR_INVALID_ARG;
+    }
+    if (N == 0 || h == 0) return CAAT_OK;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (dt == CAAT_BF16 && w_rs == 1 && K > 0) {
+        st = launch_rowpar_fwd_tc(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
+        if (st != CAAT_ERR_UNSUPPORTED) return st;
+    }
+    return launch_rowpar_fwd_simt(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, py, ldy, sel, n_sel, s);
+}
+
+extern "C" size_t caat_rowpar_linear_bwd_workspace(int t, int64_t N, int64_t h, caat_dtype dt,
+                                                   caat_bwd_mode mode)
+{
+    if (t < 1 || t > CAAT_MAX_T || N < 0 || h < 0 || !valid_dtype(dt)) return 0;
+    if (mode != CAAT_BWD_REDUCE_DOUT) return 0;
+    // one [N, h] buffer per rank for dY = PCR(dOut), each rounded up to 256 bytes
+    const size_t per = ((size_t)N * (size_t)h * (size_t)elem_size(dt) + 255) / 256 * 256;
+    return per * (size_t)t;
+}
+
+extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h,
+                                              caat_dtype dt, const void *X, int64_t ldx,
+                                              const void *W, int64_t w_rs, int64_t w_cs,
+                                              const void *const *dOut, int64_t ld_dout,
+                                              void *dX, int64_t lddx,
+                                              void *dW, int64_t dw_rs, int64_t dw_cs,
+                                              const int32_t *sel, int64_t n_sel,
+                                              caat_bwd_mode mode, void *workspace,
+                                              size_t ws_bytes, caat_stream_t stream)
+{
+    caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, sel, n_sel);
+    if (st != CAAT_OK) return st;
+    if (mode != CAAT_BWD_REDUCE_DOUT && mode != CAAT_BWD_NO_REDUCE) return CAAT_ERR_INVALID_ARG;
+    if (dOut == nullptr || ld_dout < h || lddx < K) return CAAT_ERR_INVALID_ARG;
+    if (N > 0 && K > 0 && dX == nullptr) return CAAT_ERR_INVALID_ARG;
+    if (K > 0 && h > 0) {
+        if (dW == nullptr || dw_rs < 1 || dw_cs < 1) return CAAT_ERR_INVALID_ARG;
+        const bool ok = (dw_cs == 1 && dw_rs >= h) || (dw_rs == 1 && dw_cs >= K) ||
+                        (dw_rs >= h * dw_cs) || (dw_cs >= K * dw_rs);
+        if (!ok) return CAAT_ERR_INVALID_ARG;
+    }
+    for (int r = 0; r < t; ++r)
+        if (N > 0 && h > 0 && dOut[r] == nullptr) return CAAT_ERR_INVALID_ARG;
+    const bool reduce = mode == CAAT_BWD_REDUCE_DOUT && n_sel > 0 && t > 1;
+    const size_t need = caat_rowpar_linear_bwd_workspace(t, N, h, dt, mode);
+    if (reduce && need > 0 && (workspace == nullptr || ws_bytes < need || ((uintptr_t)workspace & 255)))
+        return CAAT_ERR_INVALID_ARG;
+
+    const cudaStream_t s = (cudaStream_t)stream;
+    const int64_t es = elem_size(dt);
+    const int64_t kt = K / t;
+    ConstPtrs dy{};
+    int64_t ld_dy = ld_dout;
+    if (reduce) {
+        const size_t per = need / (size_t)t;
+        ConstPtrs src{};
+        MutPtrs dst{};
+        for (int r = 0; r < t; ++r) {
+            src.p[r] = dOut[r];
+            dst.p[r] = (char *)workspace + per * (size_t)r;
+            dy.p[r] = dst.p[r];
+        }
+        st = launch_pcr(t, N, h, dt, src, ld_dout, dst, h, false, sel, n_sel, s);
+        if (st != CAAT_OK) return st;
+        ld_dy = h;
+    } else {
+        for (int r = 0; r < t; ++r) dy.p[r] = dOut[r];
+    }
+    if (K == 0) return CAAT_OK;   // dX has no columns, dW no rows
+
+    // dX[:, shard r] = dY_r W_r^T : M = N, Nn = kt, Kk = h
+    BatchedGemm gx{};
+    gx.batches = t; gx.M = N; gx.Nn = kt; gx.Kk = h; gx.dt = dt;
+    gx.sa0 = ld_dy; gx.sa1 = 1;
+    gx.sb0 = w_cs; gx.sb1 = w_rs;
+    gx.sc0 = lddx; gx.sc1 = 1;
+    for (int r = 0; r < t; ++r) {
+        gx.A.p[r] = dy.p[r];
+        gx.B.p[r] = (const char *)W + (size_t)(r * kt * w_rs * es);
+        gx.C.p[r] = (char *)dX + (size_t)(r * kt * es);
+    }
+    if (h == 0) {
+        // no channels: the gradient of X is zero and dW has no columns
+        if (N > 0 && cudaMemset2DAsync(dX, (size_t)(lddx * es), 0, (size_t)(K * es), (size_t)N, s) != cudaSuccess)
+            return CAAT_ERR_CUDA;
+        return CAAT_OK;
+    }
+    st = launch_batched_gemm_simt(gx, s);   // no-op when N == 0
+    if (st != CAAT_OK) return st;
+
+    // dW[shard r, :] = X_r^T dY_r : M = kt, Nn = h, Kk = N
+    BatchedGemm gw{};
+    gw.batches = t; gw.M = kt; gw.Nn = h; gw.Kk = N; gw.dt = dt;
+    gw.sa0 = 1; gw.sa1 = ldx;
+    gw.sb0 = ld_dy; gw.sb1 = 1;
+    gw.sc0 = dw_rs; gw.sc1 = dw_cs;
+    for (int r = 0; r < t; ++r) {
+        gw.A.p[r] = (const char *)X + (size_t)(r * kt * es);
+        gw.B.p[r] = dy.p[r];
+        gw.C.p[r] = (char *)dW + (size_t)(r * kt * dw_rs * es);
+    }
+    return launch_batched_gemm_simt(gw, s);
+}

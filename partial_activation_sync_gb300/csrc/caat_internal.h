@@ -1,0 +1,58 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/caat.h"
+
+#define CAAT_MAX_T 64
+// Channel-membership bitmaps live in shared memory: h <= 2^18 channels = 32 KB.
+#define CAAT_MAX_H_BITMAP (1 << 18)
+
+namespace caat {
+
+struct ConstPtrs { const void *p[CAAT_MAX_T]; };
+struct MutPtrs { void *p[CAAT_MAX_T]; };
+
+// bookkeeping visible through caat_last_kernel / caat_launch_count
+void note_launch(const char *kernel_name, int launches = 1);
+
+// Device error word (one per device, zeroed by caat_get_device_status).
+int *device_error_word();          // device address for the current device, or null
+
+int num_sms();                     // SM count of the current device (cached)
+
+// ---- standalone partial channel-reduce (pcr.cu)
+caat_status launch_pcr(int t, int64_t N, int64_t h, caat_dtype dt,
+                       const ConstPtrs &in, int64_t ld_in, const MutPtrs &out, int64_t ld_out,
+                       bool in_place, const int32_t *sel, int64_t n_sel, cudaStream_t s);
+
+// ---- SIMT (CUDA-core) GEMM paths (gemm_simt.cu)
+// Row-parallel forward with the PCR epilogue, any strides, f32 or bf16.
+caat_status launch_rowpar_fwd_simt(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                   const void *X, int64_t ldx, const void *W, int64_t w_rs,
+                                   int64_t w_cs, const MutPtrs &Y, int64_t ldy,
+                                   const int32_t *sel, int64_t n_sel, cudaStream_t s);
+
+// Batched strided GEMM, C_b = A_b B_b, fp32 accumulate, one batch per rank.
+// Element (i, j) of A_b is at A[b] + i*sa0 + j*sa1 (likewise B, C).
+struct BatchedGemm {
+    int batches;
+    int64_t M, Nn, Kk;
+    caat_dtype dt;
+    ConstPtrs A; int64_t sa0, sa1;
+    ConstPtrs B; int64_t sb0, sb1;
+    MutPtrs C;   int64_t sc0, sc1;
+};
+caat_status launch_batched_gemm_simt(const BatchedGemm &g, cudaStream_t s);
+
+// ---- tcgen05 tensor-core paths (gemm_tc.cu)
+// Returns CAAT_ERR_UNSUPPORTED (without launching) when the shape/layout is not
+// one the tensor-core kernel takes; the caller then picks another kernel.
+caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h,
+                                 const void *X, int64_t ldx, const void *W, int64_t ldw,
+                                 const MutPtrs &Y, int64_t ldy,
+                                 const int32_t *sel, int64_t n_sel, cudaStream_t s);
+
+}  // namespace caat

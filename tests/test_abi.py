@@ -1,0 +1,129 @@
+"""Host-side checks of the C ABI (no GPU): the library builds, loads, exports
+every function ``include/caat.h`` declares, builds S bit-exactly like the oracle,
+and rejects invalid arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import oracle as orc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from partial_activation_sync_gb300 import build
+    build.build()
+    from partial_activation_sync_gb300 import _lib
+    return _lib.load()
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(caat_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert "caat_partial_channel_reduce" in declared
+    assert "caat_rowpar_linear_fwd" in declared
+    assert "caat_rowpar_linear_bwd" in declared
+    assert "caat_select_channels" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    from partial_activation_sync_gb300 import _lib
+    assert set(_lib.EXPORTS) <= declared
+
+
+def test_built_for_sm103a():
+    from partial_activation_sync_gb300 import build
+    assert ["-gencode", "arch=compute_103a,code=sm_103a"] == build.ARCH
+
+
+@pytest.mark.parametrize("h", [0, 1, 7, 12, 768, 2048, 4096, 5000])
+def test_select_channels_matches_oracle(lib, h):
+    import partial_activation_sync_gb300 as caat
+    for layout in (0, 1):
+        for p in (0.0, 0.25, 0.5, 0.75, 1.0, 0.3333):
+            for seed in (0, 4003, 2**63 + 5):
+                a = caat.select_channels(h, p, layout, seed)
+                b = orc.select_channels(h, p, layout, seed)
+                np.testing.assert_array_equal(a, b)
+
+
+def test_select_channels_rejects_bad_args(lib):
+    n = ctypes.c_int64(0)
+    idx = (ctypes.c_int32 * 8)()
+    assert lib.caat_select_channels(8, 1.5, 0, 0, idx, ctypes.byref(n)) == 1
+    assert lib.caat_select_channels(8, float("nan"), 0, 0, idx, ctypes.byref(n)) == 1
+    assert lib.caat_select_channels(8, 0.5, 7, 0, idx, ctypes.byref(n)) == 1
+    assert lib.caat_select_channels(-1, 0.5, 0, 0, idx, ctypes.byref(n)) == 1
+    assert lib.caat_select_channels(8, 0.5, 0, 0, None, ctypes.byref(n)) == 1
+    assert lib.caat_select_channels(8, 0.5, 0, 0, idx, None) == 1
+    assert lib.caat_select_channels(0, 0.5, 0, 0, None, ctypes.byref(n)) == 0 and n.value == 0
+
+
+def _ptrs(vals):
+    from partial_activation_sync_gb300 import _lib
+    return _lib.ptr_array(vals)
+
+
+def test_pcr_rejects_bad_args_without_launch(lib):
+    # fake, never dereferenced device addresses: every call must fail validation
+    a, b, c = 1 << 20, 2 << 20, 3 << 20
+    sel = ctypes.c_void_p(4 << 20)
+    f = lib.caat_partial_channel_reduce
+    assert f(0, 4, 8, 0, _ptrs([a]), 8, _ptrs([b]), 8, sel, 2, None) == 1        # t < 1
+    assert f(65, 4, 8, 0, _ptrs([a]), 8, _ptrs([b]), 8, sel, 2, None) == 1       # t > 64
+    assert f(1, 4, 8, 5, _ptrs([a]), 8, _ptrs([b]), 8, sel, 2, None) == 1        # dtype
+    assert f(1, 4, 8, 0, _ptrs([a]), 7, _ptrs([b]), 8, sel, 2, None) == 1        # ld_in < h
+    assert f(1, 4, 8, 0, _ptrs([a]), 8, _ptrs([b]), 8, sel, 9, None) == 1        # n_sel > h
+    assert f(1, 4, 8, 0, _ptrs([a]), 8, _ptrs([b]), 8, None, 2, None) == 1       # null sel
+    assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([a, c]), 8, sel, 2, None) == 1  # half in place
+    assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([c, c]), 8, sel, 2, None) == 1  # outputs overlap
+    assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([b + 16, c]), 8, sel, 2, None) == 1  # out hits in
+    assert f(2, 4, 8, 0, _ptrs([a, 0]), 8, _ptrs([b, c]), 8, sel, 2, None) == 1  # null pointer
+    assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([a, b]), 16, sel, 2, None) == 1  # in place, ld differ
+
+
+def test_layer_rejects_bad_args_without_launch(lib):
+    X, W, Y0, Y1 = 1 << 20, 2 << 20, 3 << 20, 4 << 20
+    sel = ctypes.c_void_p(5 << 20)
+    f = lib.caat_rowpar_linear_fwd
+    # K % t != 0
+    assert f(2, 4, 7, 8, 1, X, 7, W, 1, 7, _ptrs([Y0, Y1]), 8, sel, 2, None) == 1
+    # ldx < K
+    assert f(2, 4, 8, 8, 1, X, 4, W, 1, 8, _ptrs([Y0, Y1]), 8, sel, 2, None) == 1
+    # W strides that alias elements
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 1, _ptrs([Y0, Y1]), 8, sel, 2, None) == 1
+    # ldy < h
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 4, sel, 2, None) == 1
+    # outputs overlap
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y0]), 8, sel, 2, None) == 1
+    # n_sel > h
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, sel, 9, None) == 1
+    g = lib.caat_rowpar_linear_bwd
+    ws = lib.caat_rowpar_linear_bwd_workspace(2, 4, 8, 1, 0)
+    assert ws == 2 * 256                       # two [4, 8] bf16 buffers, 256-byte rounded
+    assert lib.caat_rowpar_linear_bwd_workspace(2, 4, 8, 1, 1) == 0
+    # workspace missing for the reduce-dOut mode
+    assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, 6 << 20, 8, 7 << 20, 1, 8,
+             sel, 2, 0, None, 0, None) == 1
+    # bad mode
+    assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, 6 << 20, 8, 7 << 20, 1, 8,
+             sel, 2, 9, None, 0, None) == 1
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert lib.caat_status_string(code).startswith(b"CAAT_")
+    assert lib.caat_status_string(99) == b"CAAT: unknown status"
