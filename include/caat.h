@@ -168,6 +168,44 @@ caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h, caat_
                                    void *workspace, size_t ws_bytes,
                                    caat_stream_t stream);
 
+/*
+ * caat_rowpar_linear_bwd_noalloc -- caat_rowpar_linear_bwd without a caller
+ * workspace.  The paper has no counterpart: this entry point exists for callers
+ * that cannot call cudaMalloc (for example a host framework that owns all device
+ * memory through its own pool allocator and forbids side allocations, or a
+ * process whose memory budget is fixed at start-up).
+ *
+ * Instead of a caller-provided workspace it uses one library-owned device array
+ * of CAAT_NOALLOC_SCRATCH_BYTES (16 MiB), declared at file scope in the library;
+ * every GPU that loads the library holds that array until the process exits.
+ * The call itself allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *  - Arguments and results are exactly those of caat_rowpar_linear_bwd (same
+ *    pointers, strides and modes), minus workspace / ws_bytes.
+ *  - Size limit: in CAAT_BWD_REDUCE_DOUT mode the reduced gradient needs
+ *    t * N * h * (2 for bf16, 4 for fp32) bytes of scratch; above 16 MiB the call
+ *    returns CAAT_ERR_INVALID_ARG and launches nothing (use caat_rowpar_linear_bwd
+ *    with a workspace instead).  CAAT_BWD_NO_REDUCE needs no scratch.
+ *  - The first call on a device that needs the scratch looks up the array's device
+ *    address (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls in the process share the one array, which keeps the last call's
+ *    contents.  Calls whose work overlaps on the GPU (different streams, or other
+ *    host threads, without ordering between them) race on it and corrupt each
+ *    other's results: order them on one stream or with events.  Nothing in the
+ *    array has to start at zero: each call writes every byte it later reads.
+ */
+#define CAAT_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+caat_status caat_rowpar_linear_bwd_noalloc(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                           const void *X, int64_t ldx,
+                                           const void *W, int64_t w_rs, int64_t w_cs,
+                                           const void *const *dOut, int64_t ld_dout,
+                                           void *dX, int64_t lddx,
+                                           void *dW, int64_t dw_rs, int64_t dw_cs,
+                                           const int32_t *sel, int64_t n_sel, caat_bwd_mode mode,
+                                           caat_stream_t stream);
+
 /* Human-readable name of a status code (static string, never null). */
 const char *caat_status_string(caat_status st);
 

@@ -212,3 +212,36 @@ def last_kernel() -> str:
 
 def launch_count() -> int:
     return int(_lib.load().caat_launch_count())
+
+
+# ------------------------------------------- backward without a workspace
+
+def rowpar_linear_bwd_noalloc(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
+                              dX=None, dW=None, stream=None):
+    """``rowpar_linear_bwd`` for callers that cannot allocate device memory: the
+    library's fixed 16 MiB scratch array replaces the workspace (the outputs dX
+    and dW must then be passed in; nothing is allocated here).  Calls that overlap
+    on the GPU race on that one array."""
+    L = _lib.load()
+    f = L.caat_rowpar_linear_bwd_noalloc
+    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                  ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                  ctypes.c_int, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    if dX is None or dW is None:
+        raise ValueError("caat: rowpar_linear_bwd_noalloc needs dX and dW passed in")
+    N, K = X.shape
+    h = W.shape[1]
+    w_rs, w_cs = _weight_strides(W, K, h)
+    dw_rs, dw_cs = _weight_strides(dW, K, h)
+    ldd = _rowmajor(dOut[0], "dOut[0]")
+    sp, ns = _sel_ptr(sel)
+    st = f(int(t), N, K, h, _dtype_code(X), ctypes.c_void_p(X.data_ptr()), _rowmajor(X, "X"),
+           ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
+           _lib.ptr_array([g.data_ptr() for g in dOut]), ldd,
+           ctypes.c_void_p(dX.data_ptr()), _rowmajor(dX, "dX"),
+           ctypes.c_void_p(dW.data_ptr()), dw_rs, dw_cs, sp, ns, int(mode), _stream_ptr(stream))
+    _check(st, "caat_rowpar_linear_bwd_noalloc")
+    return dX, dW

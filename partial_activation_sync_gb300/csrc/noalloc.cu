@@ -1,0 +1,67 @@
+// Backward of the fused row-parallel layer for callers that cannot allocate
+// device memory themselves: the library's own statically sized scratch array
+// stands in for the caller's workspace.
+//
+// Some callers cannot call cudaMalloc: a host framework that hands every byte
+// of device memory to its own pool allocator and forbids side allocations, or a
+// process that fixes its memory budget when it starts.  For them this file holds
+// a file-scope device array of CAAT_NOALLOC_SCRATCH_BYTES; every GPU that loads
+// the library keeps it until the process exits.
+#include <mutex>
+
+#include "caat_internal.h"
+
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CAAT_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[128];   // device address of g_noalloc_scratch, per device ordinal
+
+// In host code the array's name is a host-side shadow, not a device address;
+// the device address comes from the runtime, once per device, with that device
+// current.
+caat_status scratch_address(void **out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CAAT_ERR_CUDA;
+    if (dev < 0 || dev >= 128) return CAAT_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+            return CAAT_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return CAAT_OK;
+}
+
+}  // namespace
+
+extern "C" caat_status caat_rowpar_linear_bwd_noalloc(
+    int t, int64_t N, int64_t K, int64_t h, caat_dtype dt, const void *X, int64_t ldx,
+    const void *W, int64_t w_rs, int64_t w_cs, const void *const *dOut, int64_t ld_dout,
+    void *dX, int64_t lddx, void *dW, int64_t dw_rs, int64_t dw_cs, const int32_t *sel,
+    int64_t n_sel, caat_bwd_mode mode, caat_stream_t stream)
+{
+    // size check before any product that could overflow
+    if (t >= 1 && N > 0 && h > 0 && mode == CAAT_BWD_REDUCE_DOUT) {
+        const double bytes = (double)t * (double)N * (double)h * (dt == CAAT_BF16 ? 2.0 : 4.0);
+        if (bytes > (double)CAAT_NOALLOC_SCRATCH_BYTES) return CAAT_ERR_INVALID_ARG;
+    }
+    const size_t need = caat_rowpar_linear_bwd_workspace(t, N, h, dt, mode);
+    if (need > (size_t)CAAT_NOALLOC_SCRATCH_BYTES) return CAAT_ERR_INVALID_ARG;
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+    const bool uses_scratch = need > 0 && n_sel > 0 && t > 1 && mode == CAAT_BWD_REDUCE_DOUT;
+    if (uses_scratch) {
+        const caat_status st = scratch_address(&ws);
+        if (st != CAAT_OK) return st;
+        ws_bytes = (size_t)CAAT_NOALLOC_SCRATCH_BYTES;
+    }
+    // the reduced gradient fills the whole [t, N, h] region it uses before it is
+    // read, so nothing left over from an earlier call can leak into this one
+    return caat_rowpar_linear_bwd(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, dOut, ld_dout, dX, lddx,
+                                  dW, dw_rs, dw_cs, sel, n_sel, mode, ws, ws_bytes, stream);
+}
