@@ -38,6 +38,7 @@ def _inputs():
     files = [os.path.join(CSRC, f) for f in SOURCES]
     files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     files.append(os.path.join(INCLUDE, "caat.h"))
+    files.append(os.path.join(CSRC, "tc_ptx.cuh"))
     files.append(os.path.abspath(__file__))
     return files
 
@@ -81,7 +82,6 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     real_lib64 = [d for d in libdirs if not d.endswith("stubs")]
     if real_lib64:
         cmd += ["-Xlinker", "-rpath=" + real_lib64[0]]
-    cmd += ["-lcuda"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))

@@ -1,5 +1,41 @@
-// tcgen05 / TMEM / TMA tensor-core kernels (sm_103a).
+// Fused row-parallel GEMM + partial channel-reduce on the 5th-generation tensor
+// core (sm_103a): TMA tile loads, tcgen05.mma with accumulators in TMEM, and an
+// epilogue that writes the t rank outputs.
+//
+// "Tensor-Parallelism with Partially Synchronized Activations", Introduction,
+// partial channel-reduce paragraph: after the row-parallel layer (Y_r = X_r W_r,
+// K split t ways), channels in S are summed over the ranks and every rank gets
+// the sum; the other channels keep each rank's own partial result.
+//
+// One persistent CTA per SM walks output tiles of 128 rows x 256 channels.
+// Every tile streams the same k-blocks (shard 0's K slice, then shard 1's, ...),
+// so all tiles cost the same MMA work; what differs is where results go:
+//   FULL_S tile (every channel in S): one accumulation over all of K (that is
+//     X W[:, tile] = sum_r Y_r), written to all t outputs;
+//   NO_S tile (no channel in S): a fresh accumulation per shard, written to that
+//     rank's output after each shard;
+//   MIXED tile: shard r accumulates into TMEM buffer (r mod 2).  After each
+//     shard the epilogue writes the buffer to Y_r and zeroes the non-S columns,
+//     so the S columns keep summing (even shards in one buffer, odd shards in
+//     the other); after the last shard the two buffers' S columns are added and
+//     written to every rank.
+// Two 256-column fp32 accumulators (all 512 TMEM columns) alternate, so the
+// epilogue of one accumulation overlaps the MMAs of the next.
+//
+// Warp roles: warp 0 lane 0 issues TMA loads into a 4-stage ring, warp 1 lane 0
+// issues the MMAs (warp 1 also owns the TMEM allocation), warps 2..5 drain TMEM
+// (each warp reads the 32 TMEM lanes its rank within the warp quad may access).
+// The K slices are fetched through 3-D tensor maps (k within shard, shard, row),
+// so a shard whose width is not a multiple of 64 reads zeros past its end instead
+// of the next shard's columns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <cstdlib>
+
 #include "caat_internal.h"
+#include "tc_ptx.cuh"
 
 namespace caat {
 
@@ -17,11 +53,390 @@ caat_status read_and_clear_device_error()
     return CAAT_OK;
 }
 
-caat_status launch_rowpar_fwd_tc(int, int64_t, int64_t, int64_t, const void *, int64_t,
-                                 const void *, int64_t, const MutPtrs &, int64_t,
-                                 const int32_t *, int64_t, cudaStream_t)
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int MAX_H_TC = 32768;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legitimate wait
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+enum { FULL_S = 0, NO_S = 1, MIXED = 2 };
+
+struct SmemCtl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint32_t tmem_base;
+    int abort;
+    uint32_t bitmap[MAX_H_TC / 32];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+
+struct FwdParams {
+    MutPtrs Y;
+    int64_t ldy;
+    int64_t N, h;
+    int t, nkb, num_m, num_tiles;
+    const int32_t *sel;
+    int64_t n_sel;
+};
+
+__device__ __forceinline__ void fail(volatile int *abort)
 {
-    return CAAT_ERR_UNSUPPORTED;
+    *abort = 1;
+    atomicExch(&g_caat_dev_error, (int)CAAT_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ int tile_class(const uint32_t *bm, int64_t n0, int64_t h, int t)
+{
+    if (t == 1) return FULL_S;
+    bool any = false, all = true;
+#pragma unroll
+    for (int w = 0; w < BN / 32; ++w) {
+        const int64_t c = n0 + 32 * w;
+        if (c < h) {
+            const int64_t nv = h - c < 32 ? h - c : 32;
+            const uint32_t valid = nv == 32 ? 0xffffffffu : ((1u << nv) - 1u);
+            const uint32_t bits = bm[c >> 5] & valid;
+            any = any || bits != 0u;
+            all = all && bits == valid;
+        }
+    }
+    return all ? FULL_S : (any ? MIXED : NO_S);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_f32), __uint_as_float(hi_f32));
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// 32 fp32 values (one row, 32 channels from c0) -> bf16, 16-byte stores of the
+// 8-channel groups that lie below h.
+__device__ __forceinline__ void store_row32(void *Yr, int64_t ldy, int64_t row, int64_t c0,
+                                            int64_t h, const uint32_t (&w)[16])
+{
+    uint16_t *p = (uint16_t *)Yr + row * ldy + c0;
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+        if (c0 + 8 * g < h)
+            __stcs(reinterpret_cast<uint4 *>(p + 8 * g),
+                   make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]));
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                     const FwdParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *smA = base;
+    uint8_t *smB = base + STAGES * A_BYTES;
+    SmemCtl *ctl = (SmemCtl *)(base + STAGES * STAGE_BYTES);
+    volatile int *abort = &ctl->abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t words = (p.h + 31) >> 5;
+
+    for (int64_t w = tid; w < words; w += NUM_THREADS) ctl->bitmap[w] = 0u;
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+            mbar_init(smem_u32(&ctl->acc_empty[b]), 128);
+        }
+        ctl->abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmX);
+        prefetch_tmap(&tmW);
+    }
+    __syncthreads();
+    for (int64_t i = tid; i < p.n_sel; i += NUM_THREADS) {
+        const int32_t c = p.sel[i];
+        if (c >= 0 && c < p.h) atomicOr(&ctl->bitmap[c >> 5], 1u << (c & 31));
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = ctl->tmem_base;
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+                const int mb = tile % p.num_m, nb = tile / p.num_m;
+                for (int r = 0; r < p.t; ++r) {
+                    for (int kb = 0; kb < p.nkb; ++kb) {
+                        if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, WAIT_LIMIT_NS)) {
+                            fail(abort);
+                            goto done;
+                        }
+                        const uint32_t fb = smem_u32(&ctl->full[stage]);
+                        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                        tma_load_3d(smem_u32(smA + stage * A_BYTES), &tmX, fb, kb * BK, r, mb * BM);
+                        tma_load_3d(smem_u32(smB + stage * B_BYTES), &tmW, fb, kb * BK, r, nb * BN);
+                        if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0, au = 0;
+            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+                const int nb = tile / p.num_m;
+                const int cls = tile_class(ctl->bitmap, (int64_t)nb * BN, p.h, p.t);
+                for (int r = 0; r < p.t; ++r) {
+                    const bool starts = cls != FULL_S || r == 0;
+                    const bool ends = cls != FULL_S || r == p.t - 1;
+                    const uint32_t b = au & 1u;
+                    if (starts) {
+                        if (!mbar_wait(smem_u32(&ctl->acc_empty[b]), ((au >> 1) & 1u) ^ 1u, abort,
+                                       WAIT_LIMIT_NS)) {
+                            fail(abort);
+                            goto done;
+                        }
+                        fence_after_sync();
+                    }
+                    const bool fresh = cls == FULL_S ? r == 0 : (cls == NO_S ? true : r < 2);
+                    const uint32_t d = tmem + b * 256u;
+                    for (int kb = 0; kb < p.nkb; ++kb) {
+                        if (!mbar_wait(smem_u32(&ctl->full[stage]), ph, abort, WAIT_LIMIT_NS)) {
+                            fail(abort);
+                            goto done;
+                        }
+                        fence_after_sync();
+                        const uint32_t a0 = smem_u32(smA + stage * A_BYTES);
+                        const uint32_t b0 = smem_u32(smB + stage * B_BYTES);
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_f16(d, desc_kmajor_sw128(a0 + 32u * k), desc_kmajor_sw128(b0 + 32u * k),
+                                    IDESC, (fresh && kb == 0 && k == 0) ? 0u : 1u);
+                        mma_commit(smem_u32(&ctl->empty[stage]));
+                        if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                    }
+                    if (ends) {
+                        mma_commit(smem_u32(&ctl->acc_full[b]));
+                        ++au;
+                    }
+                }
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp & 3;                         // TMEM lane quarter of this warp
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        uint32_t au = 0;
+        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+            const int mb = tile % p.num_m, nb = tile / p.num_m;
+            const int64_t n0 = (int64_t)nb * BN;
+            const int cls = tile_class(ctl->bitmap, n0, p.h, p.t);
+            const int64_t row = (int64_t)mb * BM + 32 * q + lane;
+            const bool row_ok = row < p.N;
+            for (int r = 0; r < p.t; ++r) {
+                if (cls == FULL_S && r != p.t - 1) continue;
+                const uint32_t b = au & 1u;
+                bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au >> 1) & 1u, abort, WAIT_LIMIT_NS);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    fail(abort);
+                    goto done;
+                }
+                fence_after_sync();
+                const uint32_t tb = tmem + lane_off + b * 256u;
+                const uint32_t tb_other = tmem + lane_off + (b ^ 1u) * 256u;
+                const bool final_mixed = cls == MIXED && r == p.t - 1;
+                const bool zero_nons = cls == MIXED && r <= p.t - 3;
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32; ++ch) {
+                    const int64_t c0 = n0 + 32 * ch;
+                    if (c0 >= p.h) break;                 // same for the whole warp
+                    uint32_t v[32];
+                    tmem_ld32(tb + 32u * ch, v);
+                    const uint32_t smask = ctl->bitmap[c0 >> 5];
+                    if (!final_mixed) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                        if (row_ok) {
+                            if (cls == FULL_S) {
+                                for (int rr = 0; rr < p.t; ++rr) store_row32(p.Y.p[rr], p.ldy, row, c0, p.h, w);
+                            } else {
+                                // NO_S, or a MIXED shard before the last: the S columns
+                                // written here are rewritten with the sum at the end
+                                store_row32(p.Y.p[r], p.ldy, row, c0, p.h, w);
+                            }
+                        }
+                        if (zero_nons) {
+                            uint32_t z[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) z[j] = ((smask >> j) & 1u) ? v[j] : 0u;
+                            tmem_st32(tb + 32u * ch, z);
+                        }
+                    } else {
+                        uint32_t u[32];
+                        tmem_ld32(tb_other + 32u * ch, u);
+                        uint32_t sum[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            sum[j] = __float_as_uint(__uint_as_float(u[j]) + __uint_as_float(v[j]));
+                        if (row_ok) {
+                            uint32_t w[16], ws[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) {
+                                const uint32_t x0 = ((smask >> (2 * i)) & 1u) ? sum[2 * i] : v[2 * i];
+                                const uint32_t x1 = ((smask >> (2 * i + 1)) & 1u) ? sum[2 * i + 1] : v[2 * i + 1];
+                                w[i] = pack_bf16x2(x0, x1);
+                                ws[i] = pack_bf16x2(sum[2 * i], sum[2 * i + 1]);
+                            }
+                            store_row32(p.Y.p[p.t - 1], p.ldy, row, c0, p.h, w);
+                            for (int rr = 0; rr < p.t - 1; ++rr) {
+                                uint16_t *py = (uint16_t *)p.Y.p[rr] + row * p.ldy + c0;
+#pragma unroll
+                                for (int g = 0; g < 4; ++g) {
+                                    if (c0 + 8 * g >= p.h) continue;
+                                    const uint32_t gm = (smask >> (8 * g)) & 0xffu;
+                                    if (gm == 0xffu) {
+                                        __stcs(reinterpret_cast<uint4 *>(py + 8 * g),
+                                               make_uint4(ws[4 * g], ws[4 * g + 1], ws[4 * g + 2], ws[4 * g + 3]));
+                                    } else if (gm != 0u) {
+#pragma unroll
+                                        for (int e = 0; e < 8; ++e)
+                                            if ((gm >> e) & 1u) {
+                                                const uint32_t wd = ws[4 * g + (e >> 1)];
+                                                py[8 * g + e] = (uint16_t)((e & 1) ? (wd >> 16) : (wd & 0xffffu));
+                                            }
+                                    }
+                                }
+                            }
+                        }
+                    }
+                }
+                fence_before_sync();
+                if (cls != MIXED || r <= p.t - 3 || final_mixed) mbar_arrive(smem_u32(&ctl->acc_empty[b]));
+                if (final_mixed) mbar_arrive(smem_u32(&ctl->acc_empty[b ^ 1u]));
+                ++au;
+            }
+        }
+    }
+
+done:
+    fence_before_sync();
+    __syncthreads();
+    if (*abort) {
+        // let copies and MMAs already in flight land before TMEM and shared
+        // memory go away
+        if (tid == 0) {
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < 2000000ull) { }
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// The tensor-map encoder is a driver-API function; it is looked up through the
+// runtime so the library does not link libcuda itself.
+PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder()
+{
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return (PFN_cuTensorMapEncodeTiled_v12000)f;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_encoder();   // thread-safe init
+    return fn;
+}
+
+bool encode_3d(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+               uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2)
+{
+    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
+    const cuuint32_t box[3] = {b0, b1, b2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = encode(
+        tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
+                                 const void *W, int64_t ldw, const MutPtrs &Y, int64_t ldy,
+                                 const int32_t *sel, int64_t n_sel, cudaStream_t s)
+{
+    const int64_t kt = K / t;
+    // shapes and alignments this kernel takes; anything else goes to another kernel
+    if (kt < BK || kt % 8 != 0 || ldx % 8 != 0 || ldw % 8 != 0 || ldy % 8 != 0) return CAAT_ERR_UNSUPPORTED;
+    if (h % 8 != 0 || h < BN || h > MAX_H_TC || N < BM || N > (int64_t)INT32_MAX) return CAAT_ERR_UNSUPPORTED;
+    if ((uintptr_t)X % 16 != 0 || (uintptr_t)W % 16 != 0) return CAAT_ERR_UNSUPPORTED;
+    for (int r = 0; r < t; ++r)
+        if ((uintptr_t)Y.p[r] % 16 != 0) return CAAT_ERR_UNSUPPORTED;
+
+    CUtensorMap tmX, tmW;
+    if (!encode_3d(&tmX, X, (uint64_t)kt, (uint64_t)t, (uint64_t)N, (uint64_t)kt * 2, (uint64_t)ldx * 2,
+                   BK, 1, BM))
+        return CAAT_ERR_UNSUPPORTED;
+    if (!encode_3d(&tmW, W, (uint64_t)kt, (uint64_t)t, (uint64_t)h, (uint64_t)kt * 2, (uint64_t)ldw * 2,
+                   BK, 1, BN))
+        return CAAT_ERR_UNSUPPORTED;
+
+    FwdParams p{};
+    p.Y = Y;
+    p.ldy = ldy;
+    p.N = N;
+    p.h = h;
+    p.t = t;
+    p.nkb = (int)((kt + BK - 1) / BK);
+    p.num_m = (int)((N + BM - 1) / BM);
+    const int64_t num_n = (h + BN - 1) / BN;
+    const int64_t tiles = (int64_t)p.num_m * num_n;
+    if (tiles > INT32_MAX) return CAAT_ERR_UNSUPPORTED;
+    p.num_tiles = (int)tiles;
+    p.sel = sel;
+    p.n_sel = n_sel;
+    const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
+    if (cudaFuncSetAttribute(rowpar_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+        return CAAT_ERR_CUDA;
+    rowpar_fwd_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmX, tmW, p);
+    note_launch("rowpar_fwd_tc");
+    return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }
 
 }  // namespace caat

@@ -102,3 +102,111 @@ def test_bwd_zero_rows_gives_zero_dw(caat):
     dX, dW = caat.rowpar_linear_bwd(X, W, G, t, sel_dev(np.arange(4)), 0)
     T.cuda.synchronize()
     assert dX.shape == (0, K) and bool((dW == 0).all())
+
+
+# ------------------------------------------------ tensor-core (tcgen05) path
+
+TC_SHAPES = [
+    # t, N, k_t, h    -- ragged rows (N % 128), ragged channels (h % 256), k_t % 64
+    (2, 300, 64, 264),
+    (8, 256, 96, 768),
+    (3, 129, 200, 520),
+    (1, 128, 128, 256),
+    (8, 384, 344, 512),
+    (5, 640, 72, 1032),
+]
+
+
+@pytest.mark.parametrize("t,N,kt,h", TC_SHAPES)
+def test_fwd_tc_parity(caat, t, N, kt, h):
+    for p in (0.0, 0.25, 0.5, 1.0):
+        for layout in (0, 1):
+            got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=7 * t + h)
+            assert caat.last_kernel() == "rowpar_fwd_tc"
+            for r in range(t):
+                assert rel_fro(got[r], want[r]) <= TOL["bf16"], (r, p, layout)
+            for r in range(1, t):
+                assert np.array_equal(got[r][:, S], got[0][:, S])
+
+
+def test_fwd_tc_boundary_tile_mixed(caat):
+    # |S| = 300 with contiguous S: tile 0 all in S, tile 1 mixed, tile 2 outside
+    t, N, kt, h = 4, 256, 64, 768
+    X = ci.normal(901, (N, kt * t))
+    Wl = ci.normal(902, (kt * t, h), std=0.02)
+    S = np.arange(300, dtype=np.int32)
+    outs = caat.rowpar_linear_fwd(dev(X, "bf16"), _weight(Wl, "bf16", "nn"), t, sel_dev(S))
+    torch().cuda.synchronize()
+    assert caat.last_kernel() == "rowpar_fwd_tc"
+    got = np.stack([to_f64(o) for o in outs])
+    want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), t, S)
+    for r in range(t):
+        assert rel_fro(got[r], want[r]) <= TOL["bf16"]
+        # per-column check: the non-S half of the mixed tile is this rank's own sum
+        assert rel_fro(got[r][:, 300:512], want[r][:, 300:512]) <= TOL["bf16"]
+
+
+def test_fwd_tc_output_guard(caat):
+    # outputs with a row stride wider than h: the padding must stay untouched
+    T = torch()
+    t, N, kt, h, ld = 2, 200, 64, 256, 264
+    X = ci.normal(903, (N, kt * t))
+    Wl = ci.normal(904, (kt * t, h), std=0.02)
+    S = caat.select_channels(h, 0.5, 1, 5)
+    bufs = [T.full((N, ld), 7.0, dtype=T.bfloat16, device="cuda") for _ in range(t)]
+    outs = [b[:, :h] for b in bufs]
+    caat.rowpar_linear_fwd(dev(X, "bf16"), _weight(Wl, "bf16", "nn"), t, sel_dev(S), outs=outs)
+    T.cuda.synchronize()
+    assert caat.last_kernel() == "rowpar_fwd_tc"
+    for b in bufs:
+        assert bool((b[:, h:] == 7.0).all())
+    want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), t, S)
+    for r in range(t):
+        assert rel_fro(to_f64(outs[r]), want[r]) <= TOL["bf16"]
+
+
+FULL = [("130m", 0), ("130m", 1), ("1.1b", 0), ("1.1b", 1), ("7b_prefill", 0), ("7b_prefill", 1)]
+
+
+@pytest.mark.parametrize("wname,li", FULL)
+def test_fwd_full_size_sampled_rows(caat, wname, li):
+    """Full workload sizes in the benchmark's launch configuration; rows are
+    independent, so the oracle on a sample of rows gives those rows exactly."""
+    w = ci.WORKLOADS[wname]
+    X, Wl, _ = ci.layer_tensors(w, li)
+    ps = (0.0, 0.25, 0.5, 0.75, 1.0) if wname == "1.1b" else (w.p,)
+    layouts = (0, 1) if wname == "1.1b" else (0,)
+    Xd, Wd = dev(X, "bf16"), _weight(Wl, "bf16", "nn")
+    rows = np.sort(np.random.default_rng(li).choice(w.N, 6, replace=False))
+    rows[0], rows[-1] = 0, w.N - 1
+    Xs = host_values(X[rows], "bf16")
+    Wv = host_values(Wl, "bf16")
+    for p in ps:
+        for layout in layouts:
+            S = caat.select_channels(w.h, p, layout, w.seeds()["perm"])
+            outs = caat.rowpar_linear_fwd(Xd, Wd, w.t, sel_dev(S))
+            torch().cuda.synchronize()
+            assert caat.device_status() == 0
+            assert caat.last_kernel() == "rowpar_fwd_tc"
+            want, _ = orc.rowpar_fwd(Xs, Wv, w.t, S)
+            for r in range(w.t):
+                got = to_f64(outs[r][rows.tolist()])
+                assert rel_fro(got, want[r]) <= TOL["bf16"], (p, layout, r)
+            full0 = outs[0][:, S.tolist()] if S.size else None
+            for r in range(1, w.t):
+                if full0 is not None:
+                    assert bool((outs[r][:, S.tolist()] == full0).all())
+            del outs
+
+
+@pytest.mark.parametrize("Nd", [1, 8, 64])
+@pytest.mark.parametrize("li", [0, 1])
+def test_fwd_7b_decode(caat, Nd, li):
+    w = ci.WORKLOADS["7b_prefill"]
+    X, Wl, _ = ci.layer_tensors(w, li, N=Nd)
+    S = caat.select_channels(w.h, w.p, 0)
+    outs = caat.rowpar_linear_fwd(dev(X, "bf16"), _weight(Wl, "bf16", "nn"), w.t, sel_dev(S))
+    torch().cuda.synchronize()
+    want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), w.t, S)
+    for r in range(w.t):
+        assert rel_fro(to_f64(outs[r]), want[r]) <= TOL["bf16"]
