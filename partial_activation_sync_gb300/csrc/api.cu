@@ -230,6 +230,12 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
     }
     if (K == 0) return CAAT_OK;   // dX has no columns, dW no rows
 
+    if (dt == CAAT_BF16 && w_rs == 1 && dw_rs == 1 && N > 0 && h > 0 &&
+        bwd_tc_supported(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs)) {
+        st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs, s);
+        if (st != CAAT_ERR_UNSUPPORTED) return st;
+    }
+
     // dX[:, shard r] = dY_r W_r^T : M = N, Nn = kt, Kk = h
     BatchedGemm gx{};
     gx.batches = t; gx.M = N; gx.Nn = kt; gx.Kk = h; gx.dt = dt;

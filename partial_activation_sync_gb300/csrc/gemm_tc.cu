@@ -41,8 +41,12 @@ namespace caat {
 
 __device__ int g_caat_dev_error;
 
+caat_status read_and_clear_bwd_error();
+
 caat_status read_and_clear_device_error()
 {
+    const caat_status sb = read_and_clear_bwd_error();
+    if (sb != CAAT_OK) return sb;
     int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_caat_dev_error, sizeof(int)) != cudaSuccess) return CAAT_ERR_CUDA;
     if (v != 0) {
@@ -51,6 +55,40 @@ caat_status read_and_clear_device_error()
         return (caat_status)v;
     }
     return CAAT_OK;
+}
+
+// The tensor-map encoder is a driver-API function; it is looked up through the
+// runtime so the library does not link libcuda itself.
+static PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder()
+{
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return (PFN_cuTensorMapEncodeTiled_v12000)f;
+}
+
+// bf16 tensor map with the 128-byte swizzle, zero fill out of bounds.
+// dims[0] is the contiguous dimension; strides_bytes[i] is the stride of dims[i+1].
+bool encode_tmap(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box)
+{
+    static const PFN_cuTensorMapEncodeTiled_v12000 encode = lookup_encoder();   // thread-safe init
+    if (encode == nullptr || rank < 1 || rank > 5) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides_bytes[i];
+    }
+    const CUresult r = encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+                              d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 namespace {
@@ -359,39 +397,13 @@ done:
     }
 }
 
-// The tensor-map encoder is a driver-API function; it is looked up through the
-// runtime so the library does not link libcuda itself.
-PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder()
-{
-    void *f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-        return nullptr;
-    return (PFN_cuTensorMapEncodeTiled_v12000)f;
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static const PFN_cuTensorMapEncodeTiled_v12000 fn = lookup_encoder();   // thread-safe init
-    return fn;
-}
-
 bool encode_3d(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
                uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2)
 {
-    const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
-    if (encode == nullptr) return false;
-    const cuuint64_t dims[3] = {d0, d1, d2};
-    const cuuint64_t strides[2] = {s1_bytes, s2_bytes};
-    const cuuint32_t box[3] = {b0, b1, b2};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = encode(
-        tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
-        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    const uint64_t dims[3] = {d0, d1, d2};
+    const uint64_t strides[2] = {s1_bytes, s2_bytes};
+    const uint32_t box[3] = {b0, b1, b2};
+    return encode_tmap(tm, base, 3, dims, strides, box);
 }
 
 }  // namespace

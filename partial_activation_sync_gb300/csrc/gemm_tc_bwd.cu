@@ -1,0 +1,360 @@
+// Backward GEMMs of the fused row-parallel layer on the 5th-generation tensor
+// core (sm_103a): one grouped, persistent tcgen05 GEMM per gradient.
+//
+// "Tensor-Parallelism with Partially Synchronized Activations", Introduction:
+// forward and backward must agree.  With dY_r the (partially reduced) gradient
+// of rank r's output, the rank's shard of the input gradient and of the weight
+// gradient are
+//   dX[:, shard r]      = dY_r W_r^T   (M = tokens,   N = k_t, K = h)
+//   dW[shard r, :]^T    = dY_r^T X_r   (M = channels, N = k_t, K = tokens)
+// Both are batched over the t ranks.  The operand that carries the rank's K
+// shard (W_r or X_r) is read through one 3-D tensor map (k within shard, shard,
+// row); dY_r through one 2-D tensor map per rank.  W_r^T and X_r are MN-major
+// operands (their n index is contiguous in memory), dY_r^T too, so the MMA reads
+// them with the MN-major shared-memory layout instead of transposing in memory.
+//
+// Same machinery as the forward kernel: TMA into a 4-stage ring (warp 0), one
+// thread issuing tcgen05.mma into two alternating TMEM accumulators (warp 1),
+// four epilogue warps converting to bf16 and storing.  Every wait is bounded.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "caat_internal.h"
+#include "tc_ptx.cuh"
+
+namespace caat {
+
+// This file's own device error word (device symbols are not shared across
+// translation units in this build); read through read_and_clear_bwd_error().
+__device__ int g_bwd_dev_error;
+
+caat_status read_and_clear_bwd_error()
+{
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bwd_dev_error, sizeof(int)) != cudaSuccess) return CAAT_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_bwd_dev_error, &zero, sizeof(int)) != cudaSuccess) return CAAT_ERR_CUDA;
+        return (caat_status)v;
+    }
+    return CAAT_OK;
+}
+
+bool encode_tmap(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box);
+
+namespace {
+
+using namespace tc;
+
+constexpr int BM = 128, BK = 64, STAGES = 4, MAX_BN = 256;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_MAX_BYTES = MAX_BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_MAX_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
+constexpr int MAX_T_TC = 16;
+
+struct TmapArray {
+    CUtensorMap m[MAX_T_TC];
+};
+
+struct SmemCtl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+
+struct GemmParams {
+    MutPtrs C;          // per-rank output base
+    int64_t ldc;
+    int64_t M, Nn, Kk;  // per-rank GEMM
+    int t, num_m, num_n, nkb, BN, units;
+    uint32_t idesc;
+};
+
+__device__ __forceinline__ void fail(volatile int *abort)
+{
+    *abort = 1;
+    atomicExch(&g_bwd_dev_error, (int)CAAT_ERR_TIMEOUT);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32)
+{
+    const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_f32), __uint_as_float(hi_f32));
+    return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// A_MN: A is MN-major (dW: dY_r^T); otherwise K-major (dX: dY_r).  B is MN-major.
+template <bool A_MN>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_constant__ CUtensorMap bmap,
+                       const GemmParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    SmemCtl *ctl = (SmemCtl *)(base + STAGES * STAGE_BYTES);
+    volatile int *abort = &ctl->abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&ctl->acc_full[b]), 1);
+            mbar_init(smem_u32(&ctl->acc_empty[b]), 128);
+        }
+        ctl->abort = 0;
+        fence_mbar_init();
+        prefetch_tmap(&bmap);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = ctl->tmem_base;
+    const int per_rank = p.num_m * p.num_n;
+    const uint32_t b_bytes = (uint32_t)p.BN * BK * 2;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0;
+            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+                const int r = u / per_rank, rem = u - r * per_rank;
+                const int mb = rem % p.num_m, nb = rem / p.num_m;
+                const int m0 = mb * BM, n0 = nb * p.BN;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, WAIT_LIMIT_NS)) {
+                        fail(abort);
+                        goto done;
+                    }
+                    const uint32_t fb = smem_u32(&ctl->full[stage]);
+                    mbar_arrive_expect_tx(fb, A_BYTES + b_bytes);
+                    uint8_t *sa = base + stage * STAGE_BYTES;
+                    uint8_t *sb = sa + A_BYTES;
+                    const int k0 = kb * BK;
+                    if (A_MN) {
+                        tma_load_2d(smem_u32(sa), &amaps.m[r], fb, m0, k0);
+                        tma_load_2d(smem_u32(sa + 8192), &amaps.m[r], fb, m0 + 64, k0);
+                    } else {
+                        tma_load_2d(smem_u32(sa), &amaps.m[r], fb, k0, m0);
+                    }
+                    for (int i = 0; i < p.BN / 64; ++i)
+                        tma_load_3d(smem_u32(sb + i * 8192), &bmap, fb, n0 + 64 * i, r, k0);
+                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t ph = 0, au = 0;
+            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+                const uint32_t b = au & 1u;
+                if (!mbar_wait(smem_u32(&ctl->acc_empty[b]), ((au >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
+                    fail(abort);
+                    goto done;
+                }
+                fence_after_sync();
+                const uint32_t d = tmem + b * (uint32_t)p.BN;
+                for (int kb = 0; kb < p.nkb; ++kb) {
+                    if (!mbar_wait(smem_u32(&ctl->full[stage]), ph, abort, WAIT_LIMIT_NS)) {
+                        fail(abort);
+                        goto done;
+                    }
+                    fence_after_sync();
+                    const uint32_t a0 = smem_u32(base + stage * STAGE_BYTES);
+                    const uint32_t b0 = a0 + A_BYTES;
+#pragma unroll
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint64_t ad = A_MN ? desc_sw128(a0 + 2048u * k, 8192u, 1024u)
+                                                 : desc_kmajor_sw128(a0 + 32u * k);
+                        const uint64_t bd = desc_sw128(b0 + 2048u * k, 8192u, 1024u);
+                        mma_f16(d, ad, bd, p.idesc, (kb == 0 && k == 0) ? 0u : 1u);
+                    }
+                    mma_commit(smem_u32(&ctl->empty[stage]));
+                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                }
+                mma_commit(smem_u32(&ctl->acc_full[b]));
+                ++au;
+            }
+        }
+    } else {
+        const int q = warp & 3;
+        const uint32_t lane_off = (uint32_t)(32 * q) << 16;
+        uint32_t au = 0;
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+            const int r = u / per_rank, rem = u - r * per_rank;
+            const int mb = rem % p.num_m, nb = rem / p.num_m;
+            const int64_t row = (int64_t)mb * BM + 32 * q + lane;
+            const int64_t n0 = (int64_t)nb * p.BN;
+            const uint32_t b = au & 1u;
+            bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au >> 1) & 1u, abort, WAIT_LIMIT_NS);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                fail(abort);
+                goto done;
+            }
+            fence_after_sync();
+            const uint32_t tb = tmem + lane_off + b * (uint32_t)p.BN;
+            uint16_t *crow = (uint16_t *)p.C.p[r] + row * p.ldc;
+#pragma unroll 1
+            for (int ch = 0; ch < p.BN / 32; ++ch) {
+                const int64_t c0 = n0 + 32 * ch;
+                if (c0 >= p.Nn) break;
+                uint32_t v[32];
+                tmem_ld32(tb + 32u * ch, v);
+                if (row < p.M) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
+                        if (c0 + 8 * g < p.Nn) {
+                            const uint4 w = make_uint4(pack_bf16x2(v[8 * g], v[8 * g + 1]),
+                                                       pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
+                                                       pack_bf16x2(v[8 * g + 4], v[8 * g + 5]),
+                                                       pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
+                            __stcs(reinterpret_cast<uint4 *>(crow + c0 + 8 * g), w);
+                        }
+                    }
+                }
+            }
+            fence_before_sync();
+            mbar_arrive(smem_u32(&ctl->acc_empty[b]));
+            ++au;
+        }
+    }
+
+done:
+    fence_before_sync();
+    __syncthreads();
+    if (*abort) {
+        if (tid == 0) {
+            const uint64_t t0 = globaltimer();
+            while (globaltimer() - t0 < 2000000ull) { }
+        }
+        __syncthreads();
+    }
+    if (warp == 1) {
+        __syncwarp();
+        fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// smallest multiple of 64 (<= 256) that covers n in as few tiles as possible
+int pick_bn(int64_t n)
+{
+    const int64_t tiles = (n + MAX_BN - 1) / MAX_BN;
+    const int64_t per = (n + tiles - 1) / tiles;
+    return (int)((per + 63) / 64 * 64);
+}
+
+template <bool A_MN>
+caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &bmap, GemmParams &p,
+                           cudaStream_t s, const char *name)
+{
+    if (p.units <= 0) return CAAT_OK;
+    const int grid = p.units < num_sms() ? p.units : num_sms();
+    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<A_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)SMEM_BYTES) != cudaSuccess)
+        return CAAT_ERR_CUDA;
+    grouped_gemm_tc_kernel<A_MN><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, bmap, p);
+    note_launch(name);
+    return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
+                      const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy, const void *dX,
+                      int64_t lddx, const void *dW, int64_t ld_dw)
+{
+    const int64_t kt = K / t;
+    if (t > MAX_T_TC || kt < 64 || kt % 8 != 0 || N < BM || h < 256 || h % 8 != 0) return false;
+    if (N > (int64_t)INT32_MAX || h > (int64_t)INT32_MAX) return false;
+    if (ldx % 8 || ldw % 8 || ld_dy % 8 || lddx % 8 || ld_dw % 8) return false;
+    if ((uintptr_t)X % 16 || (uintptr_t)W % 16 || (uintptr_t)dX % 16 || (uintptr_t)dW % 16) return false;
+    for (int r = 0; r < t; ++r)
+        if ((uintptr_t)dY.p[r] % 16) return false;
+    return true;
+}
+
+// dX[:, shard r] = dY_r W_r^T and dW[shard r, :] = X_r^T dY_r for every rank.
+// W and dW are in the nn.Linear layout ([h, K] storage, row stride ldw / ld_dw).
+caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
+                                 const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
+                                 void *dX, int64_t lddx, void *dW, int64_t ld_dw, cudaStream_t s)
+{
+    const int64_t kt = K / t;
+    const int BN = pick_bn(kt);
+
+    // ---- dX = dY_r W_r^T: A = dY_r (K-major), B = W_r^T (MN-major)
+    {
+        TmapArray am;
+        for (int r = 0; r < t; ++r) {
+            const uint64_t dims[2] = {(uint64_t)h, (uint64_t)N};
+            const uint64_t str[1] = {(uint64_t)ld_dy * 2};
+            const uint32_t box[2] = {64, BM};
+            if (!encode_tmap(&am.m[r], dY.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
+        }
+        CUtensorMap bm;
+        const uint64_t dims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
+        const uint64_t str[2] = {(uint64_t)kt * 2, (uint64_t)ldw * 2};
+        const uint32_t box[3] = {64, 1, 64};
+        if (!encode_tmap(&bm, W, 3, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
+        GemmParams p{};
+        for (int r = 0; r < t; ++r) p.C.p[r] = (uint16_t *)dX + r * kt;
+        p.ldc = lddx;
+        p.M = N; p.Nn = kt; p.Kk = h;
+        p.t = t;
+        p.num_m = (int)((N + BM - 1) / BM);
+        p.num_n = (int)((kt + BN - 1) / BN);
+        p.nkb = (int)((h + BK - 1) / BK);
+        p.BN = BN;
+        p.units = t * p.num_m * p.num_n;
+        p.idesc = idesc_bf16_f32(BM, BN, false, true);
+        const caat_status st = launch_grouped<false>(am, bm, p, s, "rowpar_bwd_dx_tc");
+        if (st != CAAT_OK) return st;
+    }
+    // ---- dW^T = dY_r^T X_r: A = dY_r^T (MN-major), B = X_r (MN-major)
+    {
+        TmapArray am;
+        for (int r = 0; r < t; ++r) {
+            const uint64_t dims[2] = {(uint64_t)h, (uint64_t)N};
+            const uint64_t str[1] = {(uint64_t)ld_dy * 2};
+            const uint32_t box[2] = {64, 64};
+            if (!encode_tmap(&am.m[r], dY.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
+        }
+        CUtensorMap bm;
+        const uint64_t dims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)N};
+        const uint64_t str[2] = {(uint64_t)kt * 2, (uint64_t)ldx * 2};
+        const uint32_t box[3] = {64, 1, 64};
+        if (!encode_tmap(&bm, X, 3, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
+        GemmParams p{};
+        for (int r = 0; r < t; ++r) p.C.p[r] = (uint16_t *)dW + r * kt;
+        p.ldc = ld_dw;
+        p.M = h; p.Nn = kt; p.Kk = N;
+        p.t = t;
+        p.num_m = (int)((h + BM - 1) / BM);
+        p.num_n = (int)((kt + BN - 1) / BN);
+        p.nkb = (int)((N + BK - 1) / BK);
+        p.BN = BN;
+        p.units = t * p.num_m * p.num_n;
+        p.idesc = idesc_bf16_f32(BM, BN, true, true);
+        return launch_grouped<true>(am, bm, p, s, "rowpar_bwd_dw_tc");
+    }
+}
+
+}  // namespace caat

@@ -188,12 +188,39 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr)
     return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N >> 3 at [17,23), M >> 4 at [24,29).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+// Same 128-byte swizzle for an MN-major operand tile: TMA boxes of 64 MN-elements
+// (128 bytes) x k rows.  Within a box the rows are the K index; 8-row groups are
+// `sbo` bytes apart and successive 64-element MN blocks (successive boxes) are
+// `lbo` bytes apart.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo)
 {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
-           ((uint32_t)(M >> 4) << 24);
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32 (bits [4,6) = 1), A and B bf16
+// ([7,10) = 1, [10,13) = 1), A / B major-ness at bits 15 / 16 (0 = K-major,
+// 1 = MN-major), N >> 3 at [17,23), M >> 4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false,
+                                                      bool b_mn = false)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+           ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                            int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
 }
 
 }  // namespace tc

@@ -210,3 +210,43 @@ def test_fwd_7b_decode(caat, Nd, li):
     want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), w.t, S)
     for r in range(w.t):
         assert rel_fro(to_f64(outs[r]), want[r]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("t,N,kt,h", TC_SHAPES)
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bwd_tc_parity(caat, t, N, kt, h, mode):
+    for p in (0.0, 0.5, 1.0):
+        gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, p, 1, "bf16", mode, "nn", seed=3 * t + h)
+        assert caat.last_kernel() == "rowpar_bwd_dw_tc"
+        assert rel_fro(gX, wX) <= TOL["bf16"], ("dX", p)
+        assert rel_fro(gW, wW) <= TOL["bf16"], ("dW", p)
+
+
+@pytest.mark.parametrize("wname,li", [("130m", 0), ("130m", 1), ("1.1b", 0), ("1.1b", 1)])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bwd_full_size_sampled(caat, wname, li, mode):
+    """Full workload sizes: dX on sampled token rows (a row of dX needs only that
+    row of the gradient), dW on sampled channels (a column of dW needs only that
+    channel of W and of the gradient, and whether it is in S)."""
+    T = torch()
+    w = ci.WORKLOADS[wname]
+    X, Wl, G = ci.layer_tensors(w, li)
+    S = caat.select_channels(w.h, w.p, 1 if wname == "1.1b" else 0, w.seeds()["perm"])
+    Xd, Wd = dev(X, "bf16"), _weight(Wl, "bf16", "nn")
+    Gd = [dev(G[r], "bf16") for r in range(w.t)]
+    dX, dW = caat.rowpar_linear_bwd(Xd, Wd, Gd, w.t, sel_dev(S), mode)
+    T.cuda.synchronize()
+    assert caat.device_status() == 0
+    assert caat.last_kernel() == "rowpar_bwd_dw_tc"
+    Xv, Wv = host_values(X, "bf16"), host_values(Wl, "bf16")
+    Gv = np.stack([host_values(G[r], "bf16") for r in range(w.t)])
+    rng = np.random.default_rng(5 + li)
+    rows = np.sort(rng.choice(w.N, 4, replace=False))
+    wX, _ = orc.rowpar_bwd(Xv[rows], Wv, Gv[:, rows, :], w.t, S, mode)
+    assert rel_fro(to_f64(dX[rows.tolist()]), wX) <= TOL["bf16"]
+    cols = np.sort(rng.choice(w.h, 6, replace=False))
+    cols[0] = 0
+    inS = np.isin(cols, S)
+    S_sub = np.nonzero(inS)[0].astype(np.int32)
+    _, wW = orc.rowpar_bwd(Xv, Wv[:, cols], Gv[:, :, cols], w.t, S_sub, mode)
+    assert rel_fro(to_f64(dW[:, cols.tolist()]), wW) <= TOL["bf16"]
