@@ -102,6 +102,8 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_H_TC = 32768;
+constexpr int MAX_T_TC = 16;                 // rank outputs addressed through tensor maps
+constexpr int STG_BYTES = 32 * 128;          // per epilogue warp: 32 rows x 64 bf16 channels
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legitimate wait
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
 
@@ -117,7 +119,11 @@ struct SmemCtl {
     uint32_t bitmap[MAX_H_TC / 32];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * STG_BYTES + sizeof(SmemCtl);
+
+struct YMaps {
+    CUtensorMap m[MAX_T_TC];   // rank r's output [N, h], box 64 channels x 32 rows
+};
 
 struct FwdParams {
     MutPtrs Y;
@@ -173,13 +179,14 @@ __device__ __forceinline__ void store_row32(void *Yr, int64_t ldy, int64_t row, 
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                     const FwdParams p)
+                     const __grid_constant__ YMaps ymaps, const FwdParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *smA = base;
     uint8_t *smB = base + STAGES * A_BYTES;
-    SmemCtl *ctl = (SmemCtl *)(base + STAGES * STAGE_BYTES);
+    uint8_t *staging = base + STAGES * STAGE_BYTES;
+    SmemCtl *ctl = (SmemCtl *)(staging + 4 * STG_BYTES);
     volatile int *abort = &ctl->abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -305,8 +312,47 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                 const uint32_t tb_other = tmem + lane_off + (b ^ 1u) * 256u;
                 const bool final_mixed = cls == MIXED && r == p.t - 1;
                 const bool zero_nons = cls == MIXED && r <= p.t - 3;
+                if (cls != MIXED) {
+                    // Stage 32 rows x 64 channels in shared memory (128-byte swizzle:
+                    // 16-byte chunk j of row i sits at chunk j ^ (i mod 8)), then one
+                    // bulk tensor store per destination rank -- the same staged tile
+                    // serves all t ranks of a FULL_S tile.
+                    uint8_t *stg = staging + q * STG_BYTES;
+                    const uint32_t stg_a = smem_u32(stg);
+                    const int y = mb * BM + 32 * q;
 #pragma unroll 1
-                for (int ch = 0; ch < BN / 32; ++ch) {
+                    for (int c64 = 0; c64 < BN / 64; ++c64) {
+                        const int64_t c0 = n0 + 64 * c64;
+                        if (c0 >= p.h) break;             // same for the whole warp
+                        uint32_t v0[32], v1[32];
+                        tmem_ld32(tb + 64u * c64, v0);
+                        tmem_ld32(tb + 64u * c64 + 32u, v1);
+                        uint32_t w[32];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+                            w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+                        }
+                        if (lane == 0) bulk_wait_read0();    // staging free again
+                        __syncwarp();
+                        uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            rowp[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (cls == FULL_S) {
+                                for (int rr = 0; rr < p.t; ++rr) tma_store_2d(&ymaps.m[rr], stg_a, (int)c0, y);
+                            } else {
+                                tma_store_2d(&ymaps.m[r], stg_a, (int)c0, y);
+                            }
+                            bulk_commit();
+                        }
+                    }
+                }
+#pragma unroll 1
+                for (int ch = 0; ch < BN / 32 && cls == MIXED; ++ch) {
                     const int64_t c0 = n0 + 32 * ch;
                     if (c0 >= p.h) break;                 // same for the whole warp
                     uint32_t v[32];
@@ -379,6 +425,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     }
 
 done:
+    if (warp >= 2 && lane == 0) bulk_wait0();   // bulk stores done before shared memory goes away
     fence_before_sync();
     __syncthreads();
     if (*abort) {
@@ -416,9 +463,17 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     // shapes and alignments this kernel takes; anything else goes to another kernel
     if (kt < BK || kt % 8 != 0 || ldx % 8 != 0 || ldw % 8 != 0 || ldy % 8 != 0) return CAAT_ERR_UNSUPPORTED;
     if (h % 8 != 0 || h < BN || h > MAX_H_TC || N < BM || N > (int64_t)INT32_MAX) return CAAT_ERR_UNSUPPORTED;
+    if (t > MAX_T_TC) return CAAT_ERR_UNSUPPORTED;
     if ((uintptr_t)X % 16 != 0 || (uintptr_t)W % 16 != 0) return CAAT_ERR_UNSUPPORTED;
     for (int r = 0; r < t; ++r)
         if ((uintptr_t)Y.p[r] % 16 != 0) return CAAT_ERR_UNSUPPORTED;
+    YMaps ym;
+    for (int r = 0; r < t; ++r) {
+        const uint64_t dims[2] = {(uint64_t)h, (uint64_t)N};
+        const uint64_t str[1] = {(uint64_t)ldy * 2};
+        const uint32_t box[2] = {64, 32};
+        if (!encode_tmap(&ym.m[r], Y.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
+    }
 
     CUtensorMap tmX, tmW;
     if (!encode_3d(&tmX, X, (uint64_t)kt, (uint64_t)t, (uint64_t)N, (uint64_t)kt * 2, (uint64_t)ldx * 2,
@@ -446,7 +501,7 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     if (cudaFuncSetAttribute(rowpar_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return CAAT_ERR_CUDA;
-    rowpar_fwd_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmX, tmW, p);
+    rowpar_fwd_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmX, tmW, ym, p);
     note_launch("rowpar_fwd_tc");
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }

@@ -56,6 +56,7 @@ constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MAX_T_TC = 16;
+constexpr int STG_BYTES = 32 * 128;          // per epilogue warp: 32 rows x 64 bf16 columns
 
 struct TmapArray {
     CUtensorMap m[MAX_T_TC];
@@ -70,7 +71,7 @@ struct SmemCtl {
     int abort;
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * STG_BYTES + sizeof(SmemCtl);
 
 struct GemmParams {
     MutPtrs C;          // per-rank output base
@@ -96,11 +97,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
 template <bool A_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_constant__ CUtensorMap bmap,
-                       const GemmParams p)
+                       const __grid_constant__ CUtensorMap cmap, const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    SmemCtl *ctl = (SmemCtl *)(base + STAGES * STAGE_BYTES);
+    uint8_t *staging = base + STAGES * STAGE_BYTES;
+    SmemCtl *ctl = (SmemCtl *)(staging + 4 * STG_BYTES);
     volatile int *abort = &ctl->abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -199,7 +201,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const int r = u / per_rank, rem = u - r * per_rank;
             const int mb = rem % p.num_m, nb = rem / p.num_m;
-            const int64_t row = (int64_t)mb * BM + 32 * q + lane;
             const int64_t n0 = (int64_t)nb * p.BN;
             const uint32_t b = au & 1u;
             bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au >> 1) & 1u, abort, WAIT_LIMIT_NS);
@@ -210,24 +211,35 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             }
             fence_after_sync();
             const uint32_t tb = tmem + lane_off + b * (uint32_t)p.BN;
-            uint16_t *crow = (uint16_t *)p.C.p[r] + row * p.ldc;
+            // 32 rows x 64 columns per bulk store; the output map (column within
+            // shard, shard, row) clips columns past k_t and rows past M
+            uint8_t *stg = staging + q * STG_BYTES;
+            const uint32_t stg_a = smem_u32(stg);
+            const int y = mb * BM + 32 * q;
 #pragma unroll 1
-            for (int ch = 0; ch < p.BN / 32; ++ch) {
-                const int64_t c0 = n0 + 32 * ch;
+            for (int c64 = 0; c64 < p.BN / 64; ++c64) {
+                const int64_t c0 = n0 + 64 * c64;
                 if (c0 >= p.Nn) break;
-                uint32_t v[32];
-                tmem_ld32(tb + 32u * ch, v);
-                if (row < p.M) {
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tb + 64u * c64, v0);
+                tmem_ld32(tb + 64u * c64 + 32u, v1);
+                uint32_t w[32];
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        if (c0 + 8 * g < p.Nn) {
-                            const uint4 w = make_uint4(pack_bf16x2(v[8 * g], v[8 * g + 1]),
-                                                       pack_bf16x2(v[8 * g + 2], v[8 * g + 3]),
-                                                       pack_bf16x2(v[8 * g + 4], v[8 * g + 5]),
-                                                       pack_bf16x2(v[8 * g + 6], v[8 * g + 7]));
-                            __stcs(reinterpret_cast<uint4 *>(crow + c0 + 8 * g), w);
-                        }
-                    }
+                for (int i = 0; i < 16; ++i) {
+                    w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+                    w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+                }
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+                uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    rowp[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&cmap, stg_a, (int)c0, r, y);
+                    bulk_commit();
                 }
             }
             fence_before_sync();
@@ -237,6 +249,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
     }
 
 done:
+    if (warp >= 2 && lane == 0) bulk_wait0();
     fence_before_sync();
     __syncthreads();
     if (*abort) {
@@ -262,15 +275,15 @@ int pick_bn(int64_t n)
 }
 
 template <bool A_MN>
-caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &bmap, GemmParams &p,
-                           cudaStream_t s, const char *name)
+caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &bmap, const CUtensorMap &cmap,
+                           GemmParams &p, cudaStream_t s, const char *name)
 {
     if (p.units <= 0) return CAAT_OK;
     const int grid = p.units < num_sms() ? p.units : num_sms();
     if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<A_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_BYTES) != cudaSuccess)
         return CAAT_ERR_CUDA;
-    grouped_gemm_tc_kernel<A_MN><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, bmap, p);
+    grouped_gemm_tc_kernel<A_MN><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, bmap, cmap, p);
     note_launch(name);
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }
@@ -325,7 +338,12 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.BN = BN;
         p.units = t * p.num_m * p.num_n;
         p.idesc = idesc_bf16_f32(BM, BN, false, true);
-        const caat_status st = launch_grouped<false>(am, bm, p, s, "rowpar_bwd_dx_tc");
+        CUtensorMap cm;
+        const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)N};
+        const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)lddx * 2};
+        const uint32_t cbox[3] = {64, 1, 32};
+        if (!encode_tmap(&cm, dX, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
+        const caat_status st = launch_grouped<false>(am, bm, cm, p, s, "rowpar_bwd_dx_tc");
         if (st != CAAT_OK) return st;
     }
     // ---- dW^T = dY_r^T X_r: A = dY_r^T (MN-major), B = X_r (MN-major)
@@ -353,7 +371,12 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.BN = BN;
         p.units = t * p.num_m * p.num_n;
         p.idesc = idesc_bf16_f32(BM, BN, true, true);
-        return launch_grouped<true>(am, bm, p, s, "rowpar_bwd_dw_tc");
+        CUtensorMap cm;
+        const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
+        const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)ld_dw * 2};
+        const uint32_t cbox[3] = {64, 1, 32};
+        if (!encode_tmap(&cm, dW, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
+        return launch_grouped<true>(am, bm, cm, p, s, "rowpar_bwd_dw_tc");
     }
 }
 
