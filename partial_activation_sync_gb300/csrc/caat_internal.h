@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
-#include "../../include/caat.h"
+#include "caat.h"
 
 #define CAAT_MAX_T 64
 // Channel-membership bitmaps live in shared memory: h <= 2^18 channels = 32 KB.

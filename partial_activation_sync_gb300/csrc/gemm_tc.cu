@@ -95,23 +95,36 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_H_TC = 32768;
 constexpr int MAX_T_TC = 16;                 // rank outputs addressed through tensor maps
 constexpr int STG_BYTES = 32 * 128;          // per epilogue warp: 32 rows x 64 bf16 channels
+constexpr int MAX_STAGES = 6;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legitimate wait
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+
+// Per mode: PAIR = false, one CTA computes a 128 x 256 tile (4 stages of X 128 x 64
+// + W 256 x 64); PAIR = true, a CTA pair computes a 256 x 256 tile with one
+// cta_group::2 MMA (6 stages of X 128 x 64 + W 128 x 64 per CTA: each CTA holds
+// half the rows of X and half the channels of W, which halves the shared-memory
+// operand traffic per SM).
+template <bool PAIR>
+struct Cfg {
+    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;        // W rows (channels) per CTA per stage
+    static constexpr int B_BYTES = B_ROWS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;   // landing per stage (leader)
+    static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
+};
 
 enum { FULL_S = 0, NO_S = 1, MIXED = 2 };
 
 struct SmemCtl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
@@ -119,7 +132,11 @@ struct SmemCtl {
     uint32_t bitmap[MAX_H_TC / 32];
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * STG_BYTES + sizeof(SmemCtl);
+template <bool PAIR>
+constexpr size_t smem_bytes()
+{
+    return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + 4 * STG_BYTES + sizeof(SmemCtl);
+}
 
 struct YMaps {
     CUtensorMap m[MAX_T_TC];   // rank r's output [N, h], box 64 channels x 32 rows
@@ -129,7 +146,7 @@ struct FwdParams {
     MutPtrs Y;
     int64_t ldy;
     int64_t N, h;
-    int t, nkb, num_m, num_tiles;
+    int t, nkb, num_m, num_n;
     const int32_t *sel;
     int64_t n_sel;
 };
@@ -177,57 +194,74 @@ __device__ __forceinline__ void store_row32(void *Yr, int64_t ldy, int64_t row, 
                    make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]));
 }
 
+template <bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ YMaps ymaps, const FwdParams p)
 {
+    using C = Cfg<PAIR>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *smA = base;
-    uint8_t *smB = base + STAGES * A_BYTES;
-    uint8_t *staging = base + STAGES * STAGE_BYTES;
+    uint8_t *smB = base + C::STAGES * A_BYTES;
+    uint8_t *staging = base + C::STAGES * C::STAGE_BYTES;
     SmemCtl *ctl = (SmemCtl *)(staging + 4 * STG_BYTES);
     volatile int *abort = &ctl->abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t words = (p.h + 31) >> 5;
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;   // 0 = leader of the pair
 
     for (int64_t w = tid; w < words; w += NUM_THREADS) ctl->bitmap[w] = 0u;
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-            mbar_init(smem_u32(&ctl->acc_empty[b]), 128);
+            mbar_init(smem_u32(&ctl->acc_empty[b]), PAIR ? 256 : 128);
         }
         ctl->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&tmX);
         prefetch_tmap(&tmW);
     }
-    __syncthreads();
+    if (PAIR) cluster_sync();        // the peer's barriers exist before anything signals them
+    else __syncthreads();
     for (int64_t i = tid; i < p.n_sel; i += NUM_THREADS) {
         const int32_t c = p.sel[i];
         if (c >= 0 && c < p.h) atomicOr(&ctl->bitmap[c >> 5], 1u << (c & 31));
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
 
+    // work units: (group of 1 or 2 row blocks, 256-channel block); a pair's two
+    // CTAs take the two row blocks of a group
+    const int unit0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
+    const int nunits_grid = PAIR ? gridDim.x / 2 : gridDim.x;
+    const int num_mg = PAIR ? (p.num_m + 1) / 2 : p.num_m;
+    const int num_units = num_mg * p.num_n;
+
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
         if (lane == 0) {
             int stage = 0;
             uint32_t ph = 0;
-            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-                const int mb = tile % p.num_m, nb = tile / p.num_m;
+            for (int u = unit0; u < num_units; u += nunits_grid) {
+                const int mb = PAIR ? (u % num_mg) * 2 + (int)crank : u % num_mg;
+                const int nb = u / num_mg;
                 for (int r = 0; r < p.t; ++r) {
                     for (int kb = 0; kb < p.nkb; ++kb) {
                         if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, WAIT_LIMIT_NS)) {
@@ -235,21 +269,30 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             goto done;
                         }
                         const uint32_t fb = smem_u32(&ctl->full[stage]);
-                        mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                        tma_load_3d(smem_u32(smA + stage * A_BYTES), &tmX, fb, kb * BK, r, mb * BM);
-                        tma_load_3d(smem_u32(smB + stage * B_BYTES), &tmW, fb, kb * BK, r, nb * BN);
-                        if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                        if (PAIR) {
+                            // both CTAs' halves land on the leader's barrier
+                            const uint32_t fl = map_to_cta(fb, 0);
+                            if (crank == 0) mbar_arrive_expect_tx(fb, C::TX_BYTES);
+                            tma_load_3d_pair(smem_u32(smA + stage * A_BYTES), &tmX, fl, kb * BK, r, mb * BM);
+                            tma_load_3d_pair(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
+                                             nb * BN + (int)crank * C::B_ROWS);
+                        } else {
+                            mbar_arrive_expect_tx(fb, C::TX_BYTES);
+                            tma_load_3d(smem_u32(smA + stage * A_BYTES), &tmX, fb, kb * BK, r, mb * BM);
+                            tma_load_3d(smem_u32(smB + stage * C::B_BYTES), &tmW, fb, kb * BK, r, nb * BN);
+                        }
+                        if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
                     }
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && crank == 0) {
             int stage = 0;
             uint32_t ph = 0, au = 0;
-            for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-                const int nb = tile / p.num_m;
+            for (int u = unit0; u < num_units; u += nunits_grid) {
+                const int nb = u / num_mg;
                 const int cls = tile_class(ctl->bitmap, (int64_t)nb * BN, p.h, p.t);
                 for (int r = 0; r < p.t; ++r) {
                     const bool starts = cls != FULL_S || r == 0;
@@ -272,16 +315,22 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                         }
                         fence_after_sync();
                         const uint32_t a0 = smem_u32(smA + stage * A_BYTES);
-                        const uint32_t b0 = smem_u32(smB + stage * B_BYTES);
+                        const uint32_t b0 = smem_u32(smB + stage * C::B_BYTES);
 #pragma unroll
-                        for (int k = 0; k < BK / 16; ++k)
-                            mma_f16(d, desc_kmajor_sw128(a0 + 32u * k), desc_kmajor_sw128(b0 + 32u * k),
-                                    IDESC, (fresh && kb == 0 && k == 0) ? 0u : 1u);
-                        mma_commit(smem_u32(&ctl->empty[stage]));
-                        if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                        for (int k = 0; k < BK / 16; ++k) {
+                            const uint64_t ad = desc_kmajor_sw128(a0 + 32u * k);
+                            const uint64_t bd = desc_kmajor_sw128(b0 + 32u * k);
+                            const uint32_t acc = (fresh && kb == 0 && k == 0) ? 0u : 1u;
+                            if (PAIR) mma_f16_pair(d, ad, bd, C::IDESC, acc);
+                            else mma_f16(d, ad, bd, C::IDESC, acc);
+                        }
+                        if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), 3);
+                        else mma_commit(smem_u32(&ctl->empty[stage]));
+                        if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
                     }
                     if (ends) {
-                        mma_commit(smem_u32(&ctl->acc_full[b]));
+                        if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->acc_full[b]), 3);
+                        else mma_commit(smem_u32(&ctl->acc_full[b]));
                         ++au;
                     }
                 }
@@ -292,8 +341,9 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         const int q = warp & 3;                         // TMEM lane quarter of this warp
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t au = 0;
-        for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
-            const int mb = tile % p.num_m, nb = tile / p.num_m;
+        for (int u = unit0; u < num_units; u += nunits_grid) {
+            const int mb = PAIR ? (u % num_mg) * 2 + (int)crank : u % num_mg;
+            const int nb = u / num_mg;
             const int64_t n0 = (int64_t)nb * BN;
             const int cls = tile_class(ctl->bitmap, n0, p.h, p.t);
             const int64_t row = (int64_t)mb * BM + 32 * q + lane;
@@ -341,7 +391,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             rowp[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0) {
+                        if (lane == 0 && y < p.N) {
                             if (cls == FULL_S) {
                                 for (int rr = 0; rr < p.t; ++rr) tma_store_2d(&ymaps.m[rr], stg_a, (int)c0, y);
                             } else {
@@ -362,15 +412,9 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                         uint32_t w[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                        if (row_ok) {
-                            if (cls == FULL_S) {
-                                for (int rr = 0; rr < p.t; ++rr) store_row32(p.Y.p[rr], p.ldy, row, c0, p.h, w);
-                            } else {
-                                // NO_S, or a MIXED shard before the last: the S columns
-                                // written here are rewritten with the sum at the end
-                                store_row32(p.Y.p[r], p.ldy, row, c0, p.h, w);
-                            }
-                        }
+                        // a shard before the last: the S channels written here are
+                        // rewritten with the sum at the end
+                        if (row_ok) store_row32(p.Y.p[r], p.ldy, row, c0, p.h, w);
                         if (zero_nons) {
                             uint32_t z[32];
 #pragma unroll
@@ -378,12 +422,12 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             tmem_st32(tb + 32u * ch, z);
                         }
                     } else {
-                        uint32_t u[32];
-                        tmem_ld32(tb_other + 32u * ch, u);
+                        uint32_t uo[32];
+                        tmem_ld32(tb_other + 32u * ch, uo);
                         uint32_t sum[32];
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
-                            sum[j] = __float_as_uint(__uint_as_float(u[j]) + __uint_as_float(v[j]));
+                            sum[j] = __float_as_uint(__uint_as_float(uo[j]) + __uint_as_float(v[j]));
                         if (row_ok) {
                             uint32_t w[16], ws[16];
 #pragma unroll
@@ -417,8 +461,15 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                     }
                 }
                 fence_before_sync();
-                if (cls != MIXED || r <= p.t - 3 || final_mixed) mbar_arrive(smem_u32(&ctl->acc_empty[b]));
-                if (final_mixed) mbar_arrive(smem_u32(&ctl->acc_empty[b ^ 1u]));
+                // release the accumulator(s) to the MMA issuer (the pair leader's barrier)
+                const uint32_t eb = smem_u32(&ctl->acc_empty[b]);
+                const uint32_t eb2 = smem_u32(&ctl->acc_empty[b ^ 1u]);
+                if (cls != MIXED || r <= p.t - 3 || final_mixed) {
+                    if (PAIR) mbar_arrive_cluster(map_to_cta(eb, 0)); else mbar_arrive(eb);
+                }
+                if (final_mixed) {
+                    if (PAIR) mbar_arrive_cluster(map_to_cta(eb2, 0)); else mbar_arrive(eb2);
+                }
                 ++au;
             }
         }
@@ -437,10 +488,12 @@ done:
         }
         __syncthreads();
     }
+    if (PAIR) cluster_sync();        // neither CTA leaves while its peer may still signal it
     if (warp == 1) {
         __syncwarp();
         fence_after_sync();
-        tmem_dealloc(tmem, TMEM_COLS);
+        if (PAIR) tmem_dealloc_pair(tmem, TMEM_COLS);
+        else tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -451,6 +504,42 @@ bool encode_3d(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1, uint
     const uint64_t strides[2] = {s1_bytes, s2_bytes};
     const uint32_t box[3] = {b0, b1, b2};
     return encode_tmap(tm, base, 3, dims, strides, box);
+}
+
+template <bool PAIR>
+caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMaps &ym, const FwdParams &p,
+                       cudaStream_t s)
+{
+    auto kern = rowpar_fwd_tc_kernel<PAIR>;
+    constexpr size_t smem = smem_bytes<PAIR>();
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return CAAT_ERR_CUDA;
+    const int per = PAIR ? 2 : 1;
+    const int num_units = (PAIR ? (p.num_m + 1) / 2 : p.num_m) * p.num_n;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = per;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int groups = num_sms() / per;
+    if (PAIR) {
+        cfg.gridDim = dim3(groups * per);
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, (void *)kern, &cfg) != cudaSuccess || active < 1)
+            return CAAT_ERR_UNSUPPORTED;
+        if (active < groups) groups = active;
+    }
+    if (groups > num_units) groups = num_units;
+    cfg.gridDim = dim3(groups * per);
+    if (cudaLaunchKernelEx(&cfg, kern, tmX, tmW, ym, p) != cudaSuccess) return CAAT_ERR_CUDA;
+    note_launch(PAIR ? "rowpar_fwd_tc" : "rowpar_fwd_tc");
+    return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }
 
 }  // namespace
@@ -474,13 +563,17 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint32_t box[2] = {64, 32};
         if (!encode_tmap(&ym.m[r], Y.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
     }
+    // CTA pairs (256-row tiles) unless there is only one 128-row block;
+    // CAAT_FWD_PAIR=0 forces single-CTA tiles
+    bool pair = N > BM;
+    if (const char *e = std::getenv("CAAT_FWD_PAIR")) pair = pair && std::atoi(e) != 0;
 
     CUtensorMap tmX, tmW;
     if (!encode_3d(&tmX, X, (uint64_t)kt, (uint64_t)t, (uint64_t)N, (uint64_t)kt * 2, (uint64_t)ldx * 2,
                    BK, 1, BM))
         return CAAT_ERR_UNSUPPORTED;
     if (!encode_3d(&tmW, W, (uint64_t)kt, (uint64_t)t, (uint64_t)h, (uint64_t)kt * 2, (uint64_t)ldw * 2,
-                   BK, 1, BN))
+                   BK, 1, (uint32_t)(pair ? BN / 2 : BN)))
         return CAAT_ERR_UNSUPPORTED;
 
     FwdParams p{};
@@ -491,19 +584,19 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     p.t = t;
     p.nkb = (int)((kt + BK - 1) / BK);
     p.num_m = (int)((N + BM - 1) / BM);
-    const int64_t num_n = (h + BN - 1) / BN;
-    const int64_t tiles = (int64_t)p.num_m * num_n;
-    if (tiles > INT32_MAX) return CAAT_ERR_UNSUPPORTED;
-    p.num_tiles = (int)tiles;
+    p.num_n = (int)((h + BN - 1) / BN);
     p.sel = sel;
     p.n_sel = n_sel;
-    const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
-    if (cudaFuncSetAttribute(rowpar_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
-        return CAAT_ERR_CUDA;
-    rowpar_fwd_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(tmX, tmW, ym, p);
-    note_launch("rowpar_fwd_tc");
-    return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
+    if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;
+    if (pair) {
+        const caat_status st = launch_fwd<true>(tmX, tmW, ym, p, s);
+        if (st != CAAT_ERR_UNSUPPORTED) return st;
+        // no co-resident CTA pair possible: single-CTA tiles need their own W map
+        if (!encode_3d(&tmW, W, (uint64_t)kt, (uint64_t)t, (uint64_t)h, (uint64_t)kt * 2, (uint64_t)ldw * 2,
+                       BK, 1, BN))
+            return CAAT_ERR_UNSUPPORTED;
+    }
+    return launch_fwd<false>(tmX, tmW, ym, p, s);
 }
 
 }  // namespace caat

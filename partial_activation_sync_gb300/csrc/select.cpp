@@ -12,7 +12,7 @@
 #include <cstdint>
 #include <vector>
 
-#include "../../include/caat.h"
+#include "caat.h"
 
 namespace {
 

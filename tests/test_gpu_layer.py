@@ -117,8 +117,19 @@ TC_SHAPES = [
 ]
 
 
+@pytest.fixture(params=["pair", "single"])
+def fwd_mode(request, monkeypatch):
+    """The forward runs as CTA pairs (256-row tiles, cta_group::2) by default;
+    CAAT_FWD_PAIR=0 forces single-CTA 128-row tiles."""
+    if request.param == "single":
+        monkeypatch.setenv("CAAT_FWD_PAIR", "0")
+    else:
+        monkeypatch.delenv("CAAT_FWD_PAIR", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("t,N,kt,h", TC_SHAPES)
-def test_fwd_tc_parity(caat, t, N, kt, h):
+def test_fwd_tc_parity(caat, t, N, kt, h, fwd_mode):
     for p in (0.0, 0.25, 0.5, 1.0):
         for layout in (0, 1):
             got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=7 * t + h)
@@ -129,7 +140,7 @@ def test_fwd_tc_parity(caat, t, N, kt, h):
                 assert np.array_equal(got[r][:, S], got[0][:, S])
 
 
-def test_fwd_tc_boundary_tile_mixed(caat):
+def test_fwd_tc_boundary_tile_mixed(caat, fwd_mode):
     # |S| = 300 with contiguous S: tile 0 all in S, tile 1 mixed, tile 2 outside
     t, N, kt, h = 4, 256, 64, 768
     X = ci.normal(901, (N, kt * t))
@@ -146,7 +157,7 @@ def test_fwd_tc_boundary_tile_mixed(caat):
         assert rel_fro(got[r][:, 300:512], want[r][:, 300:512]) <= TOL["bf16"]
 
 
-def test_fwd_tc_output_guard(caat):
+def test_fwd_tc_output_guard(caat, fwd_mode):
     # outputs with a row stride wider than h: the padding must stay untouched
     T = torch()
     t, N, kt, h, ld = 2, 200, 64, 256, 264
