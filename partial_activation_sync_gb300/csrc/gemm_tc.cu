@@ -106,14 +106,18 @@ constexpr int MAX_STAGES = 6;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legitimate wait
 
 // Per mode: PAIR = false, one CTA computes a 128 x 256 tile (4 stages of X 128 x 64
-// + W 256 x 64); PAIR = true, a CTA pair computes a 256 x 256 tile with one
-// cta_group::2 MMA (6 stages of X 128 x 64 + W 128 x 64 per CTA: each CTA holds
-// half the rows of X and half the channels of W, which halves the shared-memory
-// operand traffic per SM).
-template <bool PAIR>
+// + W 256 x 64, one staging buffer per epilogue warp); PAIR = true, a CTA pair
+// computes a 256 x 256 tile with one cta_group::2 MMA (5 stages of X 128 x 64 +
+// W 128 x 64 per CTA: each CTA holds half the rows of X and half the channels of
+// W, which cuts the shared-memory operand traffic per SM by a third; two staging
+// buffers per epilogue warp so a bulk store can drain while the next is staged).
+template <int CLN>
 struct Cfg {
+    static constexpr bool PAIR = CLN > 1;
     static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int NBUF = 1;                // staging buffers per epilogue warp
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;        // W rows (channels) per CTA per stage
+    static constexpr int B_FETCH = CLN == 4 ? B_ROWS / 2 : B_ROWS;   // W rows this CTA fetches
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;   // landing per stage (leader)
@@ -132,10 +136,11 @@ struct SmemCtl {
     uint32_t bitmap[MAX_H_TC / 32];
 };
 
-template <bool PAIR>
+template <int CLN>
 constexpr size_t smem_bytes()
 {
-    return 1024 + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + 4 * STG_BYTES + sizeof(SmemCtl);
+    return 1024 + (size_t)Cfg<CLN>::STAGES * Cfg<CLN>::STAGE_BYTES + 4 * Cfg<CLN>::NBUF * STG_BYTES +
+           sizeof(SmemCtl);
 }
 
 struct YMaps {
@@ -194,29 +199,35 @@ __device__ __forceinline__ void store_row32(void *Yr, int64_t ldy, int64_t row, 
                    make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]));
 }
 
-template <bool PAIR>
+// CLN = CTAs per cluster: 1 (one CTA per tile), 2 (a CTA pair), 4 (two CTA
+// pairs on adjacent row blocks of the same channel block; the two CTAs that hold
+// the same half of the W tile each fetch half of it and multicast to both).
+template <int CLN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ YMaps ymaps, const FwdParams p)
 {
-    using C = Cfg<PAIR>;
+    using C = Cfg<CLN>;
+    constexpr bool PAIR = C::PAIR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *smA = base;
     uint8_t *smB = base + C::STAGES * A_BYTES;
     uint8_t *staging = base + C::STAGES * C::STAGE_BYTES;
-    SmemCtl *ctl = (SmemCtl *)(staging + 4 * STG_BYTES);
+    SmemCtl *ctl = (SmemCtl *)(staging + 4 * C::NBUF * STG_BYTES);
     volatile int *abort = &ctl->abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t words = (p.h + 31) >> 5;
-    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;   // 0 = leader of the pair
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+    const uint32_t leader = crank & ~1u;                    // even CTA of this CTA's pair
+    const bool is_leader = crank == leader;
 
     for (int64_t w = tid; w < words; w += NUM_THREADS) ctl->bitmap[w] = 0u;
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
-            mbar_init(smem_u32(&ctl->empty[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), CLN == 4 ? 2 : 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
@@ -247,11 +258,11 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
 
-    // work units: (group of 1 or 2 row blocks, 256-channel block); a pair's two
-    // CTAs take the two row blocks of a group
-    const int unit0 = PAIR ? blockIdx.x / 2 : blockIdx.x;
-    const int nunits_grid = PAIR ? gridDim.x / 2 : gridDim.x;
-    const int num_mg = PAIR ? (p.num_m + 1) / 2 : p.num_m;
+    // work units: (group of CLN row blocks, 256-channel block); the CTAs of a
+    // cluster take the row blocks of a group
+    const int unit0 = blockIdx.x / CLN;
+    const int nunits_grid = gridDim.x / CLN;
+    const int num_mg = (p.num_m + CLN - 1) / CLN;
     const int num_units = num_mg * p.num_n;
 
     if (warp == 0) {
@@ -259,8 +270,11 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         if (lane == 0) {
             int stage = 0;
             uint32_t ph = 0;
+#ifdef EXP_LOAD_HINT
+            const uint64_t pol_in = policy_evict_last();
+#endif
             for (int u = unit0; u < num_units; u += nunits_grid) {
-                const int mb = PAIR ? (u % num_mg) * 2 + (int)crank : u % num_mg;
+                const int mb = (u % num_mg) * CLN + (int)crank;
                 const int nb = u / num_mg;
                 for (int r = 0; r < p.t; ++r) {
                     for (int kb = 0; kb < p.nkb; ++kb) {
@@ -270,12 +284,28 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                         }
                         const uint32_t fb = smem_u32(&ctl->full[stage]);
                         if (PAIR) {
-                            // both CTAs' halves land on the leader's barrier
-                            const uint32_t fl = map_to_cta(fb, 0);
-                            if (crank == 0) mbar_arrive_expect_tx(fb, C::TX_BYTES);
+                            // both CTAs' halves land on the pair leader's barrier
+                            const uint32_t fl = map_to_cta(fb, leader);
+                            if (is_leader) mbar_arrive_expect_tx(fb, C::TX_BYTES);
+#ifdef EXP_LOAD_HINT
+                            tma_load_3d_pair_hint(smem_u32(smA + stage * A_BYTES), &tmX, fl, kb * BK, r, mb * BM, pol_in);
+                            tma_load_3d_pair_hint(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
+                                             nb * BN + (int)crank * C::B_ROWS, pol_in);
+#else
                             tma_load_3d_pair(smem_u32(smA + stage * A_BYTES), &tmX, fl, kb * BK, r, mb * BM);
-                            tma_load_3d_pair(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
-                                             nb * BN + (int)crank * C::B_ROWS);
+                            if (CLN == 4) {
+                                // this CTA holds W half (crank & 1); it fetches quarter
+                                // (crank >> 1) of that half for itself and for the CTA
+                                // with the same half in the other pair
+                                const uint32_t hh = crank & 1u, pi = crank >> 1;
+                                tma_load_3d_pair_mc(smem_u32(smB + stage * C::B_BYTES + pi * C::B_FETCH * 128), &tmW,
+                                                    fl, kb * BK, r, nb * BN + (int)(hh * C::B_ROWS + pi * C::B_FETCH),
+                                                    (uint16_t)((1u << hh) | (1u << (2 + hh))));
+                            } else {
+                                tma_load_3d_pair(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
+                                                 nb * BN + (int)crank * C::B_ROWS);
+                            }
+#endif
                         } else {
                             mbar_arrive_expect_tx(fb, C::TX_BYTES);
                             tma_load_3d(smem_u32(smA + stage * A_BYTES), &tmX, fb, kb * BK, r, mb * BM);
@@ -288,7 +318,9 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0 && crank == 0) {
+        if (lane == 0 && is_leader) {
+            const uint16_t pair_mask = (uint16_t)(3u << leader);
+            const uint16_t stage_mask = CLN == 4 ? (uint16_t)0xF : pair_mask;
             int stage = 0;
             uint32_t ph = 0, au = 0;
             for (int u = unit0; u < num_units; u += nunits_grid) {
@@ -324,12 +356,12 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             if (PAIR) mma_f16_pair(d, ad, bd, C::IDESC, acc);
                             else mma_f16(d, ad, bd, C::IDESC, acc);
                         }
-                        if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), 3);
+                        if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), stage_mask);
                         else mma_commit(smem_u32(&ctl->empty[stage]));
                         if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
                     }
                     if (ends) {
-                        if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->acc_full[b]), 3);
+                        if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->acc_full[b]), pair_mask);
                         else mma_commit(smem_u32(&ctl->acc_full[b]));
                         ++au;
                     }
@@ -341,8 +373,9 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         const int q = warp & 3;                         // TMEM lane quarter of this warp
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t au = 0;
+        int sbuf = 0;                                   // next staging buffer of this warp
         for (int u = unit0; u < num_units; u += nunits_grid) {
-            const int mb = PAIR ? (u % num_mg) * 2 + (int)crank : u % num_mg;
+            const int mb = (u % num_mg) * CLN + (int)crank;
             const int nb = u / num_mg;
             const int64_t n0 = (int64_t)nb * BN;
             const int cls = tile_class(ctl->bitmap, n0, p.h, p.t);
@@ -367,8 +400,6 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                     // 16-byte chunk j of row i sits at chunk j ^ (i mod 8)), then one
                     // bulk tensor store per destination rank -- the same staged tile
                     // serves all t ranks of a FULL_S tile.
-                    uint8_t *stg = staging + q * STG_BYTES;
-                    const uint32_t stg_a = smem_u32(stg);
                     const int y = mb * BM + 32 * q;
 #pragma unroll 1
                     for (int c64 = 0; c64 < BN / 64; ++c64) {
@@ -383,22 +414,63 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
                             w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
                         }
-                        if (lane == 0) bulk_wait_read0();    // staging free again
+                        uint8_t *stg = staging + (q * C::NBUF + sbuf) * STG_BYTES;
+                        const uint32_t stg_a = smem_u32(stg);
+                        if (++sbuf == C::NBUF) sbuf = 0;
+                        // the store that last used this buffer has finished reading it
+                        if (lane == 0) {
+                            if (C::NBUF == 2) bulk_wait_read1();
+                            else bulk_wait_read0();
+                        }
                         __syncwarp();
                         uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             rowp[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+#ifdef EXP_STG
+                        __syncwarp();
+                        // read back transposed: a warp instruction covers 4 rows x 128 bytes
+                        {
+                            const int cj = lane & 7;
+                            uint4 vv[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int rr = 4 * i + (lane >> 3);
+                                vv[i] = reinterpret_cast<const uint4 *>(stg + rr * 128)[cj ^ (rr & 7)];
+                            }
+                            const bool col_ok = c0 + 8 * cj < p.h;
+                            const int rlo = cls == FULL_S ? 0 : r, rhi = cls == FULL_S ? p.t : r + 1;
+                            for (int dst = rlo; dst < rhi; ++dst) {
+                                uint16_t *yb = (uint16_t *)p.Y.p[dst] + c0 + 8 * cj;
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    const int64_t grow = (int64_t)y + 4 * i + (lane >> 3);
+                                    if (col_ok && grow < p.N) __stcs(reinterpret_cast<uint4 *>(yb + grow * p.ldy), vv[i]);
+                                }
+                            }
+                        }
+                        __syncwarp();
+#else
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0 && y < p.N) {
+#ifdef EXP_STORE_HINT
+                            const uint64_t pol_out = policy_evict_first();
+                            if (cls == FULL_S) {
+                                for (int rr = 0; rr < p.t; ++rr) tma_store_2d_hint(&ymaps.m[rr], stg_a, (int)c0, y, pol_out);
+                            } else {
+                                tma_store_2d_hint(&ymaps.m[r], stg_a, (int)c0, y, pol_out);
+                            }
+#else
                             if (cls == FULL_S) {
                                 for (int rr = 0; rr < p.t; ++rr) tma_store_2d(&ymaps.m[rr], stg_a, (int)c0, y);
                             } else {
                                 tma_store_2d(&ymaps.m[r], stg_a, (int)c0, y);
                             }
+#endif
                             bulk_commit();
                         }
+#endif
                     }
                 }
 #pragma unroll 1
@@ -465,10 +537,10 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                 const uint32_t eb = smem_u32(&ctl->acc_empty[b]);
                 const uint32_t eb2 = smem_u32(&ctl->acc_empty[b ^ 1u]);
                 if (cls != MIXED || r <= p.t - 3 || final_mixed) {
-                    if (PAIR) mbar_arrive_cluster(map_to_cta(eb, 0)); else mbar_arrive(eb);
+                    if (PAIR) mbar_arrive_cluster(map_to_cta(eb, leader)); else mbar_arrive(eb);
                 }
                 if (final_mixed) {
-                    if (PAIR) mbar_arrive_cluster(map_to_cta(eb2, 0)); else mbar_arrive(eb2);
+                    if (PAIR) mbar_arrive_cluster(map_to_cta(eb2, leader)); else mbar_arrive(eb2);
                 }
                 ++au;
             }
@@ -506,16 +578,17 @@ bool encode_3d(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1, uint
     return encode_tmap(tm, base, 3, dims, strides, box);
 }
 
-template <bool PAIR>
+template <int CLN>
 caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMaps &ym, const FwdParams &p,
                        cudaStream_t s)
 {
-    auto kern = rowpar_fwd_tc_kernel<PAIR>;
-    constexpr size_t smem = smem_bytes<PAIR>();
+    constexpr bool PAIR = CLN > 1;
+    auto kern = rowpar_fwd_tc_kernel<CLN>;
+    constexpr size_t smem = smem_bytes<CLN>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return CAAT_ERR_CUDA;
-    const int per = PAIR ? 2 : 1;
-    const int num_units = (PAIR ? (p.num_m + 1) / 2 : p.num_m) * p.num_n;
+    const int per = CLN;
+    const int num_units = ((p.num_m + CLN - 1) / CLN) * p.num_n;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -563,17 +636,19 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint32_t box[2] = {64, 32};
         if (!encode_tmap(&ym.m[r], Y.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
     }
-    // CTA pairs (256-row tiles) unless there is only one 128-row block;
-    // CAAT_FWD_PAIR=0 forces single-CTA tiles
-    bool pair = N > BM;
-    if (const char *e = std::getenv("CAAT_FWD_PAIR")) pair = pair && std::atoi(e) != 0;
+    // CTAs per cluster: two CTA pairs sharing the W tile when there are at least
+    // four 128-row blocks, one pair when two, else one CTA per tile
+    // (override: CAAT_FWD_CLUSTER=1|2|4)
+    const int64_t nm = (N + BM - 1) / BM;
+    int cln = nm >= 4 ? 4 : (nm >= 2 ? 2 : 1);
+    if (const char *e = std::getenv("CAAT_FWD_CLUSTER")) {
+        const int v = std::atoi(e);
+        if ((v == 1 || v == 2 || v == 4) && v <= nm) cln = v;
+    }
 
-    CUtensorMap tmX, tmW;
+    CUtensorMap tmX;
     if (!encode_3d(&tmX, X, (uint64_t)kt, (uint64_t)t, (uint64_t)N, (uint64_t)kt * 2, (uint64_t)ldx * 2,
                    BK, 1, BM))
-        return CAAT_ERR_UNSUPPORTED;
-    if (!encode_3d(&tmW, W, (uint64_t)kt, (uint64_t)t, (uint64_t)h, (uint64_t)kt * 2, (uint64_t)ldw * 2,
-                   BK, 1, (uint32_t)(pair ? BN / 2 : BN)))
         return CAAT_ERR_UNSUPPORTED;
 
     FwdParams p{};
@@ -588,15 +663,18 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     p.sel = sel;
     p.n_sel = n_sel;
     if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;
-    if (pair) {
-        const caat_status st = launch_fwd<true>(tmX, tmW, ym, p, s);
-        if (st != CAAT_ERR_UNSUPPORTED) return st;
-        // no co-resident CTA pair possible: single-CTA tiles need their own W map
+    for (;; cln >>= 1) {
+        CUtensorMap tmW;
+        const uint32_t wrows = cln == 1 ? BN : (cln == 2 ? BN / 2 : BN / 4);
         if (!encode_3d(&tmW, W, (uint64_t)kt, (uint64_t)t, (uint64_t)h, (uint64_t)kt * 2, (uint64_t)ldw * 2,
-                       BK, 1, BN))
+                       BK, 1, wrows))
             return CAAT_ERR_UNSUPPORTED;
+        const caat_status st = cln == 4 ? launch_fwd<4>(tmX, tmW, ym, p, s)
+                             : cln == 2 ? launch_fwd<2>(tmX, tmW, ym, p, s)
+                                        : launch_fwd<1>(tmX, tmW, ym, p, s);
+        // a cluster shape that cannot be co-resident falls back to a smaller one
+        if (st != CAAT_ERR_UNSUPPORTED || cln == 1) return st;
     }
-    return launch_fwd<false>(tmX, tmW, ym, p, s);
 }
 
 }  // namespace caat

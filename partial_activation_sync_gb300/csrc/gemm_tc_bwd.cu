@@ -56,7 +56,8 @@ constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MAX_T_TC = 16;
-constexpr int STG_BYTES = 32 * 128;          // per epilogue warp: 32 rows x 64 bf16 columns
+constexpr int STG_BYTES = 32 * 128;          // 32 rows x 64 bf16 columns
+constexpr int NBUF = 2;                      // staging buffers per epilogue warp
 
 struct TmapArray {
     CUtensorMap m[MAX_T_TC];
@@ -71,7 +72,7 @@ struct SmemCtl {
     int abort;
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * STG_BYTES + sizeof(SmemCtl);
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * NBUF * STG_BYTES + sizeof(SmemCtl);
 
 struct GemmParams {
     MutPtrs C;          // per-rank output base
@@ -102,7 +103,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *staging = base + STAGES * STAGE_BYTES;
-    SmemCtl *ctl = (SmemCtl *)(staging + 4 * STG_BYTES);
+    SmemCtl *ctl = (SmemCtl *)(staging + 4 * NBUF * STG_BYTES);
     volatile int *abort = &ctl->abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -198,6 +199,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
         const int q = warp & 3;
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t au = 0;
+        int sbuf = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
             const int r = u / per_rank, rem = u - r * per_rank;
             const int mb = rem % p.num_m, nb = rem / p.num_m;
@@ -213,8 +215,6 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             const uint32_t tb = tmem + lane_off + b * (uint32_t)p.BN;
             // 32 rows x 64 columns per bulk store; the output map (column within
             // shard, shard, row) clips columns past k_t and rows past M
-            uint8_t *stg = staging + q * STG_BYTES;
-            const uint32_t stg_a = smem_u32(stg);
             const int y = mb * BM + 32 * q;
 #pragma unroll 1
             for (int c64 = 0; c64 < p.BN / 64; ++c64) {
@@ -229,7 +229,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
                     w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
                 }
-                if (lane == 0) bulk_wait_read0();
+                uint8_t *stg = staging + (q * NBUF + sbuf) * STG_BYTES;
+                const uint32_t stg_a = smem_u32(stg);
+                if (++sbuf == NBUF) sbuf = 0;
+                if (lane == 0) bulk_wait_read1();   // the store that last used this buffer has read it
                 __syncwarp();
                 uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
 #pragma unroll

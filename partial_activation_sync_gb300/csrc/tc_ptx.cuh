@@ -107,6 +107,13 @@ __device__ __forceinline__ void bulk_wait_read0()
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// wait until all but the most recent committed bulk store group have finished
+// reading shared memory
+__device__ __forceinline__ void bulk_wait_read1()
+{
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // wait until every committed bulk store is complete
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -142,6 +149,19 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Pair form with multicast: the tile lands at offset `dst` in every CTA of
+// ctaMask; each destination's completion goes to the mbarrier at offset `bar`
+// of that destination's pair leader.
+__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                                    int c1, int c2, uint16_t mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
+        : "memory");
+}
+
 // shared::cta address -> shared::cluster address of the same offset in CTA `rank`
 __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank)
 {
@@ -155,6 +175,51 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
                  : "memory");
+}
+
+// L2 eviction-priority policies for the cache_hint forms below
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                                 int c1, int c2, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                                      int c1, int c2, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d_hint(const void *tmap, uint32_t src, int c0, int c1,
+                                                  uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
+            tmap),
+        "r"(src), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()

@@ -114,17 +114,16 @@ TC_SHAPES = [
     (1, 128, 128, 256),
     (8, 384, 344, 512),
     (5, 640, 72, 1032),
+    (3, 700, 64, 520),      # six row blocks: the second cluster of four has two idle CTAs
 ]
 
 
-@pytest.fixture(params=["pair", "single"])
+@pytest.fixture(params=["4", "2", "1"])
 def fwd_mode(request, monkeypatch):
-    """The forward runs as CTA pairs (256-row tiles, cta_group::2) by default;
-    CAAT_FWD_PAIR=0 forces single-CTA 128-row tiles."""
-    if request.param == "single":
-        monkeypatch.setenv("CAAT_FWD_PAIR", "0")
-    else:
-        monkeypatch.delenv("CAAT_FWD_PAIR", raising=False)
+    """Cluster shape of the forward: 4 = two CTA pairs sharing W tiles by
+    multicast (the default from four row blocks up), 2 = one CTA pair
+    (cta_group::2, 256-row tiles), 1 = one CTA per 128-row tile."""
+    monkeypatch.setenv("CAAT_FWD_CLUSTER", request.param)
     return request.param
 
 
