@@ -154,7 +154,7 @@ def run_gpu(args, w):
     S = caat.select_channels(w.h, w.p, w.layout, w.seeds()["perm"])
     sel = torch.from_numpy(S).to(device)
     layers = [LayerData(torch, w, i, device) for i in range(len(w.layers))]
-    ws_bytes = max(caat.rowpar_linear_bwd_workspace(w.t, w.N, w.h, 1, 0), 256)
+    ws_bytes = max(max(caat.rowpar_linear_bwd_workspace(w.t, w.N, L.K, w.h, 1, 0) for L in w.layers), 256)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()

@@ -150,12 +150,19 @@ caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64_t h, caat_
  *   dX[:, shard r] = dY_r W_r^T,
  * and dW, logical [K, h] with element (k, c) at dW[k*dw_rs + c*dw_cs], with
  *   dW[shard r, :] = X_r^T dY_r.
- * workspace: device scratch of at least caat_rowpar_linear_bwd_workspace() bytes,
- *       256-byte aligned, owned by the caller and untouched after the stream reaches
- *       the end of this call; may be null when that size is 0.
+ * workspace: device scratch, 256-byte aligned, owned by the caller and no longer
+ *       used once the stream passes the end of this call.  Its layout:
+ *         [ reduced gradient: t buffers of [N, h], each rounded up to 256 bytes ]
+ *           -- required in CAAT_BWD_REDUCE_DOUT mode when S is not empty and t > 1;
+ *         [ fp32 accumulator of dW, [h, K], rounded up to 256 bytes ]
+ *           -- optional (bf16 only): with it dW is reduced over tokens in several
+ *              parts on more SMs, then rounded once to bf16.
+ *       caat_rowpar_linear_bwd_workspace() returns the size of both parts; a
+ *       workspace holding only the required part also works.  May be null when
+ *       nothing is required.
  * Errors: as caat_rowpar_linear_fwd; INVALID_ARG also when ws_bytes is too small.
  */
-size_t caat_rowpar_linear_bwd_workspace(int t, int64_t N, int64_t h, caat_dtype dt,
+size_t caat_rowpar_linear_bwd_workspace(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
                                         caat_bwd_mode mode);
 
 caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
@@ -183,9 +190,12 @@ caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h, caat_
  *  - Arguments and results are exactly those of caat_rowpar_linear_bwd (same
  *    pointers, strides and modes), minus workspace / ws_bytes.
  *  - Size limit: in CAAT_BWD_REDUCE_DOUT mode the reduced gradient needs
- *    t * N * h * (2 for bf16, 4 for fp32) bytes of scratch; above 16 MiB the call
- *    returns CAAT_ERR_INVALID_ARG and launches nothing (use caat_rowpar_linear_bwd
- *    with a workspace instead).  CAAT_BWD_NO_REDUCE needs no scratch.
+ *    t * N * h * (2 for bf16, 4 for fp32) bytes of scratch (each rank's part
+ *    rounded up to 256 bytes); above 16 MiB the call returns
+ *    CAAT_ERR_INVALID_ARG and launches nothing (use caat_rowpar_linear_bwd with a
+ *    workspace instead).  CAAT_BWD_NO_REDUCE needs no scratch.  When the rest of
+ *    the array also holds the optional fp32 dW accumulator (h * K * 4 bytes), it
+ *    is used for it as well.
  *  - The first call on a device that needs the scratch looks up the array's device
  *    address (cudaGetSymbolAddress) with that device current; make that first call
  *    before any stream capture.

@@ -153,8 +153,8 @@ def rowpar_linear_fwd(X, W, t: int, sel, outs=None, stream=None):
     return outs
 
 
-def rowpar_linear_bwd_workspace(t: int, N: int, h: int, dtype_code: int, mode: int) -> int:
-    return int(_lib.load().caat_rowpar_linear_bwd_workspace(int(t), int(N), int(h),
+def rowpar_linear_bwd_workspace(t: int, N: int, K: int, h: int, dtype_code: int, mode: int) -> int:
+    return int(_lib.load().caat_rowpar_linear_bwd_workspace(int(t), int(N), int(K), int(h),
                                                             int(dtype_code), int(mode)))
 
 
@@ -183,7 +183,7 @@ def rowpar_linear_bwd(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
             dW = torch.empty((K, h), dtype=X.dtype, device=X.device)
     dw_rs, dw_cs = _weight_strides(dW, K, h)
     dt = _dtype_code(X)
-    need = rowpar_linear_bwd_workspace(t, N, h, dt, mode)
+    need = rowpar_linear_bwd_workspace(t, N, K, h, dt, mode)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     wp = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None

@@ -47,7 +47,7 @@ def load(path: str = None) -> ctypes.CDLL:
                                          _c_p, _c_i64, _c_p, _c_i64, _c_i64,
                                          _c_pp, _c_i64, _c_p, _c_i64, _c_p]
     L.caat_rowpar_linear_fwd.restype = ctypes.c_int
-    L.caat_rowpar_linear_bwd_workspace.argtypes = [ctypes.c_int, _c_i64, _c_i64, ctypes.c_int,
+    L.caat_rowpar_linear_bwd_workspace.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
                                                    ctypes.c_int]
     L.caat_rowpar_linear_bwd_workspace.restype = ctypes.c_size_t
     L.caat_rowpar_linear_bwd.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,

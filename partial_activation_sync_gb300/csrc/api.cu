@@ -170,14 +170,32 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
     return launch_rowpar_fwd_simt(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, py, ldy, sel, n_sel, s);
 }
 
-extern "C" size_t caat_rowpar_linear_bwd_workspace(int t, int64_t N, int64_t h, caat_dtype dt,
-                                                   caat_bwd_mode mode)
+namespace {
+
+// bytes of the reduced-gradient region: one [N, h] buffer per rank, each rounded
+// up to 256 bytes (REDUCE_DOUT only)
+size_t dy_region_bytes(int t, int64_t N, int64_t h, caat_dtype dt, caat_bwd_mode mode)
 {
-    if (t < 1 || t > CAAT_MAX_T || N < 0 || h < 0 || !valid_dtype(dt)) return 0;
     if (mode != CAAT_BWD_REDUCE_DOUT) return 0;
-    // one [N, h] buffer per rank for dY = PCR(dOut), each rounded up to 256 bytes
     const size_t per = ((size_t)N * (size_t)h * (size_t)elem_size(dt) + 255) / 256 * 256;
     return per * (size_t)t;
+}
+
+// bytes of the fp32 accumulator of dW [h, K] used by the split reduction (bf16)
+size_t wacc_region_bytes(int64_t K, int64_t h, caat_dtype dt)
+{
+    if (dt != CAAT_BF16) return 0;
+    return ((size_t)K * (size_t)h * 4 + 255) / 256 * 256;
+}
+
+}  // namespace
+
+extern "C" size_t caat_rowpar_linear_bwd_workspace(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                                   caat_bwd_mode mode)
+{
+    if (t < 1 || t > CAAT_MAX_T || N < 0 || K < 0 || h < 0 || !valid_dtype(dt)) return 0;
+    if (mode != CAAT_BWD_REDUCE_DOUT && mode != CAAT_BWD_NO_REDUCE) return 0;
+    return dy_region_bytes(t, N, h, dt, mode) + wacc_region_bytes(K, h, dt);
 }
 
 extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h,
@@ -204,9 +222,15 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
     for (int r = 0; r < t; ++r)
         if (N > 0 && h > 0 && dOut[r] == nullptr) return CAAT_ERR_INVALID_ARG;
     const bool reduce = mode == CAAT_BWD_REDUCE_DOUT && n_sel > 0 && t > 1;
-    const size_t need = caat_rowpar_linear_bwd_workspace(t, N, h, dt, mode);
-    if (reduce && need > 0 && (workspace == nullptr || ws_bytes < need || ((uintptr_t)workspace & 255)))
+    // the reduced-gradient region is required; the dW accumulator after it is
+    // optional (without it dW is not split over tokens)
+    const size_t need = reduce ? dy_region_bytes(t, N, h, dt, mode) : 0;
+    if (need > 0 && (workspace == nullptr || ws_bytes < need || ((uintptr_t)workspace & 255)))
         return CAAT_ERR_INVALID_ARG;
+    float *wacc = nullptr;
+    if (workspace != nullptr && ((uintptr_t)workspace & 255) == 0 &&
+        ws_bytes >= need + wacc_region_bytes(K, h, dt) && wacc_region_bytes(K, h, dt) > 0)
+        wacc = (float *)((char *)workspace + need);
 
     const cudaStream_t s = (cudaStream_t)stream;
     const int64_t es = elem_size(dt);
@@ -232,7 +256,7 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
 
     if (dt == CAAT_BF16 && w_rs == 1 && dw_rs == 1 && N > 0 && h > 0 &&
         bwd_tc_supported(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs)) {
-        st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs, s);
+        st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs, wacc, s);
         if (st != CAAT_ERR_UNSUPPORTED) return st;
     }
 

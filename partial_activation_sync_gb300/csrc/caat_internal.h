@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "caat.h"
@@ -55,13 +56,21 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h,
                                  const MutPtrs &Y, int64_t ldy,
                                  const int32_t *sel, int64_t n_sel, cudaStream_t s);
 
+// Tensor map for TMA (gemm_tc.cu): 128-byte swizzle, zero fill out of bounds;
+// bf16 elements unless f32.
+bool encode_tmap(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,
+                 const uint64_t *strides_bytes, const uint32_t *box, bool f32 = false);
+
 // Tensor-core backward (gemm_tc_bwd.cu): dX and dW as two grouped tcgen05 GEMMs.
 // W and dW in the nn.Linear layout ([h, K] storage, row strides ldw / ld_dw).
 bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                       const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy, const void *dX,
                       int64_t lddx, const void *dW, int64_t ld_dw);
+// wacc: fp32 scratch of h * K floats for a split reduction over tokens in dW
+// (null: no split).
 caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
-                                 void *dX, int64_t lddx, void *dW, int64_t ld_dw, cudaStream_t s);
+                                 void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
+                                 cudaStream_t s);
 
 }  // namespace caat

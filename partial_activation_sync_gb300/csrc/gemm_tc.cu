@@ -70,10 +70,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 lookup_encoder()
     return (PFN_cuTensorMapEncodeTiled_v12000)f;
 }
 
-// bf16 tensor map with the 128-byte swizzle, zero fill out of bounds.
+// bf16 (or fp32) tensor map with the 128-byte swizzle, zero fill out of bounds.
 // dims[0] is the contiguous dimension; strides_bytes[i] is the stride of dims[i+1].
 bool encode_tmap(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,
-                 const uint64_t *strides_bytes, const uint32_t *box)
+                 const uint64_t *strides_bytes, const uint32_t *box, bool f32)
 {
     static const PFN_cuTensorMapEncodeTiled_v12000 encode = lookup_encoder();   // thread-safe init
     if (encode == nullptr || rank < 1 || rank > 5) return false;
@@ -85,7 +85,7 @@ bool encode_tmap(CUtensorMap *tm, const void *base, int rank, const uint64_t *di
         es[i] = 1;
         if (i + 1 < rank) st[i] = strides_bytes[i];
     }
-    const CUresult r = encode(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
+    const CUresult r = encode(tm, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void *>(base),
                               d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;

@@ -41,9 +41,6 @@ caat_status read_and_clear_bwd_error()
     return CAAT_OK;
 }
 
-bool encode_tmap(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,
-                 const uint64_t *strides_bytes, const uint32_t *box);
-
 namespace {
 
 using namespace tc;
@@ -75,10 +72,9 @@ struct SmemCtl {
 constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * NBUF * STG_BYTES + sizeof(SmemCtl);
 
 struct GemmParams {
-    MutPtrs C;          // per-rank output base
-    int64_t ldc;
     int64_t M, Nn, Kk;  // per-rank GEMM
     int t, num_m, num_n, nkb, BN, units;
+    int ksplit, kbps;   // K range split in ksplit parts of kbps k-blocks (RED only)
     uint32_t idesc;
 };
 
@@ -95,7 +91,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
 }
 
 // A_MN: A is MN-major (dW: dY_r^T); otherwise K-major (dX: dY_r).  B is MN-major.
-template <bool A_MN>
+// RED: the K range is split over several CTAs and each adds its fp32 partial
+// into an fp32 array with a TMA reduce-add (cmap is then an fp32 map);
+// otherwise the tile is rounded to bf16 and stored.
+template <bool A_MN, bool RED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_constant__ CUtensorMap bmap,
                        const __grid_constant__ CUtensorMap cmap, const GemmParams p)
@@ -129,6 +128,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
     fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
     const int per_rank = p.num_m * p.num_n;
+    // unit u -> split ks (fastest), then row block, column block, rank
     const uint32_t b_bytes = (uint32_t)p.BN * BK * 2;
 
     if (warp == 0) {
@@ -136,10 +136,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             int stage = 0;
             uint32_t ph = 0;
             for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-                const int r = u / per_rank, rem = u - r * per_rank;
+                const int ks = u % p.ksplit, v = u / p.ksplit;
+                const int r = v / per_rank, rem = v - r * per_rank;
                 const int mb = rem % p.num_m, nb = rem / p.num_m;
                 const int m0 = mb * BM, n0 = nb * p.BN;
-                for (int kb = 0; kb < p.nkb; ++kb) {
+                const int kb_lo = ks * p.kbps, kb_hi = min(p.nkb, kb_lo + p.kbps);
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, WAIT_LIMIT_NS)) {
                         fail(abort);
                         goto done;
@@ -166,6 +168,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             int stage = 0;
             uint32_t ph = 0, au = 0;
             for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+                const int ks = u % p.ksplit;
+                const int kb_lo = ks * p.kbps, kb_hi = min(p.nkb, kb_lo + p.kbps);
                 const uint32_t b = au & 1u;
                 if (!mbar_wait(smem_u32(&ctl->acc_empty[b]), ((au >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
                     fail(abort);
@@ -173,7 +177,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                 }
                 fence_after_sync();
                 const uint32_t d = tmem + b * (uint32_t)p.BN;
-                for (int kb = 0; kb < p.nkb; ++kb) {
+                for (int kb = kb_lo; kb < kb_hi; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->full[stage]), ph, abort, WAIT_LIMIT_NS)) {
                         fail(abort);
                         goto done;
@@ -186,7 +190,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                         const uint64_t ad = A_MN ? desc_sw128(a0 + 2048u * k, 8192u, 1024u)
                                                  : desc_kmajor_sw128(a0 + 32u * k);
                         const uint64_t bd = desc_sw128(b0 + 2048u * k, 8192u, 1024u);
-                        mma_f16(d, ad, bd, p.idesc, (kb == 0 && k == 0) ? 0u : 1u);
+                        mma_f16(d, ad, bd, p.idesc, (kb == kb_lo && k == 0) ? 0u : 1u);
                     }
                     mma_commit(smem_u32(&ctl->empty[stage]));
                     if (++stage == STAGES) { stage = 0; ph ^= 1u; }
@@ -201,7 +205,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
         uint32_t au = 0;
         int sbuf = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const int r = u / per_rank, rem = u - r * per_rank;
+            const int v = u / p.ksplit;
+            const int r = v / per_rank, rem = v - r * per_rank;
             const int mb = rem % p.num_m, nb = rem / p.num_m;
             const int64_t n0 = (int64_t)nb * p.BN;
             const uint32_t b = au & 1u;
@@ -216,8 +221,33 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             // 32 rows x 64 columns per bulk store; the output map (column within
             // shard, shard, row) clips columns past k_t and rows past M
             const int y = mb * BM + 32 * q;
+            if (RED) {
+                // fp32 partial: 32 rows x 32 columns (128-byte rows) per reduce-add
 #pragma unroll 1
-            for (int c64 = 0; c64 < p.BN / 64; ++c64) {
+                for (int c32 = 0; c32 < p.BN / 32; ++c32) {
+                    const int64_t c0 = n0 + 32 * c32;
+                    if (c0 >= p.Nn) break;
+                    uint32_t vv[32];
+                    tmem_ld32(tb + 32u * c32, vv);
+                    uint8_t *stg = staging + (q * NBUF + sbuf) * STG_BYTES;
+                    const uint32_t stg_a = smem_u32(stg);
+                    if (++sbuf == NBUF) sbuf = 0;
+                    if (lane == 0) bulk_wait_read1();
+                    __syncwarp();
+                    uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        rowp[j ^ (lane & 7)] = make_uint4(vv[4 * j], vv[4 * j + 1], vv[4 * j + 2], vv[4 * j + 3]);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && y < p.M) {
+                        tma_reduce_add_3d(&cmap, stg_a, (int)c0, r, y);
+                        bulk_commit();
+                    }
+                }
+            }
+#pragma unroll 1
+            for (int c64 = 0; c64 < p.BN / 64 && !RED; ++c64) {
                 const int64_t c0 = n0 + 64 * c64;
                 if (c0 >= p.Nn) break;
                 uint32_t v0[32], v1[32];
@@ -277,18 +307,52 @@ int pick_bn(int64_t n)
     return (int)((per + 63) / 64 * 64);
 }
 
-template <bool A_MN>
+template <bool A_MN, bool RED>
 caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &bmap, const CUtensorMap &cmap,
                            GemmParams &p, cudaStream_t s, const char *name)
 {
     if (p.units <= 0) return CAAT_OK;
     const int grid = p.units < num_sms() ? p.units : num_sms();
-    if (cudaFuncSetAttribute(grouped_gemm_tc_kernel<A_MN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_BYTES) != cudaSuccess)
+    auto kern = grouped_gemm_tc_kernel<A_MN, RED>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
         return CAAT_ERR_CUDA;
-    grouped_gemm_tc_kernel<A_MN><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, bmap, cmap, p);
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, bmap, cmap, p);
     note_launch(name);
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
+}
+
+// fp32 [rows, cols] (row stride lds) -> bf16 (row stride ldd), 8 columns per thread
+__global__ void __launch_bounds__(256)
+f32_rows_to_bf16_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t lds,
+                        uint16_t *__restrict__ dst, int64_t ldd)
+{
+    const int64_t per_row = cols / 8;
+    const int64_t total = rows * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t rr = i / per_row, c = (i - rr * per_row) * 8;
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + rr * lds + c));
+        const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + rr * lds + c + 4));
+        const uint4 w = make_uint4(pack_bf16x2(__float_as_uint(a.x), __float_as_uint(a.y)),
+                                   pack_bf16x2(__float_as_uint(a.z), __float_as_uint(a.w)),
+                                   pack_bf16x2(__float_as_uint(b.x), __float_as_uint(b.y)),
+                                   pack_bf16x2(__float_as_uint(b.z), __float_as_uint(b.w)));
+        *reinterpret_cast<uint4 *>(dst + rr * ldd + c) = w;
+    }
+}
+
+// split of the K range that minimises waves-of-work per split, at least 8
+// k-blocks per part
+int pick_ksplit(int units, int nkb)
+{
+    const int sms = num_sms();
+    int best = 1;
+    double best_cost = (double)((units + sms - 1) / sms);
+    for (int k = 2; k <= 8 && nkb / k >= 8; ++k) {
+        const double cost = (double)((units * k + sms - 1) / sms) / k;
+        if (cost < best_cost - 1e-9) { best = k; best_cost = cost; }
+    }
+    return best;
 }
 
 }  // namespace
@@ -311,7 +375,8 @@ bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int
 // W and dW are in the nn.Linear layout ([h, K] storage, row stride ldw / ld_dw).
 caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
-                                 void *dX, int64_t lddx, void *dW, int64_t ld_dw, cudaStream_t s)
+                                 void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
+                                 cudaStream_t s)
 {
     const int64_t kt = K / t;
     const int BN = pick_bn(kt);
@@ -331,14 +396,14 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint32_t box[3] = {64, 1, 64};
         if (!encode_tmap(&bm, W, 3, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
         GemmParams p{};
-        for (int r = 0; r < t; ++r) p.C.p[r] = (uint16_t *)dX + r * kt;
-        p.ldc = lddx;
         p.M = N; p.Nn = kt; p.Kk = h;
         p.t = t;
         p.num_m = (int)((N + BM - 1) / BM);
         p.num_n = (int)((kt + BN - 1) / BN);
         p.nkb = (int)((h + BK - 1) / BK);
         p.BN = BN;
+        p.ksplit = 1;
+        p.kbps = p.nkb;
         p.units = t * p.num_m * p.num_n;
         p.idesc = idesc_bf16_f32(BM, BN, false, true);
         CUtensorMap cm;
@@ -346,7 +411,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)lddx * 2};
         const uint32_t cbox[3] = {64, 1, 32};
         if (!encode_tmap(&cm, dX, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
-        const caat_status st = launch_grouped<false>(am, bm, cm, p, s, "rowpar_bwd_dx_tc");
+        const caat_status st = launch_grouped<false, false>(am, bm, cm, p, s, "rowpar_bwd_dx_tc");
         if (st != CAAT_OK) return st;
     }
     // ---- dW^T = dY_r^T X_r: A = dY_r^T (MN-major), B = X_r (MN-major)
@@ -364,22 +429,42 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint32_t box[3] = {64, 1, 64};
         if (!encode_tmap(&bm, X, 3, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
         GemmParams p{};
-        for (int r = 0; r < t; ++r) p.C.p[r] = (uint16_t *)dW + r * kt;
-        p.ldc = ld_dw;
         p.M = h; p.Nn = kt; p.Kk = N;
         p.t = t;
         p.num_m = (int)((h + BM - 1) / BM);
         p.num_n = (int)((kt + BN - 1) / BN);
         p.nkb = (int)((N + BK - 1) / BK);
         p.BN = BN;
-        p.units = t * p.num_m * p.num_n;
         p.idesc = idesc_bf16_f32(BM, BN, true, true);
+        const int base_units = t * p.num_m * p.num_n;
+        p.ksplit = wacc != nullptr ? pick_ksplit(base_units, p.nkb) : 1;
+        p.kbps = (p.nkb + p.ksplit - 1) / p.ksplit;
+        p.ksplit = (p.nkb + p.kbps - 1) / p.kbps;
+        p.units = base_units * p.ksplit;
+        if (p.ksplit == 1) {
+            CUtensorMap cm;
+            const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
+            const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)ld_dw * 2};
+            const uint32_t cbox[3] = {64, 1, 32};
+            if (!encode_tmap(&cm, dW, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
+            return launch_grouped<true, false>(am, bm, cm, p, s, "rowpar_bwd_dw_tc");
+        }
+        // split over tokens: fp32 partials reduce-added into wacc [h, K], then one
+        // rounding to bf16 into dW
         CUtensorMap cm;
         const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
-        const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)ld_dw * 2};
-        const uint32_t cbox[3] = {64, 1, 32};
-        if (!encode_tmap(&cm, dW, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
-        return launch_grouped<true>(am, bm, cm, p, s, "rowpar_bwd_dw_tc");
+        const uint64_t cstr[2] = {(uint64_t)kt * 4, (uint64_t)K * 4};
+        const uint32_t cbox[3] = {32, 1, 32};
+        if (!encode_tmap(&cm, wacc, 3, cdims, cstr, cbox, true)) return CAAT_ERR_UNSUPPORTED;
+        if (cudaMemsetAsync(wacc, 0, (size_t)h * (size_t)K * 4, s) != cudaSuccess) return CAAT_ERR_CUDA;
+        caat_status st = launch_grouped<true, true>(am, bm, cm, p, s, "rowpar_bwd_dw_tc");
+        if (st != CAAT_OK) return st;
+        const int64_t total = h * (K / 8);
+        int64_t blocks = (total + 255) / 256;
+        if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
+        f32_rows_to_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(wacc, h, K, K, (uint16_t *)dW, ld_dw);
+        note_launch("rowpar_bwd_dw_tc", 1);
+        return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
     }
 }
 

@@ -50,18 +50,25 @@ extern "C" caat_status caat_rowpar_linear_bwd_noalloc(
         const double bytes = (double)t * (double)N * (double)h * (dt == CAAT_BF16 ? 2.0 : 4.0);
         if (bytes > (double)CAAT_NOALLOC_SCRATCH_BYTES) return CAAT_ERR_INVALID_ARG;
     }
-    const size_t need = caat_rowpar_linear_bwd_workspace(t, N, h, dt, mode);
+    // the part of the workspace the backward cannot do without: the reduced
+    // gradient, t buffers of [N, h] rounded up to 256 bytes each
+    size_t need = 0;
+    if (t >= 1 && N > 0 && h > 0 && mode == CAAT_BWD_REDUCE_DOUT)
+        need = (size_t)t * (((size_t)N * (size_t)h * (dt == CAAT_BF16 ? 2u : 4u) + 255) / 256 * 256);
     if (need > (size_t)CAAT_NOALLOC_SCRATCH_BYTES) return CAAT_ERR_INVALID_ARG;
     void *ws = nullptr;
     size_t ws_bytes = 0;
-    const bool uses_scratch = need > 0 && n_sel > 0 && t > 1 && mode == CAAT_BWD_REDUCE_DOUT;
+    // the scratch also serves, when it is large enough, as the optional fp32
+    // accumulator of the token-split dW reduction, so offer it for any size
+    const bool uses_scratch = t >= 1 && N > 0 && h > 0 && K > 0;
     if (uses_scratch) {
         const caat_status st = scratch_address(&ws);
         if (st != CAAT_OK) return st;
         ws_bytes = (size_t)CAAT_NOALLOC_SCRATCH_BYTES;
     }
     // the reduced gradient fills the whole [t, N, h] region it uses before it is
-    // read, so nothing left over from an earlier call can leak into this one
+    // read, and the dW accumulator is cleared on the stream before use, so
+    // nothing left over from an earlier call can leak into this one
     return caat_rowpar_linear_bwd(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, dOut, ld_dout, dX, lddx,
                                   dW, dw_rs, dw_cs, sel, n_sel, mode, ws, ws_bytes, stream);
 }

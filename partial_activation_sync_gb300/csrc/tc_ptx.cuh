@@ -99,6 +99,16 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, uint32_t src, int
         : "memory");
 }
 
+// shared -> global tiled reduction: global += shared (element type of the map)
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, uint32_t src, int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            tmap),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // wait until every committed bulk store has finished reading shared memory

@@ -112,9 +112,12 @@ def test_layer_rejects_bad_args_without_launch(lib):
     # n_sel > h
     assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, sel, 9, None) == 1
     g = lib.caat_rowpar_linear_bwd
-    ws = lib.caat_rowpar_linear_bwd_workspace(2, 4, 8, 1, 0)
-    assert ws == 2 * 256                       # two [4, 8] bf16 buffers, 256-byte rounded
-    assert lib.caat_rowpar_linear_bwd_workspace(2, 4, 8, 1, 1) == 0
+    f_ws = lib.caat_rowpar_linear_bwd_workspace
+    # two [4, 8] bf16 buffers (256-byte rounded) + fp32 dW accumulator [8, 8] (256 bytes)
+    assert f_ws(2, 4, 8, 8, 1, 0) == 2 * 256 + 256
+    assert f_ws(2, 4, 8, 8, 1, 1) == 256            # no reduced gradient without the reduce
+    assert f_ws(2, 4, 8, 8, 0, 0) == 2 * 256        # fp32: no accumulator
+    assert f_ws(2, 4, 8, 8, 0, 1) == 0
     # workspace missing for the reduce-dOut mode
     assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, 6 << 20, 8, 7 << 20, 1, 8,
              sel, 2, 0, None, 0, None) == 1

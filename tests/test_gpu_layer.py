@@ -260,3 +260,29 @@ def test_bwd_full_size_sampled(caat, wname, li, mode):
     S_sub = np.nonzero(inS)[0].astype(np.int32)
     _, wW = orc.rowpar_bwd(Xv, Wv[:, cols], Gv[:, :, cols], w.t, S_sub, mode)
     assert rel_fro(to_f64(dW[:, cols.tolist()]), wW) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_bwd_tc_required_workspace_only(caat, mode):
+    """A workspace with only the reduced-gradient region (no fp32 dW accumulator)
+    takes the path without the token split; both paths match the oracle."""
+    T = torch()
+    t, N, kt, h = 8, 1024, 96, 768
+    X = ci.normal(1201, (N, kt * t))
+    Wl = ci.normal(1202, (kt * t, h), std=0.02)
+    G = ci.normal(1203, (t, N, h))
+    S = caat.select_channels(h, 0.5, 1, 9)
+    Xd, Wd = dev(X, "bf16"), _weight(Wl, "bf16", "nn")
+    Gd = [dev(G[r], "bf16") for r in range(t)]
+    wX, wW = orc.rowpar_bwd(host_values(X, "bf16"), host_values(Wl, "bf16"),
+                            np.stack([host_values(G[r], "bf16") for r in range(t)]), t, S, mode)
+    need = t * ((N * h * 2 + 255) // 256 * 256) if mode == 0 else 0
+    full = caat.rowpar_linear_bwd_workspace(t, N, kt * t, h, 1, mode)
+    assert full == need + (kt * t * h * 4 + 255) // 256 * 256
+    for ws_bytes in (need, full):
+        ws = T.empty(max(ws_bytes, 256), dtype=T.uint8, device="cuda") if ws_bytes else None
+        dX, dW = caat.rowpar_linear_bwd(Xd, Wd, Gd, t, sel_dev(S), mode, workspace=ws)
+        T.cuda.synchronize()
+        assert caat.device_status() == 0
+        assert rel_fro(to_f64(dX), wX) <= TOL["bf16"], ws_bytes
+        assert rel_fro(to_f64(dW), wW) <= TOL["bf16"], ws_bytes
