@@ -156,8 +156,14 @@ def run_gpu(args, w):
     layers = [LayerData(torch, w, i, device) for i in range(len(w.layers))]
     ws_bytes = max(max(caat.rowpar_linear_bwd_workspace(w.t, w.N, L.K, w.h, 1, 0) for L in w.layers), 256)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream()
+
+    def flush_l2():
+        # read a buffer twice the L2 size: evicts the previous step's data and
+        # leaves clean lines (a write-flush would leave 129 MB of dirty lines whose
+        # write-back then competes with the next kernel's writes)
+        return flush.sum()
 
     def step(evs=None):
         k = 0
@@ -176,7 +182,7 @@ def run_gpu(args, w):
     n_calls = len(layers) * (2 if w.backward else 1)
     for _ in range(args.warmup):
         step()
-        flush.fill_(1.0)
+        flush_l2()
     torch.cuda.synchronize()
     assert caat.device_status() == 0
 
@@ -192,7 +198,7 @@ def run_gpu(args, w):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 1)]
         step(evs)
         all_evs.append(evs)
-        flush.fill_(float(len(all_evs)))      # L2 flush between timed steps (not timed)
+        flush_l2()                            # L2 flush between timed steps (not timed)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -249,7 +255,7 @@ def run_gpu(args, w):
                    "layers": {L.name: L.K for L in layers}, "p": w.p,
                    "S": "contiguous" if w.layout == 0 else "random",
                    "fwd_and_bwd": bool(w.backward),
-                   "l2": "flushed between timed steps (2x L2 write, untimed)",
+                   "l2": "flushed between timed steps by reading a 2x L2 buffer (untimed)",
                    "parallelism": "replicas" if world > 1 else "1 GPU, t ranks emulated"},
         "breakdown_ms": breakdown,
         "gpu_launches": int(launches),
@@ -329,7 +335,7 @@ def _time_call(torch, fn, reps, flush=None):
     ts = []
     for _ in range(reps):
         if flush is not None:
-            flush.fill_(0.5)
+            flush.sum()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -345,7 +351,7 @@ def run_extras(torch, caat, device, peaks):
     fused forward at Llama2-7B prefill shapes (tensor-bound) and the standalone
     reduce on a working set far above L2 (HBM-bound)."""
     out = {}
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     # standalone PCR, bf16 and fp32, t=8, [4096, 4096], p=0.5, out of place
     for dt_name, dt, es in (("bf16", torch.bfloat16, 2), ("f32", torch.float32, 4)):
         t, N, h = 8, 4096, 4096
@@ -386,6 +392,22 @@ def run_extras(torch, caat, device, peaks):
             "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4),
             "us": round(sec * 1e6, 1), "kernel": caat.last_kernel()}
         del X, Wst, Ys
+    # 7B decode: N in {1, 8, 64} tokens, p = 0.5 -- weight streaming (HBM bound)
+    for li, L in enumerate(w.layers):
+        Wst = (torch.randn((w.h, L.K), device=device) * 0.02).to(torch.bfloat16)
+        for Nd in w.decode_N:
+            X = torch.randn((Nd, L.K), device=device).to(torch.bfloat16)
+            Ys = [torch.empty((Nd, w.h), dtype=torch.bfloat16, device=device) for _ in range(w.t)]
+            fn = lambda: caat.rowpar_linear_fwd(X, Wst.t(), w.t, sel, outs=Ys)  # noqa: E731
+            fn()
+            sec = _time_call(torch, fn, 10, flush)
+            byt = 2.0 * (L.K * w.h + Nd * L.K + w.t * Nd * w.h)
+            out["7b_decode_N%d_%s" % (Nd, L.name)] = {
+                "GB/s": round(byt / sec / 1e9, 1), "frac_hbm": round(byt / sec / 1e9 / peaks["hbm"], 4),
+                "us": round(sec * 1e6, 1), "TFLOP/s": round(2.0 * Nd * L.K * w.h / sec / 1e12, 2),
+                "kernel": caat.last_kernel()}
+            del X, Ys
+        del Wst
     torch.cuda.synchronize()
     return out
 

@@ -164,7 +164,15 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
     if (N == 0 || h == 0) return CAAT_OK;
     const cudaStream_t s = (cudaStream_t)stream;
     if (dt == CAAT_BF16 && w_rs == 1 && K > 0) {
+        // a few tokens: weight streaming on the CUDA cores; otherwise the
+        // tensor-core kernel (decode kernel again if that one declines)
+        if (N < 16) {
+            st = launch_rowpar_fwd_decode(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
+            if (st != CAAT_ERR_UNSUPPORTED) return st;
+        }
         st = launch_rowpar_fwd_tc(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
+        if (st != CAAT_ERR_UNSUPPORTED) return st;
+        st = launch_rowpar_fwd_decode(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
         if (st != CAAT_ERR_UNSUPPORTED) return st;
     }
     return launch_rowpar_fwd_simt(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, py, ldy, sel, n_sel, s);

@@ -56,6 +56,12 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h,
                                  const MutPtrs &Y, int64_t ldy,
                                  const int32_t *sel, int64_t n_sel, cudaStream_t s);
 
+// ---- few-token (decode) forward on the CUDA cores (decode.cu): 1 <= N <= 64,
+// t in {1, 2, 4, 8, 16, 32}, bf16, W in the nn.Linear layout (row stride ldw).
+caat_status launch_rowpar_fwd_decode(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
+                                     const void *W, int64_t ldw, const MutPtrs &Y, int64_t ldy,
+                                     const int32_t *sel, int64_t n_sel, cudaStream_t s);
+
 // Tensor map for TMA (gemm_tc.cu): 128-byte swizzle, zero fill out of bounds;
 // bf16 elements unless f32.
 bool encode_tmap(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,

@@ -624,7 +624,7 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     const int64_t kt = K / t;
     // shapes and alignments this kernel takes; anything else goes to another kernel
     if (kt < BK || kt % 8 != 0 || ldx % 8 != 0 || ldw % 8 != 0 || ldy % 8 != 0) return CAAT_ERR_UNSUPPORTED;
-    if (h % 8 != 0 || h < BN || h > MAX_H_TC || N < BM || N > (int64_t)INT32_MAX) return CAAT_ERR_UNSUPPORTED;
+    if (h % 8 != 0 || h < BN || h > MAX_H_TC || N < 16 || N > (int64_t)INT32_MAX) return CAAT_ERR_UNSUPPORTED;
     if (t > MAX_T_TC) return CAAT_ERR_UNSUPPORTED;
     if ((uintptr_t)X % 16 != 0 || (uintptr_t)W % 16 != 0) return CAAT_ERR_UNSUPPORTED;
     for (int r = 0; r < t; ++r)

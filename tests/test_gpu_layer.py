@@ -286,3 +286,30 @@ def test_bwd_tc_required_workspace_only(caat, mode):
         assert caat.device_status() == 0
         assert rel_fro(to_f64(dX), wX) <= TOL["bf16"], ws_bytes
         assert rel_fro(to_f64(dW), wW) <= TOL["bf16"], ws_bytes
+
+
+@pytest.mark.parametrize("t", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("N", [1, 3, 8, 9, 15])
+def test_fwd_decode_parity(caat, t, N):
+    """Few tokens: the weight-streaming decode kernel (CUDA cores)."""
+    h = 1000 if t != 16 else 520
+    kt = 96 if t <= 8 else 64
+    for p in (0.0, 0.5, 1.0):
+        for layout in (0, 1):
+            got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=11 * t + N)
+            assert caat.last_kernel() == "rowpar_fwd_decode"
+            for r in range(t):
+                assert rel_fro(got[r], want[r]) <= TOL["bf16"], (r, p, layout)
+            for r in range(1, t):
+                assert np.array_equal(got[r][:, S], got[0][:, S])
+
+
+@pytest.mark.parametrize("N", [16, 64, 100])
+def test_fwd_small_n_tensor_core(caat, N):
+    """16 <= N < 128: the tensor-core kernel with a partly empty 128-row tile."""
+    t, kt, h = 8, 128, 512
+    for layout in (0, 1):
+        got, want, S = _fwd_case(caat, t, N, kt * t, h, 0.5, layout, "bf16", "nn", seed=N)
+        assert caat.last_kernel() in ("rowpar_fwd_tc", "rowpar_fwd_decode")
+        for r in range(t):
+            assert rel_fro(got[r], want[r]) <= TOL["bf16"], (r, layout)
