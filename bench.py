@@ -9,7 +9,7 @@ forward (GEMM + partial channel-reduce into t rank outputs) and the backward
 (2NKh forward + 4NKh backward per layer, independent of p).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl caat|reference]
-                  [--workload 130m|1.1b|7b_prefill] [--no-extras]
+                  [--workload 130m|1.1b|7b_prefill|7b_decode8] [--no-extras]
 
 Under torchrun each rank runs its own replica on its own GPU (no collective on
 the data path; weak scaling); rank 0 prints one JSON line.  ``--impl reference``
@@ -500,7 +500,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["caat", "reference"], default="caat")
-    ap.add_argument("--workload", default="130m", choices=["130m", "1.1b", "7b_prefill"])
+    ap.add_argument("--workload", default="130m", choices=["130m", "1.1b", "7b_prefill", "7b_decode8"])
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

@@ -77,6 +77,10 @@ WORKLOADS = {
     "7b_prefill": Workload("7b_prefill", 4, t=8, N=4096, h=4096,
                            layers=[Layer("out_proj", 4096), Layer("down_proj", 11008)],
                            backward=False, decode_N=(1, 8, 64)),
+    # Llama2-7B decode step with 8 tokens in flight (weight streaming), fwd only
+    "7b_decode8": Workload("7b_decode8", 4, t=8, N=8, h=4096,
+                           layers=[Layer("out_proj", 4096), Layer("down_proj", 11008)],
+                           backward=False),
 }
 
 

@@ -44,16 +44,6 @@ __device__ __forceinline__ void widen8(uint4 v, float (&f)[8])
     }
 }
 
-__device__ __forceinline__ bool in_sorted(const int32_t *sel, int64_t n, int64_t c)
-{
-    int64_t lo = 0, hi = n;
-    while (lo < hi) {
-        const int64_t mid = (lo + hi) >> 1;
-        if (sel[mid] < c) lo = mid + 1; else hi = mid;
-    }
-    return lo < n && sel[lo] == c;
-}
-
 // NT token rows per pass (rows >= N read as zero and are not written), TT ranks.
 template <int NT, int TT>
 __global__ void __launch_bounds__(WARPS * 32)
@@ -62,11 +52,23 @@ rowpar_fwd_decode_kernel(const uint16_t *__restrict__ X, int64_t ldx, const uint
                          const int32_t *__restrict__ sel, int64_t n_sel)
 {
     constexpr int G = 32 / TT;                       // lanes per shard group
+    constexpr int CPB = WARPS * CPW;                 // channels per block (32)
+    __shared__ uint32_t smask;                       // bit i: channel cb + i is in S
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int r = lane / G, gl = lane % G;
     const int64_t kt = K / TT;
-    const int64_t c0 = ((int64_t)blockIdx.x * WARPS + warp) * CPW;
+    const int64_t cb = (int64_t)blockIdx.x * CPB;
+    const int64_t c0 = cb + (int64_t)warp * CPW;
     const int64_t row0 = (int64_t)blockIdx.y * NT;
+
+    // membership of this block's channels: every thread scans a slice of S
+    if (threadIdx.x == 0) smask = 0u;
+    __syncthreads();
+    for (int64_t i = threadIdx.x; i < n_sel; i += WARPS * 32) {
+        const int64_t c = sel[i];
+        if (c >= cb && c < cb + CPB) atomicOr(&smask, 1u << (uint32_t)(c - cb));
+    }
+    __syncthreads();
     if (c0 >= h) return;                             // whole warp
 
     float acc[CPW][NT];
@@ -79,6 +81,9 @@ rowpar_fwd_decode_kernel(const uint16_t *__restrict__ X, int64_t ldx, const uint
     const uint16_t *wrow[CPW];
 #pragma unroll
     for (int c = 0; c < CPW; ++c) wrow[c] = W + (c0 + c < h ? c0 + c : c0) * ldw;
+    const uint16_t *xrow[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) xrow[n] = X + (row0 + n < N ? row0 + n : row0) * ldx;
 
     for (int64_t kb = kbeg + (int64_t)gl * 8; kb < kend; kb += (int64_t)G * 8 * U) {
         uint4 wv[U][CPW];
@@ -92,18 +97,22 @@ rowpar_fwd_decode_kernel(const uint16_t *__restrict__ X, int64_t ldx, const uint
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t k = kb + (int64_t)u * G * 8;
-            if (k >= kend) break;
+            if (k < kend) {
+                float xf[NT][8];
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                if (row0 + n >= N) break;
-                float xf[8];
-                widen8(__ldg(reinterpret_cast<const uint4 *>(X + (row0 + n) * ldx + k)), xf);
+                for (int n = 0; n < NT; ++n) {
+                    const uint4 xv = row0 + n < N ? __ldg(reinterpret_cast<const uint4 *>(xrow[n] + k))
+                                                  : make_uint4(0, 0, 0, 0);
+                    widen8(xv, xf[n]);
+                }
 #pragma unroll
                 for (int c = 0; c < CPW; ++c) {
                     float wf[8];
                     widen8(wv[u][c], wf);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[c][n] = fmaf(wf[e], xf[e], acc[c][n]);
+                    for (int n = 0; n < NT; ++n)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[c][n] = fmaf(wf[e], xf[n][e], acc[c][n]);
                 }
             }
         }
@@ -131,11 +140,12 @@ rowpar_fwd_decode_kernel(const uint16_t *__restrict__ X, int64_t ldx, const uint
 
     if (gl == 0) {
         uint16_t *yr = (uint16_t *)Y.p[r];
+        const uint32_t m = smask >> (warp * CPW);
 #pragma unroll
         for (int c = 0; c < CPW; ++c) {
             const int64_t ch = c0 + c;
             if (ch >= h) break;
-            const bool s = in_sorted(sel, n_sel, ch);
+            const bool s = (m >> c) & 1u;
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 if (row0 + n >= N) break;
