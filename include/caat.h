@@ -95,8 +95,8 @@ caat_status caat_select_channels(int64_t h, double p, caat_layout layout, uint64
  * out:    host array of t device pointers, each [N, h] with row stride ld_out.
  *         out may equal in (in place: then only the channels of S are written).
  *         Otherwise the t outputs must not overlap any input.
- * sel:    device int32[n_sel], ascending, unique, each in [0, h)  (S).
- *         May be null when n_sel == 0.
+ * sel:    device int32[n_sel], ascending, unique, each in [0, h)  (S);
+ *         or null, which means the contiguous S = {0, ..., n_sel-1}.
  * Errors: INVALID_ARG for t out of range, negative sizes, ld < h, null pointers,
  *         or in/out arrays that are in place for some ranks and not for others.
  *         Unsorted or out-of-range entries of sel are not checked on the device;
@@ -123,7 +123,10 @@ caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, caat_dtype 
  *      the layout the tensor-core path takes; (h, 1) is a row-major [K, h].
  * Y:   host array of t device pointers, each [N, h] with row stride ldy; they
  *      must not overlap each other or X, W.
- * sel: device int32[n_sel], ascending and unique (S); may be null if n_sel == 0.
+ * sel: device int32[n_sel], ascending and unique (S); or null for the contiguous
+ *      S = {0, ..., n_sel-1}.  With the contiguous form and n_sel a multiple of 64,
+ *      the backward reduces only the S channels, once, instead of materialising
+ *      every rank's reduced gradient.
  * Precision: bf16 in, fp32 accumulate, one rounding to bf16; or fp32 throughout
  * (fp32 FMA, no TF32).
  * Errors: INVALID_ARG for t outside 1..64, K % t != 0, negative sizes, a stride

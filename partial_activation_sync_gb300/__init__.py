@@ -67,8 +67,14 @@ def _rowmajor(t, name):
 
 
 def _sel_ptr(sel):
+    """S as a device index tensor, or an int n for the contiguous S = {0, ..., n-1}
+    (passed to the library as a null pointer), or None for the empty set."""
     if sel is None:
         return None, 0
+    if isinstance(sel, (int, np.integer)):
+        if sel < 0:
+            raise ValueError("caat: contiguous S size must be >= 0")
+        return None, int(sel)
     if not sel.is_cuda or sel.dtype != _torch().int32 or sel.dim() != 1 or not sel.is_contiguous():
         raise ValueError("caat: sel must be a contiguous 1-D int32 CUDA tensor")
     return ctypes.c_void_p(sel.data_ptr() if sel.numel() else 0), sel.numel()

@@ -89,7 +89,6 @@ extern "C" caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, 
     if (t < 1 || t > CAAT_MAX_T || N < 0 || h < 0 || !valid_dtype(dt)) return CAAT_ERR_INVALID_ARG;
     if (in == nullptr || out == nullptr) return CAAT_ERR_INVALID_ARG;
     if (ld_in < h || ld_out < h || n_sel < 0 || n_sel > h) return CAAT_ERR_INVALID_ARG;
-    if (n_sel > 0 && sel == nullptr) return CAAT_ERR_INVALID_ARG;
     const int64_t es = elem_size(dt);
     ConstPtrs pin{};
     MutPtrs pout{};
@@ -124,7 +123,6 @@ caat_status check_layer_args(int t, int64_t N, int64_t K, int64_t h, caat_dtype 
         return CAAT_ERR_INVALID_ARG;
     if (K % t != 0) return CAAT_ERR_INVALID_ARG;
     if (ldx < K || n_sel < 0 || n_sel > h) return CAAT_ERR_INVALID_ARG;
-    if (n_sel > 0 && sel == nullptr) return CAAT_ERR_INVALID_ARG;
     if (N > 0 && K > 0 && X == nullptr) return CAAT_ERR_INVALID_ARG;
     if (K > 0 && h > 0) {
         if (W == nullptr || w_rs < 1 || w_cs < 1) return CAAT_ERR_INVALID_ARG;
@@ -245,6 +243,24 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
     const int64_t kt = K / t;
     ConstPtrs dy{};
     int64_t ld_dy = ld_dout;
+
+    // Contiguous S (sel == null) on the tensor-core path: reduce only the S
+    // channels, once, into [N, s]; the GEMMs read them from there and the other
+    // channels straight from each rank's dOut (no t-fold copy of the gradient).
+    if (reduce && sel == nullptr && n_sel % 64 == 0 && dt == CAAT_BF16 && w_rs == 1 && dw_rs == 1 &&
+        N > 0 && h > 0 && K > 0) {
+        ConstPtrs src{};
+        for (int r = 0; r < t; ++r) src.p[r] = dOut[r];
+        if (bwd_tc_supported(t, N, K, h, X, ldx, W, w_cs, src, ld_dout, dX, lddx, dW, dw_cs) &&
+            ((uintptr_t)workspace & 255) == 0) {
+            st = launch_pcr_colsum(t, N, n_sel, src, ld_dout, workspace, n_sel, s);
+            if (st == CAAT_OK)
+                st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, src, ld_dout, dX, lddx, dW, dw_cs,
+                                          wacc, n_sel, workspace, n_sel, s);
+            if (st != CAAT_ERR_UNSUPPORTED) return st;
+        }
+    }
+
     if (reduce) {
         const size_t per = need / (size_t)t;
         ConstPtrs src{};
@@ -264,7 +280,8 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
 
     if (dt == CAAT_BF16 && w_rs == 1 && dw_rs == 1 && N > 0 && h > 0 &&
         bwd_tc_supported(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs)) {
-        st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs, wacc, s);
+        st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs, wacc, 0,
+                                  nullptr, 0, s);
         if (st != CAAT_ERR_UNSUPPORTED) return st;
     }
 

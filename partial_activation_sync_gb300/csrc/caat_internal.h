@@ -29,6 +29,11 @@ caat_status launch_pcr(int t, int64_t N, int64_t h, caat_dtype dt,
                        const ConstPtrs &in, int64_t ld_in, const MutPtrs &out, int64_t ld_out,
                        bool in_place, const int32_t *sel, int64_t n_sel, cudaStream_t s);
 
+// Sum over ranks of the first s channels only, into one bf16 [N, s] buffer
+// (contiguous S; the same fold and rounding as launch_pcr's S channels).
+caat_status launch_pcr_colsum(int t, int64_t N, int64_t s, const ConstPtrs &in, int64_t ld_in, void *out,
+                              int64_t ld_out, cudaStream_t st);
+
 // ---- SIMT (CUDA-core) GEMM paths (gemm_simt.cu)
 // Row-parallel forward with the PCR epilogue, any strides, f32 or bf16.
 caat_status launch_rowpar_fwd_simt(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
@@ -73,10 +78,12 @@ bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int
                       const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy, const void *dX,
                       int64_t lddx, const void *dW, int64_t ld_dw);
 // wacc: fp32 scratch of h * K floats for a split reduction over tokens in dW
-// (null: no split).
+// (null: no split).  s_sum > 0: channels [0, s_sum) of every rank's gradient
+// are read from the one reduced buffer dsum [N, s_sum] (row stride ld_dsum) and
+// channels [s_sum, h) from dY_r; s_sum must be a multiple of 64.
 caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
                                  void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
-                                 cudaStream_t s);
+                                 int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s);
 
 }  // namespace caat

@@ -64,9 +64,14 @@ rowpar_fwd_decode_kernel(const uint16_t *__restrict__ X, int64_t ldx, const uint
     // membership of this block's channels: every thread scans a slice of S
     if (threadIdx.x == 0) smask = 0u;
     __syncthreads();
-    for (int64_t i = threadIdx.x; i < n_sel; i += WARPS * 32) {
-        const int64_t c = sel[i];
-        if (c >= cb && c < cb + CPB) atomicOr(&smask, 1u << (uint32_t)(c - cb));
+    if (sel == nullptr) {                            // S = {0, ..., n_sel-1}
+        if (threadIdx.x == 0)
+            smask = n_sel >= cb + CPB ? 0xffffffffu : (n_sel <= cb ? 0u : ((1u << (uint32_t)(n_sel - cb)) - 1u));
+    } else {
+        for (int64_t i = threadIdx.x; i < n_sel; i += WARPS * 32) {
+            const int64_t c = sel[i];
+            if (c >= cb && c < cb + CPB) atomicOr(&smask, 1u << (uint32_t)(c - cb));
+        }
     }
     __syncthreads();
     if (c0 >= h) return;                             // whole warp

@@ -80,9 +80,10 @@ __device__ __forceinline__ void mma_tile(const float (*As)[BM + 4], const float 
     }
 }
 
-// is channel c in the sorted list sel[0..n)?
+// is channel c in the sorted list sel[0..n)?  (sel == null: S = {0..n-1})
 __device__ __forceinline__ bool in_sorted(const int32_t *sel, int64_t n, int64_t c)
 {
+    if (sel == nullptr) return c < n;
     int64_t lo = 0, hi = n;
     while (lo < hi) {
         const int64_t mid = (lo + hi) >> 1;

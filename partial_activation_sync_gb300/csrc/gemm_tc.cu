@@ -240,9 +240,17 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     }
     if (PAIR) cluster_sync();        // the peer's barriers exist before anything signals them
     else __syncthreads();
-    for (int64_t i = tid; i < p.n_sel; i += NUM_THREADS) {
-        const int32_t c = p.sel[i];
-        if (c >= 0 && c < p.h) atomicOr(&ctl->bitmap[c >> 5], 1u << (c & 31));
+    if (p.sel == nullptr) {          // S = {0, ..., n_sel-1}
+        for (int64_t w = tid; w < words; w += NUM_THREADS) {
+            const int64_t lo = w * 32;
+            ctl->bitmap[w] = p.n_sel >= lo + 32 ? 0xffffffffu
+                           : (p.n_sel <= lo ? 0u : ((1u << (p.n_sel - lo)) - 1u));
+        }
+    } else {
+        for (int64_t i = tid; i < p.n_sel; i += NUM_THREADS) {
+            const int32_t c = p.sel[i];
+            if (c >= 0 && c < p.h) atomicOr(&ctl->bitmap[c >> 5], 1u << (c & 31));
+        }
     }
     if (warp == 1) {
         if (PAIR) {

@@ -74,6 +74,7 @@ constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * NBUF * S
 struct GemmParams {
     int64_t M, Nn, Kk;  // per-rank GEMM
     int t, num_m, num_n, nkb, BN, units;
+    int s_blocks;       // 64-channel blocks of the gradient read from the reduced sum (smap)
     int ksplit, kbps;   // K range split in ksplit parts of kbps k-blocks (RED only)
     uint32_t idesc;
 };
@@ -96,8 +97,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
 // otherwise the tile is rounded to bf16 and stored.
 template <bool A_MN, bool RED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_constant__ CUtensorMap bmap,
-                       const __grid_constant__ CUtensorMap cmap, const GemmParams p)
+grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_constant__ CUtensorMap smap,
+                       const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap cmap,
+                       const GemmParams p)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -151,11 +153,20 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     uint8_t *sa = base + stage * STAGE_BYTES;
                     uint8_t *sb = sa + A_BYTES;
                     const int k0 = kb * BK;
+                    // gradient channels below s_blocks*64 come from the reduced sum
+                    // (shared by all ranks), the rest from rank r's own gradient,
+                    // whose map starts at channel s_blocks*64
+                    const int sc = p.s_blocks * 64;
                     if (A_MN) {
-                        tma_load_2d(smem_u32(sa), &amaps.m[r], fb, m0, k0);
-                        tma_load_2d(smem_u32(sa + 8192), &amaps.m[r], fb, m0 + 64, k0);
+#pragma unroll
+                        for (int i = 0; i < 2; ++i) {
+                            const int c = m0 + 64 * i;
+                            if (c < sc) tma_load_2d(smem_u32(sa + 8192 * i), &smap, fb, c, k0);
+                            else tma_load_2d(smem_u32(sa + 8192 * i), &amaps.m[r], fb, c - sc, k0);
+                        }
                     } else {
-                        tma_load_2d(smem_u32(sa), &amaps.m[r], fb, k0, m0);
+                        if (k0 < sc) tma_load_2d(smem_u32(sa), &smap, fb, k0, m0);
+                        else tma_load_2d(smem_u32(sa), &amaps.m[r], fb, k0 - sc, m0);
                     }
                     for (int i = 0; i < p.BN / 64; ++i)
                         tma_load_3d(smem_u32(sb + i * 8192), &bmap, fb, n0 + 64 * i, r, k0);
@@ -308,15 +319,15 @@ int pick_bn(int64_t n)
 }
 
 template <bool A_MN, bool RED>
-caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &bmap, const CUtensorMap &cmap,
-                           GemmParams &p, cudaStream_t s, const char *name)
+caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &smap, const CUtensorMap &bmap,
+                           const CUtensorMap &cmap, GemmParams &p, cudaStream_t s, const char *name)
 {
     if (p.units <= 0) return CAAT_OK;
     const int grid = p.units < num_sms() ? p.units : num_sms();
     auto kern = grouped_gemm_tc_kernel<A_MN, RED>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
         return CAAT_ERR_CUDA;
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, bmap, cmap, p);
+    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, smap, bmap, cmap, p);
     note_launch(name);
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }
@@ -376,20 +387,35 @@ bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int
 caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
                                  void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
-                                 cudaStream_t s)
+                                 int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s)
 {
     const int64_t kt = K / t;
     const int BN = pick_bn(kt);
+    if (s_sum < 0 || s_sum > h || s_sum % 64 != 0 || (s_sum > 0 && dsum == nullptr)) return CAAT_ERR_UNSUPPORTED;
+    const int64_t h_own = h - s_sum;           // channels read from each rank's own gradient
+
+    // A-operand maps: rank r's gradient from channel s_sum on (each rank), and the
+    // reduced sum of channels [0, s_sum) (box shapes differ between dX and dW)
+    auto grad_maps = [&](TmapArray &am, CUtensorMap &sm, uint32_t box0, uint32_t box1) -> bool {
+        for (int r = 0; r < t; ++r) {
+            if (h_own == 0) { am.m[r] = CUtensorMap{}; continue; }
+            const uint64_t dims[2] = {(uint64_t)h_own, (uint64_t)N};
+            const uint64_t str[1] = {(uint64_t)ld_dy * 2};
+            const uint32_t box[2] = {box0, box1};
+            if (!encode_tmap(&am.m[r], (const uint16_t *)dY.p[r] + s_sum, 2, dims, str, box)) return false;
+        }
+        if (s_sum == 0) { sm = am.m[0]; return true; }
+        const uint64_t dims[2] = {(uint64_t)s_sum, (uint64_t)N};
+        const uint64_t str[1] = {(uint64_t)ld_dsum * 2};
+        const uint32_t box[2] = {box0, box1};
+        return encode_tmap(&sm, dsum, 2, dims, str, box);
+    };
 
     // ---- dX = dY_r W_r^T: A = dY_r (K-major), B = W_r^T (MN-major)
     {
         TmapArray am;
-        for (int r = 0; r < t; ++r) {
-            const uint64_t dims[2] = {(uint64_t)h, (uint64_t)N};
-            const uint64_t str[1] = {(uint64_t)ld_dy * 2};
-            const uint32_t box[2] = {64, BM};
-            if (!encode_tmap(&am.m[r], dY.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
-        }
+        CUtensorMap sm;
+        if (!grad_maps(am, sm, 64, BM)) return CAAT_ERR_UNSUPPORTED;
         CUtensorMap bm;
         const uint64_t dims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
         const uint64_t str[2] = {(uint64_t)kt * 2, (uint64_t)ldw * 2};
@@ -404,6 +430,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.BN = BN;
         p.ksplit = 1;
         p.kbps = p.nkb;
+        p.s_blocks = (int)(s_sum / 64);
         p.units = t * p.num_m * p.num_n;
         p.idesc = idesc_bf16_f32(BM, BN, false, true);
         CUtensorMap cm;
@@ -411,18 +438,14 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)lddx * 2};
         const uint32_t cbox[3] = {64, 1, 32};
         if (!encode_tmap(&cm, dX, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
-        const caat_status st = launch_grouped<false, false>(am, bm, cm, p, s, "rowpar_bwd_dx_tc");
+        const caat_status st = launch_grouped<false, false>(am, sm, bm, cm, p, s, "rowpar_bwd_dx_tc");
         if (st != CAAT_OK) return st;
     }
     // ---- dW^T = dY_r^T X_r: A = dY_r^T (MN-major), B = X_r (MN-major)
     {
         TmapArray am;
-        for (int r = 0; r < t; ++r) {
-            const uint64_t dims[2] = {(uint64_t)h, (uint64_t)N};
-            const uint64_t str[1] = {(uint64_t)ld_dy * 2};
-            const uint32_t box[2] = {64, 64};
-            if (!encode_tmap(&am.m[r], dY.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
-        }
+        CUtensorMap sm;
+        if (!grad_maps(am, sm, 64, 64)) return CAAT_ERR_UNSUPPORTED;
         CUtensorMap bm;
         const uint64_t dims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)N};
         const uint64_t str[2] = {(uint64_t)kt * 2, (uint64_t)ldx * 2};
@@ -436,6 +459,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.nkb = (int)((N + BK - 1) / BK);
         p.BN = BN;
         p.idesc = idesc_bf16_f32(BM, BN, true, true);
+        p.s_blocks = (int)(s_sum / 64);
         const int base_units = t * p.num_m * p.num_n;
         p.ksplit = wacc != nullptr ? pick_ksplit(base_units, p.nkb) : 1;
         p.kbps = (p.nkb + p.ksplit - 1) / p.ksplit;
@@ -447,7 +471,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
             const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)ld_dw * 2};
             const uint32_t cbox[3] = {64, 1, 32};
             if (!encode_tmap(&cm, dW, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
-            return launch_grouped<true, false>(am, bm, cm, p, s, "rowpar_bwd_dw_tc");
+            return launch_grouped<true, false>(am, sm, bm, cm, p, s, "rowpar_bwd_dw_tc");
         }
         // split over tokens: fp32 partials reduce-added into wacc [h, K], then one
         // rounding to bf16 into dW
@@ -457,7 +481,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint32_t cbox[3] = {32, 1, 32};
         if (!encode_tmap(&cm, wacc, 3, cdims, cstr, cbox, true)) return CAAT_ERR_UNSUPPORTED;
         if (cudaMemsetAsync(wacc, 0, (size_t)h * (size_t)K * 4, s) != cudaSuccess) return CAAT_ERR_CUDA;
-        caat_status st = launch_grouped<true, true>(am, bm, cm, p, s, "rowpar_bwd_dw_tc");
+        caat_status st = launch_grouped<true, true>(am, sm, bm, cm, p, s, "rowpar_bwd_dw_tc");
         if (st != CAAT_OK) return st;
         const int64_t total = h * (K / 8);
         int64_t blocks = (total + 255) / 256;

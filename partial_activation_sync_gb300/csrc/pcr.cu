@@ -22,6 +22,14 @@ __device__ __forceinline__ void build_bitmap(uint32_t *bm, int64_t h, const int3
                                              int64_t n_sel)
 {
     const int64_t words = (h + 31) >> 5;
+    if (sel == nullptr) {   // S = {0, ..., n_sel-1}
+        for (int64_t w = threadIdx.x; w < words; w += blockDim.x) {
+            const int64_t lo = w * 32;
+            bm[w] = n_sel >= lo + 32 ? 0xffffffffu : (n_sel <= lo ? 0u : ((1u << (n_sel - lo)) - 1u));
+        }
+        __syncthreads();
+        return;
+    }
     for (int64_t w = threadIdx.x; w < words; w += blockDim.x) bm[w] = 0u;
     __syncthreads();
     for (int64_t i = threadIdx.x; i < n_sel; i += blockDim.x) {
@@ -212,6 +220,37 @@ pcr_scalar_kernel(int t, int64_t N, int64_t h, ConstPtrs in, int64_t ld_in, MutP
     }
 }
 
+// out[n, c] = in_0[n, c] + ... + in_{t-1}[n, c] for c < s (bf16, fp32 left fold
+// in rank order, one rounding): the channels of a contiguous S, reduced once
+// instead of into every rank's copy.
+template <int TT>
+__global__ void __launch_bounds__(256)
+pcr_colsum_kernel(int t, int64_t N, int64_t s, ConstPtrs in, int64_t ld_in, uint16_t *__restrict__ out,
+                  int64_t ld_out)
+{
+    const int T = TT > 0 ? TT : t;
+    const int64_t cpr = s / 8;
+    for (int64_t n = blockIdx.y; n < N; n += gridDim.y) {
+        for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < cpr;
+             j += (int64_t)gridDim.x * blockDim.x) {
+            const int64_t bi = (n * ld_in + j * 8) * 2;
+            Acc<true> acc;
+            if (TT > 0) {
+                uint4 v[TT > 0 ? TT : 1];
+#pragma unroll
+                for (int r = 0; r < (TT > 0 ? TT : 1); ++r) v[r] = ld_vec((const char *)in.p[r] + bi, true);
+                acc.init(v[0]);
+#pragma unroll
+                for (int r = 1; r < (TT > 0 ? TT : 1); ++r) acc.add(v[r]);
+            } else {
+                acc.init(ld_vec((const char *)in.p[0] + bi, true));
+                for (int r = 1; r < T; ++r) acc.add(ld_vec((const char *)in.p[r] + bi, true));
+            }
+            st_vec(out + n * ld_out + j * 8, acc.mix(make_uint4(0, 0, 0, 0), 0xffu), false);
+        }
+    }
+}
+
 template <int TT, bool BF16, bool INPLACE>
 void launch_vec(dim3 grid, dim3 block, size_t smem, cudaStream_t s, int t, int64_t N, int64_t h,
                 const ConstPtrs &in, int64_t ld_in, const MutPtrs &out, int64_t ld_out,
@@ -237,6 +276,33 @@ void dispatch_vec(dim3 grid, dim3 block, size_t smem, cudaStream_t s, int t, int
 }
 
 }  // namespace
+
+caat_status launch_pcr_colsum(int t, int64_t N, int64_t s, const ConstPtrs &in, int64_t ld_in, void *out,
+                              int64_t ld_out, cudaStream_t st)
+{
+    if (N == 0 || s == 0) return CAAT_OK;
+    if (s % 8 || ld_in % 8 || ld_out % 8 || (uintptr_t)out % 16) return CAAT_ERR_UNSUPPORTED;
+    for (int r = 0; r < t; ++r)
+        if ((uintptr_t)in.p[r] % 16) return CAAT_ERR_UNSUPPORTED;
+    const int64_t units = s / 8;
+    const int bx = units >= 256 ? 256 : (int)((units + 31) / 32 * 32);
+    int64_t gx = (units + bx - 1) / bx;
+    const int64_t target = (int64_t)num_sms() * (2048 / bx) * 2;
+    if (gx > target) gx = target;
+    int64_t gy = (target + gx - 1) / gx;
+    if (gy > N) gy = N;
+    if (gy > 65535) gy = 65535;
+    const dim3 grid((unsigned)gx, (unsigned)gy);
+    uint16_t *o = (uint16_t *)out;
+    switch (t) {
+    case 2: pcr_colsum_kernel<2><<<grid, bx, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    case 4: pcr_colsum_kernel<4><<<grid, bx, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    case 8: pcr_colsum_kernel<8><<<grid, bx, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    default: pcr_colsum_kernel<0><<<grid, bx, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    }
+    note_launch("pcr_colsum");
+    return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
+}
 
 caat_status launch_pcr(int t, int64_t N, int64_t h, caat_dtype dt, const ConstPtrs &in,
                        int64_t ld_in, const MutPtrs &out, int64_t ld_out, bool in_place,

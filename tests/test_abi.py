@@ -87,7 +87,7 @@ def test_pcr_rejects_bad_args_without_launch(lib):
     assert f(1, 4, 8, 5, _ptrs([a]), 8, _ptrs([b]), 8, sel, 2, None) == 1        # dtype
     assert f(1, 4, 8, 0, _ptrs([a]), 7, _ptrs([b]), 8, sel, 2, None) == 1        # ld_in < h
     assert f(1, 4, 8, 0, _ptrs([a]), 8, _ptrs([b]), 8, sel, 9, None) == 1        # n_sel > h
-    assert f(1, 4, 8, 0, _ptrs([a]), 8, _ptrs([b]), 8, None, 2, None) == 1       # null sel
+    assert f(1, 4, 8, 0, _ptrs([a]), 8, _ptrs([b]), 8, None, -1, None) == 1      # n_sel < 0
     assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([a, c]), 8, sel, 2, None) == 1  # half in place
     assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([c, c]), 8, sel, 2, None) == 1  # outputs overlap
     assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([b + 16, c]), 8, sel, 2, None) == 1  # out hits in

@@ -313,3 +313,64 @@ def test_fwd_small_n_tensor_core(caat, N):
         assert caat.last_kernel() in ("rowpar_fwd_tc", "rowpar_fwd_decode")
         for r in range(t):
             assert rel_fro(got[r], want[r]) <= TOL["bf16"], (r, layout)
+
+
+@pytest.mark.parametrize("N,kt", [(1, 96), (8, 96), (300, 64), (2048, 96)])
+def test_fwd_contiguous_null_sel_matches_index_list(caat, N, kt):
+    """sel given as an int n (null pointer: S = first n channels) gives the same
+    bits as the explicit index list, on every forward kernel."""
+    T = torch()
+    t, h = 8, 768
+    X = ci.normal(1301, (N, kt * t))
+    Wl = ci.normal(1302, (kt * t, h), std=0.02)
+    Xd, Wd = dev(X, "bf16"), _weight(Wl, "bf16", "nn")
+    for s in (0, 100, 384, 768):
+        a = caat.rowpar_linear_fwd(Xd, Wd, t, sel_dev(np.arange(s, dtype=np.int32)))
+        ka = caat.last_kernel()
+        b = caat.rowpar_linear_fwd(Xd, Wd, t, s)
+        assert caat.last_kernel() == ka
+        T.cuda.synchronize()
+        for r in range(t):
+            assert bool((a[r].view(T.int16) == b[r].view(T.int16)).all()), (s, r)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_pcr_contiguous_null_sel_bitexact(caat, dtype):
+    t, N, h = 8, 257, 768
+    Y = ci.normal(1401, (t, N, h))
+    from tests.gpu_helpers import words
+    for s in (0, 5, 384, 768):
+        ins = [dev(Y[r], dtype) for r in range(t)]
+        outs = caat.partial_channel_reduce(ins, s)
+        torch().cuda.synchronize()
+        got = np.stack([words(o) for o in outs])
+        if dtype == "f32":
+            want = orc.pcr_f32(Y, np.arange(s))[0].view(np.uint32)
+        else:
+            want = orc.pcr_bf16(ci.bf16_words(Y), np.arange(s))[0]
+        np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("s", [0, 64, 384, 448, 768, 100])
+@pytest.mark.parametrize("kt", [96, 384])
+def test_bwd_contiguous_reduce_once(caat, s, kt):
+    """Contiguous S given as an int: with |S| a multiple of 64 the backward reduces
+    only the S channels once (the GEMMs read the other channels straight from each
+    rank's gradient); other sizes take the materialising path.  Both match the
+    oracle."""
+    T = torch()
+    t, N, h = 8, 1024, 768
+    X = ci.normal(1501 + kt, (N, kt * t))
+    Wl = ci.normal(1502 + kt, (kt * t, h), std=0.02)
+    G = ci.normal(1503 + kt, (t, N, h))
+    Xd, Wd = dev(X, "bf16"), _weight(Wl, "bf16", "nn")
+    Gd = [dev(G[r], "bf16") for r in range(t)]
+    dX, dW = caat.rowpar_linear_bwd(Xd, Wd, Gd, t, s, caat.CAAT_BWD_REDUCE_DOUT)
+    T.cuda.synchronize()
+    assert caat.device_status() == 0
+    assert caat.last_kernel() == "rowpar_bwd_dw_tc"
+    wX, wW = orc.rowpar_bwd(host_values(X, "bf16"), host_values(Wl, "bf16"),
+                            np.stack([host_values(G[r], "bf16") for r in range(t)]), t,
+                            np.arange(s), 0)
+    assert rel_fro(to_f64(dX), wX) <= TOL["bf16"]
+    assert rel_fro(to_f64(dW), wW) <= TOL["bf16"]
