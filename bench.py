@@ -152,7 +152,8 @@ def run_gpu(args, w):
     peaks = _peaks()
 
     S = caat.select_channels(w.h, w.p, w.layout, w.seeds()["perm"])
-    sel = torch.from_numpy(S).to(device)
+    # a contiguous S is passed by its size (the library's null-index form)
+    sel = int(S.size) if w.layout == 0 else torch.from_numpy(S).to(device)
     layers = [LayerData(torch, w, i, device) for i in range(len(w.layers))]
     ws_bytes = max(max(caat.rowpar_linear_bwd_workspace(w.t, w.N, L.K, w.h, 1, 0) for L in w.layers), 256)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
