@@ -645,10 +645,12 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         if (!encode_tmap(&ym.m[r], Y.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
     }
     // CTAs per cluster: two CTA pairs sharing the W tile when there are at least
-    // four 128-row blocks, one pair when two, else one CTA per tile
+    // four 128-row blocks, one pair when two, else one CTA per tile.  Short shards
+    // (k_t <= 384) make the t output copies the bottleneck; there the finer
+    // single-CTA tiles balance the writes better over the SMs.
     // (override: CAAT_FWD_CLUSTER=1|2|4)
     const int64_t nm = (N + BM - 1) / BM;
-    int cln = nm >= 4 ? 4 : (nm >= 2 ? 2 : 1);
+    int cln = kt <= 384 ? 1 : (nm >= 4 ? 4 : (nm >= 2 ? 2 : 1));
     if (const char *e = std::getenv("CAAT_FWD_CLUSTER")) {
         const int v = std::atoi(e);
         if ((v == 1 || v == 2 || v == 4) && v <= nm) cln = v;
