@@ -9,7 +9,8 @@ forward (GEMM + partial channel-reduce into t rank outputs) and the backward
 (2NKh forward + 4NKh backward per layer, independent of p).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl caat|reference]
-                  [--workload 130m|1.1b|7b_prefill|7b_decode8] [--no-extras]
+                  [--workload 130m|1.1b|7b_prefill|7b_decode8] [--layout contiguous|random]
+                  [--p P] [--no-extras]
 
 Under torchrun each rank runs its own replica on its own GPU (no collective on
 the data path; weak scaling); rank 0 prints one JSON line.  ``--impl reference``
@@ -502,12 +503,19 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["caat", "reference"], default="caat")
     ap.add_argument("--workload", default="130m", choices=["130m", "1.1b", "7b_prefill", "7b_decode8"])
+    ap.add_argument("--layout", choices=["contiguous", "random"], default=None,
+                    help="channel-set layout (default: the workload's own)")
+    ap.add_argument("--p", type=float, default=None, help="synchronized fraction (default: workload's)")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = ci.WORKLOADS[args.workload]
+    if args.layout is not None or args.p is not None:
+        import dataclasses
+        w = dataclasses.replace(w, layout=(1 if args.layout == "random" else 0) if args.layout else w.layout,
+                                p=args.p if args.p is not None else w.p)
     if args.impl == "reference":
         res = run_reference(args, w)
     else:
