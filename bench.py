@@ -9,7 +9,7 @@ forward (GEMM + partial channel-reduce into t rank outputs) and the backward
 (2NKh forward + 4NKh backward per layer, independent of p).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl caat|reference]
-                  [--workload 130m|1.1b|7b_prefill|7b_decode8] [--layout contiguous|random]
+                  [--workload 130m|1.1b|7b_prefill|7b_decode8|130m_stack] [--layout contiguous|random]
                   [--p P] [--no-extras]
 
 Under torchrun each rank runs its own replica on its own GPU (no collective on
@@ -496,13 +496,83 @@ def run_reference(args, w):
                     "d2h_bytes_per_step": 0}}
 
 
+STACK_METRIC = "130M CAAT-Net training step tokens/s (t=8 emulated ranks, p=0.5), 1 GPU"
+
+
+def run_stack(args):
+    """The full 130M block stack, one training step = forward, backward, AdamW:
+    12 layers, 16 heads, h = 768, FFN 3072, RoPE, sequence 1024, batch 8, t = 8
+    emulated ranks, p = 0.5; token ids uniform over a 32000 vocabulary; random
+    N(0, 0.02) weights.  The two row-parallel layers of every block run the fused
+    kernels; attention, norms, embedding and loss are PyTorch ops."""
+    import torch
+    import partial_activation_sync_gb300 as caat
+    from partial_activation_sync_gb300.caatnet import CAATNet, train_step
+    torch.cuda.set_device(0)
+    torch.manual_seed(5)
+    vocab, batch, seq = 32000, 8, 1024
+    model = CAATNet(vocab=vocab, h=768, heads=16, layers=12, ffn=3072, t=8, p=0.5, seq=seq)
+    model = model.cuda().to(torch.bfloat16)
+    opt = torch.optim.AdamW(model.parameters(), lr=6e-4, fused=True)
+    rng = np.random.default_rng(5005)
+    host_tok = [torch.from_numpy(rng.integers(0, vocab, (batch, seq))).pin_memory()
+                for _ in range(args.steps + args.warmup)]
+    tok = torch.empty((batch, seq), dtype=torch.int64, device="cuda")
+    tok.copy_(host_tok[0])
+    for i in range(args.warmup):
+        train_step(model, opt, tok)
+    torch.cuda.synchronize()
+    launches0 = caat.launch_count()
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    stream = torch.cuda.current_stream()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        train_step(model, opt, tok)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    launches = caat.launch_count() - launches0
+    # end to end: each step copies its tokens in and reads the loss back
+    out = torch.empty(1, dtype=torch.float32).pin_memory()
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for i in range(args.steps):
+        tok.copy_(host_tok[args.warmup + i], non_blocking=True)
+        loss = train_step(model, opt, tok)
+        out.copy_(loss.float().reshape(1), non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = f0.elapsed_time(f1)
+    ntok = batch * seq
+    return {"metric": STACK_METRIC, "value": round(ntok * args.steps / (ms * 1e-3), 1), "unit": "tokens/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (token ids uniform over 32000, N(0,0.02) weights)",
+            "config": {"workload": "130m_stack", "layers": 12, "heads": 16, "h": 768, "ffn": 3072,
+                       "seq": seq, "batch": batch, "t": 8, "p": 0.5, "optimizer": "AdamW (fused)",
+                       "l2": "working set far above L2"},
+            "gpu_launches": int(launches), "clocks": clk,
+            "loss_last": round(float(out.item()), 4),
+            "e2e": {"value": round(ntok * args.steps / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
+                    "h2d_bytes_per_step": ntok * 8, "d2h_bytes_per_step": 4}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["caat", "reference"], default="caat")
-    ap.add_argument("--workload", default="130m", choices=["130m", "1.1b", "7b_prefill", "7b_decode8"])
+    ap.add_argument("--workload", default="130m",
+                    choices=["130m", "1.1b", "7b_prefill", "7b_decode8", "130m_stack"])
     ap.add_argument("--layout", choices=["contiguous", "random"], default=None,
                     help="channel-set layout (default: the workload's own)")
     ap.add_argument("--p", type=float, default=None, help="synchronized fraction (default: workload's)")
@@ -511,6 +581,13 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.workload == "130m_stack":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the block-stack workload has no CPU arm; "
+                              "the reference arm times the layer workloads"}), flush=True)
+        elif int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_stack(args)), flush=True)
+        return
     w = ci.WORKLOADS[args.workload]
     if args.layout is not None or args.p is not None:
         import dataclasses

@@ -1,0 +1,106 @@
+"""Float64 CPU reference of the CAAT-Net block stack -- TEST INFRASTRUCTURE ONLY.
+
+Written independently of the product package (which it never imports): plain
+PyTorch CPU ops in float64, autograd for the gradients.
+
+"Tensor-Parallelism with Partially Synchronized Activations" (NeurIPS 2025),
+Introduction: each tensor-parallel all-reduce of the transformer (after the
+attention out-projection and the MLP down-projection) is replaced by the partial
+channel-reduce, so the t ranks carry different residual streams.  The readings of
+the unstated architecture (pre-norm GPT block with LayerNorm, rotary attention,
+GELU MLP, tied embeddings; ranks' final streams averaged for the loss) are the same
+ones the product documents.
+"""
+import math
+
+import torch
+
+
+def rowpar_pcr(X, W, t, s):
+    """X [N, K], W [K, h]; rank r's partial sum X_r W_r over shard r of K; the
+    first s channels summed over ranks in rank order, the rest rank-local.
+    Returns [t, N, h]."""
+    K = X.shape[1]
+    kt = K // t
+    parts = [X[:, r * kt:(r + 1) * kt] @ W[r * kt:(r + 1) * kt] for r in range(t)]
+    total = parts[0]
+    for r in range(1, t):
+        total = total + parts[r]
+    h = W.shape[1]
+    inS = (torch.arange(h) < s).to(X.dtype)
+    return torch.stack([inS * total + (1 - inS) * parts[r] for r in range(t)])
+
+
+def layer_norm(x, g, b, eps=1e-5):
+    mu = x.mean(dim=-1, keepdim=True)
+    var = ((x - mu) ** 2).mean(dim=-1, keepdim=True)
+    return (x - mu) / torch.sqrt(var + eps) * g + b
+
+
+def gelu(x):
+    return 0.5 * x * (1.0 + torch.erf(x / math.sqrt(2.0)))
+
+
+def rope(x, base=10000.0):
+    """x [..., S, hd]: pair (2i, 2i+1) at position m rotated by m * base^(-2i/hd)."""
+    S, hd = x.shape[-2], x.shape[-1]
+    i = torch.arange(hd // 2, dtype=torch.float64)
+    ang = torch.arange(S, dtype=torch.float64)[:, None] * base ** (-2.0 * i / hd)[None, :]
+    c, s = torch.cos(ang), torch.sin(ang)
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    out = torch.empty_like(x)
+    out[..., 0::2] = x1 * c - x2 * s
+    out[..., 1::2] = x1 * s + x2 * c
+    return out
+
+
+def causal_attention(q, k, v):
+    """q, k, v [..., S, hd]: softmax(q k^T / sqrt(hd) with j > i masked) v."""
+    S, hd = q.shape[-2], q.shape[-1]
+    sc = q @ k.transpose(-1, -2) / math.sqrt(hd)
+    mask = torch.triu(torch.ones(S, S, dtype=torch.bool), diagonal=1)
+    sc = sc.masked_fill(mask, float("-inf"))
+    return torch.softmax(sc, dim=-1) @ v
+
+
+def block(x, P, t, heads, s, batch, seq):
+    """x [t, N, h]; P: dict of float64 parameter tensors of one block."""
+    _, N, h = x.shape
+    hd = h // heads
+    hpr = heads // t
+    outs = []
+    for r in range(t):
+        a = layer_norm(x[r], P["ln1.weight"], P["ln1.bias"])
+        qkv = a @ P["wqkv"][r]                                  # [N, 3 h/t]
+        q, k, v = qkv.view(batch, seq, 3, hpr, hd).permute(2, 0, 3, 1, 4)   # [B, hpr, S, hd] each
+        o = causal_attention(rope(q), rope(k), v)               # [B, hpr, S, hd]
+        outs.append(o.permute(0, 2, 1, 3).reshape(N, h // t))
+    o_cat = torch.cat(outs, dim=1)                              # column block r = rank r
+    x = x + rowpar_pcr(o_cat, P["wo"].t(), t, s)
+    ups = [gelu(layer_norm(x[r], P["ln2.weight"], P["ln2.bias"]) @ P["w1"][r]) for r in range(t)]
+    return x + rowpar_pcr(torch.cat(ups, dim=1), P["w2"].t(), t, s)
+
+
+def loss(params, tokens, t, heads, layers, s):
+    """params: dict name -> float64 tensor (names as in the product's module);
+    tokens [batch, seq] int64.  Mean next-token cross-entropy."""
+    batch, seq = tokens.shape
+    N = batch * seq
+    emb = params["emb"]
+    x0 = emb[tokens.reshape(N)]
+    x = torch.stack([x0] * t)
+    for i in range(layers):
+        P = {k.split(".", 2)[2]: v for k, v in params.items() if k.startswith("blocks.%d." % i)}
+        x = block(x, P, t, heads, s, batch, seq)
+    z = layer_norm(x.mean(dim=0), params["ln_f.weight"], params["ln_f.bias"])
+    logits = (z @ emb.t()).view(batch, seq, -1)[:, :-1].reshape(-1, emb.shape[0])
+    tgt = tokens[:, 1:].reshape(-1)
+    logp = logits - torch.logsumexp(logits, dim=-1, keepdim=True)
+    return -logp[torch.arange(tgt.numel()), tgt].mean()
+
+
+def loss_and_grads(params64, tokens, t, heads, layers, s):
+    ps = {k: v.detach().clone().requires_grad_(True) for k, v in params64.items()}
+    L = loss(ps, tokens, t, heads, layers, s)
+    L.backward()
+    return float(L.detach()), {k: v.grad for k, v in ps.items()}

@@ -1,0 +1,140 @@
+"""CAAT-Net block stack on one GPU, the t tensor-parallel ranks emulated in one HBM.
+
+"Tensor-Parallelism with Partially Synchronized Activations" (NeurIPS 2025),
+Introduction: every tensor-parallel all-reduce of the transformer -- after the
+attention out-projection and after the MLP down-projection, Megatron's two
+row-parallel layers per block -- becomes a partial channel-reduce, so the
+activations of the ranks differ and the residual stream is kept as t copies
+[t, N, h].  Experiments: the 130M model has h = 768, 16 heads, 12 layers,
+sequence 1024; p = 0.5, tensor-parallel dimension 8.
+
+Readings where the pages are silent:
+  * GPT-style pre-norm blocks: LayerNorm, causal multi-head attention with rotary
+    position embeddings, a GELU MLP of width FFN (3072 = 4h), tied input/output
+    embeddings;
+  * column-parallel layers (QKV, MLP up) give rank r its heads / its FFN slice,
+    computed from rank r's own residual copy;
+  * the row-parallel layers run the library's fused GEMM + partial reduce (the
+    backward reduces the upstream gradient with the same S);
+  * norm weights and the embedding are replicated: one parameter used by all ranks;
+  * the loss needs one full reduction ("communicating only to compute the loss"):
+    the ranks' final residual copies are averaged, then LayerNorm, the tied LM head
+    and next-token cross-entropy.
+
+Only the two row-parallel layers per block run in this library's kernels;
+attention, norms, GELU, embedding and loss are PyTorch ops of the harness.
+"""
+import math
+
+import torch
+import torch.nn as nn
+import torch.nn.functional as F
+
+from . import CAAT_BWD_REDUCE_DOUT, rowpar_linear_bwd, rowpar_linear_fwd
+
+
+class RowParallelPCR(torch.autograd.Function):
+    """Y[r] = PCR_S(X_r W_r) for the t ranks (rank r's input is column block r of X).
+
+    X: [N, K]; W: logical [K, h] (an nn.Linear weight [h, K] passed as .t());
+    sel: S as a device index tensor or an int n (S = first n channels).
+    Returns Y [t, N, h]."""
+
+    @staticmethod
+    def forward(ctx, X, W, t, sel):
+        N = X.shape[0]
+        h = W.shape[1]
+        Y = torch.empty((t, N, h), dtype=X.dtype, device=X.device)
+        rowpar_linear_fwd(X, W, t, sel, outs=list(Y.unbind(0)))
+        ctx.save_for_backward(X, W)
+        ctx.t, ctx.sel = t, sel
+        return Y
+
+    @staticmethod
+    def backward(ctx, dY):
+        X, W = ctx.saved_tensors
+        dY = dY.contiguous()
+        dX, dW = rowpar_linear_bwd(X, W, list(dY.unbind(0)), ctx.t, ctx.sel, CAAT_BWD_REDUCE_DOUT)
+        return dX, dW, None, None
+
+
+def rope_tables(seq, hd, device, dtype, base=10000.0):
+    inv = 1.0 / (base ** (torch.arange(0, hd, 2, device=device, dtype=torch.float32) / hd))
+    ang = torch.arange(seq, device=device, dtype=torch.float32)[:, None] * inv[None, :]
+    return ang.cos().to(dtype), ang.sin().to(dtype)
+
+
+def apply_rope(x, cos, sin):
+    """x [..., S, hd]: rotate the pairs (x[2i], x[2i+1]) by the angle of position and i."""
+    x1, x2 = x[..., 0::2], x[..., 1::2]
+    r1 = x1 * cos - x2 * sin
+    r2 = x1 * sin + x2 * cos
+    return torch.stack((r1, r2), dim=-1).flatten(-2)
+
+
+class Block(nn.Module):
+    def __init__(self, h, heads, ffn, t, sel, std=0.02):
+        super().__init__()
+        assert heads % t == 0 and ffn % t == 0 and h % heads == 0
+        self.h, self.heads, self.ffn, self.t, self.sel = h, heads, ffn, t, sel
+        self.hd = h // heads
+        self.ln1 = nn.LayerNorm(h)
+        self.ln2 = nn.LayerNorm(h)
+        # column-parallel: rank r's slice of the QKV / up projection, [t, h, cols/t]
+        self.wqkv = nn.Parameter(torch.randn(t, h, 3 * h // t) * std)
+        self.w1 = nn.Parameter(torch.randn(t, h, ffn // t) * std)
+        # row-parallel, nn.Linear layout [out = h, in = K]; K shard r = rank r's heads / FFN slice
+        self.wo = nn.Parameter(torch.randn(h, h) * std)
+        self.w2 = nn.Parameter(torch.randn(h, ffn) * std)
+
+    def forward(self, x, cos, sin, batch, seq):
+        t, N, h = x.shape
+        hpr = self.heads // t                              # heads per rank
+        a = self.ln1(x)
+        qkv = torch.bmm(a, self.wqkv)                      # [t, N, 3 h/t]
+        qkv = qkv.view(t, batch, seq, 3, hpr, self.hd).permute(3, 0, 1, 4, 2, 5)
+        q, k, v = (z.reshape(t * batch, hpr, seq, self.hd) for z in qkv)
+        q, k = apply_rope(q, cos, sin), apply_rope(k, cos, sin)
+        o = F.scaled_dot_product_attention(q, k, v, is_causal=True)   # [t*B, hpr, S, hd]
+        o = o.view(t, batch, hpr, seq, self.hd).permute(1, 3, 0, 2, 4).reshape(N, h)
+        x = x + RowParallelPCR.apply(o, self.wo.t(), t, self.sel)
+        b = self.ln2(x)
+        u = F.gelu(torch.bmm(b, self.w1))                  # [t, N, ffn/t]
+        u = u.permute(1, 0, 2).reshape(N, self.ffn)        # column block r = rank r
+        return x + RowParallelPCR.apply(u, self.w2.t(), t, self.sel)
+
+
+class CAATNet(nn.Module):
+    """Token ids [batch, seq] -> mean next-token cross-entropy."""
+
+    def __init__(self, vocab=32000, h=768, heads=16, layers=12, ffn=3072, t=8, p=0.5, seq=1024,
+                 std=0.02):
+        super().__init__()
+        self.t, self.h, self.heads, self.seq = t, h, heads, seq
+        self.n_sel = int(math.floor(p * h + 0.5))          # contiguous S = first n_sel channels
+        self.emb = nn.Parameter(torch.randn(vocab, h) * std)
+        self.blocks = nn.ModuleList([Block(h, heads, ffn, t, self.n_sel, std) for _ in range(layers)])
+        self.ln_f = nn.LayerNorm(h)
+
+    def forward(self, tokens):
+        batch, seq = tokens.shape
+        N = batch * seq
+        x0 = F.embedding(tokens.reshape(N), self.emb)      # [N, h], identical on every rank
+        x = x0.unsqueeze(0).expand(self.t, N, self.h).contiguous()
+        cos, sin = rope_tables(seq, self.h // self.heads, x.device, x.dtype)
+        for blk in self.blocks:
+            x = blk(x, cos, sin, batch, seq)
+        z = self.ln_f(x.mean(dim=0))                       # the reduction the loss needs
+        logits = z @ self.emb.t()                          # tied LM head
+        tgt = tokens.reshape(batch, seq)[:, 1:].reshape(-1)
+        logits = logits.view(batch, seq, -1)[:, :-1].reshape(-1, logits.shape[-1])
+        return F.cross_entropy(logits.float(), tgt)
+
+
+def train_step(model, opt, tokens):
+    """One training step: forward, backward, AdamW update.  Returns the loss (device)."""
+    opt.zero_grad(set_to_none=True)
+    loss = model(tokens)
+    loss.backward()
+    opt.step()
+    return loss.detach()

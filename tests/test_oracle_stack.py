@@ -1,0 +1,104 @@
+"""Pins of the float64 block-stack reference (oracle/stack.py), no GPU."""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import oracle as orc
+from oracle import stack as ost
+
+
+def _r(seed):
+    return torch.Generator().manual_seed(seed)
+
+
+def test_rowpar_pcr_matches_c_oracle():
+    g = _r(1)
+    for t, N, K, h, s in [(2, 5, 8, 7, 3), (4, 3, 16, 12, 0), (3, 4, 9, 6, 6), (8, 2, 64, 24, 12)]:
+        X = torch.randn(N, K, generator=g, dtype=torch.float64)
+        W = torch.randn(K, h, generator=g, dtype=torch.float64)
+        got = ost.rowpar_pcr(X, W, t, s).numpy()
+        want, _ = orc.rowpar_fwd(X.numpy(), W.numpy(), t, np.arange(s))
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_matches_library_sdpa():
+    g = _r(2)
+    q, k, v = (torch.randn(2, 3, 7, 8, generator=g, dtype=torch.float64) for _ in range(3))
+    want = F.scaled_dot_product_attention(q, k, v, is_causal=True)
+    torch.testing.assert_close(ost.causal_attention(q, k, v), want, rtol=1e-12, atol=1e-12)
+
+
+def test_layer_norm_and_gelu_match_library():
+    g = _r(3)
+    x = torch.randn(5, 16, generator=g, dtype=torch.float64)
+    w = torch.randn(16, generator=g, dtype=torch.float64)
+    b = torch.randn(16, generator=g, dtype=torch.float64)
+    torch.testing.assert_close(ost.layer_norm(x, w, b), F.layer_norm(x, (16,), w, b), rtol=1e-12, atol=1e-12)
+    torch.testing.assert_close(ost.gelu(x), F.gelu(x), rtol=1e-12, atol=1e-12)
+
+
+def test_rope_properties():
+    g = _r(4)
+    S, hd = 9, 8
+    q = torch.randn(S, hd, generator=g, dtype=torch.float64)
+    k = torch.randn(S, hd, generator=g, dtype=torch.float64)
+    rq, rk = ost.rope(q), ost.rope(k)
+    torch.testing.assert_close(rq[0], q[0])                    # position 0: identity
+    torch.testing.assert_close(rq.norm(dim=-1), q.norm(dim=-1))  # rotations keep norms
+    # rotary property: <rope(x)_m, rope(y)_n> depends on m - n only
+    x = torch.randn(hd, generator=g, dtype=torch.float64)
+    y = torch.randn(hd, generator=g, dtype=torch.float64)
+    X = ost.rope(x.expand(S, hd).clone())
+    Y = ost.rope(y.expand(S, hd).clone())
+    d1 = float(X[5] @ Y[3])
+    d2 = float(X[7] @ Y[5])
+    assert abs(d1 - d2) < 1e-12
+
+
+def _tiny_params(t=2, h=8, heads=2, ffn=16, vocab=16, layers=1, seed=5):
+    g = _r(seed)
+    p = {"emb": torch.randn(vocab, h, generator=g, dtype=torch.float64) * 0.5,
+         "ln_f.weight": 1 + 0.1 * torch.randn(h, generator=g, dtype=torch.float64),
+         "ln_f.bias": 0.1 * torch.randn(h, generator=g, dtype=torch.float64)}
+    for i in range(layers):
+        pre = "blocks.%d." % i
+        p[pre + "ln1.weight"] = 1 + 0.1 * torch.randn(h, generator=g, dtype=torch.float64)
+        p[pre + "ln1.bias"] = 0.1 * torch.randn(h, generator=g, dtype=torch.float64)
+        p[pre + "ln2.weight"] = 1 + 0.1 * torch.randn(h, generator=g, dtype=torch.float64)
+        p[pre + "ln2.bias"] = 0.1 * torch.randn(h, generator=g, dtype=torch.float64)
+        p[pre + "wqkv"] = 0.3 * torch.randn(t, h, 3 * h // t, generator=g, dtype=torch.float64)
+        p[pre + "w1"] = 0.3 * torch.randn(t, h, ffn // t, generator=g, dtype=torch.float64)
+        p[pre + "wo"] = 0.3 * torch.randn(h, h, generator=g, dtype=torch.float64)
+        p[pre + "w2"] = 0.3 * torch.randn(h, ffn, generator=g, dtype=torch.float64)
+    return p
+
+
+def test_full_reduce_keeps_ranks_identical_and_empty_set_does_not():
+    t, h, heads = 2, 8, 2
+    P = {k.split(".", 2)[2]: v for k, v in _tiny_params().items() if k.startswith("blocks.0.")}
+    g = _r(6)
+    x = torch.randn(3, h, generator=g, dtype=torch.float64)
+    x = torch.stack([x, x])                       # identical streams going in
+    y1 = ost.block(x, P, t, heads, h, 1, 3)        # S = all channels: vanilla transformer
+    torch.testing.assert_close(y1[0], y1[1], rtol=0, atol=0)
+    y0 = ost.block(x, P, t, heads, 0, 1, 3)        # S empty: the ranks drift apart
+    assert (y0[0] - y0[1]).abs().max() > 1e-3
+
+
+def test_loss_gradients_match_finite_differences():
+    t, heads, layers = 2, 2, 1
+    params = _tiny_params()
+    tokens = torch.tensor([[1, 5, 3, 9], [2, 2, 7, 0]])
+    L, grads = ost.loss_and_grads(params, tokens, t, heads, layers, 4)
+    eps = 1e-6
+    for name, idx in [("blocks.0.wo", (1, 2)), ("blocks.0.w2", (3, 5)), ("blocks.0.wqkv", (1, 2, 4)),
+                      ("emb", (5, 1)), ("blocks.0.ln1.weight", (3,))]:
+        pp = {k: v.clone() for k, v in params.items()}
+        pm = {k: v.clone() for k, v in params.items()}
+        pp[name][idx] += eps
+        pm[name][idx] -= eps
+        fd = (float(ost.loss(pp, tokens, t, heads, layers, 4)) - float(ost.loss(pm, tokens, t, heads, layers, 4))) / (2 * eps)
+        assert abs(fd - float(grads[name][idx])) <= 1e-6 * (1 + abs(fd)), name
