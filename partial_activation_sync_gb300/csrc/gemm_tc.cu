@@ -186,19 +186,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// 32 fp32 values (one row, 32 channels from c0) -> bf16, 16-byte stores of the
-// 8-channel groups that lie below h.
-__device__ __forceinline__ void store_row32(void *Yr, int64_t ldy, int64_t row, int64_t c0,
-                                            int64_t h, const uint32_t (&w)[16])
-{
-    uint16_t *p = (uint16_t *)Yr + row * ldy + c0;
-#pragma unroll
-    for (int g = 0; g < 4; ++g)
-        if (c0 + 8 * g < h)
-            __stcs(reinterpret_cast<uint4 *>(p + 8 * g),
-                   make_uint4(w[4 * g], w[4 * g + 1], w[4 * g + 2], w[4 * g + 3]));
-}
-
 // CLN = CTAs per cluster: 1 (one CTA per tile), 2 (a CTA pair), 4 (two CTA
 // pairs on adjacent row blocks of the same channel block; the two CTAs that hold
 // the same half of the W tile each fetch half of it and multicast to both).
@@ -381,14 +368,11 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         const int q = warp & 3;                         // TMEM lane quarter of this warp
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t au = 0;
-        int sbuf = 0;                                   // next staging buffer of this warp
         for (int u = unit0; u < num_units; u += nunits_grid) {
             const int mb = (u % num_mg) * CLN + (int)crank;
             const int nb = u / num_mg;
             const int64_t n0 = (int64_t)nb * BN;
             const int cls = tile_class(ctl->bitmap, n0, p.h, p.t);
-            const int64_t row = (int64_t)mb * BM + 32 * q + lane;
-            const bool row_ok = row < p.N;
             for (int r = 0; r < p.t; ++r) {
                 if (cls == FULL_S && r != p.t - 1) continue;
                 const uint32_t b = au & 1u;
@@ -403,12 +387,16 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                 const uint32_t tb_other = tmem + lane_off + (b ^ 1u) * 256u;
                 const bool final_mixed = cls == MIXED && r == p.t - 1;
                 const bool zero_nons = cls == MIXED && r <= p.t - 3;
-                if (cls != MIXED) {
+                const int y = mb * BM + 32 * q;
+                uint8_t *stg = staging + q * STG_BYTES;
+                const uint32_t stg_a = smem_u32(stg);
+                if (!final_mixed) {
                     // Stage 32 rows x 64 channels in shared memory (128-byte swizzle:
                     // 16-byte chunk j of row i sits at chunk j ^ (i mod 8)), then one
                     // bulk tensor store per destination rank -- the same staged tile
-                    // serves all t ranks of a FULL_S tile.
-                    const int y = mb * BM + 32 * q;
+                    // serves all t ranks of a FULL_S tile.  A MIXED shard before the
+                    // last writes its partials whole: its S channels are rewritten
+                    // with the sum at the end.
 #pragma unroll 1
                     for (int c64 = 0; c64 < BN / 64; ++c64) {
                         const int64_t c0 = n0 + 64 * c64;
@@ -422,122 +410,114 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
                             w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
                         }
-                        uint8_t *stg = staging + (q * C::NBUF + sbuf) * STG_BYTES;
-                        const uint32_t stg_a = smem_u32(stg);
-                        if (++sbuf == C::NBUF) sbuf = 0;
-                        // the store that last used this buffer has finished reading it
-                        if (lane == 0) {
-                            if (C::NBUF == 2) bulk_wait_read1();
-                            else bulk_wait_read0();
+                        if (zero_nons) {
+                            // keep the S channels accumulating, clear the others
+                            const uint32_t m0 = ctl->bitmap[c0 >> 5], m1 = ctl->bitmap[(c0 >> 5) + 1];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                v0[j] = ((m0 >> j) & 1u) ? v0[j] : 0u;
+                                v1[j] = ((m1 >> j) & 1u) ? v1[j] : 0u;
+                            }
+                            tmem_st32(tb + 64u * c64, v0);
+                            tmem_st32(tb + 64u * c64 + 32u, v1);
                         }
+                        if (lane == 0) bulk_wait_read0();    // staging free again
                         __syncwarp();
                         uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             rowp[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-#ifdef EXP_STG
-                        __syncwarp();
-                        // read back transposed: a warp instruction covers 4 rows x 128 bytes
-                        {
-                            const int cj = lane & 7;
-                            uint4 vv[8];
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int rr = 4 * i + (lane >> 3);
-                                vv[i] = reinterpret_cast<const uint4 *>(stg + rr * 128)[cj ^ (rr & 7)];
-                            }
-                            const bool col_ok = c0 + 8 * cj < p.h;
-                            const int rlo = cls == FULL_S ? 0 : r, rhi = cls == FULL_S ? p.t : r + 1;
-                            for (int dst = rlo; dst < rhi; ++dst) {
-                                uint16_t *yb = (uint16_t *)p.Y.p[dst] + c0 + 8 * cj;
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    const int64_t grow = (int64_t)y + 4 * i + (lane >> 3);
-                                    if (col_ok && grow < p.N) __stcs(reinterpret_cast<uint4 *>(yb + grow * p.ldy), vv[i]);
-                                }
-                            }
-                        }
-                        __syncwarp();
-#else
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0 && y < p.N) {
-#ifdef EXP_STORE_HINT
-                            const uint64_t pol_out = policy_evict_first();
-                            if (cls == FULL_S) {
-                                for (int rr = 0; rr < p.t; ++rr) tma_store_2d_hint(&ymaps.m[rr], stg_a, (int)c0, y, pol_out);
-                            } else {
-                                tma_store_2d_hint(&ymaps.m[r], stg_a, (int)c0, y, pol_out);
-                            }
-#else
                             if (cls == FULL_S) {
                                 for (int rr = 0; rr < p.t; ++rr) tma_store_2d(&ymaps.m[rr], stg_a, (int)c0, y);
                             } else {
                                 tma_store_2d(&ymaps.m[r], stg_a, (int)c0, y);
                             }
-#endif
                             bulk_commit();
                         }
-#endif
                     }
-                }
+                } else {
+                    // Last shard of a MIXED tile: rank t-1's tile (S channels from
+                    // the sum of both accumulators, the others its own) by bulk
+                    // store; then the S sums into the other ranks' S channels with
+                    // row-coalesced, per-lane masked stores, after this warp's
+                    // earlier bulk stores to those rows have completed.
 #pragma unroll 1
-                for (int ch = 0; ch < BN / 32 && cls == MIXED; ++ch) {
-                    const int64_t c0 = n0 + 32 * ch;
-                    if (c0 >= p.h) break;                 // same for the whole warp
-                    uint32_t v[32];
-                    tmem_ld32(tb + 32u * ch, v);
-                    const uint32_t smask = ctl->bitmap[c0 >> 5];
-                    if (!final_mixed) {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                        // a shard before the last: the S channels written here are
-                        // rewritten with the sum at the end
-                        if (row_ok) store_row32(p.Y.p[r], p.ldy, row, c0, p.h, w);
-                        if (zero_nons) {
-                            uint32_t z[32];
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) z[j] = ((smask >> j) & 1u) ? v[j] : 0u;
-                            tmem_st32(tb + 32u * ch, z);
-                        }
-                    } else {
-                        uint32_t uo[32];
-                        tmem_ld32(tb_other + 32u * ch, uo);
-                        uint32_t sum[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            sum[j] = __float_as_uint(__uint_as_float(uo[j]) + __uint_as_float(v[j]));
-                        if (row_ok) {
-                            uint32_t w[16], ws[16];
+                    for (int c64 = 0; c64 < BN / 64; ++c64) {
+                        const int64_t c0 = n0 + 64 * c64;
+                        if (c0 >= p.h) break;
+                        const uint32_t m0 = ctl->bitmap[c0 >> 5], m1 = ctl->bitmap[(c0 >> 5) + 1];
+                        uint32_t w[32], ws[32];
+                        {
+                            uint32_t v[32], u[32];
+                            tmem_ld32(tb + 64u * c64, v);
+                            tmem_ld32(tb_other + 64u * c64, u);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
-                                const uint32_t x0 = ((smask >> (2 * i)) & 1u) ? sum[2 * i] : v[2 * i];
-                                const uint32_t x1 = ((smask >> (2 * i + 1)) & 1u) ? sum[2 * i + 1] : v[2 * i + 1];
-                                w[i] = pack_bf16x2(x0, x1);
-                                ws[i] = pack_bf16x2(sum[2 * i], sum[2 * i + 1]);
+                                const float s0 = __uint_as_float(u[2 * i]) + __uint_as_float(v[2 * i]);
+                                const float s1 = __uint_as_float(u[2 * i + 1]) + __uint_as_float(v[2 * i + 1]);
+                                ws[i] = pack_bf16x2(__float_as_uint(s0), __float_as_uint(s1));
+                                w[i] = pack_bf16x2(((m0 >> (2 * i)) & 1u) ? __float_as_uint(s0) : v[2 * i],
+                                                   ((m0 >> (2 * i + 1)) & 1u) ? __float_as_uint(s1) : v[2 * i + 1]);
                             }
-                            store_row32(p.Y.p[p.t - 1], p.ldy, row, c0, p.h, w);
-                            for (int rr = 0; rr < p.t - 1; ++rr) {
-                                uint16_t *py = (uint16_t *)p.Y.p[rr] + row * p.ldy + c0;
+                            tmem_ld32(tb + 64u * c64 + 32u, v);
+                            tmem_ld32(tb_other + 64u * c64 + 32u, u);
 #pragma unroll
-                                for (int g = 0; g < 4; ++g) {
-                                    if (c0 + 8 * g >= p.h) continue;
-                                    const uint32_t gm = (smask >> (8 * g)) & 0xffu;
-                                    if (gm == 0xffu) {
-                                        __stcs(reinterpret_cast<uint4 *>(py + 8 * g),
-                                               make_uint4(ws[4 * g], ws[4 * g + 1], ws[4 * g + 2], ws[4 * g + 3]));
-                                    } else if (gm != 0u) {
+                            for (int i = 0; i < 16; ++i) {
+                                const float s0 = __uint_as_float(u[2 * i]) + __uint_as_float(v[2 * i]);
+                                const float s1 = __uint_as_float(u[2 * i + 1]) + __uint_as_float(v[2 * i + 1]);
+                                ws[16 + i] = pack_bf16x2(__float_as_uint(s0), __float_as_uint(s1));
+                                w[16 + i] = pack_bf16x2(((m1 >> (2 * i)) & 1u) ? __float_as_uint(s0) : v[2 * i],
+                                                        ((m1 >> (2 * i + 1)) & 1u) ? __float_as_uint(s1) : v[2 * i + 1]);
+                            }
+                        }
+                        uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
+                        if (lane == 0) bulk_wait_read0();
+                        __syncwarp();
 #pragma unroll
-                                        for (int e = 0; e < 8; ++e)
-                                            if ((gm >> e) & 1u) {
-                                                const uint32_t wd = ws[4 * g + (e >> 1)];
-                                                py[8 * g + e] = (uint16_t)((e & 1) ? (wd >> 16) : (wd & 0xffffu));
-                                            }
-                                    }
+                        for (int j = 0; j < 8; ++j)
+                            rowp[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && y < p.N) {
+                            tma_store_2d(&ymaps.m[p.t - 1], stg_a, (int)c0, y);
+                            bulk_commit();
+                        }
+                        // the sums, staged the same way, once the store above has read
+                        // the staging; then every earlier bulk store of this warp (the
+                        // shards' partials in these rows) must be complete before the
+                        // generic stores below overwrite their S channels
+                        if (lane == 0) {
+                            bulk_wait0();
+                            fence_proxy_async_global();
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            rowp[j ^ (lane & 7)] = make_uint4(ws[4 * j], ws[4 * j + 1], ws[4 * j + 2], ws[4 * j + 3]);
+                        __syncwarp();
+                        // lane l owns channel c0 + l (and c0 + 32 + l) of every row
+                        const bool s_lo = (m0 >> lane) & 1u, s_hi = (m1 >> lane) & 1u;
+                        const bool ok_lo = s_lo && c0 + lane < p.h, ok_hi = s_hi && c0 + 32 + lane < p.h;
+                        if (__any_sync(0xffffffffu, ok_lo || ok_hi)) {
+                            for (int i = 0; i < 32; ++i) {
+                                const int64_t grow = (int64_t)y + i;
+                                if (grow >= p.N) break;
+                                const uint8_t *srow = stg + i * 128;
+                                const uint16_t vlo = *reinterpret_cast<const uint16_t *>(
+                                    srow + (((lane >> 3) ^ (i & 7)) << 4) + (lane & 7) * 2);
+                                const uint16_t vhi = *reinterpret_cast<const uint16_t *>(
+                                    srow + ((((lane + 32) >> 3) ^ (i & 7)) << 4) + (lane & 7) * 2);
+                                for (int rr = 0; rr < p.t - 1; ++rr) {
+                                    uint16_t *yrow = (uint16_t *)p.Y.p[rr] + grow * p.ldy + c0;
+                                    if (ok_lo) yrow[lane] = vlo;
+                                    if (ok_hi) yrow[32 + lane] = vhi;
                                 }
                             }
                         }
+                        __syncwarp();
                     }
                 }
                 fence_before_sync();

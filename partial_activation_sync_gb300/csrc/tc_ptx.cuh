@@ -127,6 +127,13 @@ __device__ __forceinline__ void bulk_wait_read1()
 // wait until every committed bulk store is complete
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// order this thread's completed async-proxy (bulk) global writes before its later
+// generic-proxy global accesses
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // make this thread's generic-proxy shared-memory writes visible to the async proxy (TMA)
 __device__ __forceinline__ void fence_proxy_async_smem()
 {
