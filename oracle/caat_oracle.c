@@ -325,3 +325,80 @@ int orc_rowpar_bwd(int t, int64_t N, int64_t K, int64_t h,
     free(dY);
     return 0;
 }
+
+/* -------------------------------------------- column-parallel linear layer */
+/*
+ * The partner of the row-parallel layer inside a transformer block (attention
+ * QKV, MLP up-projection).  Rank r multiplies its own input A_r [N][h] (A is
+ * [t][N][h]: under partial synchronization the ranks' activations differ) by its
+ * column block W1_r = W1[:, r*K/t .. (r+1)*K/t) of W1 [h][K] (row-major, double).
+ * Z [N][K] holds rank r's output in column block r.  The forward has no reduce.
+ * Returns 0, or 1 when K is not divisible by t.
+ */
+int orc_colpar_fwd(int t, int64_t N, int64_t h, int64_t K,
+                   const double *A, const double *W1, double *Z)
+{
+    int64_t kt;
+    if (t < 1 || K % t != 0) return 1;
+    kt = K / t;
+    #pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) {
+            const int r = (int)(k / kt);
+            const double *a = A + ((int64_t)r * N + n) * h;
+            double acc = 0.0;
+            for (int64_t c = 0; c < h; ++c) acc += a[c] * W1[c * K + k];
+            Z[n * K + k] = acc;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Backward of the column-parallel layer with the partial reduce placed on its
+ * input gradient (Megatron's placement; the row-parallel backward then passes
+ * each rank's gradient through unreduced).  Reading: the input channels in S are
+ * one activation shared by the ranks, so their gradient is the sum of the ranks'
+ * contributions; outside S each rank's input is its own.
+ *   P_r            = dZ_r W1_r^T     [N][h]  (dZ_r = column block r of dZ [N][K])
+ *   dA             = PCR(P) with S   [t][N][h]
+ *   dW1[:, block r] = A_r^T dZ_r     [h][K]
+ * Returns 0, or 1 on a bad argument.
+ */
+int orc_colpar_bwd(int t, int64_t N, int64_t h, int64_t K,
+                   const double *A, const double *W1, const double *dZ,
+                   const int32_t *sel, int64_t n_sel, double *dA, double *dW1)
+{
+    int64_t kt;
+    double *P;
+    if (t < 1 || K % t != 0) return 1;
+    kt = K / t;
+    P = (double *)malloc(sizeof(double) * (size_t)((int64_t)t * N * h > 0 ? (int64_t)t * N * h : 1));
+    if (!P) return 1;
+    #pragma omp parallel for schedule(static)
+    for (int64_t n = 0; n < N; ++n) {
+        for (int r = 0; r < t; ++r) {
+            double *prow = P + ((int64_t)r * N + n) * h;
+            for (int64_t c = 0; c < h; ++c) {
+                double acc = 0.0;
+                for (int64_t k = (int64_t)r * kt; k < (int64_t)(r + 1) * kt; ++k)
+                    acc += dZ[n * K + k] * W1[c * K + k];
+                prow[c] = acc;
+            }
+        }
+    }
+    orc_pcr_f64(t, N, h, P, sel, n_sel, dA);
+    free(P);
+
+    #pragma omp parallel for schedule(static)
+    for (int64_t c = 0; c < h; ++c) {
+        for (int64_t k = 0; k < K; ++k) {
+            const int r = (int)(k / kt);
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n)
+                acc += A[((int64_t)r * N + n) * h + c] * dZ[n * K + k];
+            dW1[c * K + k] = acc;
+        }
+    }
+    return 0;
+}

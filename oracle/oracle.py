@@ -46,6 +46,11 @@ def lib():
         L.orc_rowpar_bwd.argtypes = [ctypes.c_int, _i64, _i64, _i64, _p, _p, _p,
                                      _p, _i64, ctypes.c_int, _p, _p]
         L.orc_rowpar_bwd.restype = ctypes.c_int
+        L.orc_colpar_fwd.argtypes = [ctypes.c_int, _i64, _i64, _i64, _p, _p, _p]
+        L.orc_colpar_fwd.restype = ctypes.c_int
+        L.orc_colpar_bwd.argtypes = [ctypes.c_int, _i64, _i64, _i64, _p, _p, _p, _p, _i64,
+                                     _p, _p]
+        L.orc_colpar_bwd.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -172,3 +177,37 @@ def rowpar_bwd(X, W, G, t: int, sel, mode: int = REDUCE_DOUT):
     if rc != 0:
         raise ValueError("orc_rowpar_bwd: invalid argument")
     return dX, dW
+
+
+# ---------------------------------------------- column-parallel linear layer
+
+def colpar_fwd(A, W1, t: int):
+    """A [t, N, h] (rank r's own input), W1 [h, K] (float64) -> Z [N, K], column
+    block r = A_r W1[:, block r]."""
+    A = np.ascontiguousarray(A, dtype=np.float64)
+    W1 = np.ascontiguousarray(W1, dtype=np.float64)
+    t2, N, h = A.shape
+    h2, K = W1.shape
+    assert t2 == t and h2 == h
+    Z = np.empty((N, K), dtype=np.float64)
+    if lib().orc_colpar_fwd(t, N, h, K, _ptr(A), _ptr(W1), _ptr(Z)) != 0:
+        raise ValueError("orc_colpar_fwd: invalid argument")
+    return Z
+
+
+def colpar_bwd(A, W1, dZ, t: int, sel):
+    """A [t, N, h], W1 [h, K], dZ [N, K] (float64) -> (dA [t, N, h], dW1 [h, K]);
+    dA = PCR over S of the ranks' dZ_r W1_r^T."""
+    A = np.ascontiguousarray(A, dtype=np.float64)
+    W1 = np.ascontiguousarray(W1, dtype=np.float64)
+    dZ = np.ascontiguousarray(dZ, dtype=np.float64)
+    _, N, h = A.shape
+    K = W1.shape[1]
+    assert dZ.shape == (N, K)
+    s = _sel(sel)
+    dA = np.empty((t, N, h), dtype=np.float64)
+    dW1 = np.empty((h, K), dtype=np.float64)
+    if lib().orc_colpar_bwd(t, N, h, K, _ptr(A), _ptr(W1), _ptr(dZ), _ptr(s), s.size,
+                            _ptr(dA), _ptr(dW1)) != 0:
+        raise ValueError("orc_colpar_bwd: invalid argument")
+    return dA, dW1

@@ -158,3 +158,50 @@ def test_biased_shuffle_mutant_is_caught():
     exp = n / 6
     chi2 = sum((c - exp) ** 2 / exp for c in counts.values()) + exp * (6 - len(counts))
     assert chi2 >= 20.5
+
+
+# ------------------------------------------------ column-parallel backward
+
+def _colpar_bwd_from(L):
+    P = ctypes.c_void_p
+    I64 = ctypes.c_int64
+    L.orc_colpar_bwd.argtypes = [ctypes.c_int, I64, I64, I64, P, P, P, P, I64, P, P]
+
+    def bwd(A, W1, dZ, t, S):
+        A = np.ascontiguousarray(A, dtype=np.float64)
+        W1 = np.ascontiguousarray(W1, dtype=np.float64)
+        dZ = np.ascontiguousarray(dZ, dtype=np.float64)
+        _, N, h = A.shape
+        K = W1.shape[1]
+        S = np.ascontiguousarray(S, dtype=np.int32)
+        dA = np.empty((t, N, h))
+        dW1 = np.empty((h, K))
+        L.orc_colpar_bwd(t, N, h, K, _p(A), _p(W1), _p(dZ), _p(S), S.size, _p(dA), _p(dW1))
+        return dA, dW1
+    return bwd
+
+
+def _colpar_pins_hold(L):
+    from tests.test_oracle_colpar import colpar_logical_fd_errors
+    bwd = _colpar_bwd_from(L)
+    return all(colpar_logical_fd_errors(bwd, t, N, h, K, p, seed) <= 1e-8
+               for (t, N, h, K, p, seed) in [(3, 2, 5, 6, 0.4, 5), (2, 2, 4, 4, 1.0, 6)])
+
+
+def test_unmutated_colpar_passes_the_same_checks():
+    assert _colpar_pins_hold(_mutant("int orc_colpar_bwd(", "int orc_colpar_bwd("))
+
+
+@pytest.mark.parametrize("old,new", [
+    # the input gradient is not reduced at all
+    ("orc_pcr_f64(t, N, h, P, sel, n_sel, dA);",
+     "memcpy(dA, P, sizeof(double) * (size_t)((int64_t)t * N * h));"),
+    # every rank's input gradient taken over all of K (a full reduce for every channel)
+    ("for (int64_t k = (int64_t)r * kt; k < (int64_t)(r + 1) * kt; ++k)\n                    acc += dZ[n * K + k] * W1[c * K + k];",
+     "for (int64_t k = 0; k < K; ++k)\n                    acc += dZ[n * K + k] * W1[c * K + k];"),
+    # dW1 from the wrong rank's input
+    ("acc += A[((int64_t)r * N + n) * h + c] * dZ[n * K + k];",
+     "acc += A[((int64_t)((r + 1) % t) * N + n) * h + c] * dZ[n * K + k];"),
+])
+def test_colpar_mutants_are_caught(old, new):
+    assert not _colpar_pins_hold(_mutant(old, new))
