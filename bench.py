@@ -10,7 +10,7 @@ forward (GEMM + partial channel-reduce into t rank outputs) and the backward
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl caat|reference]
                   [--workload 130m|1.1b|7b_prefill|7b_decode8|130m_stack] [--layout contiguous|random]
-                  [--p P] [--no-extras]
+                  [--p P] [--placement reduce_dout|column] [--no-extras]
 
 Under torchrun each rank runs its own replica on its own GPU (no collective on
 the data path; weak scaling); rank 0 prints one JSON line.  ``--impl reference``
@@ -410,6 +410,28 @@ def run_extras(torch, caat, device, peaks):
                 "kernel": caat.last_kernel()}
             del X, Ys
         del Wst
+    # column-parallel layer at the 130M MLP up-projection (N = 8192, h = 768,
+    # FFN 3072, t = 8, p = 0.5): forward, and the backward with the partial reduce
+    # on its input gradient (Megatron's placement)
+    t, N, h, K = 8, 8192, 768, 3072
+    A = torch.randn((t, N, h), device=device).to(torch.bfloat16)
+    W1 = (torch.randn((h, K), device=device) * 0.02).to(torch.bfloat16)
+    dZ = torch.randn((N, K), device=device).to(torch.bfloat16)
+    Z = torch.empty((N, K), dtype=torch.bfloat16, device=device)
+    dA = torch.empty((t, N, h), dtype=torch.bfloat16, device=device)
+    dW1 = torch.empty_like(W1)
+    ws = torch.empty(max(caat.colpar_linear_bwd_workspace(t, N, h, K, 1), 1), dtype=torch.uint8,
+                     device=device)
+    for name, fn, flops in (
+            ("130m_colpar_up_fwd", lambda: caat.colpar_linear_fwd(A, W1, t, Z=Z), 2.0 * N * h * K),
+            ("130m_colpar_up_bwd", lambda: caat.colpar_linear_bwd(A, W1, dZ, t, h // 2, dA=dA, dW1=dW1,
+                                                                  workspace=ws), 4.0 * N * h * K)):
+        fn()
+        sec = _time_call(torch, fn, 10, flush)
+        tf = flops / sec / 1e12
+        out[name] = {"TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4),
+                     "us": round(sec * 1e6, 1), "kernel": caat.last_kernel()}
+    del A, W1, dZ, Z, dA, dW1, ws
     torch.cuda.synchronize()
     return out
 
@@ -504,14 +526,16 @@ def run_stack(args):
     12 layers, 16 heads, h = 768, FFN 3072, RoPE, sequence 1024, batch 8, t = 8
     emulated ranks, p = 0.5; token ids uniform over a 32000 vocabulary; random
     N(0, 0.02) weights.  The two row-parallel layers of every block run the fused
-    kernels; attention, norms, embedding and loss are PyTorch ops."""
+    kernels (with --placement column, the column-parallel layers' backward with the
+    partial reduce too); attention, norms, embedding and loss are PyTorch ops."""
     import torch
     import partial_activation_sync_gb300 as caat
     from partial_activation_sync_gb300.caatnet import CAATNet, train_step
     torch.cuda.set_device(0)
     torch.manual_seed(5)
     vocab, batch, seq = 32000, 8, 1024
-    model = CAATNet(vocab=vocab, h=768, heads=16, layers=12, ffn=3072, t=8, p=0.5, seq=seq)
+    model = CAATNet(vocab=vocab, h=768, heads=16, layers=12, ffn=3072, t=8, p=0.5, seq=seq,
+                    placement=args.placement)
     model = model.cuda().to(torch.bfloat16)
     opt = torch.optim.AdamW(model.parameters(), lr=6e-4, fused=True)
     rng = np.random.default_rng(5005)
@@ -558,6 +582,7 @@ def run_stack(args):
             "data": "synthetic (token ids uniform over 32000, N(0,0.02) weights)",
             "config": {"workload": "130m_stack", "layers": 12, "heads": 16, "h": 768, "ffn": 3072,
                        "seq": seq, "batch": batch, "t": 8, "p": 0.5, "optimizer": "AdamW (fused)",
+                       "placement": args.placement,
                        "l2": "working set far above L2"},
             "gpu_launches": int(launches), "clocks": clk,
             "loss_last": round(float(out.item()), 4),
@@ -576,6 +601,8 @@ def main():
     ap.add_argument("--layout", choices=["contiguous", "random"], default=None,
                     help="channel-set layout (default: the workload's own)")
     ap.add_argument("--p", type=float, default=None, help="synchronized fraction (default: workload's)")
+    ap.add_argument("--placement", choices=["reduce_dout", "column"], default="reduce_dout",
+                    help="130m_stack: where the backward reduce sits")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

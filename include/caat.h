@@ -219,6 +219,56 @@ caat_status caat_rowpar_linear_bwd_noalloc(int t, int64_t N, int64_t K, int64_t 
                                            const int32_t *sel, int64_t n_sel, caat_bwd_mode mode,
                                            caat_stream_t stream);
 
+/*
+ * The column-parallel partner of the layer above (attention QKV, MLP up), for
+ * Megatron's placement of the backward reduce: the row-parallel backward runs in
+ * CAAT_BWD_NO_REDUCE mode and the partial channel-reduce moves to this layer's
+ * input gradient ("Tensor-Parallelism with Partially Synchronized Activations",
+ * Introduction: the reduce of forward and backward must agree).  Reading: the
+ * input channels in S are one activation shared by the ranks, so their gradient
+ * is the sum of the ranks' contributions; outside S each rank's input is its own.
+ *
+ * Layouts (elements, row-major unless strides say otherwise):
+ *   A:  array of t device pointers; A[r] is rank r's input [N, h], row stride lda
+ *       (under partial synchronization the ranks' inputs differ).
+ *   W1: logical [h, K]; element (c, k) at W1[c*w1_rs + k*w1_cs].  Rank r owns the
+ *       column block W1_r = W1[:, r*k_t .. (r+1)*k_t), k_t = K/t.
+ *       This is the row-parallel W's [h, K] storage with the roles of the two
+ *       dimensions swapped: K-contiguous (w1_cs == 1) takes the tensor cores.
+ *   Z / dZ: [N, K], row stride ldz; column block r is rank r's output.
+ *
+ * caat_colpar_linear_fwd:  Z[:, block r] = A_r W1_r.  No reduce.
+ * caat_colpar_linear_bwd:
+ *   dA_r            = PCR_S(dZ_r W1_r^T)   (t buffers [N, h], row stride ldda):
+ *                     c in S: sum over q of dZ_q W1_q^T[:, c]; otherwise rank r's own;
+ *   dW1[:, block r] = A_r^T dZ_r            (element (c, k) at dW1[c*dw1_rs + k*dw1_cs]).
+ *   dA is computed by the fused row-parallel forward kernel (dZ W1^T is
+ *   row-parallel shaped), dW1 by the grouped backward GEMM.
+ *   workspace: optional device scratch, 256-byte aligned, of at least
+ *   caat_colpar_linear_bwd_workspace() bytes (bf16: an fp32 accumulator of dW1 that
+ *   lets dW1 be reduced over tokens in parts); null is allowed.
+ * Ownership: all buffers belong to the caller; nothing is kept after the call.
+ * Errors: INVALID_ARG for a bad size, null pointer, stride below the row width,
+ *   K % t != 0, n_sel outside [0, h], or outputs overlapping inputs (Z with any A_r,
+ *   dA_r with each other, with any A_q or with dZ); UNSUPPORTED / CUDA as
+ *   caat_rowpar_linear_fwd.  sel as there (null = the first n_sel channels).
+ */
+caat_status caat_colpar_linear_fwd(int t, int64_t N, int64_t h, int64_t K, caat_dtype dt,
+                                   const void *const *A, int64_t lda,
+                                   const void *W1, int64_t w1_rs, int64_t w1_cs,
+                                   void *Z, int64_t ldz, caat_stream_t stream);
+
+size_t caat_colpar_linear_bwd_workspace(int t, int64_t N, int64_t h, int64_t K, caat_dtype dt);
+
+caat_status caat_colpar_linear_bwd(int t, int64_t N, int64_t h, int64_t K, caat_dtype dt,
+                                   const void *const *A, int64_t lda,
+                                   const void *W1, int64_t w1_rs, int64_t w1_cs,
+                                   const void *dZ, int64_t ldz,
+                                   void *const *dA, int64_t ldda,
+                                   void *dW1, int64_t dw1_rs, int64_t dw1_cs,
+                                   const int32_t *sel, int64_t n_sel,
+                                   void *workspace, size_t ws_bytes, caat_stream_t stream);
+
 /* Human-readable name of a status code (static string, never null). */
 const char *caat_status_string(caat_status st);
 

@@ -20,7 +20,8 @@ CAAT_BWD_REDUCE_DOUT, CAAT_BWD_NO_REDUCE = 0, 1
 
 __all__ = [
     "select_channels", "partial_channel_reduce", "rowpar_linear_fwd", "rowpar_linear_bwd",
-    "rowpar_linear_bwd_workspace", "device_status", "last_kernel", "launch_count",
+    "rowpar_linear_bwd_workspace", "rowpar_linear_bwd_noalloc", "colpar_linear_fwd",
+    "colpar_linear_bwd", "colpar_linear_bwd_workspace", "device_status", "last_kernel", "launch_count",
     "CaatError", "CAAT_S_CONTIGUOUS", "CAAT_S_RANDOM", "CAAT_BWD_REDUCE_DOUT",
     "CAAT_BWD_NO_REDUCE",
 ]
@@ -205,6 +206,93 @@ def rowpar_linear_bwd(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
     return dX, dW
 
 
+# ------------------------------------------------- column-parallel layer
+
+def _rank_inputs(A, t: int, h: int, name: str):
+    """t rank tensors [N, h] (a list, or a [t, N, h] tensor) sharing a row stride."""
+    if not isinstance(A, (list, tuple)):
+        if A.dim() != 3:
+            raise ValueError("caat: %s must be t tensors [N, h] or one [t, N, h] tensor" % name)
+        A = list(A.unbind(0))
+    if len(A) != t:
+        raise ValueError("caat: need t tensors in %s" % name)
+    N = A[0].shape[0]
+    ld = _rowmajor(A[0], name)
+    for a in A:
+        if tuple(a.shape) != (N, h) or a.dtype != A[0].dtype or _rowmajor(a, name) != ld:
+            raise ValueError("caat: %s tensors must be [N, h] with one dtype and row stride" % name)
+    return A, N, ld
+
+
+def _w1_strides(W1, h, K, name="W1"):
+    if W1.dim() != 2 or tuple(W1.shape) != (h, K) or not W1.is_cuda:
+        raise ValueError("caat: %s must be a CUDA tensor of shape [h, K] = [%d, %d]" % (name, h, K))
+    return W1.stride(0), W1.stride(1)
+
+
+def colpar_linear_fwd(A, W1, t: int, Z=None, stream=None):
+    """Column-parallel layer: A = the t ranks' inputs [N, h] (list or [t, N, h]
+    tensor), W1 [h, K] (K-contiguous takes the tensor cores).  Returns Z [N, K]
+    with column block r = A_r W1[:, block r]."""
+    torch = _torch()
+    h, K = W1.shape
+    A, N, lda = _rank_inputs(A, t, h, "A")
+    if W1.dtype != A[0].dtype:
+        raise TypeError("caat: A and W1 must share a dtype")
+    w1_rs, w1_cs = _w1_strides(W1, h, K)
+    if Z is None:
+        Z = torch.empty((N, K), dtype=W1.dtype, device=W1.device)
+    if tuple(Z.shape) != (N, K) or Z.dtype != W1.dtype:
+        raise ValueError("caat: Z must be [N, K] of W1's dtype")
+    st = _lib.load().caat_colpar_linear_fwd(
+        int(t), N, h, K, _dtype_code(W1), _lib.ptr_array([a.data_ptr() for a in A]), lda,
+        ctypes.c_void_p(W1.data_ptr()), w1_rs, w1_cs, ctypes.c_void_p(Z.data_ptr()),
+        _rowmajor(Z, "Z"), _stream_ptr(stream))
+    _check(st, "caat_colpar_linear_fwd")
+    return Z
+
+
+def colpar_linear_bwd_workspace(t: int, N: int, h: int, K: int, dtype_code: int) -> int:
+    return int(_lib.load().caat_colpar_linear_bwd_workspace(int(t), int(N), int(h), int(K),
+                                                            int(dtype_code)))
+
+
+def colpar_linear_bwd(A, W1, dZ, t: int, sel, dA=None, dW1=None, workspace=None, stream=None):
+    """Gradients of ``colpar_linear_fwd`` with the partial reduce on the input
+    gradient: dA_r = PCR_S(dZ_r W1_r^T), dW1[:, block r] = A_r^T dZ_r.
+    Returns (dA, dW1): dA a [t, N, h] tensor (or the list passed in), dW1 [h, K]
+    with W1's strides when allocated here."""
+    torch = _torch()
+    h, K = W1.shape
+    A, N, lda = _rank_inputs(A, t, h, "A")
+    w1_rs, w1_cs = _w1_strides(W1, h, K)
+    if tuple(dZ.shape) != (N, K) or dZ.dtype != W1.dtype:
+        raise ValueError("caat: dZ must be [N, K] of W1's dtype")
+    ldz = _rowmajor(dZ, "dZ")
+    ret_dA = dA
+    if dA is None:
+        ret_dA = torch.empty((t, N, h), dtype=W1.dtype, device=W1.device)
+    dAs, _, ldda = _rank_inputs(ret_dA, t, h, "dA")
+    if dW1 is None:
+        dW1 = torch.empty_strided((h, K), W1.stride(), dtype=W1.dtype, device=W1.device)
+    dw1_rs, dw1_cs = _w1_strides(dW1, h, K, "dW1")
+    dt = _dtype_code(W1)
+    if workspace is None:
+        need = colpar_linear_bwd_workspace(t, N, h, K, dt)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=W1.device)
+    wp = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
+    wb = workspace.numel() if workspace is not None else 0
+    sp, ns = _sel_ptr(sel)
+    st = _lib.load().caat_colpar_linear_bwd(
+        int(t), N, h, K, dt, _lib.ptr_array([a.data_ptr() for a in A]), lda,
+        ctypes.c_void_p(W1.data_ptr()), w1_rs, w1_cs, ctypes.c_void_p(dZ.data_ptr()), ldz,
+        _lib.ptr_array([g.data_ptr() for g in dAs]), ldda,
+        ctypes.c_void_p(dW1.data_ptr()), dw1_rs, dw1_cs, sp, ns, wp, wb, _stream_ptr(stream))
+    _check(st, "caat_colpar_linear_bwd")
+    return ret_dA, dW1
+
+
 # ------------------------------------------------------------ diagnostics
 
 def device_status(stream=None) -> int:
@@ -228,14 +316,7 @@ def rowpar_linear_bwd_noalloc(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDU
     library's fixed 16 MiB scratch array replaces the workspace (the outputs dX
     and dW must then be passed in; nothing is allocated here).  Calls that overlap
     on the GPU race on that one array."""
-    L = _lib.load()
-    f = L.caat_rowpar_linear_bwd_noalloc
-    f.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
-                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
-                  ctypes.POINTER(ctypes.c_void_p), ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
-                  ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
-                  ctypes.c_int, ctypes.c_void_p]
-    f.restype = ctypes.c_int
+    f = _lib.load().caat_rowpar_linear_bwd_noalloc
     if dX is None or dW is None:
         raise ValueError("caat: rowpar_linear_bwd_noalloc needs dX and dW passed in")
     N, K = X.shape

@@ -18,6 +18,10 @@ EXPORTS = (
     "caat_rowpar_linear_fwd",
     "caat_rowpar_linear_bwd_workspace",
     "caat_rowpar_linear_bwd",
+    "caat_rowpar_linear_bwd_noalloc",
+    "caat_colpar_linear_fwd",
+    "caat_colpar_linear_bwd_workspace",
+    "caat_colpar_linear_bwd",
     "caat_status_string",
     "caat_get_device_status",
     "caat_last_kernel",
@@ -55,6 +59,21 @@ def load(path: str = None) -> ctypes.CDLL:
                                          _c_pp, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_i64,
                                          _c_p, _c_i64, ctypes.c_int, _c_p, ctypes.c_size_t, _c_p]
     L.caat_rowpar_linear_bwd.restype = ctypes.c_int
+    L.caat_rowpar_linear_bwd_noalloc.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
+                                                 _c_p, _c_i64, _c_p, _c_i64, _c_i64,
+                                                 _c_pp, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_i64,
+                                                 _c_p, _c_i64, ctypes.c_int, _c_p]
+    L.caat_rowpar_linear_bwd_noalloc.restype = ctypes.c_int
+    L.caat_colpar_linear_fwd.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
+                                         _c_pp, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_p]
+    L.caat_colpar_linear_fwd.restype = ctypes.c_int
+    L.caat_colpar_linear_bwd_workspace.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int]
+    L.caat_colpar_linear_bwd_workspace.restype = ctypes.c_size_t
+    L.caat_colpar_linear_bwd.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
+                                         _c_pp, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64,
+                                         _c_pp, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64,
+                                         _c_p, ctypes.c_size_t, _c_p]
+    L.caat_colpar_linear_bwd.restype = ctypes.c_int
     L.caat_status_string.argtypes = [ctypes.c_int]
     L.caat_status_string.restype = ctypes.c_char_p
     L.caat_get_device_status.argtypes = [_c_p]

@@ -14,15 +14,22 @@ Readings where the pages are silent:
     embeddings;
   * column-parallel layers (QKV, MLP up) give rank r its heads / its FFN slice,
     computed from rank r's own residual copy;
-  * the row-parallel layers run the library's fused GEMM + partial reduce (the
-    backward reduces the upstream gradient with the same S);
+  * the row-parallel layers run the library's fused GEMM + partial reduce.  Where
+    the backward reduce sits is a reading ("forward and backward must agree"):
+    placement "reduce_dout" (default) is the exact gradient, the row-parallel
+    backward reducing its upstream gradient over S; placement "column" is
+    Megatron's, the row-parallel backward passing each rank's gradient through and
+    the column-parallel layers (QKV, MLP up) reducing their input gradient over S
+    in the library's column-parallel backward;
   * norm weights and the embedding are replicated: one parameter used by all ranks;
   * the loss needs one full reduction ("communicating only to compute the loss"):
     the ranks' final residual copies are averaged, then LayerNorm, the tied LM head
     and next-token cross-entropy.
 
-Only the two row-parallel layers per block run in this library's kernels;
-attention, norms, GELU, embedding and loss are PyTorch ops of the harness.
+The row-parallel layers (and, with placement "column", the column-parallel ones)
+run in this library's kernels; attention, norms, GELU, embedding and loss are
+PyTorch ops of the harness.  Column-parallel weights are stored [h, K] with column
+block r owned by rank r (K contiguous: the layout the library's kernels take).
 """
 import math
 
@@ -30,32 +37,52 @@ import torch
 import torch.nn as nn
 import torch.nn.functional as F
 
-from . import CAAT_BWD_REDUCE_DOUT, rowpar_linear_bwd, rowpar_linear_fwd
+from . import (CAAT_BWD_NO_REDUCE, CAAT_BWD_REDUCE_DOUT, colpar_linear_bwd, colpar_linear_fwd,
+               rowpar_linear_bwd, rowpar_linear_fwd)
 
 
 class RowParallelPCR(torch.autograd.Function):
     """Y[r] = PCR_S(X_r W_r) for the t ranks (rank r's input is column block r of X).
 
     X: [N, K]; W: logical [K, h] (an nn.Linear weight [h, K] passed as .t());
-    sel: S as a device index tensor or an int n (S = first n channels).
+    sel: S as a device index tensor or an int n (S = first n channels);
+    mode: the backward's CAAT_BWD_REDUCE_DOUT or CAAT_BWD_NO_REDUCE.
     Returns Y [t, N, h]."""
 
     @staticmethod
-    def forward(ctx, X, W, t, sel):
+    def forward(ctx, X, W, t, sel, mode=CAAT_BWD_REDUCE_DOUT):
         N = X.shape[0]
         h = W.shape[1]
         Y = torch.empty((t, N, h), dtype=X.dtype, device=X.device)
         rowpar_linear_fwd(X, W, t, sel, outs=list(Y.unbind(0)))
         ctx.save_for_backward(X, W)
-        ctx.t, ctx.sel = t, sel
+        ctx.t, ctx.sel, ctx.mode = t, sel, mode
         return Y
 
     @staticmethod
     def backward(ctx, dY):
         X, W = ctx.saved_tensors
         dY = dY.contiguous()
-        dX, dW = rowpar_linear_bwd(X, W, list(dY.unbind(0)), ctx.t, ctx.sel, CAAT_BWD_REDUCE_DOUT)
-        return dX, dW, None, None
+        dX, dW = rowpar_linear_bwd(X, W, list(dY.unbind(0)), ctx.t, ctx.sel, ctx.mode)
+        return dX, dW, None, None, None
+
+
+class ColParallelPCR(torch.autograd.Function):
+    """Z[:, block r] = A_r W1_r for the t ranks (A [t, N, h]: rank r's own input;
+    W1 [h, K], block r of its columns = rank r's).  The backward reduces the input
+    gradient over S: dA_r = PCR_S(dZ_r W1_r^T).  Returns Z [N, K]."""
+
+    @staticmethod
+    def forward(ctx, A, W1, t, sel):
+        ctx.save_for_backward(A, W1)
+        ctx.t, ctx.sel = t, sel
+        return colpar_linear_fwd(A, W1, t)
+
+    @staticmethod
+    def backward(ctx, dZ):
+        A, W1 = ctx.saved_tensors
+        dA, dW1 = colpar_linear_bwd(A, W1, dZ.contiguous(), ctx.t, ctx.sel)
+        return dA, dW1, None, None
 
 
 def rope_tables(seq, hd, device, dtype, base=10000.0):
@@ -72,48 +99,61 @@ def apply_rope(x, cos, sin):
     return torch.stack((r1, r2), dim=-1).flatten(-2)
 
 
+PLACEMENTS = ("reduce_dout", "column")
+
+
 class Block(nn.Module):
-    def __init__(self, h, heads, ffn, t, sel, std=0.02):
+    def __init__(self, h, heads, ffn, t, sel, std=0.02, placement="reduce_dout"):
         super().__init__()
-        assert heads % t == 0 and ffn % t == 0 and h % heads == 0
+        assert heads % t == 0 and ffn % t == 0 and h % heads == 0 and placement in PLACEMENTS
         self.h, self.heads, self.ffn, self.t, self.sel = h, heads, ffn, t, sel
+        self.placement = placement
         self.hd = h // heads
         self.ln1 = nn.LayerNorm(h)
         self.ln2 = nn.LayerNorm(h)
-        # column-parallel: rank r's slice of the QKV / up projection, [t, h, cols/t]
-        self.wqkv = nn.Parameter(torch.randn(t, h, 3 * h // t) * std)
-        self.w1 = nn.Parameter(torch.randn(t, h, ffn // t) * std)
+        # column-parallel, [in = h, out = K]; column block r = rank r's heads / FFN slice
+        self.wqkv = nn.Parameter(torch.randn(h, 3 * h) * std)
+        self.w1 = nn.Parameter(torch.randn(h, ffn) * std)
         # row-parallel, nn.Linear layout [out = h, in = K]; K shard r = rank r's heads / FFN slice
         self.wo = nn.Parameter(torch.randn(h, h) * std)
         self.w2 = nn.Parameter(torch.randn(h, ffn) * std)
 
+    def _colpar(self, a, W1):
+        """[t, N, h] -> [t, N, K/t]: rank r's input times its column block."""
+        t, N, h = a.shape
+        kt = W1.shape[1] // t
+        if self.placement == "column":
+            return ColParallelPCR.apply(a, W1, t, self.sel).view(N, t, kt).transpose(0, 1)
+        return torch.bmm(a, W1.view(h, t, kt).transpose(0, 1))
+
     def forward(self, x, cos, sin, batch, seq):
         t, N, h = x.shape
         hpr = self.heads // t                              # heads per rank
-        a = self.ln1(x)
-        qkv = torch.bmm(a, self.wqkv)                      # [t, N, 3 h/t]
-        qkv = qkv.view(t, batch, seq, 3, hpr, self.hd).permute(3, 0, 1, 4, 2, 5)
+        mode = CAAT_BWD_NO_REDUCE if self.placement == "column" else CAAT_BWD_REDUCE_DOUT
+        qkv = self._colpar(self.ln1(x), self.wqkv)         # [t, N, 3 h/t]
+        qkv = qkv.reshape(t, batch, seq, 3, hpr, self.hd).permute(3, 0, 1, 4, 2, 5)
         q, k, v = (z.reshape(t * batch, hpr, seq, self.hd) for z in qkv)
         q, k = apply_rope(q, cos, sin), apply_rope(k, cos, sin)
         o = F.scaled_dot_product_attention(q, k, v, is_causal=True)   # [t*B, hpr, S, hd]
         o = o.view(t, batch, hpr, seq, self.hd).permute(1, 3, 0, 2, 4).reshape(N, h)
-        x = x + RowParallelPCR.apply(o, self.wo.t(), t, self.sel)
-        b = self.ln2(x)
-        u = F.gelu(torch.bmm(b, self.w1))                  # [t, N, ffn/t]
-        u = u.permute(1, 0, 2).reshape(N, self.ffn)        # column block r = rank r
-        return x + RowParallelPCR.apply(u, self.w2.t(), t, self.sel)
+        x = x + RowParallelPCR.apply(o, self.wo.t(), t, self.sel, mode)
+        u = F.gelu(self._colpar(self.ln2(x), self.w1))     # [t, N, ffn/t]
+        u = u.transpose(0, 1).reshape(N, self.ffn)         # column block r = rank r
+        return x + RowParallelPCR.apply(u, self.w2.t(), t, self.sel, mode)
 
 
 class CAATNet(nn.Module):
     """Token ids [batch, seq] -> mean next-token cross-entropy."""
 
     def __init__(self, vocab=32000, h=768, heads=16, layers=12, ffn=3072, t=8, p=0.5, seq=1024,
-                 std=0.02):
+                 std=0.02, placement="reduce_dout"):
         super().__init__()
         self.t, self.h, self.heads, self.seq = t, h, heads, seq
+        self.placement = placement
         self.n_sel = int(math.floor(p * h + 0.5))          # contiguous S = first n_sel channels
         self.emb = nn.Parameter(torch.randn(vocab, h) * std)
-        self.blocks = nn.ModuleList([Block(h, heads, ffn, t, self.n_sel, std) for _ in range(layers)])
+        self.blocks = nn.ModuleList([Block(h, heads, ffn, t, self.n_sel, std, placement)
+                                     for _ in range(layers)])
         self.ln_f = nn.LayerNorm(h)
 
     def forward(self, tokens):

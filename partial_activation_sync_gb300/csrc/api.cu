@@ -194,6 +194,63 @@ size_t wacc_region_bytes(int64_t K, int64_t h, caat_dtype dt)
     return ((size_t)K * (size_t)h * 4 + 255) / 256 * 256;
 }
 
+
+// dX[:, shard r] = dY_r W_r^T and dW[shard r, :] = X_r^T dY_r for every rank
+// (dY: t pointers [N, h], row stride ld_dy).  A null dX or dW skips that
+// product; X is read only for dW, W only for dX.
+caat_status rowpar_grads(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt, const void *X,
+                         int64_t ldx, const void *W, int64_t w_rs, int64_t w_cs, const ConstPtrs &dy,
+                         int64_t ld_dy, void *dX, int64_t lddx, void *dW, int64_t dw_rs,
+                         int64_t dw_cs, float *wacc, cudaStream_t s)
+{
+    if (K == 0) return CAAT_OK;   // dX has no columns, dW no rows
+    const int64_t es = elem_size(dt);
+    const int64_t kt = K / t;
+    caat_status st;
+    if (dt == CAAT_BF16 && (dX == nullptr || w_rs == 1) && (dW == nullptr || dw_rs == 1) && N > 0 &&
+        h > 0 &&
+        bwd_tc_supported(t, N, K, h, X, dW != nullptr ? ldx : 0, W, dX != nullptr ? w_cs : 0, dy, ld_dy,
+                         dX, dX != nullptr ? lddx : 0, dW, dW != nullptr ? dw_cs : 0)) {
+        st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs, wacc, 0,
+                                  nullptr, 0, s);
+        if (st != CAAT_ERR_UNSUPPORTED) return st;
+    }
+    if (h == 0) {
+        // no channels: the gradient of X is zero and dW has no columns
+        if (dX != nullptr && N > 0 &&
+            cudaMemset2DAsync(dX, (size_t)(lddx * es), 0, (size_t)(K * es), (size_t)N, s) != cudaSuccess)
+            return CAAT_ERR_CUDA;
+        return CAAT_OK;
+    }
+    if (dX != nullptr) {
+        // dX[:, shard r] = dY_r W_r^T : M = N, Nn = kt, Kk = h
+        BatchedGemm gx{};
+        gx.batches = t; gx.M = N; gx.Nn = kt; gx.Kk = h; gx.dt = dt;
+        gx.sa0 = ld_dy; gx.sa1 = 1;
+        gx.sb0 = w_cs; gx.sb1 = w_rs;
+        gx.sc0 = lddx; gx.sc1 = 1;
+        for (int r = 0; r < t; ++r) {
+            gx.A.p[r] = dy.p[r];
+            gx.B.p[r] = (const char *)W + (size_t)(r * kt * w_rs * es);
+            gx.C.p[r] = (char *)dX + (size_t)(r * kt * es);
+        }
+        st = launch_batched_gemm_simt(gx, s);   // no-op when N == 0
+        if (st != CAAT_OK) return st;
+    }
+    if (dW == nullptr) return CAAT_OK;
+    // dW[shard r, :] = X_r^T dY_r : M = kt, Nn = h, Kk = N
+    BatchedGemm gw{};
+    gw.batches = t; gw.M = kt; gw.Nn = h; gw.Kk = N; gw.dt = dt;
+    gw.sa0 = 1; gw.sa1 = ldx;
+    gw.sb0 = ld_dy; gw.sb1 = 1;
+    gw.sc0 = dw_rs; gw.sc1 = dw_cs;
+    for (int r = 0; r < t; ++r) {
+        gw.A.p[r] = (const char *)X + (size_t)(r * kt * es);
+        gw.B.p[r] = dy.p[r];
+        gw.C.p[r] = (char *)dW + (size_t)(r * kt * dw_rs * es);
+    }
+    return launch_batched_gemm_simt(gw, s);   // N == 0 (empty sum) writes zeros
+}
 }  // namespace
 
 extern "C" size_t caat_rowpar_linear_bwd_workspace(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
@@ -239,8 +296,6 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
         wacc = (float *)((char *)workspace + need);
 
     const cudaStream_t s = (cudaStream_t)stream;
-    const int64_t es = elem_size(dt);
-    const int64_t kt = K / t;
     ConstPtrs dy{};
     int64_t ld_dy = ld_dout;
 
@@ -276,45 +331,99 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
     } else {
         for (int r = 0; r < t; ++r) dy.p[r] = dOut[r];
     }
-    if (K == 0) return CAAT_OK;   // dX has no columns, dW no rows
+    return rowpar_grads(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, dy, ld_dy, dX, lddx, dW, dw_rs, dw_cs,
+                        wacc, s);
+}
 
-    if (dt == CAAT_BF16 && w_rs == 1 && dw_rs == 1 && N > 0 && h > 0 &&
-        bwd_tc_supported(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs)) {
-        st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs, wacc, 0,
-                                  nullptr, 0, s);
-        if (st != CAAT_ERR_UNSUPPORTED) return st;
-    }
 
-    // dX[:, shard r] = dY_r W_r^T : M = N, Nn = kt, Kk = h
-    BatchedGemm gx{};
-    gx.batches = t; gx.M = N; gx.Nn = kt; gx.Kk = h; gx.dt = dt;
-    gx.sa0 = ld_dy; gx.sa1 = 1;
-    gx.sb0 = w_cs; gx.sb1 = w_rs;
-    gx.sc0 = lddx; gx.sc1 = 1;
-    for (int r = 0; r < t; ++r) {
-        gx.A.p[r] = dy.p[r];
-        gx.B.p[r] = (const char *)W + (size_t)(r * kt * w_rs * es);
-        gx.C.p[r] = (char *)dX + (size_t)(r * kt * es);
-    }
-    if (h == 0) {
-        // no channels: the gradient of X is zero and dW has no columns
-        if (N > 0 && cudaMemset2DAsync(dX, (size_t)(lddx * es), 0, (size_t)(K * es), (size_t)N, s) != cudaSuccess)
-            return CAAT_ERR_CUDA;
-        return CAAT_OK;
-    }
-    st = launch_batched_gemm_simt(gx, s);   // no-op when N == 0
+// ------------------------------------------------- column-parallel layer
+// The column-parallel layer is the row-parallel one seen through W = W1^T
+// (logical [K, h], strides (w1_cs, w1_rs)): its forward is the dX product of the
+// row-parallel backward with dY_r = A_r, its input gradient is the fused
+// row-parallel forward on dZ (GEMM + partial reduce), its weight gradient the dW
+// product with X = dZ and dY_r = A_r.
+
+namespace {
+
+caat_status check_colpar_inputs(int t, int64_t N, int64_t h, const void *const *A, int64_t lda)
+{
+    if (A == nullptr || lda < h) return CAAT_ERR_INVALID_ARG;
+    for (int r = 0; r < t; ++r)
+        if (N > 0 && h > 0 && A[r] == nullptr) return CAAT_ERR_INVALID_ARG;
+    return CAAT_OK;
+}
+
+}  // namespace
+
+extern "C" caat_status caat_colpar_linear_fwd(int t, int64_t N, int64_t h, int64_t K, caat_dtype dt,
+                                              const void *const *A, int64_t lda,
+                                              const void *W1, int64_t w1_rs, int64_t w1_cs,
+                                              void *Z, int64_t ldz, caat_stream_t stream)
+{
+    caat_status st = check_layer_args(t, N, K, h, dt, Z, ldz, W1, w1_cs, w1_rs, nullptr, 0);
     if (st != CAAT_OK) return st;
-
-    // dW[shard r, :] = X_r^T dY_r : M = kt, Nn = h, Kk = N
-    BatchedGemm gw{};
-    gw.batches = t; gw.M = kt; gw.Nn = h; gw.Kk = N; gw.dt = dt;
-    gw.sa0 = 1; gw.sa1 = ldx;
-    gw.sb0 = ld_dy; gw.sb1 = 1;
-    gw.sc0 = dw_rs; gw.sc1 = dw_cs;
+    st = check_colpar_inputs(t, N, h, A, lda);
+    if (st != CAAT_OK) return st;
+    const int64_t es = elem_size(dt);
+    const Span sz = span_of(Z, N, K, ldz, es);
+    ConstPtrs a{};
     for (int r = 0; r < t; ++r) {
-        gw.A.p[r] = (const char *)X + (size_t)(r * kt * es);
-        gw.B.p[r] = dy.p[r];
-        gw.C.p[r] = (char *)dW + (size_t)(r * kt * dw_rs * es);
+        if (overlap(sz, span_of(A[r], N, h, lda, es))) return CAAT_ERR_INVALID_ARG;
+        a.p[r] = A[r];
     }
-    return launch_batched_gemm_simt(gw, s);
+    if (N == 0) return CAAT_OK;
+    return rowpar_grads(t, N, K, h, dt, nullptr, 0, W1, w1_cs, w1_rs, a, lda, Z, ldz, nullptr, 0, 0,
+                        nullptr, (cudaStream_t)stream);
+}
+
+extern "C" size_t caat_colpar_linear_bwd_workspace(int t, int64_t N, int64_t h, int64_t K, caat_dtype dt)
+{
+    if (t < 1 || t > CAAT_MAX_T || N < 0 || K < 0 || h < 0 || !valid_dtype(dt)) return 0;
+    return wacc_region_bytes(K, h, dt);
+}
+
+extern "C" caat_status caat_colpar_linear_bwd(int t, int64_t N, int64_t h, int64_t K, caat_dtype dt,
+                                              const void *const *A, int64_t lda,
+                                              const void *W1, int64_t w1_rs, int64_t w1_cs,
+                                              const void *dZ, int64_t ldz,
+                                              void *const *dA, int64_t ldda,
+                                              void *dW1, int64_t dw1_rs, int64_t dw1_cs,
+                                              const int32_t *sel, int64_t n_sel,
+                                              void *workspace, size_t ws_bytes, caat_stream_t stream)
+{
+    caat_status st = check_layer_args(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, sel, n_sel);
+    if (st != CAAT_OK) return st;
+    st = check_colpar_inputs(t, N, h, A, lda);
+    if (st != CAAT_OK) return st;
+    if (dA == nullptr || ldda < h) return CAAT_ERR_INVALID_ARG;
+    if (K > 0 && h > 0) {
+        if (dW1 == nullptr || dw1_rs < 1 || dw1_cs < 1) return CAAT_ERR_INVALID_ARG;
+        // logical dW = dW1^T: (k, c) strides (dw1_cs, dw1_rs)
+        const int64_t a0 = dw1_cs, a1 = dw1_rs;
+        const bool ok = (a1 == 1 && a0 >= h) || (a0 == 1 && a1 >= K) || (a0 >= h * a1) || (a1 >= K * a0);
+        if (!ok) return CAAT_ERR_INVALID_ARG;
+    }
+    const int64_t es = elem_size(dt);
+    ConstPtrs a{};
+    for (int r = 0; r < t; ++r) {
+        if (N > 0 && h > 0 && dA[r] == nullptr) return CAAT_ERR_INVALID_ARG;
+        const Span sr = span_of(dA[r], N, h, ldda, es);
+        for (int q = 0; q < t; ++q) {
+            if (overlap(sr, span_of(A[q], N, h, lda, es))) return CAAT_ERR_INVALID_ARG;
+            if (q > r && overlap(sr, span_of(dA[q], N, h, ldda, es))) return CAAT_ERR_INVALID_ARG;
+        }
+        if (overlap(sr, span_of(dZ, N, K, ldz, es))) return CAAT_ERR_INVALID_ARG;
+        a.p[r] = A[r];
+    }
+    float *wacc = nullptr;
+    if (workspace != nullptr && ((uintptr_t)workspace & 255) == 0 && wacc_region_bytes(K, h, dt) > 0 &&
+        ws_bytes >= wacc_region_bytes(K, h, dt))
+        wacc = (float *)workspace;
+    const cudaStream_t s = (cudaStream_t)stream;
+    // dW1 = A_r^T dZ_r per block (the dW product with X = dZ, dY_r = A_r)
+    st = rowpar_grads(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, a, lda, nullptr, 0, dW1, dw1_cs, dw1_rs,
+                      wacc, s);
+    if (st != CAAT_OK) return st;
+    // dA = PCR_S(dZ_r W1_r^T): the fused row-parallel forward on (dZ, W1^T)
+    return caat_rowpar_linear_fwd(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, dA, ldda, sel, n_sel, stream);
 }

@@ -384,6 +384,7 @@ bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int
 
 // dX[:, shard r] = dY_r W_r^T and dW[shard r, :] = X_r^T dY_r for every rank.
 // W and dW are in the nn.Linear layout ([h, K] storage, row stride ldw / ld_dw).
+// A null dX or dW skips that product (the column-parallel layer uses one at a time).
 caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
                                  void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
@@ -412,7 +413,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     };
 
     // ---- dX = dY_r W_r^T: A = dY_r (K-major), B = W_r^T (MN-major)
-    {
+    if (dX != nullptr) {
         TmapArray am;
         CUtensorMap sm;
         if (!grad_maps(am, sm, 64, BM)) return CAAT_ERR_UNSUPPORTED;
@@ -441,6 +442,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const caat_status st = launch_grouped<false, false>(am, sm, bm, cm, p, s, "rowpar_bwd_dx_tc");
         if (st != CAAT_OK) return st;
     }
+    if (dW == nullptr) return CAAT_OK;
     // ---- dW^T = dY_r^T X_r: A = dY_r^T (MN-major), B = X_r (MN-major)
     {
         TmapArray am;

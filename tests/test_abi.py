@@ -126,6 +126,44 @@ def test_layer_rejects_bad_args_without_launch(lib):
              sel, 2, 9, None, 0, None) == 1
 
 
+def test_colpar_rejects_bad_args_without_launch(lib):
+    A0, A1, W1, Z = 1 << 20, 2 << 20, 3 << 20, 4 << 20
+    sel = ctypes.c_void_p(5 << 20)
+    f = lib.caat_colpar_linear_fwd
+    # K % t != 0
+    assert f(2, 4, 8, 7, 1, _ptrs([A0, A1]), 8, W1, 7, 1, Z, 7, None) == 1
+    # lda < h
+    assert f(2, 4, 8, 8, 1, _ptrs([A0, A1]), 4, W1, 8, 1, Z, 8, None) == 1
+    # ldz < K
+    assert f(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, Z, 4, None) == 1
+    # W1 strides that alias elements
+    assert f(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 1, 1, Z, 8, None) == 1
+    # Z overlaps an input
+    assert f(2, 4, 8, 8, 1, _ptrs([A0, Z]), 8, W1, 8, 1, Z, 8, None) == 1
+    # null input pointer
+    assert f(2, 4, 8, 8, 1, _ptrs([A0, 0]), 8, W1, 8, 1, Z, 8, None) == 1
+    g = lib.caat_colpar_linear_bwd
+    dZ, dA0, dA1, dW1 = 6 << 20, 7 << 20, 8 << 20, 9 << 20
+    # optional fp32 accumulator of dW1 [8, 8]: 256 bytes; none for fp32
+    assert lib.caat_colpar_linear_bwd_workspace(2, 4, 8, 8, 1) == 256
+    assert lib.caat_colpar_linear_bwd_workspace(2, 4, 8, 8, 0) == 0
+    # dA outputs overlap each other
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA0]), 8,
+             dW1, 8, 1, sel, 2, None, 0, None) == 1
+    # dA overlaps an input
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, A1]), 8,
+             dW1, 8, 1, sel, 2, None, 0, None) == 1
+    # n_sel > h
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA1]), 8,
+             dW1, 8, 1, sel, 9, None, 0, None) == 1
+    # dW1 strides that alias elements
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA1]), 8,
+             dW1, 1, 1, sel, 2, None, 0, None) == 1
+    # ldda < h
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA1]), 4,
+             dW1, 8, 1, sel, 2, None, 0, None) == 1
+
+
 def test_status_strings(lib):
     for code in range(5):
         assert lib.caat_status_string(code).startswith(b"CAAT_")

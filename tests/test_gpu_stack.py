@@ -1,10 +1,11 @@
 """The CAAT-Net block stack on the GPU (row-parallel layers in this library's
 kernels, the rest PyTorch) against the float64 CPU reference of the stack.
 
-Reduced stack: 2 layers, sequence 64, batch 2, vocabulary 1024, with the 130M
-model's width (h = 768, 16 heads, FFN 3072), t = 8, p = 0.5.  Tolerances are
-relative, set by bf16 activations through two blocks: 2e-2 on the loss, 8e-2
-(relative Frobenius) on parameter gradients."""
+Both placements of the backward reduce are checked, each against the reference's
+matching placement.  Reduced stack: 2 layers, sequence 64, batch 2, vocabulary
+1024, with the 130M model's width (h = 768, 16 heads, FFN 3072), t = 8, p = 0.5.
+Tolerances are relative, set by bf16 activations through two blocks: 2e-2 on the
+loss, 8e-2 (relative Frobenius) on parameter gradients."""
 import numpy as np
 import pytest
 
@@ -13,14 +14,16 @@ from tests.gpu_helpers import rel_fro, torch
 pytestmark = pytest.mark.gpu
 
 
-def test_stack_loss_and_gradients_match_reference():
+@pytest.mark.parametrize("placement", ["reduce_dout", "column"])
+def test_stack_loss_and_gradients_match_reference(placement):
     T = torch()
     from oracle import stack as ost
     from partial_activation_sync_gb300.caatnet import CAATNet
     import partial_activation_sync_gb300 as caat
     T.manual_seed(1234)
     t, heads, layers, seq, batch, vocab = 8, 16, 2, 64, 2, 1024
-    model = CAATNet(vocab=vocab, h=768, heads=heads, layers=layers, ffn=3072, t=t, p=0.5, seq=seq)
+    model = CAATNet(vocab=vocab, h=768, heads=heads, layers=layers, ffn=3072, t=t, p=0.5, seq=seq,
+                    placement=placement)
     model = model.cuda().to(T.bfloat16)
     tokens = T.from_numpy(np.random.default_rng(7).integers(0, vocab, (batch, seq))).cuda()
     loss = model(tokens)
@@ -28,18 +31,20 @@ def test_stack_loss_and_gradients_match_reference():
     T.cuda.synchronize()
     assert caat.device_status() == 0
     params = {n: p.detach().double().cpu() for n, p in model.named_parameters()}
-    L, grads = ost.loss_and_grads(params, tokens.cpu(), t, heads, layers, model.n_sel)
+    L, grads = ost.loss_and_grads(params, tokens.cpu(), t, heads, layers, model.n_sel, placement)
     assert abs(float(loss) - L) <= 2e-2 * abs(L), (float(loss), L)
     for name, p in model.named_parameters():
         g = p.grad.double().cpu().numpy()
         assert rel_fro(g, grads[name].numpy()) <= 8e-2, name
 
 
-def test_stack_training_step_runs():
+@pytest.mark.parametrize("placement", ["reduce_dout", "column"])
+def test_stack_training_step_runs(placement):
     T = torch()
     from partial_activation_sync_gb300.caatnet import CAATNet, train_step
     T.manual_seed(5)
-    model = CAATNet(vocab=512, h=768, heads=16, layers=1, ffn=3072, t=8, p=0.5, seq=128).cuda().to(T.bfloat16)
+    model = CAATNet(vocab=512, h=768, heads=16, layers=1, ffn=3072, t=8, p=0.5, seq=128,
+                    placement=placement).cuda().to(T.bfloat16)
     opt = T.optim.AdamW(model.parameters(), lr=1e-3)
     tokens = T.randint(0, 512, (2, 128), device="cuda")
     l0 = float(train_step(model, opt, tokens))

@@ -69,8 +69,8 @@ def _tiny_params(t=2, h=8, heads=2, ffn=16, vocab=16, layers=1, seed=5):
         p[pre + "ln1.bias"] = 0.1 * torch.randn(h, generator=g, dtype=torch.float64)
         p[pre + "ln2.weight"] = 1 + 0.1 * torch.randn(h, generator=g, dtype=torch.float64)
         p[pre + "ln2.bias"] = 0.1 * torch.randn(h, generator=g, dtype=torch.float64)
-        p[pre + "wqkv"] = 0.3 * torch.randn(t, h, 3 * h // t, generator=g, dtype=torch.float64)
-        p[pre + "w1"] = 0.3 * torch.randn(t, h, ffn // t, generator=g, dtype=torch.float64)
+        p[pre + "wqkv"] = 0.3 * torch.randn(h, 3 * h, generator=g, dtype=torch.float64)
+        p[pre + "w1"] = 0.3 * torch.randn(h, ffn, generator=g, dtype=torch.float64)
         p[pre + "wo"] = 0.3 * torch.randn(h, h, generator=g, dtype=torch.float64)
         p[pre + "w2"] = 0.3 * torch.randn(h, ffn, generator=g, dtype=torch.float64)
     return p
@@ -94,7 +94,7 @@ def test_loss_gradients_match_finite_differences():
     tokens = torch.tensor([[1, 5, 3, 9], [2, 2, 7, 0]])
     L, grads = ost.loss_and_grads(params, tokens, t, heads, layers, 4)
     eps = 1e-6
-    for name, idx in [("blocks.0.wo", (1, 2)), ("blocks.0.w2", (3, 5)), ("blocks.0.wqkv", (1, 2, 4)),
+    for name, idx in [("blocks.0.wo", (1, 2)), ("blocks.0.w2", (3, 5)), ("blocks.0.wqkv", (1, 20)),
                       ("emb", (5, 1)), ("blocks.0.ln1.weight", (3,))]:
         pp = {k: v.clone() for k, v in params.items()}
         pm = {k: v.clone() for k, v in params.items()}
@@ -102,3 +102,63 @@ def test_loss_gradients_match_finite_differences():
         pm[name][idx] -= eps
         fd = (float(ost.loss(pp, tokens, t, heads, layers, 4)) - float(ost.loss(pm, tokens, t, heads, layers, 4))) / (2 * eps)
         assert abs(fd - float(grads[name][idx])) <= 1e-6 * (1 + abs(fd)), name
+
+
+SHARDED = ("wqkv", "wo", "w1", "w2")
+
+
+def test_column_placement_at_empty_set_is_the_exact_gradient():
+    # S empty: neither placement reduces anything, so the column placement's
+    # explicit backward must equal autograd's exact gradient.
+    t, heads, layers = 2, 2, 2
+    params = _tiny_params(layers=layers)
+    tokens = torch.tensor([[1, 5, 3, 9], [2, 2, 7, 0]])
+    L0, g0 = ost.loss_and_grads(params, tokens, t, heads, layers, 0)
+    L1, g1 = ost.loss_and_grads(params, tokens, t, heads, layers, 0, "column")
+    assert L0 == L1
+    for k in params:
+        torch.testing.assert_close(g1[k], g0[k], rtol=1e-10, atol=1e-12)
+
+
+def test_column_placement_at_full_set_is_megatron():
+    # S full: every rank carries the same stream, the model is the vanilla
+    # transformer, and the exact gradient is its gradient.  Megatron's placement
+    # back-propagates 1/t of the loss gradient on each rank (the loss averages the
+    # t identical streams) and reduces only at the column-parallel inputs: the
+    # replicated parameters, summed over ranks, get the exact gradient, and each
+    # sharded weight, used by one rank only, gets exactly 1/t of it.
+    t, heads, layers = 2, 2, 2
+    params = _tiny_params(layers=layers)
+    tokens = torch.tensor([[1, 5, 3, 9], [2, 2, 7, 0]])
+    h = params["emb"].shape[1]
+    _, g0 = ost.loss_and_grads(params, tokens, t, heads, layers, h)
+    _, g1 = ost.loss_and_grads(params, tokens, t, heads, layers, h, "column")
+    for k in params:
+        scale = 1.0 / t if k.split(".")[-1] in SHARDED else 1.0
+        torch.testing.assert_close(g1[k], scale * g0[k], rtol=1e-9, atol=1e-12)
+
+
+def test_column_placement_differs_at_partial_set():
+    # 0 < p < 1 with a norm between the layers: the placements differ (they are
+    # different readings, not one gradient computed two ways)
+    t, heads, layers = 2, 2, 1
+    params = _tiny_params(layers=layers)
+    tokens = torch.tensor([[1, 5, 3, 9], [2, 2, 7, 0]])
+    _, g0 = ost.loss_and_grads(params, tokens, t, heads, layers, 4)
+    _, g1 = ost.loss_and_grads(params, tokens, t, heads, layers, 4, "column")
+    assert (g1["blocks.0.w1"] - g0["blocks.0.w1"]).abs().max() > 1e-6
+
+
+def test_column_layer_matches_c_oracle():
+    g = _r(11)
+    for t, N, h, K, s in [(2, 5, 6, 8, 3), (4, 3, 8, 16, 0), (3, 4, 6, 9, 6)]:
+        A = torch.randn(t, N, h, generator=g, dtype=torch.float64, requires_grad=True)
+        W1 = torch.randn(h, K, generator=g, dtype=torch.float64, requires_grad=True)
+        dZ = torch.randn(N, K, generator=g, dtype=torch.float64)
+        Z = ost.ColReduce.apply(A, W1, t, s)
+        Z.backward(dZ)
+        np.testing.assert_allclose(Z.detach().numpy(), orc.colpar_fwd(A.detach().numpy(), W1.detach().numpy(), t),
+                                   rtol=1e-12, atol=1e-12)
+        wA, wW = orc.colpar_bwd(A.detach().numpy(), W1.detach().numpy(), dZ.numpy(), t, np.arange(s))
+        np.testing.assert_allclose(A.grad.numpy(), wA, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(W1.grad.numpy(), wW, rtol=1e-12, atol=1e-12)
