@@ -162,8 +162,16 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
     if (N == 0 || h == 0) return CAAT_OK;
     const cudaStream_t s = (cudaStream_t)stream;
     if (dt == CAAT_BF16 && w_rs == 1 && K > 0) {
-        // a few tokens: weight streaming on the CUDA cores; otherwise the
-        // tensor-core kernel (decode kernel again if that one declines)
+        // a few tokens: the swapped-operand tensor-core kernel (one cluster of
+        // shard-CTAs per channel block), else weight streaming on the CUDA cores;
+        // otherwise the tile kernel (decode kernel again if that one declines).
+        // CAAT_FWD_SKINNY=0 turns the first one off (for comparisons).
+        const char *skinny_env = std::getenv("CAAT_FWD_SKINNY");
+        const bool skinny_on = skinny_env == nullptr || std::strcmp(skinny_env, "0") != 0;
+        if (N <= 64 && skinny_on) {
+            st = launch_rowpar_fwd_skinny(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
+            if (st != CAAT_ERR_UNSUPPORTED) return st;
+        }
         if (N < 16) {
             st = launch_rowpar_fwd_decode(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
             if (st != CAAT_ERR_UNSUPPORTED) return st;

@@ -42,11 +42,14 @@ namespace caat {
 __device__ int g_caat_dev_error;
 
 caat_status read_and_clear_bwd_error();
+caat_status read_and_clear_skinny_error();
 
 caat_status read_and_clear_device_error()
 {
     const caat_status sb = read_and_clear_bwd_error();
     if (sb != CAAT_OK) return sb;
+    const caat_status ss = read_and_clear_skinny_error();
+    if (ss != CAAT_OK) return ss;
     int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_caat_dev_error, sizeof(int)) != cudaSuccess) return CAAT_ERR_CUDA;
     if (v != 0) {
@@ -227,18 +230,6 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     }
     if (PAIR) cluster_sync();        // the peer's barriers exist before anything signals them
     else __syncthreads();
-    if (p.sel == nullptr) {          // S = {0, ..., n_sel-1}
-        for (int64_t w = tid; w < words; w += NUM_THREADS) {
-            const int64_t lo = w * 32;
-            ctl->bitmap[w] = p.n_sel >= lo + 32 ? 0xffffffffu
-                           : (p.n_sel <= lo ? 0u : ((1u << (p.n_sel - lo)) - 1u));
-        }
-    } else {
-        for (int64_t i = tid; i < p.n_sel; i += NUM_THREADS) {
-            const int32_t c = p.sel[i];
-            if (c >= 0 && c < p.h) atomicOr(&ctl->bitmap[c >> 5], 1u << (c & 31));
-        }
-    }
     if (warp == 1) {
         if (PAIR) {
             tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -252,6 +243,30 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
+    if (warp != 0) {
+        // The channel bitmap of S, built by the MMA and epilogue warps while the
+        // producer already streams the first stages (it needs no bitmap): every
+        // index of S is read once, eight independent loads per thread in flight.
+        const int e = tid - 32;
+        constexpr int NB = NUM_THREADS - 32;
+        if (p.sel == nullptr) {      // S = {0, ..., n_sel-1}
+            for (int64_t w = e; w < words; w += NB) {
+                const int64_t lo = w * 32;
+                ctl->bitmap[w] = p.n_sel >= lo + 32 ? 0xffffffffu
+                               : (p.n_sel <= lo ? 0u : ((1u << (p.n_sel - lo)) - 1u));
+            }
+        } else {
+            for (int64_t i0 = e; i0 < p.n_sel; i0 += (int64_t)NB * 8) {
+                int32_t v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) v[u] = i0 + NB * u < p.n_sel ? __ldg(p.sel + i0 + NB * u) : -1;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (v[u] >= 0 && v[u] < p.h) atomicOr(&ctl->bitmap[v[u] >> 5], 1u << (v[u] & 31));
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(NB) : "memory");   // warps 1..5
+    }
 
     // work units: (group of CLN row blocks, 256-channel block); the CTAs of a
     // cluster take the row blocks of a group

@@ -290,8 +290,10 @@ def test_bwd_tc_required_workspace_only(caat, mode):
 
 @pytest.mark.parametrize("t", [1, 2, 4, 8, 16])
 @pytest.mark.parametrize("N", [1, 3, 8, 9, 15])
-def test_fwd_decode_parity(caat, t, N):
-    """Few tokens: the weight-streaming decode kernel (CUDA cores)."""
+def test_fwd_decode_parity(caat, t, N, monkeypatch):
+    """Few tokens: the weight-streaming decode kernel (CUDA cores; the
+    swapped-operand tensor-core kernel switched off)."""
+    monkeypatch.setenv("CAAT_FWD_SKINNY", "0")
     h = 1000 if t != 16 else 520
     kt = 96 if t <= 8 else 64
     for p in (0.0, 0.5, 1.0):
@@ -305,8 +307,10 @@ def test_fwd_decode_parity(caat, t, N):
 
 
 @pytest.mark.parametrize("N", [16, 64, 100])
-def test_fwd_small_n_tensor_core(caat, N):
-    """16 <= N < 128: the tensor-core kernel with a partly empty 128-row tile."""
+def test_fwd_small_n_tensor_core(caat, N, monkeypatch):
+    """16 <= N < 128: the tile kernel with a partly empty 128-row tile (the
+    swapped-operand kernel switched off)."""
+    monkeypatch.setenv("CAAT_FWD_SKINNY", "0")
     t, kt, h = 8, 128, 512
     for layout in (0, 1):
         got, want, S = _fwd_case(caat, t, N, kt * t, h, 0.5, layout, "bf16", "nn", seed=N)
@@ -374,3 +378,51 @@ def test_bwd_contiguous_reduce_once(caat, s, kt):
                             np.arange(s), 0)
     assert rel_fro(to_f64(dX), wX) <= TOL["bf16"]
     assert rel_fro(to_f64(dW), wW) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("t", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("N", [1, 3, 8, 15, 16, 17, 33, 48, 64])
+def test_fwd_skinny_parity(caat, t, N):
+    """Few tokens (N <= 64, t <= 8): the swapped-operand tensor-core kernel, one
+    cluster of t shard-CTAs per 128-channel block; ragged channel blocks (h = 1000)
+    and ragged shards (k_t = 136: the last 64-wide k block is part zero fill)."""
+    for h, kt in ((1000, 136), (512, 64)):
+        for p in (0.0, 0.5, 1.0):
+            for layout in (0, 1):
+                got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=13 * t + N + h)
+                assert caat.last_kernel() == "rowpar_fwd_skinny_tc"
+                for r in range(t):
+                    assert rel_fro(got[r], want[r]) <= TOL["bf16"], (h, r, p, layout)
+                for r in range(1, t):
+                    assert np.array_equal(got[r][:, S], got[0][:, S])
+
+
+def test_fwd_skinny_declines_to_other_kernels(caat):
+    """Shapes the swapped-operand kernel does not take still run: t = 16 (above
+    the portable cluster size) and k_t < 64 go to the CUDA-core decode kernel."""
+    for t, kt in ((16, 64), (8, 32)):
+        got, want, _ = _fwd_case(caat, t, 4, kt * t, 256, 0.5, 1, "bf16", "nn", seed=t + kt)
+        assert caat.last_kernel() == "rowpar_fwd_decode"
+        for r in range(t):
+            assert rel_fro(got[r], want[r]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("N", [5, 40])
+def test_fwd_skinny_output_guard(caat, N):
+    # rank outputs with a row stride wider than h and a ragged last channel block
+    # (h = 200): the padding columns must stay untouched
+    T = torch()
+    t, kt, h, ld = 4, 64, 200, 264
+    X = ci.normal(905, (N, kt * t))
+    Wl = ci.normal(906, (kt * t, h), std=0.02)
+    S = caat.select_channels(h, 0.5, 1, 6)
+    bufs = [T.full((N + 1, ld), 7.0, dtype=T.bfloat16, device="cuda") for _ in range(t)]
+    outs = [b[:N, :h] for b in bufs]
+    caat.rowpar_linear_fwd(dev(X, "bf16"), _weight(Wl, "bf16", "nn"), t, sel_dev(S), outs=outs)
+    T.cuda.synchronize()
+    assert caat.last_kernel() == "rowpar_fwd_skinny_tc"
+    for b in bufs:
+        assert bool((b[:, h:] == 7.0).all()) and bool((b[N] == 7.0).all())
+    want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), t, S)
+    for r in range(t):
+        assert rel_fro(to_f64(outs[r]), want[r]) <= TOL["bf16"]
