@@ -39,9 +39,15 @@ def _check(st: int, where: str):
         raise CaatError(st, where)
 
 
+_TORCH = None
+
+
 def _torch():
-    import torch
-    return torch
+    global _TORCH
+    if _TORCH is None:
+        import torch
+        _TORCH = torch
+    return _TORCH
 
 
 def _dtype_code(t):
@@ -53,10 +59,32 @@ def _dtype_code(t):
     raise TypeError("caat: dtype must be float32 or bfloat16, got %s" % t.dtype)
 
 
-def _stream_ptr(stream):
+def _stream_ptr(stream, like=None):
+    """The CUDA stream handle: `stream`, else torch's current stream on the device
+    of tensor `like` (read straight from torch's stream registry when it offers
+    that, which is several times cheaper than building a Stream object)."""
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream)
     torch = _torch()
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None and like is not None:
+        return ctypes.c_void_p(raw(like.get_device()))
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _same_layout(ts, first, name):
+    """Row stride shared by the 2-D tensors `ts` (all shaped, typed and strided like
+    ts[0], which `_rowmajor` checks); raises otherwise."""
+    ld = _rowmajor(ts[0], name)
+    shp, st, dt = ts[0].shape, ts[0].stride(), ts[0].dtype
+    for x in ts:
+        if x.shape != shp or x.dtype != dt or not x.is_cuda:
+            raise ValueError("caat: all %s tensors need one shape, dtype and device type" % name)
+        if x.stride() != st and _rowmajor(x, name) != ld:
+            raise ValueError("caat: all %s tensors need one row stride" % name)
+    if first is not None and tuple(shp) != tuple(first):
+        raise ValueError("caat: %s tensors must be %s" % (name, list(first)))
+    return ld
 
 
 def _rowmajor(t, name):
@@ -107,20 +135,18 @@ def partial_channel_reduce(ins, sel, outs=None, stream=None):
     if t == 0:
         raise ValueError("caat: need at least one input")
     N, h = ins[0].shape
-    ld_in = _rowmajor(ins[0], "ins[0]")
-    for x in ins:
-        if x.shape != ins[0].shape or x.dtype != ins[0].dtype or _rowmajor(x, "ins") != ld_in:
-            raise ValueError("caat: all inputs need one shape, dtype and row stride")
+    ld_in = _same_layout(ins, None, "ins")
     if outs is None:
         outs = [torch.empty_like(x) for x in ins]
-    ld_out = _rowmajor(outs[0], "outs[0]")
-    for y in outs:
-        if y.shape != ins[0].shape or y.dtype != ins[0].dtype or _rowmajor(y, "outs") != ld_out:
-            raise ValueError("caat: all outputs need the inputs' shape and dtype, one row stride")
+    if len(outs) != t:
+        raise ValueError("caat: need as many outputs as inputs")
+    ld_out = _same_layout(outs, (N, h), "outs")
+    if outs[0].dtype != ins[0].dtype:
+        raise ValueError("caat: outputs need the inputs' dtype")
     sp, ns = _sel_ptr(sel)
     st = _lib.load().caat_partial_channel_reduce(
         t, N, h, _dtype_code(ins[0]), _lib.ptr_array([x.data_ptr() for x in ins]), ld_in,
-        _lib.ptr_array([y.data_ptr() for y in outs]), ld_out, sp, ns, _stream_ptr(stream))
+        _lib.ptr_array([y.data_ptr() for y in outs]), ld_out, sp, ns, _stream_ptr(stream, ins[0]))
     _check(st, "caat_partial_channel_reduce")
     return outs
 
@@ -147,15 +173,14 @@ def rowpar_linear_fwd(X, W, t: int, sel, outs=None, stream=None):
         outs = [torch.empty((N, h), dtype=X.dtype, device=X.device) for _ in range(t)]
     if len(outs) != t:
         raise ValueError("caat: need t output tensors")
-    ldy = _rowmajor(outs[0], "outs[0]")
-    for y in outs:
-        if tuple(y.shape) != (N, h) or y.dtype != X.dtype or _rowmajor(y, "outs") != ldy:
-            raise ValueError("caat: outputs must be [N, h] of X's dtype with one row stride")
+    ldy = _same_layout(outs, (N, h), "outs")
+    if outs[0].dtype != X.dtype:
+        raise TypeError("caat: outputs must have X's dtype")
     sp, ns = _sel_ptr(sel)
     st = _lib.load().caat_rowpar_linear_fwd(
         int(t), N, K, h, _dtype_code(X), ctypes.c_void_p(X.data_ptr()), ldx,
         ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
-        _lib.ptr_array([y.data_ptr() for y in outs]), ldy, sp, ns, _stream_ptr(stream))
+        _lib.ptr_array([y.data_ptr() for y in outs]), ldy, sp, ns, _stream_ptr(stream, X))
     _check(st, "caat_rowpar_linear_fwd")
     return outs
 
@@ -176,10 +201,9 @@ def rowpar_linear_bwd(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
     w_rs, w_cs = _weight_strides(W, K, h)
     if len(dOut) != t:
         raise ValueError("caat: need t upstream gradients")
-    ldd = _rowmajor(dOut[0], "dOut[0]")
-    for g in dOut:
-        if tuple(g.shape) != (N, h) or g.dtype != X.dtype or _rowmajor(g, "dOut") != ldd:
-            raise ValueError("caat: dOut tensors must be [N, h] of X's dtype with one row stride")
+    ldd = _same_layout(dOut, (N, h), "dOut")
+    if dOut[0].dtype != X.dtype:
+        raise TypeError("caat: dOut must have X's dtype")
     if dX is None:
         dX = torch.empty((N, K), dtype=X.dtype, device=X.device)
     lddx = _rowmajor(dX, "dX")
@@ -201,7 +225,7 @@ def rowpar_linear_bwd(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
         ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
         _lib.ptr_array([g.data_ptr() for g in dOut]), ldd,
         ctypes.c_void_p(dX.data_ptr()), lddx, ctypes.c_void_p(dW.data_ptr()), dw_rs, dw_cs,
-        sp, ns, int(mode), wp, wb, _stream_ptr(stream))
+        sp, ns, int(mode), wp, wb, _stream_ptr(stream, X))
     _check(st, "caat_rowpar_linear_bwd")
     return dX, dW
 
@@ -217,10 +241,7 @@ def _rank_inputs(A, t: int, h: int, name: str):
     if len(A) != t:
         raise ValueError("caat: need t tensors in %s" % name)
     N = A[0].shape[0]
-    ld = _rowmajor(A[0], name)
-    for a in A:
-        if tuple(a.shape) != (N, h) or a.dtype != A[0].dtype or _rowmajor(a, name) != ld:
-            raise ValueError("caat: %s tensors must be [N, h] with one dtype and row stride" % name)
+    ld = _same_layout(A, (N, h), name)
     return A, N, ld
 
 
@@ -247,7 +268,7 @@ def colpar_linear_fwd(A, W1, t: int, Z=None, stream=None):
     st = _lib.load().caat_colpar_linear_fwd(
         int(t), N, h, K, _dtype_code(W1), _lib.ptr_array([a.data_ptr() for a in A]), lda,
         ctypes.c_void_p(W1.data_ptr()), w1_rs, w1_cs, ctypes.c_void_p(Z.data_ptr()),
-        _rowmajor(Z, "Z"), _stream_ptr(stream))
+        _rowmajor(Z, "Z"), _stream_ptr(stream, W1))
     _check(st, "caat_colpar_linear_fwd")
     return Z
 
@@ -288,7 +309,7 @@ def colpar_linear_bwd(A, W1, dZ, t: int, sel, dA=None, dW1=None, workspace=None,
         int(t), N, h, K, dt, _lib.ptr_array([a.data_ptr() for a in A]), lda,
         ctypes.c_void_p(W1.data_ptr()), w1_rs, w1_cs, ctypes.c_void_p(dZ.data_ptr()), ldz,
         _lib.ptr_array([g.data_ptr() for g in dAs]), ldda,
-        ctypes.c_void_p(dW1.data_ptr()), dw1_rs, dw1_cs, sp, ns, wp, wb, _stream_ptr(stream))
+        ctypes.c_void_p(dW1.data_ptr()), dw1_rs, dw1_cs, sp, ns, wp, wb, _stream_ptr(stream, W1))
     _check(st, "caat_colpar_linear_bwd")
     return ret_dA, dW1
 

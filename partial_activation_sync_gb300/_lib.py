@@ -88,7 +88,6 @@ def load(path: str = None) -> ctypes.CDLL:
 
 
 def ptr_array(ptrs):
-    arr = (ctypes.c_void_p * max(len(ptrs), 1))()
-    for i, p in enumerate(ptrs):
-        arr[i] = p
-    return arr
+    if not ptrs:
+        return (ctypes.c_void_p * 1)()
+    return (ctypes.c_void_p * len(ptrs))(*ptrs)
