@@ -300,45 +300,99 @@ def run_gpu(args, w):
 
 
 def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
-    stream = torch.cuda.current_stream()
+    """End to end through the public API with host buffers: every step copies its
+    inputs (X and the t upstream gradients of every layer) from pinned host memory
+    and reads its results (dX and dW, or rank 0's output without a backward) back.
+
+    The copies run on their own streams and overlap the compute of the neighbouring
+    steps: step i+1's inputs go in while step i computes, and step i-1's results come
+    out meanwhile.  Two device buffer sets alternate, and events order every reuse.
+    The timed region runs from before the first input copy to after the last read."""
+    comp = torch.cuda.current_stream()
+    h2d_s = torch.cuda.Stream(device=device)
+    d2h_s = torch.cuda.Stream(device=device)
     hostX = [torch.from_numpy(L.X_host.view(np.int16)).pin_memory() for L in layers]
     hostG = [[torch.from_numpy(g.view(np.int16)).pin_memory() for g in L.G_host]
              if w.backward else [] for L in layers]
-    outdX = [torch.empty(L.dX.shape, dtype=torch.int16).pin_memory() for L in layers]
-    outdW = [torch.empty(L.dWstore.shape, dtype=torch.int16).pin_memory() for L in layers]
-    outY0 = [torch.empty(L.Y[0].shape, dtype=torch.int16).pin_memory() for L in layers]
+
+    def dev_set(own):
+        """One device buffer set per layer: the layer's own buffers, or fresh ones."""
+        out = []
+        for L in layers:
+            if own:
+                out.append({"X": L.X, "G": L.G, "Y": L.Y, "dX": L.dX, "dW": L.dW, "dWs": L.dWstore})
+                continue
+            dWs = torch.empty_like(L.dWstore)
+            out.append({"X": torch.empty_like(L.X), "G": [torch.empty_like(g) for g in (L.G or [])],
+                        "Y": [torch.empty_like(y) for y in L.Y], "dX": torch.empty_like(L.dX),
+                        "dW": dWs.t(),
+                        "dWs": dWs})
+        return out
+
+    sets = [dev_set(True), dev_set(False)]
+    outs = [[{"dX": torch.empty(L.dX.shape, dtype=torch.int16).pin_memory(),
+              "dW": torch.empty(L.dWstore.shape, dtype=torch.int16).pin_memory(),
+              "Y0": torch.empty(L.Y[0].shape, dtype=torch.int16).pin_memory()} for L in layers]
+            for _ in range(2)]
     h2d = sum(x.numel() * 2 for x in hostX) + sum(g.numel() * 2 for gs in hostG for g in gs)
     if w.backward:
-        d2h = sum(x.numel() * 2 for x in outdX) + sum(x.numel() * 2 for x in outdW)
+        d2h = sum(L.dX.numel() * 2 + L.dWstore.numel() * 2 for L in layers)
     else:
-        d2h = sum(x.numel() * 2 for x in outY0)
+        d2h = sum(L.Y[0].numel() * 2 for L in layers)
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for li, L in enumerate(layers):
-            L.X.view(torch.int16).copy_(hostX[li], non_blocking=True)
+    def step(i):
+        j = i % 2
+        S, O = sets[j], outs[j]
+        with torch.cuda.stream(h2d_s):
+            if i >= 2:
+                h2d_s.wait_event(comp_done[j])          # step i-2 is done with these inputs
+            for li in range(len(layers)):
+                S[li]["X"].view(torch.int16).copy_(hostX[li], non_blocking=True)
+                for r in range(len(hostG[li])):
+                    S[li]["G"][r].view(torch.int16).copy_(hostG[li][r], non_blocking=True)
+            in_ready[j].record(h2d_s)
+        comp.wait_event(in_ready[j])
+        if i >= 2:
+            comp.wait_event(out_done[j])                # step i-2's results have been read
+        for li in range(len(layers)):
+            L, B = layers[li], S[li]
+            caat.rowpar_linear_fwd(B["X"], L.W, w.t, sel, outs=B["Y"])
             if w.backward:
-                for r in range(w.t):
-                    L.G[r].view(torch.int16).copy_(hostG[li][r], non_blocking=True)
-            caat.rowpar_linear_fwd(L.X, L.W, w.t, sel, outs=L.Y)
-            if w.backward:
-                caat.rowpar_linear_bwd(L.X, L.W, L.G, w.t, sel, caat.CAAT_BWD_REDUCE_DOUT,
-                                       dX=L.dX, dW=L.dW, workspace=ws)
-                outdX[li].copy_(L.dX.view(torch.int16), non_blocking=True)
-                outdW[li].copy_(L.dWstore.view(torch.int16), non_blocking=True)
-            else:
-                outY0[li].copy_(L.Y[0].view(torch.int16), non_blocking=True)
+                caat.rowpar_linear_bwd(B["X"], L.W, B["G"], w.t, sel, caat.CAAT_BWD_REDUCE_DOUT,
+                                       dX=B["dX"], dW=B["dW"], workspace=ws)
+        comp_done[j].record(comp)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(comp_done[j])
+            for li in range(len(layers)):
+                B = S[li]
+                if w.backward:
+                    O[li]["dX"].copy_(B["dX"].view(torch.int16), non_blocking=True)
+                    O[li]["dW"].copy_(B["dWs"].view(torch.int16), non_blocking=True)
+                else:
+                    O[li]["Y0"].copy_(B["Y"][0].view(torch.int16), non_blocking=True)
+            out_done[j].record(d2h_s)
 
-    for _ in range(max(1, args.warmup)):
-        step()
+    def run(n):
+        for i in range(n):
+            step(i)
+        comp.wait_event(out_done[(n - 1) % 2])
+        if n >= 2:
+            comp.wait_event(out_done[n % 2])
+
+    run(max(2, args.warmup))
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
+    e0.record(comp)
+    h2d_s.wait_event(e0)
+    d2h_s.wait_event(e0)
+    run(args.steps)
+    e1.record(comp)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     if dist is not None:
@@ -349,7 +403,8 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
     flops = sum(L.flops_fwd + L.flops_bwd for L in layers)
     return {"value": round(flops * args.steps * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms / args.steps, 4),
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "overlap": "inputs of step i+1 and results of step i-1 copy on two streams while step i computes"}
 
 
 def _time_call(torch, fn, reps, flush=None):
