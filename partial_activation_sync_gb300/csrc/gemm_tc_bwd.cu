@@ -45,45 +45,38 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BK = 64, MAX_STAGES = 8, MAX_BN = 256;
+constexpr int BM = 128, BK = 64, STAGES = 4, MAX_BN = 256;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr size_t SMEM_LIMIT = 227 * 1024;    // dynamic shared memory a CTA may have
+constexpr int B_MAX_BYTES = MAX_BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_MAX_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MAX_T_TC = 16;
 constexpr int STG_BYTES = 32 * 128;          // 32 rows x 64 bf16 columns
-constexpr int MAX_NBUF = 2;                  // staging buffers per epilogue warp
+constexpr int NBUF = 2;                      // staging buffers per epilogue warp
 
 struct TmapArray {
     CUtensorMap m[MAX_T_TC];
 };
 
 struct SmemCtl {
-    uint64_t full[MAX_STAGES];
-    uint64_t empty[MAX_STAGES];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort;
 };
 
-// shared memory of a launch: the ring of `nst` stages of A (128 x 64) + B (BN x 64),
-// `nbuf` staging buffers per epilogue warp, the control block
-constexpr size_t smem_bytes(int nst, int stage_bytes, int nbuf)
-{
-    return 1024 + (size_t)nst * stage_bytes + 4 * (size_t)nbuf * STG_BYTES + sizeof(SmemCtl);
-}
+constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * NBUF * STG_BYTES + sizeof(SmemCtl);
 
 struct GemmParams {
     int64_t M, Nn, Kk;  // per-rank GEMM
     int t, num_m, num_n, nkb, BN, units;
     int s_blocks;       // 64-channel blocks of the gradient read from the reduced sum (smap)
     int ksplit, kbps;   // K range split in ksplit parts of kbps k-blocks (RED only)
-    int nst, stage_bytes, nbuf;   // ring stages, bytes per stage (A + B), staging buffers per warp
-    int nacc;           // TMEM accumulators (2 alternate when 2*BN columns fit, else 1)
-    int mma_n;          // N of one MMA instruction (BN, or BN/2 for BN = 384)
-    uint32_t idesc;     // instruction descriptor for M = 128, N = mma_n
+    uint32_t idesc;
 };
 
 __device__ __forceinline__ void fail(volatile int *abort)
@@ -110,15 +103,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const int NST = p.nst, NBUF = p.nbuf;
-    const uint32_t STAGE_BYTES = (uint32_t)p.stage_bytes;
-    uint8_t *staging = base + NST * STAGE_BYTES;
+    uint8_t *staging = base + STAGES * STAGE_BYTES;
     SmemCtl *ctl = (SmemCtl *)(staging + 4 * NBUF * STG_BYTES);
     volatile int *abort = &ctl->abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int s = 0; s < NST; ++s) {
+        for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
@@ -179,7 +170,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     }
                     for (int i = 0; i < p.BN / 64; ++i)
                         tma_load_3d(smem_u32(sb + i * 8192), &bmap, fb, n0 + 64 * i, r, k0);
-                    if (++stage == NST) { stage = 0; ph ^= 1u; }
+                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                 }
             }
         }
@@ -190,9 +181,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
                 const int ks = u % p.ksplit;
                 const int kb_lo = ks * p.kbps, kb_hi = min(p.nkb, kb_lo + p.kbps);
-                const uint32_t b = au % (uint32_t)p.nacc;
-                if (!mbar_wait(smem_u32(&ctl->acc_empty[b]), ((au / (uint32_t)p.nacc) & 1u) ^ 1u, abort,
-                               WAIT_LIMIT_NS)) {
+                const uint32_t b = au & 1u;
+                if (!mbar_wait(smem_u32(&ctl->acc_empty[b]), ((au >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
                     fail(abort);
                     goto done;
                 }
@@ -210,17 +200,11 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     for (int k = 0; k < BK / 16; ++k) {
                         const uint64_t ad = A_MN ? desc_sw128(a0 + 2048u * k, 8192u, 1024u)
                                                  : desc_kmajor_sw128(a0 + 32u * k);
-                        // BN = 384: two MMAs of N = 192, on B columns 0..191 and
-                        // 192..383 (three 64-column boxes each) into adjacent TMEM columns
-                        for (int hh = 0; hh * p.mma_n < p.BN; ++hh) {
-                            const uint64_t bd = desc_sw128(b0 + (uint32_t)hh * (uint32_t)(p.mma_n / 64) * 8192u +
-                                                               2048u * k, 8192u, 1024u);
-                            mma_f16(d + (uint32_t)(hh * p.mma_n), ad, bd, p.idesc,
-                                    (kb == kb_lo && k == 0) ? 0u : 1u);
-                        }
+                        const uint64_t bd = desc_sw128(b0 + 2048u * k, 8192u, 1024u);
+                        mma_f16(d, ad, bd, p.idesc, (kb == kb_lo && k == 0) ? 0u : 1u);
                     }
                     mma_commit(smem_u32(&ctl->empty[stage]));
-                    if (++stage == NST) { stage = 0; ph ^= 1u; }
+                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
                 }
                 mma_commit(smem_u32(&ctl->acc_full[b]));
                 ++au;
@@ -236,8 +220,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             const int r = v / per_rank, rem = v - r * per_rank;
             const int mb = rem % p.num_m, nb = rem / p.num_m;
             const int64_t n0 = (int64_t)nb * p.BN;
-            const uint32_t b = au % (uint32_t)p.nacc;
-            bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au / (uint32_t)p.nacc) & 1u, abort, WAIT_LIMIT_NS);
+            const uint32_t b = au & 1u;
+            bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au >> 1) & 1u, abort, WAIT_LIMIT_NS);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 fail(abort);
@@ -259,9 +243,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     uint8_t *stg = staging + (q * NBUF + sbuf) * STG_BYTES;
                     const uint32_t stg_a = smem_u32(stg);
                     if (++sbuf == NBUF) sbuf = 0;
-                    if (lane == 0) {             // the store that last used this buffer has read it
-                        if (NBUF == 1) bulk_wait_read0(); else bulk_wait_read1();
-                    }
+                    if (lane == 0) bulk_wait_read1();
                     __syncwarp();
                     uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
 #pragma unroll
@@ -291,9 +273,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                 uint8_t *stg = staging + (q * NBUF + sbuf) * STG_BYTES;
                 const uint32_t stg_a = smem_u32(stg);
                 if (++sbuf == NBUF) sbuf = 0;
-                if (lane == 0) {                 // the store that last used this buffer has read it
-                    if (NBUF == 1) bulk_wait_read0(); else bulk_wait_read1();
-                }
+                if (lane == 0) bulk_wait_read1();   // the store that last used this buffer has read it
                 __syncwarp();
                 uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
 #pragma unroll
@@ -330,15 +310,9 @@ done:
     }
 }
 
-// Tile width over the N dimension: 384 (two MMAs of 192) when it pads no more
-// than 256-wide tiles would -- wider tiles read each A row fewer times --
-// else the 64-multiple that splits n into the fewest tiles of at most 256.
+// smallest multiple of 64 (<= 256) that covers n in as few tiles as possible
 int pick_bn(int64_t n)
 {
-    if (n > MAX_BN) {
-        const int64_t pad384 = (n + 383) / 384 * 384 - n, pad256 = (n + 255) / 256 * 256 - n;
-        if (pad384 <= pad256) return 384;
-    }
     const int64_t tiles = (n + MAX_BN - 1) / MAX_BN;
     const int64_t per = (n + tiles - 1) / tiles;
     return (int)((per + 63) / 64 * 64);
@@ -351,17 +325,6 @@ caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &smap, cons
     if (p.units <= 0) return CAAT_OK;
     const int grid = p.units < num_sms() ? p.units : num_sms();
     auto kern = grouped_gemm_tc_kernel<A_MN, RED>;
-    // as many ring stages as fit for this BN; one staging buffer per warp when
-    // that buys a stage
-    p.stage_bytes = A_BYTES + p.BN * BK * 2;
-    p.nacc = 2 * p.BN <= (int)TMEM_COLS ? 2 : 1;
-    p.nbuf = MAX_NBUF;
-    int nst = (int)((SMEM_LIMIT - smem_bytes(0, 0, MAX_NBUF)) / (size_t)p.stage_bytes);
-    const int nst1 = (int)((SMEM_LIMIT - smem_bytes(0, 0, 1)) / (size_t)p.stage_bytes);
-    if (nst1 > nst) { nst = nst1; p.nbuf = 1; }
-    p.nst = nst < MAX_STAGES ? nst : MAX_STAGES;
-    if (p.nst < 2) return CAAT_ERR_UNSUPPORTED;
-    const size_t SMEM_BYTES = smem_bytes(p.nst, p.stage_bytes, p.nbuf);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
         return CAAT_ERR_CUDA;
     kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, smap, bmap, cmap, p);
@@ -470,8 +433,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.kbps = p.nkb;
         p.s_blocks = (int)(s_sum / 64);
         p.units = t * p.num_m * p.num_n;
-        p.mma_n = BN <= MAX_BN ? BN : BN / 2;
-        p.idesc = idesc_bf16_f32(BM, p.mma_n, false, true);
+        p.idesc = idesc_bf16_f32(BM, BN, false, true);
         CUtensorMap cm;
         const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)N};
         const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)lddx * 2};
@@ -498,8 +460,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.num_n = (int)((kt + BN - 1) / BN);
         p.nkb = (int)((N + BK - 1) / BK);
         p.BN = BN;
-        p.mma_n = BN <= MAX_BN ? BN : BN / 2;
-        p.idesc = idesc_bf16_f32(BM, p.mma_n, true, true);
+        p.idesc = idesc_bf16_f32(BM, BN, true, true);
         p.s_blocks = (int)(s_sum / 64);
         const int base_units = t * p.num_m * p.num_n;
         p.ksplit = wacc != nullptr ? pick_ksplit(base_units, p.nkb) : 1;

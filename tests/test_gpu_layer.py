@@ -426,3 +426,44 @@ def test_fwd_skinny_output_guard(caat, N):
     want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), t, S)
     for r in range(t):
         assert rel_fro(to_f64(outs[r]), want[r]) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("t,N,kt,h", [(64, 9, 2, 24), (64, 130, 4, 40), (32, 3, 8, 16)])
+def test_layer_maximum_rank_count(caat, dtype, t, N, kt, h):
+    """t up to 64: forward and both backward placements on the kernels that take it."""
+    for p in (0.0, 0.5, 1.0):
+        got, want, S = _fwd_case(caat, t, N, kt * t, h, p, 1, dtype, "nn", seed=t + N)
+        for r in range(t):
+            assert rel_fro(got[r], want[r]) <= TOL[dtype], ("fwd", r, p)
+        for r in range(1, t):
+            assert np.array_equal(got[r][:, S], got[0][:, S])
+        for mode in (0, 1):
+            gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, p, 1, dtype, mode, "nn", seed=t + N)
+            assert rel_fro(gX, wX) <= TOL[dtype], ("dX", mode, p)
+            assert rel_fro(gW, wW) <= TOL[dtype], ("dW", mode, p)
+
+
+@pytest.mark.parametrize("t", [16, 17])
+def test_layer_tensor_core_rank_limit(caat, t):
+    """t = 16 is the largest rank count of the tile kernels (one output tensor map
+    per rank); t = 17 falls back to the CUDA-core kernels.  Both match the oracle."""
+    N, kt, h = 256, 64, 256
+    got, want, S = _fwd_case(caat, t, N, kt * t, h, 0.5, 1, "bf16", "nn", seed=t)
+    assert caat.last_kernel() == ("rowpar_fwd_tc" if t <= 16 else "rowpar_fwd_simt")
+    for r in range(t):
+        assert rel_fro(got[r], want[r]) <= TOL["bf16"]
+    gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, 0.5, 1, "bf16", 0, "nn", seed=t)
+    assert rel_fro(gX, wX) <= TOL["bf16"] and rel_fro(gW, wW) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("t,N,kt,h", [(2, 1, 1, 1), (3, 4, 1, 2), (1, 1, 1, 1), (4, 17, 1, 5)])
+def test_layer_degenerate_shapes(caat, dtype, t, N, kt, h):
+    """One channel, one token, one element per shard."""
+    for p in (0.0, 1.0):
+        got, want, S = _fwd_case(caat, t, N, kt * t, h, p, 0, dtype, "rm", seed=t + h)
+        for r in range(t):
+            assert rel_fro(got[r], want[r]) <= TOL[dtype]
+        gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, p, 0, dtype, 0, "rm", seed=t + h)
+        assert rel_fro(gX, wX) <= TOL[dtype] and rel_fro(gW, wW) <= TOL[dtype]

@@ -121,3 +121,22 @@ def test_full_size_sampled_rows(caat, dtype, t, N, h):
         # S channels identical on all ranks, everywhere
         for r in range(1, t):
             np.testing.assert_array_equal(got[r][:, S], got[0][:, S])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("t", [16, 32, 64])
+def test_maximum_rank_count_bitexact(caat, dtype, t):
+    """Up to the largest t the library takes (64): the rank-order fold stays exact."""
+    N, h = 19, 136
+    Y = ci.normal(23 + t, (t, N, h))
+    for p, layout in ((0.5, 0), (0.5, 1), (1.0, 0)):
+        S = caat.select_channels(h, p, layout, 4004)
+        want, _ = _ref(Y, dtype, S)
+        np.testing.assert_array_equal(_run(caat, Y, dtype, S), want)
+
+
+def test_rank_count_above_maximum_is_rejected(caat):
+    T = torch()
+    ins = [T.zeros((2, 8), device="cuda") for _ in range(65)]
+    with pytest.raises(caat.CaatError):
+        caat.partial_channel_reduce(ins, sel_dev(np.arange(4)))
