@@ -20,6 +20,9 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "caat_internal.h"
 #include "tc_ptx.cuh"
 
@@ -368,6 +371,45 @@ int pick_ksplit(int units, int nkb)
 
 }  // namespace
 
+namespace {
+
+// A second stream per host thread and device, with a fork and a join event: the
+// dW chain of the backward runs on it next to dX (they only read shared inputs),
+// so dW's CTAs take SMs as soon as dX's retire instead of after dX has drained.
+// Created on first use outside stream capture; per thread, so that concurrent
+// callers never interleave their fork/join events.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream t_side[64];
+
+SideStream *side_stream(cudaStream_t main)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    SideStream &sd = t_side[dev];
+    if (sd.s == nullptr) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(main, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone) return nullptr;
+        cudaStream_t s2 = nullptr;
+        cudaEvent_t f = nullptr, j = nullptr;
+        if (cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        if (cudaEventCreateWithFlags(&f, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&j, cudaEventDisableTiming) != cudaSuccess) {
+            if (f) cudaEventDestroy(f);
+            cudaStreamDestroy(s2);
+            return nullptr;
+        }
+        sd.s = s2;
+        sd.fork = f;
+        sd.join = j;
+    }
+    return &sd;
+}
+
+}  // namespace
+
 bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                       const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy, const void *dX,
                       int64_t lddx, const void *dW, int64_t ld_dw)
@@ -412,6 +454,22 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         return encode_tmap(&sm, dsum, 2, dims, str, box);
     };
 
+    // dW on the side stream when both products are wanted
+    cudaStream_t sw = s;
+    const char *side_env = std::getenv("CAAT_BWD_SIDE_STREAM");     // "0": one stream
+    const bool side_on = side_env == nullptr || std::strcmp(side_env, "0") != 0;
+    SideStream *side = (side_on && dX != nullptr && dW != nullptr) ? side_stream(s) : nullptr;
+    if (side != nullptr) {
+        if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+            return CAAT_ERR_CUDA;
+        sw = side->s;
+    }
+    auto join = [&](caat_status st) -> caat_status {
+        if (side == nullptr) return st;
+        if (cudaEventRecord(side->join, sw) != cudaSuccess || cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess)
+            return CAAT_ERR_CUDA;
+        return st;
+    };
     // ---- dX = dY_r W_r^T: A = dY_r (K-major), B = W_r^T (MN-major)
     if (dX != nullptr) {
         TmapArray am;
@@ -444,7 +502,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     }
     if (dW == nullptr) return CAAT_OK;
     // ---- dW^T = dY_r^T X_r: A = dY_r^T (MN-major), B = X_r (MN-major)
-    {
+    auto dw_chain = [&]() -> caat_status {
         TmapArray am;
         CUtensorMap sm;
         if (!grad_maps(am, sm, 64, 64)) return CAAT_ERR_UNSUPPORTED;
@@ -473,7 +531,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
             const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)ld_dw * 2};
             const uint32_t cbox[3] = {64, 1, 32};
             if (!encode_tmap(&cm, dW, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
-            return launch_grouped<true, false>(am, sm, bm, cm, p, s, "rowpar_bwd_dw_tc");
+            return launch_grouped<true, false>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc");
         }
         // split over tokens: fp32 partials reduce-added into wacc [h, K], then one
         // rounding to bf16 into dW
@@ -482,16 +540,17 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint64_t cstr[2] = {(uint64_t)kt * 4, (uint64_t)K * 4};
         const uint32_t cbox[3] = {32, 1, 32};
         if (!encode_tmap(&cm, wacc, 3, cdims, cstr, cbox, true)) return CAAT_ERR_UNSUPPORTED;
-        if (cudaMemsetAsync(wacc, 0, (size_t)h * (size_t)K * 4, s) != cudaSuccess) return CAAT_ERR_CUDA;
-        caat_status st = launch_grouped<true, true>(am, sm, bm, cm, p, s, "rowpar_bwd_dw_tc");
+        if (cudaMemsetAsync(wacc, 0, (size_t)h * (size_t)K * 4, sw) != cudaSuccess) return CAAT_ERR_CUDA;
+        caat_status st = launch_grouped<true, true>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc");
         if (st != CAAT_OK) return st;
         const int64_t total = h * (K / 8);
         int64_t blocks = (total + 255) / 256;
         if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
-        f32_rows_to_bf16_kernel<<<(unsigned)blocks, 256, 0, s>>>(wacc, h, K, K, (uint16_t *)dW, ld_dw);
+        f32_rows_to_bf16_kernel<<<(unsigned)blocks, 256, 0, sw>>>(wacc, h, K, K, (uint16_t *)dW, ld_dw);
         note_launch("rowpar_bwd_dw_tc", 1);
         return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
-    }
+    };
+    return join(dw_chain());
 }
 
 }  // namespace caat
