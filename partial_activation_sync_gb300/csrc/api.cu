@@ -428,10 +428,22 @@ extern "C" caat_status caat_colpar_linear_bwd(int t, int64_t N, int64_t h, int64
         ws_bytes >= wacc_region_bytes(K, h, dt))
         wacc = (float *)workspace;
     const cudaStream_t s = (cudaStream_t)stream;
+    // dW1 and dA only read shared inputs: dW1 runs on the side stream next to dA
+    SideStream *side = (N > 0 && K > 0 && h > 0) ? side_stream(s) : nullptr;
+    cudaStream_t sw = s;
+    if (side != nullptr) {
+        if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
+            return CAAT_ERR_CUDA;
+        sw = side->s;
+    }
     // dW1 = A_r^T dZ_r per block (the dW product with X = dZ, dY_r = A_r)
     st = rowpar_grads(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, a, lda, nullptr, 0, dW1, dw1_cs, dw1_rs,
-                      wacc, s);
+                      wacc, sw);
     if (st != CAAT_OK) return st;
     // dA = PCR_S(dZ_r W1_r^T): the fused row-parallel forward on (dZ, W1^T)
-    return caat_rowpar_linear_fwd(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, dA, ldda, sel, n_sel, stream);
+    st = caat_rowpar_linear_fwd(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, dA, ldda, sel, n_sel, stream);
+    if (side != nullptr &&
+        (cudaEventRecord(side->join, sw) != cudaSuccess || cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess))
+        return CAAT_ERR_CUDA;
+    return st;
 }

@@ -87,6 +87,14 @@ bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int
 // (null: no split).  s_sum > 0: channels [0, s_sum) of every rank's gradient
 // are read from the one reduced buffer dsum [N, s_sum] (row stride ld_dsum) and
 // channels [s_sum, h) from dY_r; s_sum must be a multiple of 64.
+// per host thread and device: a second stream and a fork / join event pair for
+// running independent parts of one call side by side (null: stay on `main`)
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+SideStream *side_stream(cudaStream_t main);
+
 caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
                                  void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,

@@ -372,20 +372,20 @@ int pick_ksplit(int units, int nkb)
 }  // namespace
 
 namespace {
+thread_local SideStream t_side[64];
+}  // namespace
 
 // A second stream per host thread and device, with a fork and a join event: the
 // dW chain of the backward runs on it next to dX (they only read shared inputs),
 // so dW's CTAs take SMs as soon as dX's retire instead of after dX has drained.
 // Created on first use outside stream capture; per thread, so that concurrent
-// callers never interleave their fork/join events.
-struct SideStream {
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-thread_local SideStream t_side[64];
+// callers never interleave their fork/join events.  "CAAT_BWD_SIDE_STREAM=0"
+// (or no stream could be made) gives null: everything stays on `main`.
 
 SideStream *side_stream(cudaStream_t main)
 {
+    const char *env = std::getenv("CAAT_BWD_SIDE_STREAM");
+    if (env != nullptr && std::strcmp(env, "0") == 0) return nullptr;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
     SideStream &sd = t_side[dev];
@@ -407,8 +407,6 @@ SideStream *side_stream(cudaStream_t main)
     }
     return &sd;
 }
-
-}  // namespace
 
 bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                       const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy, const void *dX,
@@ -456,9 +454,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
 
     // dW on the side stream when both products are wanted
     cudaStream_t sw = s;
-    const char *side_env = std::getenv("CAAT_BWD_SIDE_STREAM");     // "0": one stream
-    const bool side_on = side_env == nullptr || std::strcmp(side_env, "0") != 0;
-    SideStream *side = (side_on && dX != nullptr && dW != nullptr) ? side_stream(s) : nullptr;
+    SideStream *side = (dX != nullptr && dW != nullptr) ? side_stream(s) : nullptr;
     if (side != nullptr) {
         if (cudaEventRecord(side->fork, s) != cudaSuccess || cudaStreamWaitEvent(side->s, side->fork, 0) != cudaSuccess)
             return CAAT_ERR_CUDA;
