@@ -46,8 +46,8 @@ STEP_SPIN_CYCLES = 400000
 # layer without a capture reports null.  Output lines still dirty in L2 when the
 # kernel ends are not in the count.
 DRAM_TRAFFIC = {
-    ("130m", "down_proj"): 84.29e6 + 54.20e6,
-    ("130m", "out_proj"): 14.69e6 + 46.77e6,
+    ("130m", "down_proj"): 97.72e6 + 49.30e6,
+    ("130m", "out_proj"): 15.58e6 + 36.25e6,
 }
 
 

@@ -114,17 +114,17 @@ constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legit
 // W 128 x 64 per CTA: each CTA holds half the rows of X and half the channels of
 // W, which cuts the shared-memory operand traffic per SM by a third; two staging
 // buffers per epilogue warp so a bulk store can drain while the next is staged).
-template <int CLN>
+template <int CLN, int BNT>
 struct Cfg {
     static constexpr bool PAIR = CLN > 1;
     static constexpr int STAGES = PAIR ? 6 : 4;
     static constexpr int NBUF = 1;                // staging buffers per epilogue warp
-    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;        // W rows (channels) per CTA per stage
+    static constexpr int B_ROWS = PAIR ? BNT / 2 : BNT;        // W rows (channels) per CTA per stage
     static constexpr int B_FETCH = CLN == 4 ? B_ROWS / 2 : B_ROWS;   // W rows this CTA fetches
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;   // landing per stage (leader)
-    static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * BM : BM, BN);
+    static constexpr uint32_t IDESC = idesc_bf16_f32(PAIR ? 2 * BM : BM, BNT);
 };
 
 enum { FULL_S = 0, NO_S = 1, MIXED = 2 };
@@ -139,10 +139,10 @@ struct SmemCtl {
     uint32_t bitmap[MAX_H_TC / 32];
 };
 
-template <int CLN>
+template <int CLN, int BNT>
 constexpr size_t smem_bytes()
 {
-    return 1024 + (size_t)Cfg<CLN>::STAGES * Cfg<CLN>::STAGE_BYTES + 4 * Cfg<CLN>::NBUF * STG_BYTES +
+    return 1024 + (size_t)Cfg<CLN, BNT>::STAGES * Cfg<CLN, BNT>::STAGE_BYTES + 4 * Cfg<CLN, BNT>::NBUF * STG_BYTES +
            sizeof(SmemCtl);
 }
 
@@ -165,12 +165,13 @@ __device__ __forceinline__ void fail(volatile int *abort)
     atomicExch(&g_caat_dev_error, (int)CAAT_ERR_TIMEOUT);
 }
 
+template <int BNT>
 __device__ __forceinline__ int tile_class(const uint32_t *bm, int64_t n0, int64_t h, int t)
 {
     if (t == 1) return FULL_S;
     bool any = false, all = true;
 #pragma unroll
-    for (int w = 0; w < BN / 32; ++w) {
+    for (int w = 0; w < BNT / 32; ++w) {
         const int64_t c = n0 + 32 * w;
         if (c < h) {
             const int64_t nv = h - c < 32 ? h - c : 32;
@@ -192,12 +193,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
 // CLN = CTAs per cluster: 1 (one CTA per tile), 2 (a CTA pair), 4 (two CTA
 // pairs on adjacent row blocks of the same channel block; the two CTAs that hold
 // the same half of the W tile each fetch half of it and multicast to both).
-template <int CLN>
+template <int CLN, int BNT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ YMaps ymaps, const FwdParams p)
 {
-    using C = Cfg<CLN>;
+    using C = Cfg<CLN, BNT>;
     constexpr bool PAIR = C::PAIR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -300,7 +301,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
 #ifdef EXP_LOAD_HINT
                             tma_load_3d_pair_hint(smem_u32(smA + stage * A_BYTES), &tmX, fl, kb * BK, r, mb * BM, pol_in);
                             tma_load_3d_pair_hint(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
-                                             nb * BN + (int)crank * C::B_ROWS, pol_in);
+                                             nb * BNT + (int)crank * C::B_ROWS, pol_in);
 #else
                             tma_load_3d_pair(smem_u32(smA + stage * A_BYTES), &tmX, fl, kb * BK, r, mb * BM);
                             if (CLN == 4) {
@@ -309,17 +310,17 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                                 // with the same half in the other pair
                                 const uint32_t hh = crank & 1u, pi = crank >> 1;
                                 tma_load_3d_pair_mc(smem_u32(smB + stage * C::B_BYTES + pi * C::B_FETCH * 128), &tmW,
-                                                    fl, kb * BK, r, nb * BN + (int)(hh * C::B_ROWS + pi * C::B_FETCH),
+                                                    fl, kb * BK, r, nb * BNT + (int)(hh * C::B_ROWS + pi * C::B_FETCH),
                                                     (uint16_t)((1u << hh) | (1u << (2 + hh))));
                             } else {
                                 tma_load_3d_pair(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
-                                                 nb * BN + (int)crank * C::B_ROWS);
+                                                 nb * BNT + (int)crank * C::B_ROWS);
                             }
 #endif
                         } else {
                             mbar_arrive_expect_tx(fb, C::TX_BYTES);
                             tma_load_3d(smem_u32(smA + stage * A_BYTES), &tmX, fb, kb * BK, r, mb * BM);
-                            tma_load_3d(smem_u32(smB + stage * C::B_BYTES), &tmW, fb, kb * BK, r, nb * BN);
+                            tma_load_3d(smem_u32(smB + stage * C::B_BYTES), &tmW, fb, kb * BK, r, nb * BNT);
                         }
                         if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
                     }
@@ -335,7 +336,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
             uint32_t ph = 0, au = 0;
             for (int u = unit0; u < num_units; u += nunits_grid) {
                 const int nb = u / num_mg;
-                const int cls = tile_class(ctl->bitmap, (int64_t)nb * BN, p.h, p.t);
+                const int cls = tile_class<BNT>(ctl->bitmap, (int64_t)nb * BNT, p.h, p.t);
                 for (int r = 0; r < p.t; ++r) {
                     const bool starts = cls != FULL_S || r == 0;
                     const bool ends = cls != FULL_S || r == p.t - 1;
@@ -386,8 +387,8 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         for (int u = unit0; u < num_units; u += nunits_grid) {
             const int mb = (u % num_mg) * CLN + (int)crank;
             const int nb = u / num_mg;
-            const int64_t n0 = (int64_t)nb * BN;
-            const int cls = tile_class(ctl->bitmap, n0, p.h, p.t);
+            const int64_t n0 = (int64_t)nb * BNT;
+            const int cls = tile_class<BNT>(ctl->bitmap, n0, p.h, p.t);
             for (int r = 0; r < p.t; ++r) {
                 if (cls == FULL_S && r != p.t - 1) continue;
                 const uint32_t b = au & 1u;
@@ -413,7 +414,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                     // last writes its partials whole: its S channels are rewritten
                     // with the sum at the end.
 #pragma unroll 1
-                    for (int c64 = 0; c64 < BN / 64; ++c64) {
+                    for (int c64 = 0; c64 < BNT / 64; ++c64) {
                         const int64_t c0 = n0 + 64 * c64;
                         if (c0 >= p.h) break;             // same for the whole warp
                         uint32_t v0[32], v1[32];
@@ -460,7 +461,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                     // row-coalesced, per-lane masked stores, after this warp's
                     // earlier bulk stores to those rows have completed.
 #pragma unroll 1
-                    for (int c64 = 0; c64 < BN / 64; ++c64) {
+                    for (int c64 = 0; c64 < BNT / 64; ++c64) {
                         const int64_t c0 = n0 + 64 * c64;
                         if (c0 >= p.h) break;
                         const uint32_t m0 = ctl->bitmap[c0 >> 5], m1 = ctl->bitmap[(c0 >> 5) + 1];
@@ -581,13 +582,13 @@ bool encode_3d(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1, uint
     return encode_tmap(tm, base, 3, dims, strides, box);
 }
 
-template <int CLN>
+template <int CLN, int BNT>
 caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMaps &ym, const FwdParams &p,
                        cudaStream_t s)
 {
     constexpr bool PAIR = CLN > 1;
-    auto kern = rowpar_fwd_tc_kernel<CLN>;
-    constexpr size_t smem = smem_bytes<CLN>();
+    auto kern = rowpar_fwd_tc_kernel<CLN, BNT>;
+    constexpr size_t smem = smem_bytes<CLN, BNT>();
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return CAAT_ERR_CUDA;
     const int per = CLN;
@@ -627,7 +628,9 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     const int64_t kt = K / t;
     // shapes and alignments this kernel takes; anything else goes to another kernel
     if (kt < BK || kt % 8 != 0 || ldx % 8 != 0 || ldw % 8 != 0 || ldy % 8 != 0) return CAAT_ERR_UNSUPPORTED;
-    if (h % 8 != 0 || h < BN || h > MAX_H_TC || N < 16 || N > (int64_t)INT32_MAX) return CAAT_ERR_UNSUPPORTED;
+    // (h < 256 only as 192-wide single-CTA tiles)
+    if (h % 8 != 0 || h < (h % 192 == 0 ? 192 : BN) || h > MAX_H_TC || N < 16 || N > (int64_t)INT32_MAX)
+        return CAAT_ERR_UNSUPPORTED;
     if (t > MAX_T_TC) return CAAT_ERR_UNSUPPORTED;
     if ((uintptr_t)X % 16 != 0 || (uintptr_t)W % 16 != 0) return CAAT_ERR_UNSUPPORTED;
     for (int r = 0; r < t; ++r)
@@ -664,19 +667,35 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     p.t = t;
     p.nkb = (int)((kt + BK - 1) / BK);
     p.num_m = (int)((N + BM - 1) / BM);
-    p.num_n = (int)((h + BN - 1) / BN);
     p.sel = sel;
     p.n_sel = n_sel;
-    if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;
+    // Tile width of the single-CTA mode: 192 channels instead of 256 when h is a
+    // multiple of 192, the tiles then take fewer SM-rounds of work (rounds x
+    // width), and a contiguous S ends on a tile edge (no MIXED tiles).  At the
+    // 130M shapes (h = 768, S = [0, 384)) this is 256 tiles of 3/4 the work in
+    // the same two rounds as 192 full tiles.  (override: CAAT_FWD_BN=192|256)
+    auto rounds = [&](int64_t bn) { return (p.num_m * ((h + bn - 1) / bn) + num_sms() - 1) / num_sms(); };
+    bool bn192 = h % 192 == 0 && rounds(192) * 192 < rounds(256) * 256 && (sel != nullptr || n_sel % 192 == 0);
+    if (const char *e = std::getenv("CAAT_FWD_BN")) {
+        const int v = std::atoi(e);
+        if (v == 192 && h % 192 == 0) bn192 = true;
+        if (v == 256 && h >= BN) bn192 = false;
+    }
+    if (h < BN) bn192 = true;
     for (;; cln >>= 1) {
+        if (cln > 1 && h < BN) continue;           // the cluster modes need 256 channels
+        const int bn = (cln == 1 && bn192) ? 192 : BN;
+        p.num_n = (int)((h + bn - 1) / bn);
+        if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;
         CUtensorMap tmW;
-        const uint32_t wrows = cln == 1 ? BN : (cln == 2 ? BN / 2 : BN / 4);
+        const uint32_t wrows = cln == 1 ? bn : (cln == 2 ? BN / 2 : BN / 4);
         if (!encode_3d(&tmW, W, (uint64_t)kt, (uint64_t)t, (uint64_t)h, (uint64_t)kt * 2, (uint64_t)ldw * 2,
                        BK, 1, wrows))
             return CAAT_ERR_UNSUPPORTED;
-        const caat_status st = cln == 4 ? launch_fwd<4>(tmX, tmW, ym, p, s)
-                             : cln == 2 ? launch_fwd<2>(tmX, tmW, ym, p, s)
-                                        : launch_fwd<1>(tmX, tmW, ym, p, s);
+        const caat_status st = cln == 4 ? launch_fwd<4, BN>(tmX, tmW, ym, p, s)
+                             : cln == 2 ? launch_fwd<2, BN>(tmX, tmW, ym, p, s)
+                             : bn == 192 ? launch_fwd<1, 192>(tmX, tmW, ym, p, s)
+                                         : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
         // a cluster shape that cannot be co-resident falls back to a smaller one
         if (st != CAAT_ERR_UNSUPPORTED || cln == 1) return st;
     }

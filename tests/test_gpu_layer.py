@@ -116,18 +116,26 @@ TC_SHAPES = [
     (5, 640, 72, 1032),
     (3, 700, 64, 520),      # six row blocks: the second cluster of four has two idle CTAs
 ]
+# the forward also takes h = 192 (one 192-wide tile; the backward kernels need h >= 256)
+TC_FWD_SHAPES = TC_SHAPES + [
+    (4, 200, 64, 192),      # the smallest h: one 192-wide tile
+    (3, 260, 128, 576),     # 192-wide tiles: three per row block
+]
 
 
-@pytest.fixture(params=["4", "2", "1"])
+@pytest.fixture(params=["4", "2", "1", "1/192"])
 def fwd_mode(request, monkeypatch):
     """Cluster shape of the forward: 4 = two CTA pairs sharing W tiles by
     multicast (the default from four row blocks up), 2 = one CTA pair
-    (cta_group::2, 256-row tiles), 1 = one CTA per 128-row tile."""
-    monkeypatch.setenv("CAAT_FWD_CLUSTER", request.param)
+    (cta_group::2, 256-row tiles), 1 = one CTA per 128 x 256 tile, 1/192 = one
+    CTA per 128 x 192 tile (where h is a multiple of 192)."""
+    cl, _, bn = request.param.partition("/")
+    monkeypatch.setenv("CAAT_FWD_CLUSTER", cl)
+    monkeypatch.setenv("CAAT_FWD_BN", bn or "256")
     return request.param
 
 
-@pytest.mark.parametrize("t,N,kt,h", TC_SHAPES)
+@pytest.mark.parametrize("t,N,kt,h", TC_FWD_SHAPES)
 def test_fwd_tc_parity(caat, t, N, kt, h, fwd_mode):
     for p in (0.0, 0.25, 0.5, 1.0):
         for layout in (0, 1):
