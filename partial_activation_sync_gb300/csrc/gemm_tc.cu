@@ -682,20 +682,27 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         if (v == 256 && h >= BN) bn192 = false;
     }
     if (h < BN) bn192 = true;
+    const char *bn_env = std::getenv("CAAT_FWD_BN");
+    const bool bn192_clusters = bn_env != nullptr && std::atoi(bn_env) == 192 && h % 192 == 0;
     for (;; cln >>= 1) {
         if (cln > 1 && h < BN) continue;           // the cluster modes need 256 channels
-        const int bn = (cln == 1 && bn192) ? 192 : BN;
+        const int bn = ((cln == 1 && bn192) || (cln > 1 && bn192_clusters)) ? 192 : BN;
         p.num_n = (int)((h + bn - 1) / bn);
         if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;
         CUtensorMap tmW;
-        const uint32_t wrows = cln == 1 ? bn : (cln == 2 ? BN / 2 : BN / 4);
+        const uint32_t wrows = cln == 1 ? bn : (cln == 2 ? bn / 2 : bn / 4);
         if (!encode_3d(&tmW, W, (uint64_t)kt, (uint64_t)t, (uint64_t)h, (uint64_t)kt * 2, (uint64_t)ldw * 2,
                        BK, 1, wrows))
             return CAAT_ERR_UNSUPPORTED;
-        const caat_status st = cln == 4 ? launch_fwd<4, BN>(tmX, tmW, ym, p, s)
-                             : cln == 2 ? launch_fwd<2, BN>(tmX, tmW, ym, p, s)
-                             : bn == 192 ? launch_fwd<1, 192>(tmX, tmW, ym, p, s)
-                                         : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
+        caat_status st;
+        if (bn == 192)
+            st = cln == 4 ? launch_fwd<4, 192>(tmX, tmW, ym, p, s)
+               : cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s)
+                          : launch_fwd<1, 192>(tmX, tmW, ym, p, s);
+        else
+            st = cln == 4 ? launch_fwd<4, BN>(tmX, tmW, ym, p, s)
+               : cln == 2 ? launch_fwd<2, BN>(tmX, tmW, ym, p, s)
+                          : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
         // a cluster shape that cannot be co-resident falls back to a smaller one
         if (st != CAAT_ERR_UNSUPPORTED || cln == 1) return st;
     }
