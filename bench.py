@@ -542,14 +542,16 @@ def _oracle_sample(w, rows, threads):
 
 def _calibrate_rows(w, threads, budget_s):
     """Rows of the workload the oracle processes in about budget_s seconds."""
-    rows = 4 * max(threads, 4)
+    rows = min(w.N, 4 * max(threads, 4))
     while True:      # grow until a sample costs a quarter of the budget (cost is not linear)
         _, s = _oracle_sample(w, rows, threads)
         if s >= budget_s / 4 or rows >= w.N:
             break
         rows = int(min(w.N, rows * min(8.0, max(2.0, budget_s / 4 / max(s, 1e-3)))))
     rows = int(min(w.N, max(threads, rows * budget_s / max(s, 1e-3))))
-    return max(threads, rows // threads * threads)
+    if rows >= threads:
+        rows = rows // threads * threads     # whole rows per thread
+    return max(1, min(w.N, rows))
 
 
 def cpu_baseline(w, budget_s=12.0):
