@@ -15,7 +15,18 @@
  *
  * Conventions shared by every call
  *  - Every compute call is asynchronous on the stream `stream` (a cudaStream_t;
- *    NULL = the legacy default stream) and keeps no state between calls.
+ *    NULL = the legacy default stream) and keeps no data between calls.  The
+ *    backward calls may run part of their work on a library-owned side stream
+ *    (one per host thread and device, created on first use outside stream
+ *    capture): it forks from `stream` and joins back to it through events, so
+ *    the call stays ordered on `stream` and can be captured in a CUDA graph.
+ *    A caller that drives one host thread on several streams at once shares
+ *    that side stream between them (still correct, possibly less concurrent).
+ *  - Tuning switches read from the environment at each call (for comparisons
+ *    and tests; the defaults choose by shape): CAAT_FWD_CLUSTER=1|2|4 (CTAs per
+ *    cluster of the forward tile kernel), CAAT_FWD_BN=192|256 (its tile width),
+ *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
+ *    (backward on `stream` only).
  *  - "device pointer" = memory the caller allocated on the current CUDA device;
  *    the library never allocates or frees device memory and never keeps a pointer
  *    after the call returns.  Arrays "of t device pointers" are HOST arrays whose
