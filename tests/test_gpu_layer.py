@@ -123,15 +123,17 @@ TC_FWD_SHAPES = TC_SHAPES + [
 ]
 
 
-@pytest.fixture(params=["4", "2", "1", "1/192", "2/192", "4/192"])
+@pytest.fixture(params=["4", "2", "1", "1/192", "2/192", "4/192", "1:m", "4:m", "1/192:m"])
 def fwd_mode(request, monkeypatch):
     """Cluster shape of the forward: 4 = two CTA pairs sharing W tiles by
     multicast (the default from four row blocks up), 2 = one CTA pair
     (cta_group::2, 256-row tiles), 1 = one CTA per 128 x 256 tile; "/192": the
     same with 192-channel tiles (where h is a multiple of 192)."""
-    cl, _, bn = request.param.partition("/")
+    mode, _, order = request.param.partition(":")    # ":m": row-block-major work order
+    cl, _, bn = mode.partition("/")
     monkeypatch.setenv("CAAT_FWD_CLUSTER", cl)
     monkeypatch.setenv("CAAT_FWD_BN", bn or "256")
+    monkeypatch.setenv("CAAT_FWD_ORDER", order or "n")
     return request.param
 
 
