@@ -118,7 +118,9 @@ template <int CLN, int BNT>
 struct Cfg {
     static constexpr bool PAIR = CLN > 1;
     static constexpr int STAGES = PAIR ? 6 : 4;
-    static constexpr int NBUF = 1;                // staging buffers per epilogue warp
+    // staging buffers per epilogue warp: two (a bulk store drains one while the
+    // next chunk fills the other) where shared memory allows, i.e. below 256-wide
+    static constexpr int NBUF = BNT < 256 ? 2 : 1;
     static constexpr int B_ROWS = PAIR ? BNT / 2 : BNT;        // W rows (channels) per CTA per stage
     static constexpr int B_FETCH = CLN == 4 ? B_ROWS / 2 : B_ROWS;   // W rows this CTA fetches
     static constexpr int B_BYTES = B_ROWS * BK * 2;
@@ -385,6 +387,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         const int q = warp & 3;                         // TMEM lane quarter of this warp
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t au = 0;
+        int sbuf = 0;                                   // staging buffer the next chunk fills
         for (int u = unit0; u < num_units; u += nunits_grid) {
             const int mb = (p.mmajor ? u / p.num_n : u % num_mg) * CLN + (int)crank;
             const int nb = p.mmajor ? u % p.num_n : u / num_mg;
@@ -405,8 +408,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                 const bool final_mixed = cls == MIXED && r == p.t - 1;
                 const bool zero_nons = cls == MIXED && r <= p.t - 3;
                 const int y = mb * BM + 32 * q;
-                uint8_t *stg = staging + q * STG_BYTES;
-                const uint32_t stg_a = smem_u32(stg);
+                uint8_t *stg = staging + q * C::NBUF * STG_BYTES;   // this warp's first buffer
                 if (!final_mixed) {
                     // Stage 32 rows x 64 channels in shared memory (128-byte swizzle:
                     // 16-byte chunk j of row i sits at chunk j ^ (i mod 8)), then one
@@ -438,24 +440,34 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             tmem_st32(tb + 64u * c64, v0);
                             tmem_st32(tb + 64u * c64 + 32u, v1);
                         }
-                        if (lane == 0) bulk_wait_read0();    // staging free again
+                        // the buffer to fill: every earlier bulk group but the last has
+                        // read its staging (the last one read the other buffer)
+                        uint8_t *stgc = stg + sbuf * STG_BYTES;
+                        const uint32_t stgc_a = smem_u32(stgc);
+                        if (lane == 0) {
+                            if (C::NBUF > 1) bulk_wait_read1(); else bulk_wait_read0();
+                        }
                         __syncwarp();
-                        uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
+                        uint4 *rowp = reinterpret_cast<uint4 *>(stgc + lane * 128);
 #pragma unroll
                         for (int j = 0; j < 8; ++j)
                             rowp[j ^ (lane & 7)] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
                         fence_proxy_async_smem();
                         __syncwarp();
-                        if (lane == 0 && y < p.N) {
-                            if (cls == FULL_S) {
-                                for (int rr = 0; rr < p.t; ++rr) tma_store_2d(&ymaps.m[rr], stg_a, (int)c0, y);
-                            } else {
-                                tma_store_2d(&ymaps.m[r], stg_a, (int)c0, y);
+                        if (y < p.N) {                     // same for the whole warp
+                            if (lane == 0) {
+                                if (cls == FULL_S) {
+                                    for (int rr = 0; rr < p.t; ++rr) tma_store_2d(&ymaps.m[rr], stgc_a, (int)c0, y);
+                                } else {
+                                    tma_store_2d(&ymaps.m[r], stgc_a, (int)c0, y);
+                                }
+                                bulk_commit();
                             }
-                            bulk_commit();
+                            if (C::NBUF > 1) sbuf ^= 1;    // one bulk group per filled buffer
                         }
                     }
                 } else {
+                    const uint32_t stg_a = smem_u32(stg);
                     // Last shard of a MIXED tile: rank t-1's tile (S channels from
                     // the sum of both accumulators, the others its own) by bulk
                     // store; then the S sums into the other ranks' S channels with
@@ -669,12 +681,15 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     p.nkb = (int)((kt + BK - 1) / BK);
     p.num_m = (int)((N + BM - 1) / BM);
     // Work-unit order: row-block-major when X is large and has many more rows than
-    // W has channels -- the channel blocks of a row block then run in the same
-    // round and read X from DRAM once (1.1B: -4 to -6 %, 130M down-proj: -2 %);
-    // channel-block-major otherwise, which keeps W tiles hot when N ~ h (7B
-    // prefill) or X fits in L2 anyway.  (override: CAAT_FWD_ORDER=m|n)
-    p.mmajor = (N * K * 2 >= ((int64_t)32 << 20) && N >= 2 * h) ? 1 : 0;
-    if (const char *e = std::getenv("CAAT_FWD_ORDER")) p.mmajor = e[0] == 'm' ? 1 : 0;
+    // W has channels, and a contiguous S ends on a tile edge -- the channel blocks
+    // of a row block then run in the same round and read X from DRAM once (1.1B:
+    // -4 to -6 %, 130M down-proj: -2 %); channel-block-major otherwise, which keeps
+    // W tiles hot when N ~ h (7B prefill) or X fits in L2 anyway.
+    // (override: CAAT_FWD_ORDER=m|n)
+    // (decided per tile width below: only without MIXED tiles, whose slow per-shard
+    // epilogues would then pile up on the CTAs that run two units)
+    const bool mmajor_size = N * K * 2 >= ((int64_t)32 << 20) && N >= 2 * h;
+    const char *order_env = std::getenv("CAAT_FWD_ORDER");
     p.sel = sel;
     p.n_sel = n_sel;
     // Tile width of the single-CTA mode: 192 channels instead of 256 when h is a
@@ -695,6 +710,8 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     for (;; cln >>= 1) {
         if (cln > 1 && h < BN) continue;           // the cluster modes need 256 channels
         const int bn = ((cln == 1 && bn192) || (cln > 1 && bn192_clusters)) ? 192 : BN;
+        p.mmajor = (mmajor_size && sel == nullptr && n_sel % bn == 0) ? 1 : 0;
+        if (order_env != nullptr) p.mmajor = order_env[0] == 'm' ? 1 : 0;
         p.num_n = (int)((h + bn - 1) / bn);
         if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;
         CUtensorMap tmW;
