@@ -421,8 +421,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                         const int64_t c0 = n0 + 64 * c64;
                         if (c0 >= p.h) break;             // same for the whole warp
                         uint32_t v0[32], v1[32];
-                        tmem_ld32(tb + 64u * c64, v0);
-                        tmem_ld32(tb + 64u * c64 + 32u, v1);
+                        tmem_ld32x2(tb + 64u * c64, tb + 64u * c64 + 32u, v0, v1);
                         uint32_t w[32];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
@@ -481,8 +480,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                         uint32_t w[32], ws[32];
                         {
                             uint32_t v[32], u[32];
-                            tmem_ld32(tb + 64u * c64, v);
-                            tmem_ld32(tb_other + 64u * c64, u);
+                            tmem_ld32x2(tb + 64u * c64, tb_other + 64u * c64, v, u);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const float s0 = __uint_as_float(u[2 * i]) + __uint_as_float(v[2 * i]);
@@ -491,8 +489,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                                 w[i] = pack_bf16x2(((m0 >> (2 * i)) & 1u) ? __float_as_uint(s0) : v[2 * i],
                                                    ((m0 >> (2 * i + 1)) & 1u) ? __float_as_uint(s1) : v[2 * i + 1]);
                             }
-                            tmem_ld32(tb + 64u * c64 + 32u, v);
-                            tmem_ld32(tb_other + 64u * c64 + 32u, u);
+                            tmem_ld32x2(tb + 64u * c64 + 32u, tb_other + 64u * c64 + 32u, v, u);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) {
                                 const float s0 = __uint_as_float(u[2 * i]) + __uint_as_float(v[2 * i]);

@@ -236,27 +236,33 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             // shard, shard, row) clips columns past k_t and rows past M
             const int y = mb * BM + 32 * q;
             if (RED) {
-                // fp32 partial: 32 rows x 32 columns (128-byte rows) per reduce-add
+                // fp32 partial: 32 rows x 32 columns (128-byte rows) per reduce-add;
+                // 64 columns are read from TMEM under one wait (BN is a multiple of 64)
 #pragma unroll 1
-                for (int c32 = 0; c32 < p.BN / 32; ++c32) {
-                    const int64_t c0 = n0 + 32 * c32;
-                    if (c0 >= p.Nn) break;
-                    uint32_t vv[32];
-                    tmem_ld32(tb + 32u * c32, vv);
-                    uint8_t *stg = staging + (q * NBUF + sbuf) * STG_BYTES;
-                    const uint32_t stg_a = smem_u32(stg);
-                    if (++sbuf == NBUF) sbuf = 0;
-                    if (lane == 0) bulk_wait_read1();
-                    __syncwarp();
-                    uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
+                for (int c64 = 0; c64 < p.BN / 64; ++c64) {
+                    if (n0 + 64 * c64 >= p.Nn) break;
+                    uint32_t vv[2][32];
+                    tmem_ld32x2(tb + 64u * c64, tb + 64u * c64 + 32u, vv[0], vv[1]);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        rowp[j ^ (lane & 7)] = make_uint4(vv[4 * j], vv[4 * j + 1], vv[4 * j + 2], vv[4 * j + 3]);
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0 && y < p.M) {
-                        tma_reduce_add_3d(&cmap, stg_a, (int)c0, r, y);
-                        bulk_commit();
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int64_t c0 = n0 + 64 * c64 + 32 * hf;
+                        if (c0 >= p.Nn) break;         // same for the whole warp
+                        uint8_t *stg = staging + (q * NBUF + sbuf) * STG_BYTES;
+                        const uint32_t stg_a = smem_u32(stg);
+                        if (++sbuf == NBUF) sbuf = 0;
+                        if (lane == 0) bulk_wait_read1();
+                        __syncwarp();
+                        uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            rowp[j ^ (lane & 7)] =
+                                make_uint4(vv[hf][4 * j], vv[hf][4 * j + 1], vv[hf][4 * j + 2], vv[hf][4 * j + 3]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0 && y < p.M) {
+                            tma_reduce_add_3d(&cmap, stg_a, (int)c0, r, y);
+                            bulk_commit();
+                        }
                     }
                 }
             }
@@ -265,8 +271,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                 const int64_t c0 = n0 + 64 * c64;
                 if (c0 >= p.Nn) break;
                 uint32_t v0[32], v1[32];
-                tmem_ld32(tb + 64u * c64, v0);
-                tmem_ld32(tb + 64u * c64 + 32u, v1);
+                tmem_ld32x2(tb + 64u * c64, tb + 64u * c64 + 32u, v0, v1);
                 uint32_t w[32];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {

@@ -223,6 +223,8 @@ pcr_scalar_kernel(int t, int64_t N, int64_t h, ConstPtrs in, int64_t ld_in, MutP
 // out[n, c] = in_0[n, c] + ... + in_{t-1}[n, c] for c < s (bf16, fp32 left fold
 // in rank order, one rounding): the channels of a contiguous S, reduced once
 // instead of into every rank's copy.
+// Block (x, y): x walks the 8-channel chunks of a row, y the rows of the block's
+// row group, so a row narrower than 256 chunks still fills whole warps.
 template <int TT>
 __global__ void __launch_bounds__(256)
 pcr_colsum_kernel(int t, int64_t N, int64_t s, ConstPtrs in, int64_t ld_in, uint16_t *__restrict__ out,
@@ -230,7 +232,7 @@ pcr_colsum_kernel(int t, int64_t N, int64_t s, ConstPtrs in, int64_t ld_in, uint
 {
     const int T = TT > 0 ? TT : t;
     const int64_t cpr = s / 8;
-    for (int64_t n = blockIdx.y; n < N; n += gridDim.y) {
+    for (int64_t n = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; n < N; n += (int64_t)gridDim.y * blockDim.y) {
         for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < cpr;
              j += (int64_t)gridDim.x * blockDim.x) {
             const int64_t bi = (n * ld_in + j * 8) * 2;
@@ -284,21 +286,23 @@ caat_status launch_pcr_colsum(int t, int64_t N, int64_t s, const ConstPtrs &in, 
     if (s % 8 || ld_in % 8 || ld_out % 8 || (uintptr_t)out % 16) return CAAT_ERR_UNSUPPORTED;
     for (int r = 0; r < t; ++r)
         if ((uintptr_t)in.p[r] % 16) return CAAT_ERR_UNSUPPORTED;
+    // blocks of about 256 threads: units (8-channel chunks) of a row across x,
+    // as many rows as fit across y; at most eight blocks per SM, rows strided
     const int64_t units = s / 8;
-    const int bx = units >= 256 ? 256 : (int)((units + 31) / 32 * 32);
-    int64_t gx = (units + bx - 1) / bx;
-    const int64_t target = (int64_t)num_sms() * (2048 / bx) * 2;
-    if (gx > target) gx = target;
-    int64_t gy = (target + gx - 1) / gx;
-    if (gy > N) gy = N;
+    const int bx = units >= 256 ? 256 : (int)units;
+    const int by = 256 / bx;
+    const int64_t gx = (units + bx - 1) / bx;
+    int64_t gy = (N + by - 1) / by;
+    const int64_t cap = ((int64_t)num_sms() * 8 + gx - 1) / gx;
+    if (gy > cap) gy = cap;
     if (gy > 65535) gy = 65535;
-    const dim3 grid((unsigned)gx, (unsigned)gy);
+    const dim3 grid((unsigned)gx, (unsigned)gy), bx2((unsigned)bx, (unsigned)by);
     uint16_t *o = (uint16_t *)out;
     switch (t) {
-    case 2: pcr_colsum_kernel<2><<<grid, bx, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
-    case 4: pcr_colsum_kernel<4><<<grid, bx, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
-    case 8: pcr_colsum_kernel<8><<<grid, bx, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
-    default: pcr_colsum_kernel<0><<<grid, bx, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    case 2: pcr_colsum_kernel<2><<<grid, bx2, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    case 4: pcr_colsum_kernel<4><<<grid, bx2, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    case 8: pcr_colsum_kernel<8><<<grid, bx2, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    default: pcr_colsum_kernel<0><<<grid, bx2, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
     }
     note_launch("pcr_colsum");
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
