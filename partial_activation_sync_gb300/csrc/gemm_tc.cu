@@ -7,7 +7,8 @@
 // K split t ways), channels in S are summed over the ranks and every rank gets
 // the sum; the other channels keep each rank's own partial result.
 //
-// One persistent CTA per SM walks output tiles of 128 rows x 256 channels.
+// One persistent CTA per SM walks output tiles of 128 rows x 256 channels (or
+// 192 channels where h is a multiple of 192; CTA pairs take 256-row tiles).
 // Every tile streams the same k-blocks (shard 0's K slice, then shard 1's, ...),
 // so all tiles cost the same MMA work; what differs is where results go:
 //   FULL_S tile (every channel in S): one accumulation over all of K (that is
@@ -19,8 +20,8 @@
 //     so the S columns keep summing (even shards in one buffer, odd shards in
 //     the other); after the last shard the two buffers' S columns are added and
 //     written to every rank.
-// Two 256-column fp32 accumulators (all 512 TMEM columns) alternate, so the
-// epilogue of one accumulation overlaps the MMAs of the next.
+// Two fp32 accumulators (256 TMEM columns apart; all 512 columns allocated)
+// alternate, so the epilogue of one accumulation overlaps the MMAs of the next.
 //
 // Warp roles: warp 0 lane 0 issues TMA loads into a 4-stage ring, warp 1 lane 0
 // issues the MMAs (warp 1 also owns the TMEM allocation), warps 2..5 drain TMEM

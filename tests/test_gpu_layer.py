@@ -390,6 +390,29 @@ def test_bwd_contiguous_reduce_once(caat, s, kt):
     assert rel_fro(to_f64(dW), wW) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("s", [64, 2048, 3072, 4096])
+def test_bwd_contiguous_reduce_once_wide(caat, s):
+    """The reduce-once path at h = 4096: S from 64 channels (8 chunks of 8 per row, many
+    rows per block) to 4096 (512 chunks per row, two blocks across a row), ragged
+    token count."""
+    T = torch()
+    t, N, kt, h = 4, 200, 64, 4096
+    X = ci.normal(1701, (N, kt * t))
+    Wl = ci.normal(1702, (kt * t, h), std=0.02)
+    G = ci.normal(1703, (t, N, h))
+    Xd, Wd = dev(X, "bf16"), _weight(Wl, "bf16", "nn")
+    Gd = [dev(G[r], "bf16") for r in range(t)]
+    dX, dW = caat.rowpar_linear_bwd(Xd, Wd, Gd, t, s, caat.CAAT_BWD_REDUCE_DOUT)
+    T.cuda.synchronize()
+    assert caat.device_status() == 0
+    assert caat.last_kernel() == "rowpar_bwd_dw_tc"
+    wX, wW = orc.rowpar_bwd(host_values(X, "bf16"), host_values(Wl, "bf16"),
+                            np.stack([host_values(G[r], "bf16") for r in range(t)]), t,
+                            np.arange(s), 0)
+    assert rel_fro(to_f64(dX), wX) <= TOL["bf16"]
+    assert rel_fro(to_f64(dW), wW) <= TOL["bf16"]
+
+
 @pytest.mark.parametrize("t", [1, 2, 3, 4, 8])
 @pytest.mark.parametrize("N", [1, 3, 8, 15, 16, 17, 33, 48, 64])
 def test_fwd_skinny_parity(caat, t, N):
