@@ -134,7 +134,7 @@ caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, caat_dtype 
  *      (w_rs, w_cs) = (1, K) is torch's nn.Linear weight [h, K] (K contiguous),
  *      the layout the tensor-core path takes; (h, 1) is a row-major [K, h].
  * Y:   host array of t device pointers, each [N, h] with row stride ldy; they
- *      must not overlap each other or X, W.
+ *      must not overlap each other, X, W or sel (else INVALID_ARG).
  * sel: device int32[n_sel], ascending and unique (S); or null for the contiguous
  *      S = {0, ..., n_sel-1}.  With the contiguous form and n_sel a multiple of 64,
  *      the backward reduces only the S channels, once, instead of materialising
@@ -175,7 +175,9 @@ caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64_t h, caat_
  *       caat_rowpar_linear_bwd_workspace() returns the size of both parts; a
  *       workspace holding only the required part also works.  May be null when
  *       nothing is required.
- * Errors: as caat_rowpar_linear_fwd; INVALID_ARG also when ws_bytes is too small.
+ * Errors: as caat_rowpar_linear_fwd; INVALID_ARG also when ws_bytes is too small,
+ *   or when dX, dW and the part of the workspace the call uses overlap each other
+ *   or any input (X, W, a dOut_r, sel).
  */
 size_t caat_rowpar_linear_bwd_workspace(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
                                         caat_bwd_mode mode);
@@ -261,8 +263,10 @@ caat_status caat_rowpar_linear_bwd_noalloc(int t, int64_t N, int64_t K, int64_t 
  *   lets dW1 be reduced over tokens in parts); null is allowed.
  * Ownership: all buffers belong to the caller; nothing is kept after the call.
  * Errors: INVALID_ARG for a bad size, null pointer, stride below the row width,
- *   K % t != 0, n_sel outside [0, h], or outputs overlapping inputs (Z with any A_r,
- *   dA_r with each other, with any A_q or with dZ); UNSUPPORTED / CUDA as
+ *   K % t != 0, n_sel outside [0, h], or outputs overlapping inputs (Z with any A_r
+ *   or W1; dA_r with each other, any A_q, dZ, W1 or sel; dW1 and the fp32
+ *   accumulator the call uses with each other and with every other buffer of the
+ *   call); UNSUPPORTED / CUDA as
  *   caat_rowpar_linear_fwd.  sel as there (null = the first n_sel channels).
  */
 caat_status caat_colpar_linear_fwd(int t, int64_t N, int64_t h, int64_t K, caat_dtype dt,

@@ -1,6 +1,7 @@
 // C-ABI entry points: argument validation, kernel choice, launch bookkeeping.
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 
 #include "caat_internal.h"
@@ -51,7 +52,17 @@ inline Span span_of(const void *p, int64_t rows, int64_t cols, int64_t ld, int64
     const int64_t n = rows > 0 && cols > 0 ? ((rows - 1) * ld + cols) * es : 0;
     return {lo, lo + (uintptr_t)n};
 }
+// [lo, hi) byte range of a [rows, cols] matrix with element strides (rs, cs)
+inline Span span_strided(const void *p, int64_t rows, int64_t cols, int64_t rs, int64_t cs, int64_t es)
+{
+    const uintptr_t lo = (uintptr_t)p;
+    const int64_t n = rows > 0 && cols > 0 ? ((rows - 1) * rs + (cols - 1) * cs + 1) * es : 0;
+    return {lo, lo + (uintptr_t)n};
+}
+inline Span span_bytes(const void *p, size_t n) { return {(uintptr_t)p, (uintptr_t)p + n}; }
 inline bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+// the device index list of S (int32[n_sel]) when one is given
+inline Span span_sel(const int32_t *sel, int64_t n_sel) { return span_bytes(sel, sel != nullptr && n_sel > 0 ? (size_t)n_sel * 4 : 0); }
 
 }  // namespace
 }  // namespace caat
@@ -157,7 +168,9 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
         const Span so = span_of(Y[r], N, h, ldy, es);
         for (int q = r + 1; q < t; ++q)
             if (overlap(so, span_of(Y[q], N, h, ldy, es))) return CAAT_ERR_INVALID_ARG;
-        if (overlap(so, span_of(X, N, K, ldx, es))) return CAAT_ERR_INVALID_ARG;
+        if (overlap(so, span_of(X, N, K, ldx, es)) || overlap(so, span_strided(W, K, h, w_rs, w_cs, es)) ||
+            overlap(so, span_sel(sel, n_sel)))
+            return CAAT_ERR_INVALID_ARG;
     }
     if (N == 0 || h == 0) return CAAT_OK;
     const cudaStream_t s = (cudaStream_t)stream;
@@ -303,6 +316,24 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
         ws_bytes >= need + wacc_region_bytes(K, h, dt) && wacc_region_bytes(K, h, dt) > 0)
         wacc = (float *)((char *)workspace + need);
 
+    // written regions (dX, dW, the part of the workspace this call uses) must not
+    // overlap each other or any input
+    {
+        const int64_t es = elem_size(dt);
+        const Span w_dx = span_of(dX, N, K, lddx, es);
+        const Span w_dw = span_strided(dW, K, h, dw_rs, dw_cs, es);
+        const Span w_ws = span_bytes(workspace, need + (wacc != nullptr ? wacc_region_bytes(K, h, dt) : 0));
+        const Span outs[3] = {w_dx, w_dw, w_ws};
+        if (overlap(w_dx, w_dw) || overlap(w_dx, w_ws) || overlap(w_dw, w_ws)) return CAAT_ERR_INVALID_ARG;
+        for (const Span &o : outs) {
+            if (overlap(o, span_of(X, N, K, ldx, es)) || overlap(o, span_strided(W, K, h, w_rs, w_cs, es)) ||
+                overlap(o, span_sel(sel, n_sel)))
+                return CAAT_ERR_INVALID_ARG;
+            for (int r = 0; r < t; ++r)
+                if (overlap(o, span_of(dOut[r], N, h, ld_dout, es))) return CAAT_ERR_INVALID_ARG;
+        }
+    }
+
     const cudaStream_t s = (cudaStream_t)stream;
     ConstPtrs dy{};
     int64_t ld_dy = ld_dout;
@@ -374,6 +405,7 @@ extern "C" caat_status caat_colpar_linear_fwd(int t, int64_t N, int64_t h, int64
     if (st != CAAT_OK) return st;
     const int64_t es = elem_size(dt);
     const Span sz = span_of(Z, N, K, ldz, es);
+    if (overlap(sz, span_strided(W1, h, K, w1_rs, w1_cs, es))) return CAAT_ERR_INVALID_ARG;
     ConstPtrs a{};
     for (int r = 0; r < t; ++r) {
         if (overlap(sz, span_of(A[r], N, h, lda, es))) return CAAT_ERR_INVALID_ARG;
@@ -420,13 +452,28 @@ extern "C" caat_status caat_colpar_linear_bwd(int t, int64_t N, int64_t h, int64
             if (overlap(sr, span_of(A[q], N, h, lda, es))) return CAAT_ERR_INVALID_ARG;
             if (q > r && overlap(sr, span_of(dA[q], N, h, ldda, es))) return CAAT_ERR_INVALID_ARG;
         }
-        if (overlap(sr, span_of(dZ, N, K, ldz, es))) return CAAT_ERR_INVALID_ARG;
+        if (overlap(sr, span_of(dZ, N, K, ldz, es)) || overlap(sr, span_strided(W1, h, K, w1_rs, w1_cs, es)) ||
+            overlap(sr, span_sel(sel, n_sel)))
+            return CAAT_ERR_INVALID_ARG;
         a.p[r] = A[r];
     }
     float *wacc = nullptr;
     if (workspace != nullptr && ((uintptr_t)workspace & 255) == 0 && wacc_region_bytes(K, h, dt) > 0 &&
         ws_bytes >= wacc_region_bytes(K, h, dt))
         wacc = (float *)workspace;
+    {
+        const Span w_dw = span_strided(dW1, h, K, dw1_rs, dw1_cs, es);
+        const Span w_ws = span_bytes(wacc, wacc != nullptr ? wacc_region_bytes(K, h, dt) : 0);
+        if (overlap(w_dw, w_ws)) return CAAT_ERR_INVALID_ARG;
+        for (const Span &o : {w_dw, w_ws}) {
+            if (overlap(o, span_of(dZ, N, K, ldz, es)) || overlap(o, span_strided(W1, h, K, w1_rs, w1_cs, es)) ||
+                overlap(o, span_sel(sel, n_sel)))
+                return CAAT_ERR_INVALID_ARG;
+            for (int r = 0; r < t; ++r)
+                if (overlap(o, span_of(A[r], N, h, lda, es)) || overlap(o, span_of(dA[r], N, h, ldda, es)))
+                    return CAAT_ERR_INVALID_ARG;
+        }
+    }
     const cudaStream_t s = (cudaStream_t)stream;
     // dW1 and dA only read shared inputs: dW1 runs on the side stream next to dA
     SideStream *side = (N > 0 && K > 0 && h > 0) ? side_stream(s) : nullptr;

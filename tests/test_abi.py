@@ -111,6 +111,9 @@ def test_layer_rejects_bad_args_without_launch(lib):
     assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y0]), 8, sel, 2, None) == 1
     # n_sel > h
     assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, sel, 9, None) == 1
+    # an output overlaps W (column-major [8, 8] bf16: 128 bytes from W) or the index list
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, W + 64]), 8, sel, 2, None) == 1
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, (5 << 20) - 16]), 8, sel, 2, None) == 1
     g = lib.caat_rowpar_linear_bwd
     f_ws = lib.caat_rowpar_linear_bwd_workspace
     # two [4, 8] bf16 buffers (256-byte rounded) + fp32 dW accumulator [8, 8] (256 bytes)
@@ -124,6 +127,23 @@ def test_layer_rejects_bad_args_without_launch(lib):
     # bad mode
     assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, 6 << 20, 8, 7 << 20, 1, 8,
              sel, 2, 9, None, 0, None) == 1
+    # written regions that overlap an input or each other (mode NO_REDUCE: no workspace
+    # needed, so only the overlap can fail the call)
+    dX, dW = 6 << 20, 7 << 20
+    assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, Y1 + 32, 8, dW, 1, 8,
+             sel, 2, 1, None, 0, None) == 1                       # dX over a gradient
+    assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, dX, 8, X + 16, 1, 8,
+             sel, 2, 1, None, 0, None) == 1                       # dW over X
+    assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, dX, 8, W, 1, 8,
+             sel, 2, 1, None, 0, None) == 1                       # dW over W
+    assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, dX, 8, dX + 32, 1, 8,
+             sel, 2, 1, None, 0, None) == 1                       # dX and dW overlap
+    # the used workspace (256-byte aligned) over dX, and over a gradient
+    ws = 8 << 20
+    assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, Y1]), 8, ws + 64, 8, dW, 1, 8,
+             sel, 2, 0, ws, 768, None) == 1
+    assert g(2, 4, 8, 8, 1, X, 8, W, 1, 8, _ptrs([Y0, ws + 256]), 8, dX, 8, dW, 1, 8,
+             sel, 2, 0, ws, 768, None) == 1
 
 
 def test_colpar_rejects_bad_args_without_launch(lib):
@@ -142,6 +162,8 @@ def test_colpar_rejects_bad_args_without_launch(lib):
     assert f(2, 4, 8, 8, 1, _ptrs([A0, Z]), 8, W1, 8, 1, Z, 8, None) == 1
     # null input pointer
     assert f(2, 4, 8, 8, 1, _ptrs([A0, 0]), 8, W1, 8, 1, Z, 8, None) == 1
+    # Z overlaps W1
+    assert f(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, W1 + 32, 8, None) == 1
     g = lib.caat_colpar_linear_bwd
     dZ, dA0, dA1, dW1 = 6 << 20, 7 << 20, 8 << 20, 9 << 20
     # optional fp32 accumulator of dW1 [8, 8]: 256 bytes; none for fp32
@@ -162,6 +184,18 @@ def test_colpar_rejects_bad_args_without_launch(lib):
     # ldda < h
     assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA1]), 4,
              dW1, 8, 1, sel, 2, None, 0, None) == 1
+    # dA overlaps W1; dW1 overlaps dZ, an input block or an output block
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, W1 + 16]), 8,
+             dW1, 8, 1, sel, 2, None, 0, None) == 1
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA1]), 8,
+             dZ + 16, 8, 1, sel, 2, None, 0, None) == 1
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA1]), 8,
+             A1, 8, 1, sel, 2, None, 0, None) == 1
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA1]), 8,
+             dA1 + 8, 8, 1, sel, 2, None, 0, None) == 1
+    # the fp32 accumulator (256-byte aligned workspace) over dZ
+    assert g(2, 4, 8, 8, 1, _ptrs([A0, A1]), 8, W1, 8, 1, dZ, 8, _ptrs([dA0, dA1]), 8,
+             dW1, 8, 1, sel, 2, dZ, 256, None) == 1
 
 
 def test_status_strings(lib):
