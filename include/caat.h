@@ -106,7 +106,8 @@ caat_status caat_select_channels(int64_t h, double p, caat_layout layout, uint64
  * in:     host array of t device pointers, each [N, h] with row stride ld_in.
  * out:    host array of t device pointers, each [N, h] with row stride ld_out.
  *         out may equal in (in place: then only the channels of S are written).
- *         Otherwise the t outputs must not overlap any input.
+ *         Otherwise the t outputs must not overlap any input.  No output may
+ *         overlap sel.
  * sel:    device int32[n_sel], ascending, unique, each in [0, h)  (S);
  *         or null, which means the contiguous S = {0, ..., n_sel-1}.
  * Errors: INVALID_ARG for t out of range, negative sizes, ld < h, null pointers,

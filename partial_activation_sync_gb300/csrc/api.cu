@@ -115,6 +115,7 @@ extern "C" caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, 
     if (in_place && ld_in != ld_out) return CAAT_ERR_INVALID_ARG;
     for (int r = 0; r < t; ++r) {
         const Span so = span_of(out[r], N, h, ld_out, es);
+        if (overlap(so, span_sel(sel, n_sel))) return CAAT_ERR_INVALID_ARG;
         for (int q = 0; q < t; ++q) {
             if (q != r && overlap(so, span_of(out[q], N, h, ld_out, es))) return CAAT_ERR_INVALID_ARG;
             if (!in_place && overlap(so, span_of(in[q], N, h, ld_in, es))) return CAAT_ERR_INVALID_ARG;

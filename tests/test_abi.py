@@ -93,6 +93,7 @@ def test_pcr_rejects_bad_args_without_launch(lib):
     assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([b + 16, c]), 8, sel, 2, None) == 1  # out hits in
     assert f(2, 4, 8, 0, _ptrs([a, 0]), 8, _ptrs([b, c]), 8, sel, 2, None) == 1  # null pointer
     assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([a, b]), 16, sel, 2, None) == 1  # in place, ld differ
+    assert f(2, 4, 8, 0, _ptrs([a, b]), 8, _ptrs([c, (4 << 20) - 8]), 8, sel, 2, None) == 1  # out hits sel
 
 
 def test_layer_rejects_bad_args_without_launch(lib):
