@@ -95,6 +95,22 @@ def _rowmajor(t, name):
     return t.stride(0) if t.shape[0] > 1 else max(t.shape[1], 1)
 
 
+def _check_like(x, shape, dtype, name):
+    """A tensor the library writes: it must have the shape and dtype the call
+    implies, or the kernels would write past its end."""
+    if tuple(x.shape) != tuple(shape) or x.dtype != dtype or not x.is_cuda:
+        raise ValueError("caat: %s must be a CUDA tensor %s of dtype %s" % (name, list(shape), dtype))
+
+
+def _workspace(workspace):
+    """(pointer, bytes) of a caller's workspace tensor (contiguous, on the GPU)."""
+    if workspace is None:
+        return None, 0
+    if not workspace.is_cuda or not workspace.is_contiguous():
+        raise ValueError("caat: workspace must be a contiguous CUDA tensor")
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
 def _sel_ptr(sel):
     """S as a device index tensor, or an int n for the contiguous S = {0, ..., n-1}
     (passed to the library as a null pointer), or None for the empty set."""
@@ -204,21 +220,24 @@ def rowpar_linear_bwd(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
     ldd = _same_layout(dOut, (N, h), "dOut")
     if dOut[0].dtype != X.dtype:
         raise TypeError("caat: dOut must have X's dtype")
+    if W.dtype != X.dtype:
+        raise TypeError("caat: X and W must share a dtype")
     if dX is None:
         dX = torch.empty((N, K), dtype=X.dtype, device=X.device)
+    _check_like(dX, (N, K), X.dtype, "dX")
     lddx = _rowmajor(dX, "dX")
     if dW is None:
         if w_rs == 1:    # same layout as an nn.Linear weight: [h, K] storage
             dW = torch.empty((h, K), dtype=X.dtype, device=X.device).t()
         else:
             dW = torch.empty((K, h), dtype=X.dtype, device=X.device)
+    _check_like(dW, (K, h), X.dtype, "dW")
     dw_rs, dw_cs = _weight_strides(dW, K, h)
     dt = _dtype_code(X)
     need = rowpar_linear_bwd_workspace(t, N, K, h, dt, mode)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
-    wp = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
-    wb = workspace.numel() if workspace is not None else 0
+    wp, wb = _workspace(workspace)
     sp, ns = _sel_ptr(sel)
     st = _lib.load().caat_rowpar_linear_bwd(
         int(t), N, K, h, dt, ctypes.c_void_p(X.data_ptr()), ldx,
@@ -294,16 +313,17 @@ def colpar_linear_bwd(A, W1, dZ, t: int, sel, dA=None, dW1=None, workspace=None,
     if dA is None:
         ret_dA = torch.empty((t, N, h), dtype=W1.dtype, device=W1.device)
     dAs, _, ldda = _rank_inputs(ret_dA, t, h, "dA")
+    _check_like(dAs[0], (N, h), W1.dtype, "dA")
     if dW1 is None:
         dW1 = torch.empty_strided((h, K), W1.stride(), dtype=W1.dtype, device=W1.device)
+    _check_like(dW1, (h, K), W1.dtype, "dW1")
     dw1_rs, dw1_cs = _w1_strides(dW1, h, K, "dW1")
     dt = _dtype_code(W1)
     if workspace is None:
         need = colpar_linear_bwd_workspace(t, N, h, K, dt)
         if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=W1.device)
-    wp = ctypes.c_void_p(workspace.data_ptr()) if workspace is not None else None
-    wb = workspace.numel() if workspace is not None else 0
+    wp, wb = _workspace(workspace)
     sp, ns = _sel_ptr(sel)
     st = _lib.load().caat_colpar_linear_bwd(
         int(t), N, h, K, dt, _lib.ptr_array([a.data_ptr() for a in A]), lda,
@@ -343,8 +363,16 @@ def rowpar_linear_bwd_noalloc(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDU
     N, K = X.shape
     h = W.shape[1]
     w_rs, w_cs = _weight_strides(W, K, h)
+    if W.dtype != X.dtype:
+        raise TypeError("caat: X and W must share a dtype")
+    if len(dOut) != t:
+        raise ValueError("caat: need t upstream gradients")
+    ldd = _same_layout(dOut, (N, h), "dOut")
+    if dOut[0].dtype != X.dtype:
+        raise TypeError("caat: dOut must have X's dtype")
+    _check_like(dX, (N, K), X.dtype, "dX")
+    _check_like(dW, (K, h), X.dtype, "dW")
     dw_rs, dw_cs = _weight_strides(dW, K, h)
-    ldd = _rowmajor(dOut[0], "dOut[0]")
     sp, ns = _sel_ptr(sel)
     st = f(int(t), N, K, h, _dtype_code(X), ctypes.c_void_p(X.data_ptr()), _rowmajor(X, "X"),
            ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
