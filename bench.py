@@ -456,8 +456,25 @@ def run_extras(torch, caat, device, peaks):
     fn = lambda: caat.partial_channel_reduce(ins, sel, outs=outs)  # noqa: E731
     fn()
     sec = _time_call(torch, fn, 50)
-    out["pcr_f32_t2_256x768"] = {"GB/s": round(2.0 * 2 * 256 * 768 * 4 / sec / 1e9, 1),
-                                 "us": round(sec * 1e6, 2)}
+    # the same call 100 times in one CUDA graph: device time per call without the
+    # launch cost of each (the case is launch-latency bound)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(100):
+            fn()
+    graph.replay()
+    sec_g = _time_call(torch, graph.replay, 20) / 100
+    pcr_bytes = 2.0 * 2 * 256 * 768 * 4
+    out["pcr_f32_t2_256x768"] = {"GB/s": round(pcr_bytes / sec / 1e9, 1), "us": round(sec * 1e6, 2),
+                                 "graph_GB/s": round(pcr_bytes / sec_g / 1e9, 1),
+                                 "graph_us": round(sec_g * 1e6, 3)}
+    del graph
     # 7B prefill forward (out-proj K=4096, down-proj K=11008), p = 0.5
     w = ci.WORKLOADS["7b_prefill"]
     S = caat.select_channels(w.h, w.p, 0)
