@@ -149,6 +149,20 @@ class LayerData:
         self.bytes_fwd = 2.0 * (w.N * L.K + L.K * w.h + w.t * w.N * w.h)
 
 
+def job_rate(dist, device, ms_local, flops_per_step, steps):
+    """Whole-job time and throughput of a weak-scaling run: every rank did
+    `steps` steps of `flops_per_step`, so the job did world times one rank's work,
+    in the time of its slowest rank (the maximum over ranks of `ms_local`).
+    Returns (ms, TFLOP/s); dist is torch.distributed or None for one process."""
+    ms, world = float(ms_local), 1
+    if dist is not None:
+        import torch
+        tt = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, world = float(tt.item()), dist.get_world_size()
+    return ms, flops_per_step * steps * world / (ms * 1e-3) / 1e12
+
+
 def run_gpu(args, w):
     import torch
     import partial_activation_sync_gb300 as caat
@@ -230,14 +244,9 @@ def run_gpu(args, w):
     for evs in all_evs:
         for i in range(n_calls):
             per_call[i] += evs[i].elapsed_time(evs[i + 1])
-    total_ms = float(per_call.sum())
-    if dist is not None:
-        tt = torch.tensor([total_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
     flops_step = sum(L.flops_fwd + L.flops_bwd for L in layers)
+    total_ms, tflops = job_rate(dist, device, float(per_call.sum()), flops_step, args.steps)
     ms_step = total_ms / args.steps
-    tflops = flops_step * args.steps * world / (total_ms * 1e-3) / 1e12
 
     # per-call breakdown (ms per step) and the dominant kernel's roofline
     names = []
@@ -394,14 +403,9 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
     run(args.steps)
     e1.record(comp)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist is not None:
-        tt = torch.tensor([ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    world = dist.get_world_size() if dist is not None else 1
     flops = sum(L.flops_fwd + L.flops_bwd for L in layers)
-    return {"value": round(flops * args.steps * world / (ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+    ms, rate = job_rate(dist, device, e0.elapsed_time(e1), flops, args.steps)
+    return {"value": round(rate, 3), "unit": "TFLOP/s",
             "ms_per_step": round(ms / args.steps, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "overlap": "inputs of step i+1 and results of step i-1 copy on two streams while step i computes"}
