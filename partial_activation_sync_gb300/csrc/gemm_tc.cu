@@ -626,7 +626,7 @@ caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMa
     if (groups > num_units) groups = num_units;
     cfg.gridDim = dim3(groups * per);
     if (cudaLaunchKernelEx(&cfg, kern, tmX, tmW, ym, p) != cudaSuccess) return CAAT_ERR_CUDA;
-    note_launch(PAIR ? "rowpar_fwd_tc" : "rowpar_fwd_tc");
+    note_launch("rowpar_fwd_tc");
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }
 
