@@ -1,16 +1,18 @@
 """Benchmark of the fused row-parallel GEMM + partial channel-reduce hot path.
 
 One step = one pass of the whole path over one synthetic batch of the chosen
-workload (default: the 130M-shaped layers, h = 768, FFN 3072, t = 8 emulated
-tensor-parallel ranks, N = 8 x 1024 tokens, p = 0.5): for each row-parallel layer
-(attention out-projection K = 768, MLP down-projection K = 3072) the fused
-forward (GEMM + partial channel-reduce into t rank outputs) and the backward
-(partial reduce of the upstream gradient, dX, dW).  Metric: algorithmic TFLOP/s
-(2NKh forward + 4NKh backward per layer, independent of p).
+workload.  Default: the Llama2-7B-shaped layers at prefill (h = 4096, t = 8
+emulated tensor-parallel ranks, N = 4096 tokens, p = 0.5, contiguous S): the
+fused forward (GEMM + partial channel-reduce into t rank outputs) of the
+attention out-projection (K = 4096) and of the MLP down-projection (K = 11008).
+The training workloads (130M, 1.1B) add each layer's backward (partial reduce
+of the upstream gradient, dX, dW).  Metric: algorithmic TFLOP/s (2NKh forward,
+4NKh backward per layer, independent of p).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl caat|reference]
-                  [--workload 130m|1.1b|7b_prefill|7b_decode8|130m_stack] [--layout contiguous|random]
-                  [--p P] [--placement reduce_dout|column] [--no-extras]
+                  [--workload 7b_prefill|130m|1.1b|7b_decode8|130m_stack]
+                  [--layout contiguous|random] [--p P] [--placement reduce_dout|column]
+                  [--no-extras] [--no-stack]
 
 Under torchrun each rank runs its own replica on its own GPU (no collective on
 the data path; weak scaling); rank 0 prints one JSON line.  ``--impl reference``
@@ -163,10 +165,9 @@ def job_rate(dist, device, ms_local, flops_per_step, steps):
     return ms, flops_per_step * steps * world / (ms * 1e-3) / 1e12
 
 
-def run_gpu(args, w):
+def _setup_dist():
+    """(dist or None, rank, world, device) of this process (one GPU per rank)."""
     import torch
-    import partial_activation_sync_gb300 as caat
-
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -177,103 +178,132 @@ def run_gpu(args, w):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     else:
         torch.cuda.set_device(0)
-    device = torch.device("cuda", torch.cuda.current_device())
-    peaks = _peaks()
+    return dist, rank, world, torch.device("cuda", torch.cuda.current_device())
 
-    S = caat.select_channels(w.h, w.p, w.layout, w.seeds()["perm"])
-    # a contiguous S is passed by its size (the library's null-index form)
-    sel = int(S.size) if w.layout == 0 else torch.from_numpy(S).to(device)
-    layers = [LayerData(torch, w, i, device) for i in range(len(w.layers))]
-    ws_bytes = max(max(caat.rowpar_linear_bwd_workspace(w.t, w.N, L.K, w.h, 1, 0) for L in w.layers), 256)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
-    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream()
 
-    def flush_l2():
-        # read a buffer twice the L2 size: evicts the previous step's data and
-        # leaves clean lines (a write-flush would leave 129 MB of dirty lines whose
-        # write-back then competes with the next kernel's writes)
-        return flush.sum()
+class LayerStep:
+    """One workload's layers resident on the device, with its channel set and the
+    backward workspace: `run(evs)` issues one step (every layer's fused forward,
+    then its backward when the workload trains), recording an event before each
+    call and one after the last."""
 
-    def step(evs=None):
+    def __init__(self, torch, caat, w, device):
+        self.torch, self.caat, self.w = torch, caat, w
+        S = caat.select_channels(w.h, w.p, w.layout, w.seeds()["perm"])
+        # a contiguous S is passed by its size (the library's null-index form)
+        self.sel = int(S.size) if w.layout == 0 else torch.from_numpy(S).to(device)
+        self.layers = [LayerData(torch, w, i, device) for i in range(len(w.layers))]
+        ws_bytes = max([caat.rowpar_linear_bwd_workspace(w.t, w.N, L.K, w.h, 1, 0) for L in w.layers] + [256])
+        self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+        self.names = []
+        for L in self.layers:
+            self.names.append("fwd_" + L.name)
+            if w.backward:
+                self.names.append("bwd_" + L.name)
+        self.flops = sum(L.flops_fwd + L.flops_bwd for L in self.layers)
+
+    def run(self, evs=None):
+        caat, w, stream = self.caat, self.w, self.torch.cuda.current_stream()
         k = 0
-        for L in layers:
+        for L in self.layers:
             if evs is not None:
                 evs[k].record(stream); k += 1
-            caat.rowpar_linear_fwd(L.X, L.W, w.t, sel, outs=L.Y)
+            caat.rowpar_linear_fwd(L.X, L.W, w.t, self.sel, outs=L.Y)
             if w.backward:
                 if evs is not None:
                     evs[k].record(stream); k += 1
-                caat.rowpar_linear_bwd(L.X, L.W, L.G, w.t, sel, caat.CAAT_BWD_REDUCE_DOUT,
-                                       dX=L.dX, dW=L.dW, workspace=ws)
+                caat.rowpar_linear_bwd(L.X, L.W, L.G, w.t, self.sel, caat.CAAT_BWD_REDUCE_DOUT,
+                                       dX=L.dX, dW=L.dW, workspace=self.ws)
         if evs is not None:
             evs[k].record(stream)
 
-    n_calls = len(layers) * (2 if w.backward else 1)
-    for _ in range(args.warmup):
-        step()
-        flush_l2()
+
+def time_steps(torch, caat, ls, steps, warmup, device, dist=None, clocks=None):
+    """W untimed warm-up steps, then exactly `steps` timed steps between a barrier
+    and a synchronize on both sides.  Every call of a step is bracketed by CUDA
+    events on the launching stream; an untimed spin kernel before each step lets
+    the host queue the whole step (its calls then run back to back), and the L2 is
+    flushed between steps by reading a buffer twice its size (untimed).
+    Returns (per-call ms summed over the steps, library launches in the region,
+    clock record or None)."""
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    n_calls = len(ls.names)
+    for _ in range(warmup):
+        ls.run()
+        flush.sum()
     torch.cuda.synchronize()
     assert caat.device_status() == 0
-
-    clocks = ClockSampler(device.index)
-    clocks.start()
-    time.sleep(0.3)
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
     launches0 = caat.launch_count()
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     all_evs = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_calls + 1)]
-        # untimed head start: the GPU spins (~200 us) while the host queues the
-        # whole step, so the step's kernels then run back to back and no host
-        # launch work falls inside the timed region
         torch.cuda._sleep(STEP_SPIN_CYCLES)
-        step(evs)
+        ls.run(evs)
         all_evs.append(evs)
-        flush_l2()                            # L2 flush between timed steps (not timed)
+        flush.sum()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     launches = caat.launch_count() - launches0
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks is not None else None
     assert caat.device_status() == 0
-
     per_call = np.zeros(n_calls)
     for evs in all_evs:
         for i in range(n_calls):
             per_call[i] += evs[i].elapsed_time(evs[i + 1])
-    flops_step = sum(L.flops_fwd + L.flops_bwd for L in layers)
-    total_ms, tflops = job_rate(dist, device, float(per_call.sum()), flops_step, args.steps)
-    ms_step = total_ms / args.steps
+    del flush
+    return per_call, launches, clk
 
-    # per-call breakdown (ms per step) and the dominant kernel's roofline
-    names = []
-    for L in layers:
-        names.append("fwd_" + L.name)
-        if w.backward:
-            names.append("bwd_" + L.name)
-    breakdown = {n: round(float(v) / args.steps, 4) for n, v in zip(names, per_call)}
-    fwd_idx = [i for i, n in enumerate(names) if n.startswith("fwd_")]
+
+def roofline_of(ls, per_call, steps, peaks, kernel_name):
+    """Roofline object of the dominant forward call of a step: algorithmic FLOPs
+    (or bytes, below the ridge) per launch over its mean event-timed duration."""
+    w = ls.w
+    fwd_idx = [i for i, n in enumerate(ls.names) if n.startswith("fwd_")]
     dom = max(fwd_idx, key=lambda i: per_call[i])
-    Ld = layers[fwd_idx.index(dom)]
-    t_dom = per_call[dom] / args.steps * 1e-3
+    Ld = ls.layers[fwd_idx.index(dom)]
+    t_dom = per_call[dom] / steps * 1e-3
     ai = Ld.flops_fwd / Ld.bytes_fwd
     ridge = peaks["bf16"] * 1e12 / (peaks["hbm"] * 1e9)
     if ai >= ridge:
         ach = Ld.flops_fwd / t_dom / 1e12
-        roof = {"kernel": "rowpar_fwd (%s, %s)" % (Ld.name, caat.last_kernel()), "bound": "tensor",
+        roof = {"kernel": "%s (%s forward)" % (kernel_name, Ld.name), "bound": "tensor",
                 "achieved": round(ach, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
                 "frac": round(ach / peaks["bf16"], 4)}
+        roof["peak_kind"] = "dense bf16 burst (cuBLAS 8192^3, best of 10)"
     else:
         ach = Ld.bytes_fwd / t_dom / 1e9
-        roof = {"kernel": "rowpar_fwd (%s)" % Ld.name, "bound": "hbm",
+        roof = {"kernel": "%s (%s forward)" % (kernel_name, Ld.name), "bound": "hbm",
                 "achieved": round(ach, 1), "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": round(ach / peaks["hbm"], 4)}
-    roof["peak_source"] = peaks["source"] + " (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "fallback"
+        roof["peak_kind"] = "copy bandwidth (read + write)"
+    roof["peak_source"] = "of measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "of fallback"
     roof["traffic"] = DRAM_TRAFFIC.get((w.name, Ld.name))
     roof["algorithmic_per_launch"] = {"flops": Ld.flops_fwd, "bytes": Ld.bytes_fwd}
+    roof["us_per_launch"] = round(t_dom * 1e6, 2)
+    return roof
+
+
+def run_gpu(args, w):
+    import torch
+    import partial_activation_sync_gb300 as caat
+
+    dist, rank, world, device = _setup_dist()
+    peaks = _peaks()
+    ls = LayerStep(torch, caat, w, device)
+    clocks = ClockSampler(device.index)
+    per_call, launches, clk = time_steps(torch, caat, ls, args.steps, args.warmup, device, dist, clocks)
+    kernel_name = caat.last_kernel()
+    total_ms, tflops = job_rate(dist, device, float(per_call.sum()), ls.flops, args.steps)
+    ms_step = total_ms / args.steps
+    breakdown = {n: round(float(v) / args.steps, 4) for n, v in zip(ls.names, per_call)}
+    roof = roofline_of(ls, per_call, args.steps, peaks, "rowpar_fwd_tc" if w.N > 64 else kernel_name)
 
     result = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world,
@@ -281,7 +311,7 @@ def run_gpu(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations/gradients, N(0,0.02) weights)",
         "config": {"workload": w.name, "t": w.t, "N": w.N, "h": w.h,
-                   "layers": {L.name: L.K for L in layers}, "p": w.p,
+                   "layers": {L.name: L.K for L in ls.layers}, "p": w.p,
                    "S": "contiguous" if w.layout == 0 else "random",
                    "fwd_and_bwd": bool(w.backward),
                    "l2": "flushed between timed steps by reading a 2x L2 buffer (untimed)",
@@ -294,13 +324,13 @@ def run_gpu(args, w):
         "roofline": roof,
     }
 
-    # end to end through the public API with host buffers (pinned), per step:
-    # H2D of the step's activations X and upstream gradients dOut, D2H of dX, dW
-    e2e = run_e2e(torch, caat, w, layers, sel, ws, args, device, dist)
-    result["e2e"] = e2e
+    # end to end through the public API with host buffers (pinned), per step
+    result["e2e"] = run_e2e(torch, caat, w, ls.layers, ls.sel, ls.ws, args, device, dist)
+    del ls
+    torch.cuda.empty_cache()
 
     if rank == 0 and not args.no_extras:
-        result["extras"] = run_extras(torch, caat, device, peaks)
+        result["extras"] = run_extras(torch, caat, device, peaks, args)
     if rank == 0:
         result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
     if dist is not None:
@@ -311,7 +341,7 @@ def run_gpu(args, w):
 def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
     """End to end through the public API with host buffers: every step copies its
     inputs (X and the t upstream gradients of every layer) from pinned host memory
-    and reads its results (dX and dW, or rank 0's output without a backward) back.
+    and reads its results (dX and dW; without a backward, all t rank outputs) back.
 
     The copies run on their own streams and overlap the compute of the neighbouring
     steps: step i+1's inputs go in while step i computes, and step i-1's results come
@@ -341,13 +371,14 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
     sets = [dev_set(True), dev_set(False)]
     outs = [[{"dX": torch.empty(L.dX.shape, dtype=torch.int16).pin_memory(),
               "dW": torch.empty(L.dWstore.shape, dtype=torch.int16).pin_memory(),
-              "Y0": torch.empty(L.Y[0].shape, dtype=torch.int16).pin_memory()} for L in layers]
+              "Y": ([torch.empty(y.shape, dtype=torch.int16).pin_memory() for y in L.Y]
+                    if not w.backward else [])} for L in layers]
             for _ in range(2)]
     h2d = sum(x.numel() * 2 for x in hostX) + sum(g.numel() * 2 for gs in hostG for g in gs)
     if w.backward:
         d2h = sum(L.dX.numel() * 2 + L.dWstore.numel() * 2 for L in layers)
     else:
-        d2h = sum(L.Y[0].numel() * 2 for L in layers)
+        d2h = sum(y.numel() * 2 for L in layers for y in L.Y)
     in_ready = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
     out_done = [torch.cuda.Event() for _ in range(2)]
@@ -381,7 +412,8 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
                     O[li]["dX"].copy_(B["dX"].view(torch.int16), non_blocking=True)
                     O[li]["dW"].copy_(B["dWs"].view(torch.int16), non_blocking=True)
                 else:
-                    O[li]["Y0"].copy_(B["Y"][0].view(torch.int16), non_blocking=True)
+                    for r in range(w.t):
+                        O[li]["Y"][r].copy_(B["Y"][r].view(torch.int16), non_blocking=True)
             out_done[j].record(d2h_s)
 
     def run(n):
@@ -432,11 +464,27 @@ def _time_call(torch, fn, reps, flush=None):
     return statistics.median(a.elapsed_time(b) for a, b in ts) * 1e-3
 
 
-def run_extras(torch, caat, device, peaks):
-    """Short side measurements for the two targets named with the metric: the
-    fused forward at Llama2-7B prefill shapes (tensor-bound) and the standalone
-    reduce on a working set far above L2 (HBM-bound)."""
+def run_extras(torch, caat, device, peaks, args):
+    """Side measurements next to the headline step: the 130M-shaped training step
+    (forward and backward of both row-parallel layers) with its own roofline, the
+    standalone reduce on a working set far above L2 (HBM-bound) and at the small
+    fp32 configuration, Llama2-7B decode, the column-parallel layer, and the
+    full 130M CAAT-Net training step in both placements of the backward reduce."""
     out = {}
+    # 130M-shaped layers, forward + backward, p = 0.5 contiguous
+    w130 = ci.WORKLOADS["130m"]
+    ls = LayerStep(torch, caat, w130, device)
+    steps130 = 10
+    per_call, launches, _ = time_steps(torch, caat, ls, steps130, 3, device)
+    ms = float(per_call.sum()) / steps130
+    out["130m_step"] = {
+        "TFLOP/s": round(ls.flops / (ms * 1e-3) / 1e12, 1), "ms": round(ms, 4),
+        "frac_bf16": round(ls.flops / (ms * 1e-3) / 1e12 / peaks["bf16"], 4),
+        "breakdown_ms": {n: round(float(v) / steps130, 4) for n, v in zip(ls.names, per_call)},
+        "roofline_fwd": roofline_of(ls, per_call, steps130, peaks, "rowpar_fwd_tc"),
+        "gpu_launches_per_step": int(launches) // steps130}
+    del ls
+    torch.cuda.empty_cache()
     flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     # standalone PCR, bf16 and fp32, t=8, [4096, 4096], p=0.5, out of place
     for dt_name, dt, es in (("bf16", torch.bfloat16, 2), ("f32", torch.float32, 4)):
@@ -479,9 +527,9 @@ def run_extras(torch, caat, device, peaks):
                                  "graph_GB/s": round(pcr_bytes / sec_g / 1e9, 1),
                                  "graph_us": round(sec_g * 1e6, 3)}
     del graph
-    # 7B prefill forward (out-proj K=4096, down-proj K=11008), p = 0.5
+    # 7B prefill forward with a random S (seeded permutation), p = 0.5
     w = ci.WORKLOADS["7b_prefill"]
-    S = caat.select_channels(w.h, w.p, 0)
+    S = caat.select_channels(w.h, w.p, caat.CAAT_S_RANDOM, w.seeds()["perm"])
     sel = torch.from_numpy(S).to(device)
     for li, L in enumerate(w.layers):
         X = torch.randn((w.N, L.K), device=device).to(torch.bfloat16)
@@ -491,7 +539,7 @@ def run_extras(torch, caat, device, peaks):
         fn()
         sec = _time_call(torch, fn, 10, flush)
         tf = 2.0 * w.N * L.K * w.h / sec / 1e12
-        out["7b_prefill_fwd_" + L.name] = {
+        out["7b_prefill_random_S_fwd_" + L.name] = {
             "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4),
             "us": round(sec * 1e6, 1), "kernel": caat.last_kernel()}
         del X, Wst, Ys
@@ -532,8 +580,18 @@ def run_extras(torch, caat, device, peaks):
         tf = flops / sec / 1e12
         out[name] = {"TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4),
                      "us": round(sec * 1e6, 1), "kernel": caat.last_kernel()}
-    del A, W1, dZ, Z, dA, dW1, ws
+    del A, W1, dZ, Z, dA, dW1, ws, flush
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    # the full 130M CAAT-Net training step (forward, backward, AdamW), both
+    # placements of the backward reduce
+    if not args.no_stack:
+        for placement in ("reduce_dout", "column"):
+            r = stack_rate(placement, steps=5, warmup=3)
+            out["130m_stack_" + placement] = {
+                "tokens/s": r["value"], "ms_per_step": r["ms_per_step"],
+                "gpu_launches_per_step": r["gpu_launches"] // 5, "loss_last": r["loss_last"]}
+            torch.cuda.empty_cache()
     return out
 
 
@@ -621,10 +679,90 @@ def run_reference(args, w):
                     "d2h_bytes_per_step": 0}}
 
 
+PCR_WORKLOADS = {"pcr_bf16_t8_4096x4096": ("bf16", 8, 4096, 4096),
+                 "pcr_f32_t8_4096x4096": ("f32", 8, 4096, 4096)}
+
+
+def run_pcr(args):
+    """The standalone partial channel-reduce as the step: t = 8 partial tensors of
+    [4096, 4096], p = 0.5 (S = the first 2048 channels, as an index list), out of
+    place.  Metric: algorithmic GB/s = 2 t N h bytes per call (every input read
+    once, every output written once) over its event-timed duration."""
+    import torch
+    import partial_activation_sync_gb300 as caat
+    dist, rank, world, device = _setup_dist()
+    peaks = _peaks()
+    dname, t, N, h = PCR_WORKLOADS[args.workload]
+    dt, es = (torch.bfloat16, 2) if dname == "bf16" else (torch.float32, 4)
+    Y = [torch.from_numpy(ci.normal(5000 + r, (N, h))).to(device).to(dt) for r in range(t)]
+    outs = [torch.empty_like(y) for y in Y]
+    sel = torch.from_numpy(caat.select_channels(h, 0.5)).to(device)
+    flush = torch.ones(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    for _ in range(args.warmup):
+        caat.partial_channel_reduce(Y, sel, outs=outs)
+        flush.sum()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = caat.launch_count()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    evs = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(100000)
+        a.record(stream)
+        caat.partial_channel_reduce(Y, sel, outs=outs)
+        b.record(stream)
+        evs.append((a, b))
+        flush.sum()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    launches = caat.launch_count() - launches0
+    clk = clocks.stop()
+    assert caat.device_status() == 0
+    ms_local = sum(a.elapsed_time(b) for a, b in evs)
+    byts = 2.0 * t * N * h * es
+    ms, world_n = float(ms_local), 1
+    if dist is not None:
+        tt = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms, world_n = float(tt.item()), dist.get_world_size()
+    gbs = byts * args.steps * world_n / (ms * 1e-3) / 1e9
+    per = ms / args.steps
+    res = {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world_n,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per, 5),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": dname,
+           "data": "synthetic (seeded N(0,1) partial tensors)",
+           "config": {"workload": args.workload, "t": t, "N": N, "h": h, "p": 0.5,
+                      "S": "first 2048 channels (index list)", "in_place": False,
+                      "l2": "flushed between timed steps by reading a 2x L2 buffer (untimed)"},
+           "gpu_launches": int(launches), "clocks": clk,
+           "roofline": {"kernel": caat.last_kernel(), "bound": "hbm",
+                        "achieved": round(byts / (per * 1e-3) / 1e9, 1), "peak": peaks["hbm"],
+                        "unit": "GB/s", "frac": round(byts / (per * 1e-3) / 1e9 / peaks["hbm"], 4),
+                        "peak_source": "of measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured"
+                        else "of fallback",
+                        "traffic": DRAM_TRAFFIC.get((args.workload, "pcr")),
+                        "algorithmic_per_launch": {"bytes": byts}}}
+    if dist is not None:
+        dist.destroy_process_group()
+    return res if rank == 0 else None
+
+
 STACK_METRIC = "130M CAAT-Net training step tokens/s (t=8 emulated ranks, p=0.5), 1 GPU"
 
 
 def run_stack(args):
+    """The full 130M block stack as the step (see stack_rate), with clocks and e2e."""
+    return stack_rate(args.placement, args.steps, args.warmup, full=True)
+
+
+def stack_rate(placement, steps, warmup, full=False):
     """The full 130M block stack, one training step = forward, backward, AdamW:
     12 layers, 16 heads, h = 768, FFN 3072, RoPE, sequence 1024, batch 8, t = 8
     emulated ranks, p = 0.5; token ids uniform over a 32000 vocabulary; random
@@ -638,31 +776,32 @@ def run_stack(args):
     torch.manual_seed(5)
     vocab, batch, seq = 32000, 8, 1024
     model = CAATNet(vocab=vocab, h=768, heads=16, layers=12, ffn=3072, t=8, p=0.5, seq=seq,
-                    placement=args.placement)
+                    placement=placement)
     model = model.cuda().to(torch.bfloat16)
     opt = torch.optim.AdamW(model.parameters(), lr=6e-4, fused=True)
     rng = np.random.default_rng(5005)
     host_tok = [torch.from_numpy(rng.integers(0, vocab, (batch, seq))).pin_memory()
-                for _ in range(args.steps + args.warmup)]
+                for _ in range(steps + warmup)]
     tok = torch.empty((batch, seq), dtype=torch.int64, device="cuda")
     tok.copy_(host_tok[0])
-    for i in range(args.warmup):
+    for i in range(warmup):
         train_step(model, opt, tok)
     torch.cuda.synchronize()
     launches0 = caat.launch_count()
-    clocks = ClockSampler(0)
-    clocks.start()
-    time.sleep(0.3)
+    clocks = ClockSampler(0) if full else None
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
     stream = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for i in range(args.steps):
+    for i in range(steps):
         train_step(model, opt, tok)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    clk = clocks.stop()
+    clk = clocks.stop() if clocks is not None else None
     launches = caat.launch_count() - launches0
     # end to end: each step copies its tokens in and reads the loss back
     out = torch.empty(1, dtype=torch.float32).pin_memory()
@@ -670,26 +809,26 @@ def run_stack(args):
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for i in range(args.steps):
-        tok.copy_(host_tok[args.warmup + i], non_blocking=True)
+    for i in range(steps):
+        tok.copy_(host_tok[warmup + i], non_blocking=True)
         loss = train_step(model, opt, tok)
         out.copy_(loss.float().reshape(1), non_blocking=True)
     f1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = f0.elapsed_time(f1)
     ntok = batch * seq
-    return {"metric": STACK_METRIC, "value": round(ntok * args.steps / (ms * 1e-3), 1), "unit": "tokens/s",
-            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True, "scaling": "weak",
+    return {"metric": STACK_METRIC, "value": round(ntok * steps / (ms * 1e-3), 1), "unit": "tokens/s",
+            "n_gpus": 1, "steps": steps, "warmup": warmup,
+            "ms_per_step": round(ms / steps, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (token ids uniform over 32000, N(0,0.02) weights)",
             "config": {"workload": "130m_stack", "layers": 12, "heads": 16, "h": 768, "ffn": 3072,
                        "seq": seq, "batch": batch, "t": 8, "p": 0.5, "optimizer": "AdamW (fused)",
-                       "placement": args.placement,
+                       "placement": placement,
                        "l2": "working set far above L2"},
             "gpu_launches": int(launches), "clocks": clk,
             "loss_last": round(float(out.item()), 4),
-            "e2e": {"value": round(ntok * args.steps / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
+            "e2e": {"value": round(ntok * steps / (ms_e2e * 1e-3), 1), "unit": "tokens/s",
                     "h2d_bytes_per_step": ntok * 8, "d2h_bytes_per_step": 4}}
 
 
@@ -699,14 +838,15 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["caat", "reference"], default="caat")
-    ap.add_argument("--workload", default="130m",
-                    choices=["130m", "1.1b", "7b_prefill", "7b_decode8", "130m_stack"])
+    ap.add_argument("--workload", default="7b_prefill",
+                    choices=["7b_prefill", "130m", "1.1b", "7b_decode8", "130m_stack"] + list(PCR_WORKLOADS))
     ap.add_argument("--layout", choices=["contiguous", "random"], default=None,
                     help="channel-set layout (default: the workload's own)")
     ap.add_argument("--p", type=float, default=None, help="synchronized fraction (default: workload's)")
     ap.add_argument("--placement", choices=["reduce_dout", "column"], default="reduce_dout",
                     help="130m_stack: where the backward reduce sits")
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-stack", action="store_true", help="leave the 130M stack out of the extras")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()
     if args.warmup < 3:
@@ -717,6 +857,15 @@ def main():
                               "the reference arm times the layer workloads"}), flush=True)
         elif int(os.environ.get("RANK", "0")) == 0:
             print(json.dumps(run_stack(args)), flush=True)
+        return
+    if args.workload in PCR_WORKLOADS:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the standalone-reduce workloads have no "
+                              "CPU arm; the reference arm times the layer workloads"}), flush=True)
+            return
+        res = run_pcr(args)
+        if res is not None:
+            print(json.dumps(res), flush=True)
         return
     w = ci.WORKLOADS[args.workload]
     if args.layout is not None or args.p is not None:

@@ -23,7 +23,7 @@
  *    A caller that drives one host thread on several streams at once shares
  *    that side stream between them (still correct, possibly less concurrent).
  *  - Tuning switches read from the environment at each call (for comparisons
- *    and tests; the defaults choose by shape): CAAT_FWD_CLUSTER=1|2|4 (CTAs per
+ *    and tests; the defaults choose by shape): CAAT_FWD_CLUSTER=1|2 (CTAs per
  *    cluster of the forward tile kernel), CAAT_FWD_BN=192|256 (its tile width),
  *    CAAT_FWD_ORDER=m|n (its work units row- or channel-block-major),
  *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0

@@ -123,7 +123,6 @@ struct Cfg {
     // next chunk fills the other) where shared memory allows, i.e. below 256-wide
     static constexpr int NBUF = BNT < 256 ? 2 : 1;
     static constexpr int B_ROWS = PAIR ? BNT / 2 : BNT;        // W rows (channels) per CTA per stage
-    static constexpr int B_FETCH = CLN == 4 ? B_ROWS / 2 : B_ROWS;   // W rows this CTA fetches
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TX_BYTES = (PAIR ? 2 : 1) * STAGE_BYTES;   // landing per stage (leader)
@@ -194,9 +193,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// CLN = CTAs per cluster: 1 (one CTA per tile), 2 (a CTA pair), 4 (two CTA
-// pairs on adjacent row blocks of the same channel block; the two CTAs that hold
-// the same half of the W tile each fetch half of it and multicast to both).
+// CLN = CTAs per cluster: 1 (one CTA per tile) or 2 (a CTA pair).  Each CTA
+// fetches its own X and W tiles from this GPU's memory; no load is multicast.
 template <int CLN, int BNT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -222,7 +220,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
-            mbar_init(smem_u32(&ctl->empty[s]), CLN == 4 ? 2 : 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
@@ -308,18 +306,8 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                                              nb * BNT + (int)crank * C::B_ROWS, pol_in);
 #else
                             tma_load_3d_pair(smem_u32(smA + stage * A_BYTES), &tmX, fl, kb * BK, r, mb * BM);
-                            if (CLN == 4) {
-                                // this CTA holds W half (crank & 1); it fetches quarter
-                                // (crank >> 1) of that half for itself and for the CTA
-                                // with the same half in the other pair
-                                const uint32_t hh = crank & 1u, pi = crank >> 1;
-                                tma_load_3d_pair_mc(smem_u32(smB + stage * C::B_BYTES + pi * C::B_FETCH * 128), &tmW,
-                                                    fl, kb * BK, r, nb * BNT + (int)(hh * C::B_ROWS + pi * C::B_FETCH),
-                                                    (uint16_t)((1u << hh) | (1u << (2 + hh))));
-                            } else {
-                                tma_load_3d_pair(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
-                                                 nb * BNT + (int)crank * C::B_ROWS);
-                            }
+                            tma_load_3d_pair(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
+                                             nb * BNT + (int)crank * C::B_ROWS);
 #endif
                         } else {
                             mbar_arrive_expect_tx(fb, C::TX_BYTES);
@@ -335,7 +323,6 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && is_leader) {
             const uint16_t pair_mask = (uint16_t)(3u << leader);
-            const uint16_t stage_mask = CLN == 4 ? (uint16_t)0xF : pair_mask;
             int stage = 0;
             uint32_t ph = 0, au = 0;
             for (int u = unit0; u < num_units; u += nunits_grid) {
@@ -371,7 +358,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             if (PAIR) mma_f16_pair(d, ad, bd, C::IDESC, acc);
                             else mma_f16(d, ad, bd, C::IDESC, acc);
                         }
-                        if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), stage_mask);
+                        if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), pair_mask);
                         else mma_commit(smem_u32(&ctl->empty[stage]));
                         if (++stage == C::STAGES) { stage = 0; ph ^= 1u; }
                     }
@@ -653,16 +640,15 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint32_t box[2] = {64, 32};
         if (!encode_tmap(&ym.m[r], Y.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
     }
-    // CTAs per cluster: two CTA pairs sharing the W tile when there are at least
-    // four 128-row blocks, one pair when two, else one CTA per tile.  Short shards
-    // (k_t <= 384) make the t output copies the bottleneck; there the finer
-    // single-CTA tiles balance the writes better over the SMs.
-    // (override: CAAT_FWD_CLUSTER=1|2|4)
+    // CTAs per cluster: a CTA pair when there are at least two 128-row blocks,
+    // else one CTA per tile.  Short shards (k_t <= 384) make the t output copies
+    // the bottleneck; there the finer single-CTA tiles balance the writes better
+    // over the SMs.  (override: CAAT_FWD_CLUSTER=1|2)
     const int64_t nm = (N + BM - 1) / BM;
-    int cln = kt <= 384 ? 1 : (nm >= 4 ? 4 : (nm >= 2 ? 2 : 1));
+    int cln = kt <= 384 ? 1 : (nm >= 2 ? 2 : 1);
     if (const char *e = std::getenv("CAAT_FWD_CLUSTER")) {
         const int v = std::atoi(e);
-        if ((v == 1 || v == 2 || v == 4) && v <= nm) cln = v;
+        if ((v == 1 || v == 2) && v <= nm) cln = v;
     }
 
     CUtensorMap tmX;
@@ -713,19 +699,15 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.num_n = (int)((h + bn - 1) / bn);
         if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;
         CUtensorMap tmW;
-        const uint32_t wrows = cln == 1 ? bn : (cln == 2 ? bn / 2 : bn / 4);
+        const uint32_t wrows = cln == 1 ? bn : bn / 2;
         if (!encode_3d(&tmW, W, (uint64_t)kt, (uint64_t)t, (uint64_t)h, (uint64_t)kt * 2, (uint64_t)ldw * 2,
                        BK, 1, wrows))
             return CAAT_ERR_UNSUPPORTED;
         caat_status st;
         if (bn == 192)
-            st = cln == 4 ? launch_fwd<4, 192>(tmX, tmW, ym, p, s)
-               : cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s)
-                          : launch_fwd<1, 192>(tmX, tmW, ym, p, s);
+            st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s) : launch_fwd<1, 192>(tmX, tmW, ym, p, s);
         else
-            st = cln == 4 ? launch_fwd<4, BN>(tmX, tmW, ym, p, s)
-               : cln == 2 ? launch_fwd<2, BN>(tmX, tmW, ym, p, s)
-                          : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
+            st = cln == 2 ? launch_fwd<2, BN>(tmX, tmW, ym, p, s) : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
         // a cluster shape that cannot be co-resident falls back to a smaller one
         if (st != CAAT_ERR_UNSUPPORTED || cln == 1) return st;
     }

@@ -140,19 +140,6 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Same load, written to the same shared-memory offset of every CTA in ctaMask
-// (thread-block cluster); each destination CTA's mbarrier at offset `bar`
-// receives the byte count.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void *tmap, uint32_t bar, int c0,
-                                               int c1, int c2, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-        : "memory");
-}
-
 // Pair form (cta_group::2): the destination is this CTA's shared memory, the
 // completion goes to the mbarrier at cluster address `bar`, which may belong to
 // the peer CTA of the pair.
@@ -163,19 +150,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
-
-// Pair form with multicast: the tile lands at offset `dst` in every CTA of
-// ctaMask; each destination's completion goes to the mbarrier at offset `bar`
-// of that destination's pair leader.
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const void *tmap, uint32_t bar, int c0,
-                                                    int c1, int c2, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
         : "memory");
 }
 
@@ -305,17 +279,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// Arrive once on the mbarrier at offset `bar` of every CTA in ctaMask when every
-// tcgen05 operation this thread issued so far is done.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar),
-        "h"(mask)
         : "memory");
 }
 

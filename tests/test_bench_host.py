@@ -94,7 +94,7 @@ def test_reference_arm_json_line():
         assert key in d, key
     assert d["impl"] == "reference"
     assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
-    assert d["config"]["workload"] == "130m"
+    assert d["config"]["workload"] == "7b_prefill"
     assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

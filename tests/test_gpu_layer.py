@@ -114,7 +114,7 @@ TC_SHAPES = [
     (1, 128, 128, 256),
     (8, 384, 344, 512),
     (5, 640, 72, 1032),
-    (3, 700, 64, 520),      # six row blocks: the second cluster of four has two idle CTAs
+    (3, 700, 64, 520),      # six row blocks: three CTA pairs, ragged last block
 ]
 # the forward also takes h = 192 (one 192-wide tile; the backward kernels need h >= 256)
 TC_FWD_SHAPES = TC_SHAPES + [
@@ -123,12 +123,12 @@ TC_FWD_SHAPES = TC_SHAPES + [
 ]
 
 
-@pytest.fixture(params=["4", "2", "1", "1/192", "2/192", "4/192", "1:m", "4:m", "1/192:m"])
+@pytest.fixture(params=["2", "1", "1/192", "2/192", "1:m", "2:m", "1/192:m"])
 def fwd_mode(request, monkeypatch):
-    """Cluster shape of the forward: 4 = two CTA pairs sharing W tiles by
-    multicast (the default from four row blocks up), 2 = one CTA pair
-    (cta_group::2, 256-row tiles), 1 = one CTA per 128 x 256 tile; "/192": the
-    same with 192-channel tiles (where h is a multiple of 192)."""
+    """Cluster shape of the forward: 2 = one CTA pair (cta_group::2, 256-row
+    tiles; the default for long shards from two row blocks up), 1 = one CTA per
+    128 x 256 tile; "/192": the same with 192-channel tiles (where h is a
+    multiple of 192)."""
     mode, _, order = request.param.partition(":")    # ":m": row-block-major work order
     cl, _, bn = mode.partition("/")
     monkeypatch.setenv("CAAT_FWD_CLUSTER", cl)
