@@ -207,16 +207,18 @@ caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h, caat_
  * library routine.
  *  - Arguments and results are exactly those of caat_rowpar_linear_bwd (same
  *    pointers, strides and modes), minus workspace / ws_bytes.
- *  - Size limit: in CAAT_BWD_REDUCE_DOUT mode the reduced gradient needs
- *    t * N * h * (2 for bf16, 4 for fp32) bytes of scratch (each rank's part
- *    rounded up to 256 bytes); above 16 MiB the call returns
+ *  - Size limit: in CAAT_BWD_REDUCE_DOUT mode with S not empty and t > 1 the
+ *    reduced gradient needs t * N * h * (2 for bf16, 4 for fp32) bytes of scratch
+ *    (each rank's part rounded up to 256 bytes); above 16 MiB the call returns
  *    CAAT_ERR_INVALID_ARG and launches nothing (use caat_rowpar_linear_bwd with a
- *    workspace instead).  CAAT_BWD_NO_REDUCE needs no scratch.  When the rest of
- *    the array also holds the optional fp32 dW accumulator (h * K * 4 bytes), it
- *    is used for it as well.
+ *    workspace instead).  CAAT_BWD_NO_REDUCE, an empty S or t == 1 need no
+ *    scratch.  When the rest of the array also holds the optional fp32 dW
+ *    accumulator (h * K * 4 bytes), it is used for it as well.
  *  - The first call on a device that needs the scratch looks up the array's device
- *    address (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture.
+ *    address (cudaGetSymbolAddress) with that device current and keeps it for the
+ *    life of the process; make that first call before any stream capture.  The
+ *    kept address does not survive cudaDeviceReset (the array may then move):
+ *    a process that resets a device must not call this entry point on it again.
  *  - All calls in the process share the one array, which keeps the last call's
  *    contents.  Calls whose work overlaps on the GPU (different streams, or other
  *    host threads, without ordering between them) race on it and corrupt each
@@ -297,6 +299,30 @@ const char *caat_status_string(caat_status st);
  * Returns CAAT_ERR_CUDA when the synchronization itself fails.
  */
 caat_status caat_get_device_status(caat_stream_t stream);
+
+/*
+ * caat_debug_set_wait -- test hook for the device-side failure path.  Not part of
+ * the computation; production code leaves it alone.
+ *
+ * Sets, for every later launch of the forward tile kernel (the tcgen05 kernel
+ * that caat_rowpar_linear_fwd uses from 65 tokens up, and caat_colpar_linear_bwd
+ * through it), the limit of each of its mbarrier waits (limit_ns; 0 restores the
+ * default of 2 s; else 1 us .. 10 s) and an injected failure:
+ *   CAAT_INJECT_NONE        normal operation;
+ *   CAAT_INJECT_SKIP_LOADS  the kernel's TMA producer issues no load, so the MMA
+ *                           issuer's first wait for operands can never complete.
+ *                           That wait gives up after limit_ns, the kernel records
+ *                           CAAT_ERR_TIMEOUT, every role leaves its loop, and the
+ *                           CTA exits after releasing its TMEM.  The outputs are
+ *                           then undefined; caat_get_device_status reports (and
+ *                           clears) the timeout.  Nothing is in flight when the
+ *                           kernel ends: no copy and no MMA was ever issued.
+ * The setting is process-wide and read at each launch.  Errors: INVALID_ARG for a
+ * limit outside the range or an unknown injection.
+ */
+typedef enum { CAAT_INJECT_NONE = 0, CAAT_INJECT_SKIP_LOADS = 1 } caat_inject;
+
+caat_status caat_debug_set_wait(uint64_t limit_ns, caat_inject inject);
 
 /*
  * caat_last_kernel -- which kernel the last successful launch on this host

@@ -22,6 +22,7 @@ __all__ = [
     "select_channels", "partial_channel_reduce", "rowpar_linear_fwd", "rowpar_linear_bwd",
     "rowpar_linear_bwd_workspace", "rowpar_linear_bwd_noalloc", "colpar_linear_fwd",
     "colpar_linear_bwd", "colpar_linear_bwd_workspace", "device_status", "last_kernel", "launch_count",
+    "debug_set_wait", "CAAT_INJECT_NONE", "CAAT_INJECT_SKIP_LOADS",
     "CaatError", "CAAT_S_CONTIGUOUS", "CAAT_S_RANDOM", "CAAT_BWD_REDUCE_DOUT",
     "CAAT_BWD_NO_REDUCE",
 ]
@@ -347,6 +348,16 @@ def last_kernel() -> str:
 
 def launch_count() -> int:
     return int(_lib.load().caat_launch_count())
+
+
+CAAT_INJECT_NONE, CAAT_INJECT_SKIP_LOADS = 0, 1
+
+
+def debug_set_wait(limit_ns: int = 0, inject: int = CAAT_INJECT_NONE) -> None:
+    """Test hook of the failure path: the wait limit of the forward tile kernel's
+    mbarrier waits (0 = the default 2 s) and an injected failure
+    (CAAT_INJECT_SKIP_LOADS: its producer issues no load, so a wait runs out)."""
+    _check(_lib.load().caat_debug_set_wait(int(limit_ns), int(inject)), "caat_debug_set_wait")
 
 
 # ------------------------------------------- backward without a workspace

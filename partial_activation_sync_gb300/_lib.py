@@ -26,6 +26,7 @@ EXPORTS = (
     "caat_get_device_status",
     "caat_last_kernel",
     "caat_launch_count",
+    "caat_debug_set_wait",
 )
 
 _lib = None
@@ -82,6 +83,8 @@ def load(path: str = None) -> ctypes.CDLL:
     L.caat_last_kernel.restype = ctypes.c_char_p
     L.caat_launch_count.argtypes = []
     L.caat_launch_count.restype = ctypes.c_uint64
+    L.caat_debug_set_wait.argtypes = [ctypes.c_uint64, ctypes.c_int]
+    L.caat_debug_set_wait.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L

@@ -33,6 +33,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdlib>
 
 #include "caat_internal.h"
@@ -109,6 +110,11 @@ constexpr int STG_BYTES = 32 * 128;          // per epilogue warp: 32 rows x 64 
 constexpr int MAX_STAGES = 6;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legitimate wait
 
+// failure-path test hooks (caat_debug_set_wait): the wait limit and the injected
+// failure the next launches take
+std::atomic<uint64_t> g_wait_ns{WAIT_LIMIT_NS};
+std::atomic<int> g_inject{CAAT_INJECT_NONE};
+
 // Per mode: PAIR = false, one CTA computes a 128 x 256 tile (4 stages of X 128 x 64
 // + W 256 x 64, one staging buffer per epilogue warp); PAIR = true, a CTA pair
 // computes a 256 x 256 tile with one cta_group::2 MMA (5 stages of X 128 x 64 +
@@ -160,6 +166,8 @@ struct FwdParams {
     int mmajor;         // work units ordered row-block-major (else channel-block-major)
     const int32_t *sel;
     int64_t n_sel;
+    uint64_t wait_ns;   // limit of every mbarrier wait
+    int inject;         // CAAT_INJECT_SKIP_LOADS: the producer issues nothing
 };
 
 __device__ __forceinline__ void fail(volatile int *abort)
@@ -280,7 +288,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
-        if (lane == 0) {
+        if (lane == 0 && p.inject != CAAT_INJECT_SKIP_LOADS) {
             int stage = 0;
             uint32_t ph = 0;
 #ifdef EXP_LOAD_HINT
@@ -291,7 +299,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                 const int nb = p.mmajor ? u % p.num_n : u / num_mg;
                 for (int r = 0; r < p.t; ++r) {
                     for (int kb = 0; kb < p.nkb; ++kb) {
-                        if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, WAIT_LIMIT_NS)) {
+                        if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, p.wait_ns)) {
                             fail(abort);
                             goto done;
                         }
@@ -334,7 +342,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                     const uint32_t b = au & 1u;
                     if (starts) {
                         if (!mbar_wait(smem_u32(&ctl->acc_empty[b]), ((au >> 1) & 1u) ^ 1u, abort,
-                                       WAIT_LIMIT_NS)) {
+                                       p.wait_ns)) {
                             fail(abort);
                             goto done;
                         }
@@ -343,7 +351,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                     const bool fresh = cls == FULL_S ? r == 0 : (cls == NO_S ? true : r < 2);
                     const uint32_t d = tmem + b * 256u;
                     for (int kb = 0; kb < p.nkb; ++kb) {
-                        if (!mbar_wait(smem_u32(&ctl->full[stage]), ph, abort, WAIT_LIMIT_NS)) {
+                        if (!mbar_wait(smem_u32(&ctl->full[stage]), ph, abort, p.wait_ns)) {
                             fail(abort);
                             goto done;
                         }
@@ -384,7 +392,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
             for (int r = 0; r < p.t; ++r) {
                 if (cls == FULL_S && r != p.t - 1) continue;
                 const uint32_t b = au & 1u;
-                bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au >> 1) & 1u, abort, WAIT_LIMIT_NS);
+                bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au >> 1) & 1u, abort, p.wait_ns);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
                     fail(abort);
@@ -676,6 +684,8 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     const char *order_env = std::getenv("CAAT_FWD_ORDER");
     p.sel = sel;
     p.n_sel = n_sel;
+    p.wait_ns = g_wait_ns.load();
+    p.inject = g_inject.load();
     // Tile width of the single-CTA mode: 192 channels instead of 256 when h is a
     // multiple of 192, the tiles then take fewer SM-rounds of work (rounds x
     // width), and a contiguous S ends on a tile edge (no MIXED tiles).  At the
@@ -714,3 +724,12 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
 }
 
 }  // namespace caat
+
+extern "C" caat_status caat_debug_set_wait(uint64_t limit_ns, caat_inject inject)
+{
+    if (limit_ns != 0 && (limit_ns < 1000ull || limit_ns > 10000000000ull)) return CAAT_ERR_INVALID_ARG;
+    if (inject != CAAT_INJECT_NONE && inject != CAAT_INJECT_SKIP_LOADS) return CAAT_ERR_INVALID_ARG;
+    caat::g_wait_ns.store(limit_ns == 0 ? caat::WAIT_LIMIT_NS : limit_ns);
+    caat::g_inject.store((int)inject);
+    return CAAT_OK;
+}

@@ -45,15 +45,19 @@ extern "C" caat_status caat_rowpar_linear_bwd_noalloc(
     void *dX, int64_t lddx, void *dW, int64_t dw_rs, int64_t dw_cs, const int32_t *sel,
     int64_t n_sel, caat_bwd_mode mode, caat_stream_t stream)
 {
-    // size check before any product that could overflow
-    if (t >= 1 && N > 0 && h > 0 && mode == CAAT_BWD_REDUCE_DOUT) {
+    // The reduced gradient is needed only when the backward sums something: the
+    // reduce placement, a non-empty S and more than one rank (the same condition
+    // as caat_rowpar_linear_bwd's).  Size check before any product that could
+    // overflow.
+    const bool reduce = mode == CAAT_BWD_REDUCE_DOUT && n_sel > 0 && t > 1;
+    if (reduce && N > 0 && h > 0) {
         const double bytes = (double)t * (double)N * (double)h * (dt == CAAT_BF16 ? 2.0 : 4.0);
         if (bytes > (double)CAAT_NOALLOC_SCRATCH_BYTES) return CAAT_ERR_INVALID_ARG;
     }
     // the part of the workspace the backward cannot do without: the reduced
     // gradient, t buffers of [N, h] rounded up to 256 bytes each
     size_t need = 0;
-    if (t >= 1 && N > 0 && h > 0 && mode == CAAT_BWD_REDUCE_DOUT)
+    if (reduce && N > 0 && h > 0)
         need = (size_t)t * (((size_t)N * (size_t)h * (dt == CAAT_BF16 ? 2u : 4u) + 255) / 256 * 256);
     if (need > (size_t)CAAT_NOALLOC_SCRATCH_BYTES) return CAAT_ERR_INVALID_ARG;
     void *ws = nullptr;

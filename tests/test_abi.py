@@ -203,3 +203,13 @@ def test_status_strings(lib):
     for code in range(5):
         assert lib.caat_status_string(code).startswith(b"CAAT_")
     assert lib.caat_status_string(99) == b"CAAT: unknown status"
+
+
+def test_debug_set_wait_validates(lib):
+    """The failure-path test hook rejects limits outside 1 us .. 10 s and unknown
+    injections, and accepts the reset (0, none); it launches nothing."""
+    assert lib.caat_debug_set_wait(999, 0) == 1
+    assert lib.caat_debug_set_wait(10_000_000_001, 0) == 1
+    assert lib.caat_debug_set_wait(1_000_000, 7) == 1
+    assert lib.caat_debug_set_wait(1_000_000, 1) == 0
+    assert lib.caat_debug_set_wait(0, 0) == 0

@@ -36,7 +36,10 @@ def _fn():
 
 
 def _call_noalloc(f, _lib, t, X, Wst, G, dX, dWst, sel, mode):
+    """sel: a device int32 tensor of S, or an int s for the contiguous S = the
+    first s channels (passed as a null index pointer)."""
     T = torch()
+    sp, ns = (None, int(sel)) if isinstance(sel, int) else (sel.data_ptr(), sel.numel())
     N, K = X.shape
     h = Wst.shape[0]
     code = 1 if X.dtype == T.bfloat16 else 0
@@ -44,7 +47,7 @@ def _call_noalloc(f, _lib, t, X, Wst, G, dX, dWst, sel, mode):
     # W and dW in the nn.Linear layout: logical [K, h] with strides (1, K)
     return f(t, N, K, h, code, X.data_ptr(), K, Wst.data_ptr(), 1, K,
              _lib.ptr_array([g.data_ptr() for g in G]), h, dX.data_ptr(), K,
-             dWst.data_ptr(), 1, K, sel.data_ptr(), sel.numel(), mode, stream)
+             dWst.data_ptr(), 1, K, sp, ns, mode, stream)
 
 
 @pytest.mark.parametrize("dtype,t,N,K,h", [("bf16", 8, 512, 3072, 768), ("f32", 4, 200, 256, 520)])
@@ -73,7 +76,44 @@ def test_noalloc_matches_workspace_entry_point_twice(dtype, t, N, K, h):
         assert rel_fro(to_f64(dWst.t()), to_f64(dW_ref)) <= TOL[dtype], call
 
 
+# Shapes whose scratch also holds the fp32 dW accumulator, so the token-split dW
+# reduction runs out of the shared array too:
+#  - contiguous S given by its size (n_sel a multiple of 64): the sum of the S
+#    channels [N, n_sel] sits at the start of the array and the accumulator after
+#    the reduced-gradient region (8 x 512 x 768 x 2 B = 6 MiB + 768 x 768 x 4 B);
+#  - the placement without the reduce: the accumulator alone, from offset 0.
+@pytest.mark.parametrize("mode,sel_kind", [(0, "contiguous"), (1, "random"), (1, "contiguous")])
+def test_noalloc_accumulator_paths_match_twice(mode, sel_kind):
+    import partial_activation_sync_gb300 as caat
+    T = torch()
+    f, _lib = _fn()
+    t, N, K, h = 8, 512, 768, 768
+    need = t * N * h * 2 if mode == 0 else 0
+    assert need + K * h * 4 <= MAX_BYTES
+    if sel_kind == "contiguous":
+        sel = h // 2
+    else:
+        sel = sel_dev(caat.select_channels(h, 0.5, caat.CAAT_S_RANDOM, 321))
+    for call, seed in enumerate((3, 4)):
+        X = ci.normal(80 + seed, (N, K))
+        Wl = ci.normal(90 + seed, (K, h), std=0.02)
+        G = ci.normal(100 + seed, (t, N, h))
+        Xd = dev(X, "bf16")
+        Wst = dev(np.ascontiguousarray(Wl.T), "bf16")
+        Gd = [dev(G[r], "bf16") for r in range(t)]
+        dX_ref, dW_ref = caat.rowpar_linear_bwd(Xd, Wst.t(), Gd, t, sel, mode)
+        dX = T.full((N, K), float("nan"), dtype=Xd.dtype, device="cuda")
+        dWst = T.full((h, K), float("nan"), dtype=Xd.dtype, device="cuda")
+        st = _call_noalloc(f, _lib, t, Xd, Wst, Gd, dX, dWst, sel, mode)
+        assert st == 0, _lib.load().caat_status_string(st)
+        T.cuda.synchronize()
+        assert caat.device_status() == 0
+        assert rel_fro(to_f64(dX), to_f64(dX_ref)) <= TOL["bf16"], call
+        assert rel_fro(to_f64(dWst.t()), to_f64(dW_ref)) <= TOL["bf16"], call
+
+
 def test_noalloc_rejects_sizes_beyond_the_scratch():
+    import partial_activation_sync_gb300 as caat
     T = torch()
     f, _lib = _fn()
     t, N, K, h = 8, 2048, 64, 1024          # 8 * 2048 * 1024 * 2 B = 32 MiB > 16 MiB
@@ -84,6 +124,14 @@ def test_noalloc_rejects_sizes_beyond_the_scratch():
     dWst = T.zeros((h, K), dtype=T.bfloat16, device="cuda")
     sel = sel_dev(np.arange(h // 2, dtype=np.int32))
     assert _call_noalloc(f, _lib, t, X, Wst, G, dX, dWst, sel, 0) == 1   # CAAT_ERR_INVALID_ARG
-    # the same size without the reduce needs no scratch and runs
+    # the same size without the reduce needs no scratch and runs; so does the
+    # reduce with an empty S or with one rank (nothing to sum)
     assert _call_noalloc(f, _lib, t, X, Wst, G, dX, dWst, sel, 1) == 0
+    assert _call_noalloc(f, _lib, t, X, Wst, G, dX, dWst, 0, 0) == 0
+    Xw = T.zeros((N, t * K), dtype=T.bfloat16, device="cuda")
+    Ww = T.zeros((h, t * K), dtype=T.bfloat16, device="cuda")
+    dXw = T.zeros((N, t * K), dtype=T.bfloat16, device="cuda")
+    dWw = T.zeros((h, t * K), dtype=T.bfloat16, device="cuda")
+    assert _call_noalloc(f, _lib, 1, Xw, Ww, G[:1], dXw, dWw, sel, 0) == 0
     T.cuda.synchronize()
+    assert caat.device_status() == 0
