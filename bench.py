@@ -543,7 +543,8 @@ def run_extras(torch, caat, device, peaks, args):
             "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4),
             "us": round(sec * 1e6, 1), "kernel": caat.last_kernel()}
         del X, Wst, Ys
-    # 7B decode: N in {1, 8, 64} tokens, p = 0.5 -- weight streaming (HBM bound)
+    # 7B decode: N in {1, 8, 64} tokens, p = 0.5, contiguous S -- weight streaming (HBM bound)
+    sel = torch.from_numpy(caat.select_channels(w.h, w.p, caat.CAAT_S_CONTIGUOUS)).to(device)
     for li, L in enumerate(w.layers):
         Wst = (torch.randn((w.h, L.K), device=device) * 0.02).to(torch.bfloat16)
         for Nd in w.decode_N:

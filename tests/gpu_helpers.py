@@ -53,3 +53,40 @@ def sel_dev(S: np.ndarray):
 
 
 TOL = {"f32": 1e-5, "bf16": 1e-2}
+
+
+# Element-wise bound next to the relative Frobenius one:
+#   |got - want| <= REL * |want| + TAU * rms(want)
+# REL covers the one rounding of the result to its dtype (bf16: half an ulp is
+# 2^-9 relative, fp32: 2^-24) with a factor-2 margin for the fp32 accumulation.
+# TAU is an absolute floor at a fixed share of the result's scale, for elements
+# near zero where a relative bound means nothing: the fp32 accumulation errors
+# of a K-term sum stay far below it, while any misplaced, missing or extra term
+# (a wrong tile, shard, rank, sign or channel) moves an element by O(rms).
+# The backward's floor is twice the forward's: with the contiguous S the summed
+# gradient of the S channels is rounded once to bf16 before it enters the GEMMs
+# (2^-9 relative per term, random sign), which the float64 oracle never does.
+ELEM = {"bf16": (2.0 ** -8, 2.0 ** -7), "f32": (2.0 ** -18, 2.0 ** -16)}
+ELEM_BWD = {"bf16": (2.0 ** -8, 2.0 ** -6), "f32": (2.0 ** -18, 2.0 ** -15)}
+
+
+def check(got: np.ndarray, want: np.ndarray, dtype: str, bwd: bool = False, what=""):
+    """Relative Frobenius error within TOL[dtype], and every element within the
+    element-wise bound above (NaN or inf in `got` fails)."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    e = rel_fro(got, want)
+    assert e <= TOL[dtype], ("relative Frobenius", what, e)
+    if want.size == 0:
+        return
+    rel, tau = (ELEM_BWD if bwd else ELEM)[dtype]
+    rms = float(np.sqrt(np.mean(want * want)))
+    err = np.abs(got - want)
+    bound = rel * np.abs(want) + tau * rms
+    ok = err <= bound                      # NaN compares false: it fails
+    if not ok.all():
+        bad = np.argwhere(~ok)
+        i = tuple(bad[0])
+        raise AssertionError("element-wise bound: %s, %d of %d elements outside; first at %s: got %r, "
+                             "want %r, bound %r" % (what, len(bad), want.size, i, got[i], want[i], bound[i]))

@@ -9,7 +9,7 @@ import pytest
 
 import caat_inputs as ci
 from oracle import oracle as orc
-from tests.gpu_helpers import TOL, dev, host_values, rel_fro, sel_dev, to_f64, torch
+from tests.gpu_helpers import check, dev, host_values, sel_dev, to_f64, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -56,10 +56,10 @@ def _run(caat, t, N, h, K, p, layout_S, dtype, wl="rm", seed=0):
 def _check(got, want, S, t, dtype):
     gZ, gA, gW = got
     wZ, wA, wW = want
-    assert rel_fro(gZ, wZ) <= TOL[dtype]
+    check(gZ, wZ, dtype)
     for r in range(t):
-        assert rel_fro(gA[r], wA[r]) <= TOL[dtype], r
-    assert rel_fro(gW, wW) <= TOL[dtype]
+        check(gA[r], wA[r], dtype, what=r)
+    check(gW, wW, dtype)
     for r in range(1, t):
         assert np.array_equal(gA[r][:, S], gA[0][:, S])
 
@@ -127,11 +127,11 @@ def test_colpar_full_size_sampled(caat):
     wZ = orc.colpar_fwd(hA[:, rows], hW, t)
     wA, _ = orc.colpar_bwd(hA[:, rows], hW, hZ[rows], t, S)
     gZ = to_f64(Z)[rows]
-    assert rel_fro(gZ, wZ) <= TOL["bf16"]
+    check(gZ, wZ, "bf16")
     gA = to_f64(dA)[:, rows]
     for r in range(t):
-        assert rel_fro(gA[r], wA[r]) <= TOL["bf16"]
+        check(gA[r], wA[r], "bf16")
     kt = K // t
     cols = np.concatenate([r * kt + np.sort(rng.choice(kt, 4, replace=False)) for r in range(t)])
     _, wW = orc.colpar_bwd(hA, hW[:, cols], hZ[:, cols], t, S)
-    assert rel_fro(to_f64(dW1)[:, cols], wW) <= TOL["bf16"]
+    check(to_f64(dW1)[:, cols], wW, "bf16")
