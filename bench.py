@@ -14,9 +14,13 @@ of the upstream gradient, dX, dW).  Metric: algorithmic TFLOP/s (2NKh forward,
                   [--layout contiguous|random] [--p P] [--placement reduce_dout|column]
                   [--no-extras] [--no-stack]
 
-Under torchrun each rank runs its own replica on its own GPU (no collective on
-the data path; weak scaling); rank 0 prints one JSON line.  ``--impl reference``
-times the CPU oracle on the host cores instead.
+Under torchrun (N GPUs) the workload's t ranks are spread over the GPUs, t / N on
+each: every process runs the fused forward of its own ranks and the partial
+channel-reduce across processes (NCCL all-to-all and all-gather of the S
+channels, folded in rank order); the channels outside S never leave their GPU.
+The layer is the same for every N (strong scaling); rank 0 prints one JSON line
+with the slowest rank's time.  ``--impl reference`` times the CPU oracle on the
+host cores instead.
 """
 import argparse
 import json
@@ -218,6 +222,83 @@ class LayerStep:
             evs[k].record(stream)
 
 
+class TPLayer:
+    """One layer's data on process g of `world`: the t ranks of the workload are
+    spread over the processes, t / world on each GPU; this process holds the input
+    columns and weight rows of its own ranks (the same seeded draws as one GPU
+    holding all t)."""
+
+    def __init__(self, torch, w, li, device, g, world):
+        L = w.layers[li]
+        X, Wl, G = ci.layer_tensors(w, li)
+        self.t_local = w.t // world
+        kl = L.K // world
+        cols = slice(g * kl, (g + 1) * kl)
+        bf = torch.bfloat16
+
+        def dev(a):
+            return torch.from_numpy(ci.bf16_words(np.ascontiguousarray(a)).view(np.int16)).to(device).view(bf)
+
+        self.name, self.K, self.kl = L.name, L.K, kl
+        self.X_host = ci.bf16_words(np.ascontiguousarray(X[:, cols]))
+        self.X = dev(X[:, cols])
+        self.Wstore = dev(np.ascontiguousarray(Wl[cols, :].T))      # nn.Linear layout [h, kl]
+        self.W = self.Wstore.t()
+        ranks = range(g * self.t_local, (g + 1) * self.t_local)
+        self.G_host = [ci.bf16_words(G[r]) for r in ranks] if G is not None else None
+        self.G = [dev(G[r]) for r in ranks] if G is not None else None
+        self.Y = [torch.empty((w.N, w.h), dtype=bf, device=device) for _ in range(self.t_local)]
+        self.dY = [torch.empty((w.N, w.h), dtype=bf, device=device) for _ in range(self.t_local)] \
+            if G is not None else None
+        self.dX = torch.empty((w.N, kl), dtype=bf, device=device)
+        self.dWstore = torch.empty((w.h, kl), dtype=bf, device=device)
+        self.dW = self.dWstore.t()
+        # this process's share of the layer's algorithmic work
+        self.flops_fwd = 2.0 * w.N * kl * w.h
+        self.flops_bwd = 4.0 * w.N * kl * w.h if w.backward else 0.0
+        self.bytes_fwd = 2.0 * (w.N * kl + kl * w.h + self.t_local * w.N * w.h)
+
+
+class TPStep:
+    """The workload's step with its t ranks spread over the processes of the
+    default group (one GPU each): per layer the forward with the partial
+    channel-reduce across processes, then (training workloads) the backward with
+    the reduce on the upstream gradient across processes."""
+
+    def __init__(self, torch, caat, w, device, g, world):
+        from partial_activation_sync_gb300 import tp
+        if w.t % world != 0:
+            raise SystemExit("bench: %d ranks do not split over %d GPUs" % (w.t, world))
+        self.torch, self.caat, self.w, self.tp = torch, caat, w, tp
+        S = caat.select_channels(w.h, w.p, w.layout, w.seeds()["perm"])
+        self.sel = int(S.size) if w.layout == 0 else torch.from_numpy(S).to(device)
+        self.layers = [TPLayer(torch, w, i, device, g, world) for i in range(len(w.layers))]
+        self.pr = tp.PartialReduce()
+        self.side = torch.cuda.Stream(device=device)
+        self.names = []
+        for L in self.layers:
+            self.names.append("fwd_" + L.name)
+            if w.backward:
+                self.names.append("bwd_" + L.name)
+        self.flops = sum(L.flops_fwd + L.flops_bwd for L in self.layers)
+
+    def run(self, evs=None, io=None):
+        stream = self.torch.cuda.current_stream()
+        k = 0
+        for li, L in enumerate(self.layers):
+            B = io[li] if io is not None else L
+            if evs is not None:
+                evs[k].record(stream); k += 1
+            self.tp.rowpar_linear_fwd_tp(B.X, L.W, L.t_local, self.sel, self.pr, outs=B.Y, side=self.side)
+            if self.w.backward:
+                if evs is not None:
+                    evs[k].record(stream); k += 1
+                self.tp.rowpar_linear_bwd_tp(B.X, L.W, B.G, L.t_local, self.sel, self.pr, dX=B.dX, dW=B.dW,
+                                             dY=L.dY)
+        if evs is not None:
+            evs[k].record(stream)
+
+
 def time_steps(torch, caat, ls, steps, warmup, device, dist=None, clocks=None):
     """W untimed warm-up steps, then exactly `steps` timed steps between a barrier
     and a synchronize on both sides.  Every call of a step is bracketed by CUDA
@@ -284,7 +365,8 @@ def roofline_of(ls, per_call, steps, peaks, kernel_name):
                 "frac": round(ach / peaks["hbm"], 4)}
         roof["peak_kind"] = "copy bandwidth (read + write)"
     roof["peak_source"] = "of measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "of fallback"
-    roof["traffic"] = DRAM_TRAFFIC.get((w.name, Ld.name))
+    # DRAM counters exist for the one-GPU launch configuration only
+    roof["traffic"] = DRAM_TRAFFIC.get((w.name, Ld.name)) if isinstance(ls, LayerStep) else None
     roof["algorithmic_per_launch"] = {"flops": Ld.flops_fwd, "bytes": Ld.bytes_fwd}
     roof["us_per_launch"] = round(t_dom * 1e6, 2)
     return roof
@@ -296,19 +378,24 @@ def run_gpu(args, w):
 
     dist, rank, world, device = _setup_dist()
     peaks = _peaks()
-    ls = LayerStep(torch, caat, w, device)
+    # one GPU: the t ranks emulated in its memory; several: the ranks spread over
+    # the GPUs, with the partial channel-reduce across them (strong scaling: the
+    # layer is the same whatever the GPU count)
+    ls = LayerStep(torch, caat, w, device) if world == 1 else TPStep(torch, caat, w, device, rank, world)
     clocks = ClockSampler(device.index)
     per_call, launches, clk = time_steps(torch, caat, ls, args.steps, args.warmup, device, dist, clocks)
     kernel_name = caat.last_kernel()
     total_ms, tflops = job_rate(dist, device, float(per_call.sum()), ls.flops, args.steps)
     ms_step = total_ms / args.steps
     breakdown = {n: round(float(v) / args.steps, 4) for n, v in zip(ls.names, per_call)}
-    roof = roofline_of(ls, per_call, args.steps, peaks, "rowpar_fwd_tc" if w.N > 64 else kernel_name)
+    roof = roofline_of(ls, per_call, args.steps, peaks,
+                       ("rowpar_fwd_tc" if w.N > 64 else kernel_name) + ("" if world == 1 else " + exchange"))
 
     result = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak" if world == 1 else "strong", "vs_baseline": None,
+        "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) activations/gradients, N(0,0.02) weights)",
         "config": {"workload": w.name, "t": w.t, "N": w.N, "h": w.h,
                    "layers": {L.name: L.K for L in ls.layers}, "p": w.p,
@@ -317,7 +404,10 @@ def run_gpu(args, w):
                    "l2": "flushed between timed steps by reading a 2x L2 buffer (untimed)",
                    "timing": "CUDA events around each call of a step; an untimed spin kernel before "
                              "each step lets the host queue it, so the calls run back to back",
-                   "parallelism": "replicas" if world > 1 else "1 GPU, t ranks emulated"},
+                   "parallelism": ("1 GPU, t ranks emulated" if world == 1 else
+                                   "tp%d: %d ranks per GPU, partial channel-reduce across GPUs (NCCL "
+                                   "all-to-all + all-gather of the S channels, fold in rank order)"
+                                   % (world, w.t // world))},
         "breakdown_ms": breakdown,
         "gpu_launches": int(launches),
         "clocks": clk,
@@ -325,7 +415,10 @@ def run_gpu(args, w):
     }
 
     # end to end through the public API with host buffers (pinned), per step
-    result["e2e"] = run_e2e(torch, caat, w, ls.layers, ls.sel, ls.ws, args, device, dist)
+    if world == 1:
+        result["e2e"] = run_e2e(torch, caat, w, ls.layers, ls.sel, ls.ws, args, device, dist)
+    else:
+        result["e2e"] = run_e2e_tp(torch, ls, args, device, dist)
     del ls
     torch.cuda.empty_cache()
 
@@ -441,6 +534,55 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
             "ms_per_step": round(ms / args.steps, 4),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "overlap": "inputs of step i+1 and results of step i-1 copy on two streams while step i computes"}
+
+
+def run_e2e_tp(torch, ls, args, device, dist):
+    """End to end for the step spread over processes: every step copies this
+    process's inputs (its columns of X, its ranks' upstream gradients) in from
+    pinned host memory, runs the step, and reads its results (dX and dW, or its
+    ranks' outputs without a backward) back, all on one stream."""
+    import types
+    w = ls.w
+    hostX = [torch.from_numpy(L.X_host.view(np.int16)).pin_memory() for L in ls.layers]
+    hostG = [[torch.from_numpy(g.view(np.int16)).pin_memory() for g in L.G_host] if w.backward else []
+             for L in ls.layers]
+    outs = []
+    for L in ls.layers:
+        if w.backward:
+            outs.append([torch.empty(L.dX.shape, dtype=torch.int16).pin_memory(),
+                         torch.empty(L.dWstore.shape, dtype=torch.int16).pin_memory()])
+        else:
+            outs.append([torch.empty(y.shape, dtype=torch.int16).pin_memory() for y in L.Y])
+    io = [types.SimpleNamespace(X=L.X, G=L.G, Y=L.Y, dX=L.dX, dW=L.dW) for L in ls.layers]
+
+    def step():
+        for li, L in enumerate(ls.layers):
+            L.X.view(torch.int16).copy_(hostX[li], non_blocking=True)
+            for r, g in enumerate(hostG[li]):
+                L.G[r].view(torch.int16).copy_(g, non_blocking=True)
+        ls.run(io=io)
+        for li, L in enumerate(ls.layers):
+            src = [L.dX, L.dWstore] if w.backward else L.Y
+            for o, d in zip(outs[li], src):
+                o.copy_(d.view(torch.int16), non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    h2d = sum(x.numel() * 2 for x in hostX) + sum(g.numel() * 2 for gs in hostG for g in gs)
+    d2h = sum(o.numel() * 2 for os_ in outs for o in os_)
+    ms, rate = job_rate(dist, device, e0.elapsed_time(e1), ls.flops, args.steps)
+    return {"value": round(rate, 3), "unit": "TFLOP/s", "ms_per_step": round(ms / args.steps, 4),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "overlap": "none: copies in, step, copies out on one stream (per process)"}
 
 
 def _time_call(torch, fn, reps, flush=None):

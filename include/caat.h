@@ -26,6 +26,8 @@
  *    and tests; the defaults choose by shape): CAAT_FWD_CLUSTER=1|2 (CTAs per
  *    cluster of the forward tile kernel), CAAT_FWD_BN=192|256 (its tile width),
  *    CAAT_FWD_ORDER=m|n (its work units row- or channel-block-major),
+ *    CAAT_FWD_SCHED=rounds (every tile of it whole, in rounds, instead of cutting
+ *    the tiles outside S into per-shard pieces that even out the SMs' load),
  *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
  *    (backward on `stream` only).
  *  - "device pointer" = memory the caller allocated on the current CUDA device;
@@ -287,6 +289,47 @@ caat_status caat_colpar_linear_bwd(int t, int64_t N, int64_t h, int64_t K, caat_
                                    void *dW1, int64_t dw1_rs, int64_t dw1_cs,
                                    const int32_t *sel, int64_t n_sel,
                                    void *workspace, size_t ws_bytes, caat_stream_t stream);
+
+/*
+ * The partial channel-reduce across processes, one GPU each.  "Tensor-Parallelism
+ * with Partially Synchronized Activations", Introduction: the partial
+ * channel-reduce replaces the all-reduce after a row-parallel layer; only the
+ * channels of S are summed over the ranks, the others stay on their rank.  Across
+ * GPUs that sum is an all-reduce of an [N, |S|] buffer, which the caller's
+ * collectives move; these three calls are the steps that run on each GPU:
+ *   1. caat_pcr_pack:   P[n, i] = Y[n, S_i]        (the send buffer, dense)
+ *   2. the collectives give each rank a block of rows of every rank's P;
+ *      caat_rank_fold sums them in rank order      (fp32 left fold, one rounding)
+ *   3. the collectives gather the folded rows; caat_pcr_unpack writes them back:
+ *      Y_k[n, S_i] = P[n, i] for each of the n_out outputs of this process.
+ * The fold order makes the result independent of how the rows were split.
+ *
+ * Common to the three: asynchronous on `stream`, device pointers owned by the
+ * caller, strides in elements, bf16 or fp32 elements moved bit for bit (the fold
+ * widens bf16 exactly and rounds once).  sel: device int32[n_sel], the channels of
+ * S in [0, h) (ascending, unique), or null for S = {0, ..., n_sel-1}.  Errors:
+ * INVALID_ARG for negative sizes, n_sel > h, a leading dimension below its row
+ * width, null pointers where data is moved, or written buffers that overlap the
+ * buffers they are computed from (or sel, or each other).  Out-of-range entries
+ * of sel are not checked on the device.
+ */
+/* Y: [N, h], row stride ldy.  P: [N, n_sel], row stride ldp (>= n_sel). */
+caat_status caat_pcr_pack(int64_t N, int64_t h, caat_dtype dt, const void *Y, int64_t ldy,
+                          const int32_t *sel, int64_t n_sel, void *P, int64_t ldp,
+                          caat_stream_t stream);
+
+/* P: [N, n_sel], row stride ldp.  Y: host array of n_out (1 .. 64) device
+ * pointers, each [N, h] with row stride ldy; only the channels of S are written. */
+caat_status caat_pcr_unpack(int64_t N, int64_t h, caat_dtype dt, const void *P, int64_t ldp,
+                            const int32_t *sel, int64_t n_sel, void *const *Y, int n_out,
+                            int64_t ldy, caat_stream_t stream);
+
+/* in: t (1 .. 4096) blocks of [rows, cols], row stride ld_in, block q starting
+ * rank_stride elements after block q-1 (>= the span of one block).
+ * out[n, c] = in_0[n, c] + in_1[n, c] + ... + in_{t-1}[n, c] (row stride ld_out). */
+caat_status caat_rank_fold(int t, int64_t rows, int64_t cols, caat_dtype dt, const void *in,
+                           int64_t ld_in, int64_t rank_stride, void *out, int64_t ld_out,
+                           caat_stream_t stream);
 
 /* Human-readable name of a status code (static string, never null). */
 const char *caat_status_string(caat_status st);

@@ -22,7 +22,7 @@ __all__ = [
     "select_channels", "partial_channel_reduce", "rowpar_linear_fwd", "rowpar_linear_bwd",
     "rowpar_linear_bwd_workspace", "rowpar_linear_bwd_noalloc", "colpar_linear_fwd",
     "colpar_linear_bwd", "colpar_linear_bwd_workspace", "device_status", "last_kernel", "launch_count",
-    "debug_set_wait", "CAAT_INJECT_NONE", "CAAT_INJECT_SKIP_LOADS",
+    "debug_set_wait", "CAAT_INJECT_NONE", "CAAT_INJECT_SKIP_LOADS", "pcr_pack", "pcr_unpack", "rank_fold",
     "CaatError", "CAAT_S_CONTIGUOUS", "CAAT_S_RANDOM", "CAAT_BWD_REDUCE_DOUT",
     "CAAT_BWD_NO_REDUCE",
 ]
@@ -333,6 +333,47 @@ def colpar_linear_bwd(A, W1, dZ, t: int, sel, dA=None, dW1=None, workspace=None,
         ctypes.c_void_p(dW1.data_ptr()), dw1_rs, dw1_cs, sp, ns, wp, wb, _stream_ptr(stream, W1))
     _check(st, "caat_colpar_linear_bwd")
     return ret_dA, dW1
+
+
+# ------------------------------------ partial reduce across processes (steps)
+
+def pcr_pack(Y, sel, P, stream=None):
+    """P[:, i] = Y[:, S_i]: the channels of S of Y [N, h] into P [N, |S|]."""
+    N, h = Y.shape
+    sp, ns = _sel_ptr(sel)
+    _check_like(P, (N, ns), Y.dtype, "P")
+    st = _lib.load().caat_pcr_pack(N, h, _dtype_code(Y), ctypes.c_void_p(Y.data_ptr()), _rowmajor(Y, "Y"),
+                                   sp, ns, ctypes.c_void_p(P.data_ptr()), _rowmajor(P, "P"),
+                                   _stream_ptr(stream, Y))
+    _check(st, "caat_pcr_pack")
+    return P
+
+
+def pcr_unpack(P, sel, Ys, stream=None):
+    """Ys[k][:, S_i] = P[:, i] for every tensor of the list Ys (each [N, h])."""
+    N, h = Ys[0].shape
+    sp, ns = _sel_ptr(sel)
+    _check_like(P, (N, ns), Ys[0].dtype, "P")
+    ldy = _same_layout(Ys, (N, h), "Ys")
+    st = _lib.load().caat_pcr_unpack(N, h, _dtype_code(P), ctypes.c_void_p(P.data_ptr()), _rowmajor(P, "P"),
+                                     sp, ns, _lib.ptr_array([y.data_ptr() for y in Ys]), len(Ys), ldy,
+                                     _stream_ptr(stream, P))
+    _check(st, "caat_pcr_unpack")
+    return Ys
+
+
+def rank_fold(R, out, stream=None):
+    """out = R[0] + R[1] + ... + R[t-1] (fp32 left fold in rank order, one rounding).
+    R: contiguous [t, rows, cols]; out: [rows, cols]."""
+    if R.dim() != 3 or not R.is_contiguous() or not R.is_cuda:
+        raise ValueError("caat: R must be a contiguous CUDA tensor [t, rows, cols]")
+    t, rows, cols = R.shape
+    _check_like(out, (rows, cols), R.dtype, "out")
+    st = _lib.load().caat_rank_fold(int(t), rows, cols, _dtype_code(R), ctypes.c_void_p(R.data_ptr()), cols,
+                                    rows * cols, ctypes.c_void_p(out.data_ptr()), _rowmajor(out, "out"),
+                                    _stream_ptr(stream, R))
+    _check(st, "caat_rank_fold")
+    return out
 
 
 # ------------------------------------------------------------ diagnostics

@@ -27,6 +27,9 @@ EXPORTS = (
     "caat_last_kernel",
     "caat_launch_count",
     "caat_debug_set_wait",
+    "caat_pcr_pack",
+    "caat_pcr_unpack",
+    "caat_rank_fold",
 )
 
 _lib = None
@@ -85,6 +88,14 @@ def load(path: str = None) -> ctypes.CDLL:
     L.caat_launch_count.restype = ctypes.c_uint64
     L.caat_debug_set_wait.argtypes = [ctypes.c_uint64, ctypes.c_int]
     L.caat_debug_set_wait.restype = ctypes.c_int
+    L.caat_pcr_pack.argtypes = [_c_i64, _c_i64, ctypes.c_int, _c_p, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_p]
+    L.caat_pcr_pack.restype = ctypes.c_int
+    L.caat_pcr_unpack.argtypes = [_c_i64, _c_i64, ctypes.c_int, _c_p, _c_i64, _c_p, _c_i64, _c_pp, ctypes.c_int,
+                                  _c_i64, _c_p]
+    L.caat_pcr_unpack.restype = ctypes.c_int
+    L.caat_rank_fold.argtypes = [ctypes.c_int, _c_i64, _c_i64, ctypes.c_int, _c_p, _c_i64, _c_i64, _c_p, _c_i64,
+                                 _c_p]
+    L.caat_rank_fold.restype = ctypes.c_int
     if path is None:
         _lib = L
     return L

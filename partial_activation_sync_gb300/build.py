@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libcaat.so")
 
-SOURCES = ["api.cu", "select.cpp", "pcr.cu", "gemm_simt.cu", "gemm_tc.cu", "gemm_tc_bwd.cu", "decode.cu", "skinny_tc.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "select.cpp", "pcr.cu", "gemm_simt.cu", "gemm_tc.cu", "gemm_tc_bwd.cu", "decode.cu", "skinny_tc.cu", "noalloc.cu", "exchange.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -107,7 +107,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int MAX_H_TC = 32768;
 constexpr int MAX_T_TC = 16;                 // rank outputs addressed through tensor maps
 constexpr int STG_BYTES = 32 * 128;          // per epilogue warp: 32 rows x 64 bf16 channels
-constexpr int MAX_STAGES = 6;
+constexpr int MAX_STAGES = 8;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;   // 2 s: far beyond any legitimate wait
 
 // failure-path test hooks (caat_debug_set_wait): the wait limit and the injected
@@ -121,13 +121,23 @@ std::atomic<int> g_inject{CAAT_INJECT_NONE};
 // W 128 x 64 per CTA: each CTA holds half the rows of X and half the channels of
 // W, which cuts the shared-memory operand traffic per SM by a third; two staging
 // buffers per epilogue warp so a bulk store can drain while the next is staged).
+// Ring depth of the pair mode and the staging buffers per epilogue warp of its
+// 256-wide tiles (compile-time tuning; shared memory holds stages x 32 KB plus
+// 4 x NBUF x 4 KB of staging).
+#ifndef CAAT_FWD_PAIR_STAGES
+#define CAAT_FWD_PAIR_STAGES 6
+#endif
+#ifndef CAAT_FWD_PAIR_NBUF256
+#define CAAT_FWD_PAIR_NBUF256 1
+#endif
+
 template <int CLN, int BNT>
 struct Cfg {
     static constexpr bool PAIR = CLN > 1;
-    static constexpr int STAGES = PAIR ? 6 : 4;
-    // staging buffers per epilogue warp: two (a bulk store drains one while the
-    // next chunk fills the other) where shared memory allows, i.e. below 256-wide
-    static constexpr int NBUF = BNT < 256 ? 2 : 1;
+    static constexpr int STAGES = PAIR ? CAAT_FWD_PAIR_STAGES : 4;
+    // staging buffers per epilogue warp: several (bulk stores drain the earlier
+    // ones while the next chunk fills one) where shared memory allows
+    static constexpr int NBUF = BNT < 256 ? 2 : (PAIR ? CAAT_FWD_PAIR_NBUF256 : 1);
     static constexpr int B_ROWS = PAIR ? BNT / 2 : BNT;        // W rows (channels) per CTA per stage
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -150,6 +160,7 @@ struct SmemCtl {
 template <int CLN, int BNT>
 constexpr size_t smem_bytes()
 {
+    static_assert(Cfg<CLN, BNT>::STAGES <= MAX_STAGES, "ring deeper than the barrier arrays");
     return 1024 + (size_t)Cfg<CLN, BNT>::STAGES * Cfg<CLN, BNT>::STAGE_BYTES + 4 * Cfg<CLN, BNT>::NBUF * STG_BYTES +
            sizeof(SmemCtl);
 }
@@ -158,12 +169,21 @@ struct YMaps {
     CUtensorMap m[MAX_T_TC];   // rank r's output [N, h], box 64 channels x 32 rows
 };
 
+constexpr int MAX_NB = (MAX_H_TC + 191) / 192;   // channel blocks at the narrowest tile
+
 struct FwdParams {
     MutPtrs Y;
     int64_t ldy;
     int64_t N, h;
     int t, nkb, num_m, num_n;
     int mmajor;         // work units ordered row-block-major (else channel-block-major)
+    // Balanced schedule (contiguous S, some channel blocks outside S): the first
+    // n_whole entries of nbl are the channel blocks whose tiles run whole (FULL_S,
+    // MIXED), the rest the NO_S blocks, whose tiles are cut into one piece per
+    // shard.  balanced == 0: every tile runs whole, in unit order.
+    int balanced;
+    int n_whole;
+    uint8_t nbl[MAX_NB];
     const int32_t *sel;
     int64_t n_sel;
     uint64_t wait_ns;   // limit of every mbarrier wait
@@ -174,6 +194,95 @@ __device__ __forceinline__ void fail(volatile int *abort)
 {
     *abort = 1;
     atomicExch(&g_caat_dev_error, (int)CAAT_ERR_TIMEOUT);
+}
+
+// ------------------------------------------------------------ work schedule
+// Workers are CTAs (CTA pairs in the pair mode), g = 0 .. G-1.  Every shard of
+// every tile costs the same MMA work, so a tile that runs whole costs t shards
+// and a NO_S tile can be cut into t independent one-shard pieces (each writes
+// only its own rank's output).  Whole tiles go round-robin to the workers (in
+// unit order).  The pieces are numbered shard-major (all tiles' shard 0, then
+// shard 1, ...) and also dealt round-robin, so at any moment the workers run
+// neighbouring tiles at the same shard and share their X and W blocks in L2.
+// When the whole tiles leave some workers one tile short (the "light" workers),
+// the first light x t pieces go to those alone, which evens out the load.
+struct Work {
+    int mg, nb;    // row group (CLN row blocks) and channel block
+    int r0, r1;    // shards [r0, r1) of the tile
+    int piece;     // 1: a one-shard piece of a NO_S tile
+};
+
+struct Cursor {
+    int i;            // next whole unit
+    int j, step, end; // next piece, stride, end of the current phase
+    int phase;        // 0: pieces for the light workers, 1: pieces for all, 2: done
+};
+
+__device__ __forceinline__ void cursor_init(Cursor &c, const FwdParams &p, int g, int G, int num_mg)
+{
+    c.i = g;
+    c.phase = 2;
+    if (!p.balanced) return;
+    const int nW = num_mg * p.n_whole;
+    const int rem = nW % G;
+    const int light = rem > 0 ? G - rem : 0;
+    const int P = num_mg * (p.num_n - p.n_whole) * p.t;
+    const int A = min(P, light * p.t);
+    if (light > 0 && g >= rem && g - rem < A) {
+        c.phase = 0;
+        c.j = g - rem;
+        c.step = light;
+        c.end = A;
+    } else {
+        c.phase = 1;
+        c.j = A + g;
+        c.step = G;
+        c.end = P;
+    }
+}
+
+__device__ __forceinline__ bool next_work(Cursor &c, const FwdParams &p, int g, int G, int num_mg, Work &w)
+{
+    if (!p.balanced) {
+        if (c.i >= num_mg * p.num_n) return false;
+        const int u = c.i;
+        c.i += G;
+        w.mg = p.mmajor ? u / p.num_n : u % num_mg;
+        w.nb = p.mmajor ? u % p.num_n : u / num_mg;
+        w.r0 = 0;
+        w.r1 = p.t;
+        w.piece = 0;
+        return true;
+    }
+    const int nW = num_mg * p.n_whole;
+    if (c.i < nW) {
+        const int i = c.i;
+        c.i += G;
+        w.mg = p.mmajor ? i / p.n_whole : i % num_mg;
+        w.nb = p.nbl[p.mmajor ? i % p.n_whole : i / num_mg];
+        w.r0 = 0;
+        w.r1 = p.t;
+        w.piece = 0;
+        return true;
+    }
+    if (c.phase == 0 && c.j >= c.end) {
+        // the light workers' share is done: continue with the pieces dealt to all
+        c.phase = 1;
+        c.j = c.end + g;
+        c.step = G;
+        c.end = num_mg * (p.num_n - p.n_whole) * p.t;
+    }
+    if (c.phase == 2 || c.j >= c.end) return false;
+    const int nsb = p.num_n - p.n_whole;
+    const int ntiles = num_mg * nsb;
+    const int r = c.j / ntiles, tile = c.j - r * ntiles;
+    w.r0 = r;
+    w.r1 = r + 1;
+    w.mg = p.mmajor ? tile / nsb : tile % num_mg;
+    w.nb = p.nbl[p.n_whole + (p.mmajor ? tile % nsb : tile / num_mg)];
+    w.piece = 1;
+    c.j += c.step;
+    return true;
 }
 
 template <int BNT>
@@ -279,12 +388,11 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         asm volatile("bar.sync 1, %0;" ::"n"(NB) : "memory");   // warps 1..5
     }
 
-    // work units: (group of CLN row blocks, 256-channel block); the CTAs of a
-    // cluster take the row blocks of a group
-    const int unit0 = blockIdx.x / CLN;
-    const int nunits_grid = gridDim.x / CLN;
+    // work items: (group of CLN row blocks, channel block, shard range); the CTAs
+    // of a cluster take the row blocks of a group
+    const int worker = blockIdx.x / CLN;
+    const int nworkers = gridDim.x / CLN;
     const int num_mg = (p.num_m + CLN - 1) / CLN;
-    const int num_units = num_mg * p.num_n;
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
@@ -294,10 +402,13 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
 #ifdef EXP_LOAD_HINT
             const uint64_t pol_in = policy_evict_last();
 #endif
-            for (int u = unit0; u < num_units; u += nunits_grid) {
-                const int mb = (p.mmajor ? u / p.num_n : u % num_mg) * CLN + (int)crank;
-                const int nb = p.mmajor ? u % p.num_n : u / num_mg;
-                for (int r = 0; r < p.t; ++r) {
+            Cursor cur;
+            cursor_init(cur, p, worker, nworkers, num_mg);
+            Work wk;
+            while (next_work(cur, p, worker, nworkers, num_mg, wk)) {
+                const int mb = wk.mg * CLN + (int)crank;
+                const int nb = wk.nb;
+                for (int r = wk.r0; r < wk.r1; ++r) {
                     for (int kb = 0; kb < p.nkb; ++kb) {
                         if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, p.wait_ns)) {
                             fail(abort);
@@ -333,10 +444,13 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
             const uint16_t pair_mask = (uint16_t)(3u << leader);
             int stage = 0;
             uint32_t ph = 0, au = 0;
-            for (int u = unit0; u < num_units; u += nunits_grid) {
-                const int nb = p.mmajor ? u % p.num_n : u / num_mg;
-                const int cls = tile_class<BNT>(ctl->bitmap, (int64_t)nb * BNT, p.h, p.t);
-                for (int r = 0; r < p.t; ++r) {
+            Cursor cur;
+            cursor_init(cur, p, worker, nworkers, num_mg);
+            Work wk;
+            while (next_work(cur, p, worker, nworkers, num_mg, wk)) {
+                const int nb = wk.nb;
+                const int cls = wk.piece ? (int)NO_S : tile_class<BNT>(ctl->bitmap, (int64_t)nb * BNT, p.h, p.t);
+                for (int r = wk.r0; r < wk.r1; ++r) {
                     const bool starts = cls != FULL_S || r == 0;
                     const bool ends = cls != FULL_S || r == p.t - 1;
                     const uint32_t b = au & 1u;
@@ -384,12 +498,15 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t au = 0;
         int sbuf = 0;                                   // staging buffer the next chunk fills
-        for (int u = unit0; u < num_units; u += nunits_grid) {
-            const int mb = (p.mmajor ? u / p.num_n : u % num_mg) * CLN + (int)crank;
-            const int nb = p.mmajor ? u % p.num_n : u / num_mg;
+        Cursor cur;
+        cursor_init(cur, p, worker, nworkers, num_mg);
+        Work wk;
+        while (next_work(cur, p, worker, nworkers, num_mg, wk)) {
+            const int mb = wk.mg * CLN + (int)crank;
+            const int nb = wk.nb;
             const int64_t n0 = (int64_t)nb * BNT;
-            const int cls = tile_class<BNT>(ctl->bitmap, n0, p.h, p.t);
-            for (int r = 0; r < p.t; ++r) {
+            const int cls = wk.piece ? (int)NO_S : tile_class<BNT>(ctl->bitmap, n0, p.h, p.t);
+            for (int r = wk.r0; r < wk.r1; ++r) {
                 if (cls == FULL_S && r != p.t - 1) continue;
                 const uint32_t b = au & 1u;
                 bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au >> 1) & 1u, abort, p.wait_ns);
@@ -440,7 +557,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                         uint8_t *stgc = stg + sbuf * STG_BYTES;
                         const uint32_t stgc_a = smem_u32(stgc);
                         if (lane == 0) {
-                            if (C::NBUF > 1) bulk_wait_read1(); else bulk_wait_read0();
+                            bulk_wait_read_n<C::NBUF - 1>();
                         }
                         __syncwarp();
                         uint4 *rowp = reinterpret_cast<uint4 *>(stgc + lane * 128);
@@ -458,7 +575,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                                 }
                                 bulk_commit();
                             }
-                            if (C::NBUF > 1) sbuf ^= 1;    // one bulk group per filled buffer
+                            if (C::NBUF > 1) sbuf = sbuf + 1 == C::NBUF ? 0 : sbuf + 1;   // one bulk group per filled buffer
                         }
                     }
                 } else {
@@ -595,10 +712,14 @@ caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMa
     constexpr bool PAIR = CLN > 1;
     auto kern = rowpar_fwd_tc_kernel<CLN, BNT>;
     constexpr size_t smem = smem_bytes<CLN, BNT>();
+    static_assert(smem <= 227 * 1024, "shared memory beyond the per-CTA limit");
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return CAAT_ERR_CUDA;
     const int per = CLN;
-    const int num_units = ((p.num_m + CLN - 1) / CLN) * p.num_n;
+    const int num_mg = (p.num_m + CLN - 1) / CLN;
+    // work items available: whole tiles, plus t pieces per NO_S tile when balanced
+    const int num_units = p.balanced ? num_mg * p.n_whole + num_mg * (p.num_n - p.n_whole) * p.t
+                                     : num_mg * p.num_n;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -682,6 +803,7 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     // epilogues would then pile up on the CTAs that run two units)
     const bool mmajor_size = N * K * 2 >= ((int64_t)32 << 20) && N >= 2 * h;
     const char *order_env = std::getenv("CAAT_FWD_ORDER");
+    const char *sched_env = std::getenv("CAAT_FWD_SCHED");
     p.sel = sel;
     p.n_sel = n_sel;
     p.wait_ns = g_wait_ns.load();
@@ -707,6 +829,26 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.mmajor = (mmajor_size && sel == nullptr && n_sel % bn == 0) ? 1 : 0;
         if (order_env != nullptr) p.mmajor = order_env[0] == 'm' ? 1 : 0;
         p.num_n = (int)((h + bn - 1) / bn);
+        // Balanced schedule where the host knows every tile's class: a contiguous S
+        // (passed by its size) with t > 1 and at least one channel block outside
+        // S.  A block is NO_S when it starts at or after s, whole otherwise (FULL_S
+        // when it ends by s, MIXED across the boundary).  (override:
+        // CAAT_FWD_SCHED=rounds keeps every tile whole)
+        p.balanced = 0;
+        p.n_whole = p.num_n;
+        if (sel == nullptr && t > 1 && p.num_n <= MAX_NB && !(sched_env != nullptr && sched_env[0] == 'r')) {
+            int nw = 0, ns = 0;
+            uint8_t no_s[MAX_NB];
+            for (int nb = 0; nb < p.num_n; ++nb) {
+                if ((int64_t)nb * bn >= n_sel) no_s[ns++] = (uint8_t)nb;
+                else p.nbl[nw++] = (uint8_t)nb;
+            }
+            if (ns > 0) {
+                for (int k = 0; k < ns; ++k) p.nbl[nw + k] = no_s[k];
+                p.n_whole = nw;
+                p.balanced = 1;
+            }
+        }
         if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;
         CUtensorMap tmW;
         const uint32_t wrows = cln == 1 ? bn : bn / 2;

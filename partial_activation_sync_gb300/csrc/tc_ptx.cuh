@@ -124,6 +124,14 @@ __device__ __forceinline__ void bulk_wait_read1()
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// wait until all but the N most recent committed bulk store groups have finished
+// reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read_n()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
 // wait until every committed bulk store is complete
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 

@@ -213,3 +213,28 @@ def test_debug_set_wait_validates(lib):
     assert lib.caat_debug_set_wait(1_000_000, 7) == 1
     assert lib.caat_debug_set_wait(1_000_000, 1) == 0
     assert lib.caat_debug_set_wait(0, 0) == 0
+
+
+def test_exchange_steps_reject_bad_args_without_launch(lib):
+    """pack / unpack / fold: sizes, leading dimensions, null data pointers and
+    overlapping buffers are rejected before any launch (fake device addresses)."""
+    vp = ctypes.c_void_p
+    Y, P = vp(0x100000), vp(0x900000)
+    # pack: n_sel > h, ld below the row, null P, P overlapping Y
+    assert lib.caat_pcr_pack(4, 8, 1, Y, 8, None, 9, P, 9, None) == 1
+    assert lib.caat_pcr_pack(4, 8, 1, Y, 7, None, 4, P, 4, None) == 1
+    assert lib.caat_pcr_pack(4, 8, 1, Y, 8, None, 4, None, 4, None) == 1
+    assert lib.caat_pcr_pack(4, 8, 1, Y, 8, None, 4, vp(0x100000 + 8), 4, None) == 1
+    assert lib.caat_pcr_pack(0, 8, 1, Y, 8, None, 4, P, 4, None) == 0          # nothing to move
+    # unpack: no outputs, too many, overlapping outputs, output overlapping P
+    arr = (ctypes.c_void_p * 2)(0x100000, 0x100000 + 16)
+    assert lib.caat_pcr_unpack(4, 8, 1, P, 4, None, 4, arr, 0, 8, None) == 1
+    assert lib.caat_pcr_unpack(4, 8, 1, P, 4, None, 4, arr, 65, 8, None) == 1
+    assert lib.caat_pcr_unpack(4, 8, 1, P, 4, None, 4, arr, 2, 8, None) == 1
+    one = (ctypes.c_void_p * 1)(0x900000 + 4)
+    assert lib.caat_pcr_unpack(4, 8, 1, P, 4, None, 4, one, 1, 8, None) == 1
+    # fold: t out of range, blocks overlapping each other, output inside the input
+    assert lib.caat_rank_fold(0, 4, 8, 1, Y, 8, 32, P, 8, None) == 1
+    assert lib.caat_rank_fold(2, 4, 8, 1, Y, 8, 16, P, 8, None) == 1
+    assert lib.caat_rank_fold(2, 4, 8, 1, Y, 8, 32, vp(0x100000 + 40), 8, None) == 1
+    assert lib.caat_rank_fold(2, 0, 8, 1, Y, 8, 32, P, 8, None) == 0         # nothing to fold

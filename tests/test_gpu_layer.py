@@ -45,12 +45,14 @@ def _oracle_fwd(key, Xv, Wv, t, S):
     return want
 
 
-def _fwd_case(caat, t, N, K, h, p, layout_S, dtype, wl="nn", seed=0):
+def _fwd_case(caat, t, N, K, h, p, layout_S, dtype, wl="nn", seed=0, by_size=False):
+    """by_size: a contiguous S passed by its size (the null index list), which is
+    what lets the tile kernel cut its NO_S tiles into per-shard pieces."""
     X = ci.normal(1000 + seed, (N, K))
     Wl = ci.normal(2000 + seed, (K, h), std=0.02)
     S = caat.select_channels(h, p, layout_S, 4000 + seed)
     Xd, Wd = dev(X, dtype), _weight(Wl, dtype, wl)
-    outs = caat.rowpar_linear_fwd(Xd, Wd, t, sel_dev(S))
+    outs = caat.rowpar_linear_fwd(Xd, Wd, t, int(S.size) if by_size else sel_dev(S))
     torch().cuda.synchronize()
     assert caat.device_status() == 0
     got = np.stack([to_f64(o) for o in outs])
@@ -141,17 +143,20 @@ TC_FWD_SHAPES = TC_SHAPES + [
 ]
 
 
-@pytest.fixture(params=["2", "1", "1/192", "2/192", "1:m", "2:m", "1/192:m"])
+@pytest.fixture(params=["2", "1", "1/192", "2/192", "1:m", "2:m", "1/192:m", "2:r", "1/192:r"])
 def fwd_mode(request, monkeypatch):
     """Cluster shape of the forward: 2 = one CTA pair (cta_group::2, 256-row
     tiles; the default for long shards from two row blocks up), 1 = one CTA per
     128 x 256 tile; "/192": the same with 192-channel tiles (where h is a
     multiple of 192)."""
-    mode, _, order = request.param.partition(":")    # ":m": row-block-major work order
+    # ":m": row-block-major work order; ":r": every tile whole, in rounds (no
+    # per-shard pieces of NO_S tiles)
+    mode, _, opt = request.param.partition(":")
     cl, _, bn = mode.partition("/")
     monkeypatch.setenv("CAAT_FWD_CLUSTER", cl)
     monkeypatch.setenv("CAAT_FWD_BN", bn or "256")
-    monkeypatch.setenv("CAAT_FWD_ORDER", order or "n")
+    monkeypatch.setenv("CAAT_FWD_ORDER", "m" if opt == "m" else "n")
+    monkeypatch.setenv("CAAT_FWD_SCHED", "rounds" if opt == "r" else "balanced")
     return request.param
 
 
@@ -159,8 +164,10 @@ def fwd_mode(request, monkeypatch):
 def test_fwd_tc_parity(caat, t, N, kt, h, fwd_mode):
     # p = 1/h and 1 - 1/h: a single channel in S, a single channel outside it
     for p in (0.0, 1.0 / h, 0.25, 0.5, 0.75, 1.0 - 1.0 / h, 1.0):
-        for layout in (0, 1):
-            got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=7 * t + h)
+        # contiguous S by size (balanced schedule) and as an index list; random S
+        for layout, by_size in ((0, True), (0, False), (1, False)):
+            got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=7 * t + h,
+                                     by_size=by_size)
             assert caat.last_kernel() == "rowpar_fwd_tc"
             for r in range(t):
                 check(got[r], want[r], "bf16", what=(r, p, layout))
