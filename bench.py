@@ -48,12 +48,15 @@ STEP_SPIN_CYCLES = 400000
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # dominant forward kernel, from an ncu capture of the same workload with the
-# kernels as they are now (full workload, one launch per layer); a workload or
-# layer without a capture reports null.  Output lines still dirty in L2 when the
-# kernel ends are not in the count.
+# kernels as they are now (7B prefill: the full capture of one step; 130M: the
+# one-pass launch list, averaged over its steps); a workload or layer without a
+# capture reports null.  Output lines still dirty in L2 when the kernel ends are
+# not in the count.
 DRAM_TRAFFIC = {
-    ("130m", "down_proj"): 57.84e6 + 43.74e6,
-    ("130m", "out_proj"): 15.81e6 + 39.40e6,
+    ("7b_prefill", "out_proj"): 124.69e6 + 211.19e6,
+    ("7b_prefill", "down_proj"): 360.64e6 + 231.02e6,
+    ("130m", "out_proj"): 14.90e6 + 36.48e6,
+    ("130m", "down_proj"): 82.42e6 + 43.84e6,
 }
 
 

@@ -26,9 +26,8 @@ Readings where the pages are silent:
     the ranks' final residual copies are averaged, then LayerNorm, the tied LM head
     and next-token cross-entropy.
 
-The row-parallel layers (and, with placement "column", the column-parallel ones)
-run in this library's kernels; attention, norms, GELU, embedding and loss are
-PyTorch ops of the harness.  Column-parallel weights are stored [h, K] with column
+The row-parallel and column-parallel layers run in this library's kernels;
+attention, norms, GELU, embedding and loss are PyTorch ops of the harness.  Column-parallel weights are stored [h, K] with column
 block r owned by rank r (K contiguous: the layout the library's kernels take).
 """
 import math
@@ -119,12 +118,14 @@ class Block(nn.Module):
         self.w2 = nn.Parameter(torch.randn(h, ffn) * std)
 
     def _colpar(self, a, W1):
-        """[t, N, h] -> [t, N, K/t]: rank r's input times its column block."""
+        """[t, N, h] -> [t, N, K/t]: rank r's input times its column block, in the
+        library's column-parallel kernels.  Placement "column" reduces the input
+        gradient over S; the default placement reduces nothing there (an empty S:
+        each rank's input gradient is its own dZ_r W1_r^T)."""
         t, N, h = a.shape
         kt = W1.shape[1] // t
-        if self.placement == "column":
-            return ColParallelPCR.apply(a, W1, t, self.sel).view(N, t, kt).transpose(0, 1)
-        return torch.bmm(a, W1.view(h, t, kt).transpose(0, 1))
+        sel = self.sel if self.placement == "column" else 0
+        return ColParallelPCR.apply(a, W1, t, sel).view(N, t, kt).transpose(0, 1)
 
     def forward(self, x, cos, sin, batch, seq):
         t, N, h = x.shape
