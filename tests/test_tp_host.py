@@ -206,3 +206,66 @@ def test_partial_reduce_across_processes_gloo(case):
         assert ok is True, (rank, rel)
         assert rel <= tol, (rank, rel)
     assert all(pr.exitcode == 0 for pr in procs)
+
+
+def _bytes_worker(rank, world, port, N, h, ps, q):
+    """Count the bytes this process hands to the collectives for one exchange per p."""
+    try:
+        import torch
+        import torch.distributed as dist
+        os.environ["MASTER_ADDR"] = "127.0.0.1"
+        os.environ["MASTER_PORT"] = str(port)
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+        from partial_activation_sync_gb300 import tp
+        sent = {"n": 0}
+        a2a, ag = dist.all_to_all_single, dist.all_gather
+
+        def count_a2a(out, inp, *a, **k):
+            # every block but this process's own leaves it
+            sent["n"] += inp.numel() * inp.element_size() * (world - 1) // world
+            return a2a(out, inp, *a, **k)
+
+        def count_ag(outs, inp, *a, **k):
+            # this process's block goes to every other process
+            sent["n"] += inp.numel() * inp.element_size() * (world - 1)
+            return ag(outs, inp, *a, **k)
+
+        dist.all_to_all_single, dist.all_gather = count_a2a, count_ag
+        res = []
+        for p in ps:
+            S = orc.select_channels(h, p, 0, 0)
+            Y = [torch.from_numpy(ci.normal(9000 + rank, (N, h))).to(torch.bfloat16)]
+            sent["n"] = 0
+            tp.PartialReduce(ops=OracleOps("bf16"))(Y, int(S.size))
+            res.append(sent["n"])
+        dist.all_to_all_single, dist.all_gather = a2a, ag
+        q.put((rank, res))
+        dist.destroy_process_group()
+    except Exception as e:  # pragma: no cover
+        import traceback
+        q.put((rank, "%s\n%s" % (e, traceback.format_exc())))
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_exchange_bytes_are_the_p_fraction_of_an_all_reduce(world):
+    """The pages' communication claim ("up to 50% less" at p = 0.5): each process
+    sends 2 (P-1)/P N |S| elem bytes, where a ring all-reduce of all h channels
+    sends 2 (P-1)/P N h elem -- the ratio is p exactly (N a multiple of P)."""
+    import torch.multiprocessing as mp
+    N, h, ps = 64, 96, (0.25, 0.5, 1.0)
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_bytes_worker, args=(r, world, port, N, h, ps, q)) for r in range(world)]
+    for pr in procs:
+        pr.start()
+    res = [q.get(timeout=120) for _ in range(world)]
+    for pr in procs:
+        pr.join(timeout=60)
+    allreduce = 2 * (world - 1) * N * h * 2 // world
+    for rank, counts in res:
+        assert isinstance(counts, list), counts
+        for p, n in zip(ps, counts):
+            s = int(p * h + 0.5)
+            assert n == 2 * (world - 1) * N * s * 2 // world, (rank, p, n)
+            assert n / allreduce == pytest.approx(p), (rank, p)
