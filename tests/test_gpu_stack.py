@@ -4,8 +4,12 @@ kernels, the rest PyTorch) against the float64 CPU reference of the stack.
 Both placements of the backward reduce are checked, each against the reference's
 matching placement.  Reduced stack: 2 layers, sequence 64, batch 2, vocabulary
 1024, with the 130M model's width (h = 768, 16 heads, FFN 3072), t = 8, p = 0.5.
-Tolerances are relative, set by bf16 activations through two blocks: 2e-2 on the
-loss, 8e-2 (relative Frobenius) on parameter gradients."""
+Tolerances are relative. The parameters and every activation are bf16, so each op
+rounds to 2^-9 relative; through two blocks, forward and backward, the measured
+relative Frobenius error of the parameter gradients is at most 0.0078 (about four
+bf16 roundings' worth; both placements, seeds 1234 and 99) and that of the loss
+4.2e-5.  The bounds are 2e-2 on gradients (2.5 times the largest seen, about ten
+roundings) and 1e-3 on the loss."""
 import numpy as np
 import pytest
 
@@ -32,10 +36,10 @@ def test_stack_loss_and_gradients_match_reference(placement):
     assert caat.device_status() == 0
     params = {n: p.detach().double().cpu() for n, p in model.named_parameters()}
     L, grads = ost.loss_and_grads(params, tokens.cpu(), t, heads, layers, model.n_sel, placement)
-    assert abs(float(loss) - L) <= 2e-2 * abs(L), (float(loss), L)
+    assert abs(float(loss.detach()) - L) <= 1e-3 * abs(L), (float(loss.detach()), L)
     for name, p in model.named_parameters():
         g = p.grad.double().cpu().numpy()
-        assert rel_fro(g, grads[name].numpy()) <= 8e-2, name
+        assert rel_fro(g, grads[name].numpy()) <= 2e-2, name
 
 
 @pytest.mark.parametrize("placement", ["reduce_dout", "column"])
