@@ -26,8 +26,10 @@
  *    and tests; the defaults choose by shape): CAAT_FWD_CLUSTER=1|2 (CTAs per
  *    cluster of the forward tile kernel), CAAT_FWD_BN=192|256 (its tile width),
  *    CAAT_FWD_ORDER=m|n (its work units row- or channel-block-major),
- *    CAAT_FWD_SCHED=rounds (every tile of it whole, in rounds, instead of cutting
- *    the tiles outside S into per-shard pieces that even out the SMs' load),
+ *    CAAT_FWD_SCHED=rounds|first (every tile of it whole, in rounds, instead of
+ *    cutting the tiles outside S into per-shard pieces that even out the SMs'
+ *    load; or the whole tiles first and the pieces after them, instead of the
+ *    pieces in runs around each worker's whole tiles),
  *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
  *    (backward on `stream` only).
  *  - "device pointer" = memory the caller allocated on the current CUDA device;

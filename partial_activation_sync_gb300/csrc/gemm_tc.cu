@@ -216,55 +216,42 @@ struct Cursor {
     int i;            // next whole unit
     int j, step, end; // next piece, stride, end of the current phase
     int phase;        // 0: pieces for the light workers, 1: pieces for all, 2: done
+    int wleft;        // whole units still to come (interleaved order)
+    int batch, inb;   // pieces between two whole units, pieces of the current run
 };
 
 __device__ __forceinline__ void cursor_init(Cursor &c, const FwdParams &p, int g, int G, int num_mg)
 {
     c.i = g;
     c.phase = 2;
+    c.wleft = c.batch = c.inb = 0;
     if (!p.balanced) return;
     const int nW = num_mg * p.n_whole;
     const int rem = nW % G;
     const int light = rem > 0 ? G - rem : 0;
     const int P = num_mg * (p.num_n - p.n_whole) * p.t;
     const int A = min(P, light * p.t);
+    int q = 0;    // this worker's pieces
     if (light > 0 && g >= rem && g - rem < A) {
         c.phase = 0;
         c.j = g - rem;
         c.step = light;
         c.end = A;
+        q = (A - c.j + light - 1) / light;
     } else {
         c.phase = 1;
         c.j = A + g;
         c.step = G;
         c.end = P;
     }
+    if (A + g < P) q += (P - (A + g) + G - 1) / G;
+    c.wleft = g < nW ? (nW - 1 - g) / G + 1 : 0;
+    // interleaved order: the pieces in wleft + 1 equal runs around the whole units
+    c.batch = (q + c.wleft) / (c.wleft + 1);
 }
 
-__device__ __forceinline__ bool next_work(Cursor &c, const FwdParams &p, int g, int G, int num_mg, Work &w)
+__device__ __forceinline__ bool next_piece(Cursor &c, const FwdParams &p, int g, int G, int num_mg, Work &w)
 {
-    if (!p.balanced) {
-        if (c.i >= num_mg * p.num_n) return false;
-        const int u = c.i;
-        c.i += G;
-        w.mg = p.mmajor ? u / p.num_n : u % num_mg;
-        w.nb = p.mmajor ? u % p.num_n : u / num_mg;
-        w.r0 = 0;
-        w.r1 = p.t;
-        w.piece = 0;
-        return true;
-    }
-    const int nW = num_mg * p.n_whole;
-    if (c.i < nW) {
-        const int i = c.i;
-        c.i += G;
-        w.mg = p.mmajor ? i / p.n_whole : i % num_mg;
-        w.nb = p.nbl[p.mmajor ? i % p.n_whole : i / num_mg];
-        w.r0 = 0;
-        w.r1 = p.t;
-        w.piece = 0;
-        return true;
-    }
     if (c.phase == 0 && c.j >= c.end) {
         // the light workers' share is done: continue with the pieces dealt to all
         c.phase = 1;
@@ -283,6 +270,52 @@ __device__ __forceinline__ bool next_work(Cursor &c, const FwdParams &p, int g, 
     w.piece = 1;
     c.j += c.step;
     return true;
+}
+
+__device__ __forceinline__ bool next_whole(Cursor &c, const FwdParams &p, int G, int num_mg, Work &w)
+{
+    const int nW = num_mg * p.n_whole;
+    if (c.i >= nW) return false;
+    const int i = c.i;
+    c.i += G;
+    w.mg = p.mmajor ? i / p.n_whole : i % num_mg;
+    w.nb = p.nbl[p.mmajor ? i % p.n_whole : i / num_mg];
+    w.r0 = 0;
+    w.r1 = p.t;
+    w.piece = 0;
+    return true;
+}
+
+// The next work item of worker g.  balanced == 1: the whole units first, then the
+// pieces; balanced == 2: the pieces in equal runs before, between and after the
+// whole units, which spreads the pieces' output writes over the whole kernel.
+__device__ __forceinline__ bool next_work(Cursor &c, const FwdParams &p, int g, int G, int num_mg, Work &w)
+{
+    if (!p.balanced) {
+        if (c.i >= num_mg * p.num_n) return false;
+        const int u = c.i;
+        c.i += G;
+        w.mg = p.mmajor ? u / p.num_n : u % num_mg;
+        w.nb = p.mmajor ? u % p.num_n : u / num_mg;
+        w.r0 = 0;
+        w.r1 = p.t;
+        w.piece = 0;
+        return true;
+    }
+    if (p.balanced == 1) {
+        if (next_whole(c, p, G, num_mg, w)) return true;
+        return next_piece(c, p, g, G, num_mg, w);
+    }
+    if (c.inb < c.batch && next_piece(c, p, g, G, num_mg, w)) {
+        ++c.inb;
+        return true;
+    }
+    if (c.wleft > 0 && next_whole(c, p, G, num_mg, w)) {
+        --c.wleft;
+        c.inb = 0;
+        return true;
+    }
+    return next_piece(c, p, g, G, num_mg, w);
 }
 
 template <int BNT>
@@ -832,8 +865,9 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         // Balanced schedule where the host knows every tile's class: a contiguous S
         // (passed by its size) with t > 1 and at least one channel block outside
         // S.  A block is NO_S when it starts at or after s, whole otherwise (FULL_S
-        // when it ends by s, MIXED across the boundary).  (override:
-        // CAAT_FWD_SCHED=rounds keeps every tile whole)
+        // when it ends by s, MIXED across the boundary).  The pieces run in equal
+        // runs around each worker's whole tiles.  (override: CAAT_FWD_SCHED=rounds
+        // keeps every tile whole; CAAT_FWD_SCHED=first runs the whole tiles first)
         p.balanced = 0;
         p.n_whole = p.num_n;
         if (sel == nullptr && t > 1 && p.num_n <= MAX_NB && !(sched_env != nullptr && sched_env[0] == 'r')) {
@@ -846,7 +880,7 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
             if (ns > 0) {
                 for (int k = 0; k < ns; ++k) p.nbl[nw + k] = no_s[k];
                 p.n_whole = nw;
-                p.balanced = 1;
+                p.balanced = (sched_env != nullptr && sched_env[0] == 'f') ? 1 : 2;
             }
         }
         if ((int64_t)p.num_m * p.num_n > INT32_MAX / 4) return CAAT_ERR_UNSUPPORTED;

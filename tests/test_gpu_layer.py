@@ -143,20 +143,20 @@ TC_FWD_SHAPES = TC_SHAPES + [
 ]
 
 
-@pytest.fixture(params=["2", "1", "1/192", "2/192", "1:m", "2:m", "1/192:m", "2:r", "1/192:r"])
+@pytest.fixture(params=["2", "1", "1/192", "2/192", "1:m", "2:m", "1/192:m", "2:r", "1/192:r", "2:f", "1:f"])
 def fwd_mode(request, monkeypatch):
     """Cluster shape of the forward: 2 = one CTA pair (cta_group::2, 256-row
     tiles; the default for long shards from two row blocks up), 1 = one CTA per
     128 x 256 tile; "/192": the same with 192-channel tiles (where h is a
     multiple of 192)."""
     # ":m": row-block-major work order; ":r": every tile whole, in rounds (no
-    # per-shard pieces of NO_S tiles)
+    # per-shard pieces of NO_S tiles); ":f": whole tiles first, pieces after
     mode, _, opt = request.param.partition(":")
     cl, _, bn = mode.partition("/")
     monkeypatch.setenv("CAAT_FWD_CLUSTER", cl)
     monkeypatch.setenv("CAAT_FWD_BN", bn or "256")
     monkeypatch.setenv("CAAT_FWD_ORDER", "m" if opt == "m" else "n")
-    monkeypatch.setenv("CAAT_FWD_SCHED", "rounds" if opt == "r" else "balanced")
+    monkeypatch.setenv("CAAT_FWD_SCHED", {"r": "rounds", "f": "first"}.get(opt, "interleaved"))
     return request.param
 
 
