@@ -688,10 +688,17 @@ def run_extras(torch, caat, device, peaks, args):
             "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4),
             "us": round(sec * 1e6, 1), "kernel": caat.last_kernel()}
         del X, Wst, Ys
-    # 7B decode: N in {1, 8, 64} tokens, p = 0.5, contiguous S -- weight streaming (HBM bound)
+    # 7B decode: N in {1, 8, 64} tokens, p = 0.5, contiguous S -- weight streaming (HBM
+    # bound).  Each call alone (CUDA events around one launch, so the launch latency
+    # is in the time), and per call inside a CUDA graph that runs the layer for 8
+    # different weight sets in turn (8 layers of a decode step: 269 / 722 MB of
+    # weights, more than L2, so every call streams its weights from HBM; the launch
+    # cost is paid once per graph)
     sel = torch.from_numpy(caat.select_channels(w.h, w.p, caat.CAAT_S_CONTIGUOUS)).to(device)
+    nsets = 8
     for li, L in enumerate(w.layers):
-        Wst = (torch.randn((w.h, L.K), device=device) * 0.02).to(torch.bfloat16)
+        Wsets = [(torch.randn((w.h, L.K), device=device) * 0.02).to(torch.bfloat16) for _ in range(nsets)]
+        Wst = Wsets[0]
         for Nd in w.decode_N:
             X = torch.randn((Nd, L.K), device=device).to(torch.bfloat16)
             Ys = [torch.empty((Nd, w.h), dtype=torch.bfloat16, device=device) for _ in range(w.t)]
@@ -699,12 +706,27 @@ def run_extras(torch, caat, device, peaks, args):
             fn()
             sec = _time_call(torch, fn, 10, flush)
             byt = 2.0 * (L.K * w.h + Nd * L.K + w.t * Nd * w.h)
-            out["7b_decode_N%d_%s" % (Nd, L.name)] = {
-                "GB/s": round(byt / sec / 1e9, 1), "frac_hbm": round(byt / sec / 1e9 / peaks["hbm"], 4),
-                "us": round(sec * 1e6, 1), "TFLOP/s": round(2.0 * Nd * L.K * w.h / sec / 1e12, 2),
-                "kernel": caat.last_kernel()}
-            del X, Ys
-        del Wst
+            rec = {"GB/s": round(byt / sec / 1e9, 1), "frac_hbm": round(byt / sec / 1e9 / peaks["hbm"], 4),
+                   "us": round(sec * 1e6, 1), "TFLOP/s": round(2.0 * Nd * L.K * w.h / sec / 1e12, 2),
+                   "kernel": caat.last_kernel()}
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                for Wk in Wsets:
+                    caat.rowpar_linear_fwd(X, Wk.t(), w.t, sel, outs=Ys)
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for Wk in Wsets:
+                    caat.rowpar_linear_fwd(X, Wk.t(), w.t, sel, outs=Ys)
+            graph.replay()
+            sec_g = _time_call(torch, graph.replay, 10, flush) / nsets
+            rec.update({"graph_us": round(sec_g * 1e6, 2), "graph_GB/s": round(byt / sec_g / 1e9, 1),
+                        "graph_frac_hbm": round(byt / sec_g / 1e9 / peaks["hbm"], 4)})
+            out["7b_decode_N%d_%s" % (Nd, L.name)] = rec
+            del X, Ys, graph
+        del Wsets, Wst
     # column-parallel layer at the 130M MLP up-projection (N = 8192, h = 768,
     # FFN 3072, t = 8, p = 0.5): forward, and the backward with the partial reduce
     # on its input gradient (Megatron's placement)

@@ -42,6 +42,10 @@
  *    is written and nothing is launched.
  *  - bf16 data is stored as 16-bit words; all arithmetic accumulates in fp32.
  *  - No C++ exception crosses this interface.
+ *  - Per device, the library sets each kernel's shared-memory limit and looks up
+ *    its cluster occupancy once, on the kernel's first launch, and keeps the
+ *    answers for the life of the process.  They do not survive cudaDeviceReset:
+ *    a process that resets a device should not call the library on it again.
  */
 #ifndef CAAT_H
 #define CAAT_H
@@ -370,9 +374,9 @@ typedef enum { CAAT_INJECT_NONE = 0, CAAT_INJECT_SKIP_LOADS = 1 } caat_inject;
 caat_status caat_debug_set_wait(uint64_t limit_ns, caat_inject inject);
 
 /*
- * caat_last_kernel -- which kernel the last successful launch on this host
- * thread used (static string, e.g. "pcr_vec", "rowpar_fwd_tc", "rowpar_fwd_simt").
- * For tests and benchmarks.
+ * caat_last_kernel -- which kernel the last successful call on this host thread
+ * used (static string, e.g. "pcr_vec", "rowpar_fwd_tc", "rowpar_fwd_simt"); for a
+ * call that launches several kernels, its main one.  For tests and benchmarks.
  */
 const char *caat_last_kernel(void);
 

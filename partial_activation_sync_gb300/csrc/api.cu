@@ -35,6 +35,56 @@ int num_sms()
     return g_sms[dev];
 }
 
+namespace {
+struct KernelKey {
+    int dev;
+    const void *kern;
+    int a, b;
+};
+std::mutex g_kmu;
+KernelKey g_smem_done[256];
+int g_n_smem = 0;
+struct ClusterEntry {
+    KernelKey k;
+    int active;
+};
+ClusterEntry g_clusters[256];
+int g_n_clusters = 0;
+}  // namespace
+
+caat_status prepare_kernel_smem(const void *kern, int smem_bytes)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CAAT_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_kmu);
+    for (int i = 0; i < g_n_smem; ++i)
+        if (g_smem_done[i].dev == dev && g_smem_done[i].kern == kern && g_smem_done[i].a >= smem_bytes)
+            return CAAT_OK;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+        return CAAT_ERR_CUDA;
+    if (g_n_smem < 256) g_smem_done[g_n_smem++] = {dev, kern, smem_bytes, 0};
+    return CAAT_OK;
+}
+
+int max_active_clusters(const void *kern, const cudaLaunchConfig_t &cfg)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    int cl = 1;
+    for (unsigned i = 0; i < cfg.numAttrs; ++i)
+        if (cfg.attrs[i].id == cudaLaunchAttributeClusterDimension) cl = (int)cfg.attrs[i].val.clusterDim.x;
+    const int smem = (int)cfg.dynamicSmemBytes;
+    std::lock_guard<std::mutex> lk(g_kmu);
+    for (int i = 0; i < g_n_clusters; ++i) {
+        const KernelKey &k = g_clusters[i].k;
+        if (k.dev == dev && k.kern == kern && k.a == cl && k.b == smem) return g_clusters[i].active;
+    }
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess) return -1;
+    if (g_n_clusters < 256) g_clusters[g_n_clusters++] = {{dev, kern, cl, smem}, active};
+    return active;
+}
+
 // defined next to the kernels that own the device error word
 caat_status read_and_clear_device_error();
 

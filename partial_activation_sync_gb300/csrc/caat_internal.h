@@ -24,6 +24,13 @@ int *device_error_word();          // device address for the current device, or 
 
 int num_sms();                     // SM count of the current device (cached)
 
+// Per-call host work done once per device and kernel: the kernel's dynamic
+// shared-memory limit (set on first use) and, for cluster launches, how many
+// clusters of the given shape can be co-resident (queried on first use; cfg's
+// grid is ignored).  Both cache the answer per (device, kernel, size).
+caat_status prepare_kernel_smem(const void *kern, int smem_bytes);
+int max_active_clusters(const void *kern, const cudaLaunchConfig_t &cfg);   // < 1: none / error
+
 // ---- standalone partial channel-reduce (pcr.cu)
 caat_status launch_pcr(int t, int64_t N, int64_t h, caat_dtype dt,
                        const ConstPtrs &in, int64_t ld_in, const MutPtrs &out, int64_t ld_out,

@@ -746,8 +746,7 @@ caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMa
     auto kern = rowpar_fwd_tc_kernel<CLN, BNT>;
     constexpr size_t smem = smem_bytes<CLN, BNT>();
     static_assert(smem <= 227 * 1024, "shared memory beyond the per-CTA limit");
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return CAAT_ERR_CUDA;
+    if (prepare_kernel_smem((const void *)kern, (int)smem) != CAAT_OK) return CAAT_ERR_CUDA;
     const int per = CLN;
     const int num_mg = (p.num_m + CLN - 1) / CLN;
     // work items available: whole tiles, plus t pieces per NO_S tile when balanced
@@ -767,9 +766,8 @@ caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMa
     int groups = num_sms() / per;
     if (PAIR) {
         cfg.gridDim = dim3(groups * per);
-        int active = 0;
-        if (cudaOccupancyMaxActiveClusters(&active, (void *)kern, &cfg) != cudaSuccess || active < 1)
-            return CAAT_ERR_UNSUPPORTED;
+        const int active = max_active_clusters((const void *)kern, cfg);
+        if (active < 1) return CAAT_ERR_UNSUPPORTED;
         if (active < groups) groups = active;
     }
     if (groups > num_units) groups = num_units;
@@ -870,7 +868,22 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         // keeps every tile whole; CAAT_FWD_SCHED=first runs the whole tiles first)
         p.balanced = 0;
         p.n_whole = p.num_n;
-        if (sel == nullptr && t > 1 && p.num_n <= MAX_NB && !(sched_env != nullptr && sched_env[0] == 'r')) {
+        const bool rounds_env = sched_env != nullptr && sched_env[0] == 'r';
+        // An index list of S with 0 < |S| < h (a random S): its tiles would be MIXED
+        // -- per-shard epilogues, the S channels summed in TMEM across shards, and
+        // masked stores of the sums to every rank -- and MIXED tiles cannot be cut
+        // into pieces.  Instead every tile runs as per-shard pieces (each rank's
+        // partial, all channels) and the S channels are then summed over the ranks
+        // in place by the standalone partial reduce (rank-order fp32 fold of the
+        // bf16 partials).  (CAAT_FWD_SCHED=rounds keeps the MIXED tiles)
+        const bool pieces_then_reduce = sel != nullptr && n_sel > 0 && n_sel < h && t > 1 &&
+                                        p.num_n <= MAX_NB && !rounds_env;
+        if (pieces_then_reduce) {
+            for (int nb = 0; nb < p.num_n; ++nb) p.nbl[nb] = (uint8_t)nb;
+            p.n_whole = 0;
+            p.balanced = 2;
+        }
+        if (sel == nullptr && t > 1 && p.num_n <= MAX_NB && !rounds_env) {
             int nw = 0, ns = 0;
             uint8_t no_s[MAX_NB];
             for (int nb = 0; nb < p.num_n; ++nb) {
@@ -894,6 +907,13 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
             st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s) : launch_fwd<1, 192>(tmX, tmW, ym, p, s);
         else
             st = cln == 2 ? launch_fwd<2, BN>(tmX, tmW, ym, p, s) : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
+        if (st == CAAT_OK && pieces_then_reduce) {
+            ConstPtrs yin{};
+            for (int r = 0; r < t; ++r) yin.p[r] = Y.p[r];
+            st = launch_pcr(t, N, h, CAAT_BF16, yin, ldy, Y, ldy, true, sel, n_sel, s);
+            if (st == CAAT_OK) note_launch("rowpar_fwd_tc", 0);   // the call's main kernel
+            return st;
+        }
         // a cluster shape that cannot be co-resident falls back to a smaller one
         if (st != CAAT_ERR_UNSUPPORTED || cln == 1) return st;
     }

@@ -333,8 +333,7 @@ caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &smap, cons
     if (p.units <= 0) return CAAT_OK;
     const int grid = p.units < num_sms() ? p.units : num_sms();
     auto kern = grouped_gemm_tc_kernel<A_MN, RED>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) != cudaSuccess)
-        return CAAT_ERR_CUDA;
+    if (prepare_kernel_smem((const void *)kern, (int)SMEM_BYTES) != CAAT_OK) return CAAT_ERR_CUDA;
     kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, smap, bmap, cmap, p);
     note_launch(name);
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;

@@ -357,8 +357,7 @@ caat_status launch_nt(const CUtensorMap &tmX, const CUtensorMap &tmW, const Skin
 {
     auto kern = rowpar_fwd_skinny_kernel<NT>;
     constexpr size_t smem = skinny_smem<NT>();
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return CAAT_ERR_CUDA;
+    if (prepare_kernel_smem((const void *)kern, (int)smem) != CAAT_OK) return CAAT_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -371,9 +370,7 @@ caat_status launch_nt(const CUtensorMap &tmX, const CUtensorMap &tmW, const Skin
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    int active = 0;
-    if (cudaOccupancyMaxActiveClusters(&active, (void *)kern, &cfg) != cudaSuccess || active < 1)
-        return CAAT_ERR_UNSUPPORTED;
+    if (max_active_clusters((const void *)kern, cfg) < 1) return CAAT_ERR_UNSUPPORTED;
     if (cudaLaunchKernelEx(&cfg, kern, tmX, tmW, p) != cudaSuccess) return CAAT_ERR_CUDA;
     note_launch("rowpar_fwd_skinny_tc");
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
