@@ -130,11 +130,15 @@ std::atomic<int> g_inject{CAAT_INJECT_NONE};
 #ifndef CAAT_FWD_PAIR_NBUF256
 #define CAAT_FWD_PAIR_NBUF256 1
 #endif
+// ring depth of the single-CTA mode (stages of 16 KB of X + 32 / 24 KB of W)
+#ifndef CAAT_FWD_SINGLE_STAGES
+#define CAAT_FWD_SINGLE_STAGES 4
+#endif
 
 template <int CLN, int BNT>
 struct Cfg {
     static constexpr bool PAIR = CLN > 1;
-    static constexpr int STAGES = PAIR ? CAAT_FWD_PAIR_STAGES : 4;
+    static constexpr int STAGES = PAIR ? CAAT_FWD_PAIR_STAGES : CAAT_FWD_SINGLE_STAGES;
     // staging buffers per epilogue warp: several (bulk stores drain the earlier
     // ones while the next chunk fills one) where shared memory allows
     static constexpr int NBUF = BNT < 256 ? 2 : (PAIR ? CAAT_FWD_PAIR_NBUF256 : 1);

@@ -70,9 +70,14 @@ ELEM = {"bf16": (2.0 ** -8, 2.0 ** -7), "f32": (2.0 ** -18, 2.0 ** -16)}
 ELEM_BWD = {"bf16": (2.0 ** -8, 2.0 ** -6), "f32": (2.0 ** -18, 2.0 ** -15)}
 
 
-def check(got: np.ndarray, want: np.ndarray, dtype: str, bwd: bool = False, what=""):
+def check(got: np.ndarray, want: np.ndarray, dtype: str, bwd: bool = False, what="", spread=None):
     """Relative Frobenius error within TOL[dtype], and every element within the
-    element-wise bound above (NaN or inf in `got` fails)."""
+    element-wise bound above (NaN or inf in `got` fails).
+
+    spread: for results that sum the ranks' partials after rounding each to the
+    dtype (the forward with an index list of S, whose S channels are the rank-order
+    fold of the rounded partials), sum_r |Y_r| per element; each rounded partial
+    adds up to half an ulp of itself, so REL * spread joins the bound there."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, (what, got.shape, want.shape)
@@ -84,6 +89,8 @@ def check(got: np.ndarray, want: np.ndarray, dtype: str, bwd: bool = False, what
     rms = float(np.sqrt(np.mean(want * want)))
     err = np.abs(got - want)
     bound = rel * np.abs(want) + tau * rms
+    if spread is not None:
+        bound = bound + rel * np.asarray(spread, dtype=np.float64)
     ok = err <= bound                      # NaN compares false: it fails
     if not ok.all():
         bad = np.argwhere(~ok)

@@ -50,15 +50,22 @@ def _run(caat, t, N, h, K, p, layout_S, dtype, wl="rm", seed=0):
     wZ = orc.colpar_fwd(hA, hW, t)
     wA, wW = orc.colpar_bwd(hA, hW, hZ, t, S)
     got = (to_f64(Z), np.stack([to_f64(dA[r]) for r in range(t)]), to_f64(dW1))
-    return got, (wZ, wA, wW), S, (fwd_kernel, bwd_kernel)
+    # S as an index list: the S channels of dA may fold the ranks' rounded
+    # partials dZ_r W1_r^T (the tile kernel); their magnitudes bound that rounding
+    spread = None
+    if 0 < S.size < h and t > 1:
+        parts, _ = orc.colpar_bwd(hA, hW, hZ, t, np.zeros(0, np.int32))
+        spread = np.zeros(wA.shape[1:])
+        spread[:, S] = np.abs(parts).sum(axis=0)[:, S]
+    return got, (wZ, wA, wW, spread), S, (fwd_kernel, bwd_kernel)
 
 
 def _check(got, want, S, t, dtype):
     gZ, gA, gW = got
-    wZ, wA, wW = want
+    wZ, wA, wW, spread = want
     check(gZ, wZ, dtype)
     for r in range(t):
-        check(gA[r], wA[r], dtype, what=r)
+        check(gA[r], wA[r], dtype, what=r, spread=spread)
     check(gW, wW, dtype)
     for r in range(1, t):
         assert np.array_equal(gA[r][:, S], gA[0][:, S])
@@ -86,14 +93,27 @@ def test_colpar_tensor_core_shapes(caat, t, N, h, K, p, layout):
 
 
 def test_colpar_contiguous_set_by_size(caat):
-    # S passed as a size (null index list) gives the same result as the index list
+    # S passed as a size (null index list) against the index list of the same S:
+    # dW1 and the channels of dA outside S are computed alike (the same bits); the
+    # S channels of dA are summed in fp32 over all of K (size) or folded from the
+    # ranks' rounded partials (index list), and both match the oracle
     t, N, h, K = 8, 256, 768, 3072
     A, W1, dZ = _inputs(t, N, h, K, 9)
     Ad, W1d, dZd = dev(A, "bf16"), dev(W1, "bf16"), dev(dZ, "bf16")
     dA1, dW1a = caat.colpar_linear_bwd(Ad, W1d, dZd, t, 384)
     dA2, dW1b = caat.colpar_linear_bwd(Ad, W1d, dZd, t, sel_dev(np.arange(384)))
     torch().cuda.synchronize()
-    assert bool((dA1 == dA2).all()) and bool((dW1a == dW1b).all())
+    assert bool((dW1a == dW1b).all())
+    assert bool((dA1[:, :, 384:] == dA2[:, :, 384:]).all())
+    hA, hW, hZ = host_values(A, "bf16"), host_values(W1, "bf16"), host_values(dZ, "bf16")
+    S = np.arange(384, dtype=np.int32)
+    wA, _ = orc.colpar_bwd(hA, hW, hZ, t, S)
+    parts, _ = orc.colpar_bwd(hA, hW, hZ, t, np.zeros(0, np.int32))
+    spread = np.zeros((N, h))
+    spread[:, S] = np.abs(parts).sum(axis=0)[:, S]
+    for r in range(t):
+        check(to_f64(dA1[r]), wA[r], "bf16")
+        check(to_f64(dA2[r]), wA[r], "bf16", spread=spread)
 
 
 def test_colpar_empty_sizes(caat):

@@ -28,6 +28,15 @@ def _weight(Wl32, dtype, layout):
     return dev(Wl32, dtype)
 
 
+def _spread(Xv, Wv, t, S):
+    """sum_r |Y_r| on the channels of S (zero elsewhere): the scale of the rounding
+    of the ranks' partials when the S channels fold them after rounding."""
+    parts, _ = orc.rowpar_fwd(Xv, Wv, t, np.zeros(0, np.int32))
+    spread = np.zeros(parts.shape[1:])
+    spread[:, S] = np.abs(parts).sum(axis=0)[:, S]
+    return spread
+
+
 # oracle results by case: the same case runs under several kernel modes
 _ORACLE_CACHE = {}
 _ORACLE_CACHE_BYTES = [0]
@@ -56,9 +65,15 @@ def _fwd_case(caat, t, N, K, h, p, layout_S, dtype, wl="nn", seed=0, by_size=Fal
     torch().cuda.synchronize()
     assert caat.device_status() == 0
     got = np.stack([to_f64(o) for o in outs])
-    want = _oracle_fwd((t, N, K, h, S.tobytes(), dtype, seed), host_values(X, dtype),
-                       host_values(Wl, dtype), t, S)
-    return got, want, S
+    Xv, Wv = host_values(X, dtype), host_values(Wl, dtype)
+    want = _oracle_fwd((t, N, K, h, S.tobytes(), dtype, seed), Xv, Wv, t, S)
+    spread = None
+    if not by_size and 0 < S.size < h and t > 1:
+        # an index list of S: the S channels fold the ranks' rounded partials
+        parts = _oracle_fwd((t, N, K, h, b"", dtype, seed), Xv, Wv, t, np.zeros(0, np.int32))
+        spread = np.zeros((N, h))
+        spread[:, S] = np.abs(parts).sum(axis=0)[:, S]
+    return got, want, S, spread
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -68,9 +83,9 @@ def _fwd_case(caat, t, N, K, h, p, layout_S, dtype, wl="nn", seed=0, by_size=Fal
 def test_fwd_small_shapes(caat, dtype, t, N, kt, h, wl):
     for p in (0.0, 0.5, 1.0):
         for layout in (0, 1):
-            got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, dtype, wl, seed=t + N)
+            got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, p, layout, dtype, wl, seed=t + N)
             for r in range(t):
-                check(got[r], want[r], dtype, what=(r, p, layout))
+                check(got[r], want[r], dtype, what=(r, p, layout), spread=spread)
             for r in range(1, t):    # S channels bit-identical across ranks
                 assert np.array_equal(got[r][:, S], got[0][:, S])
 
@@ -166,11 +181,11 @@ def test_fwd_tc_parity(caat, t, N, kt, h, fwd_mode):
     for p in (0.0, 1.0 / h, 0.25, 0.5, 0.75, 1.0 - 1.0 / h, 1.0):
         # contiguous S by size (balanced schedule) and as an index list; random S
         for layout, by_size in ((0, True), (0, False), (1, False)):
-            got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=7 * t + h,
+            got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=7 * t + h,
                                      by_size=by_size)
             assert caat.last_kernel() == "rowpar_fwd_tc"
             for r in range(t):
-                check(got[r], want[r], "bf16", what=(r, p, layout))
+                check(got[r], want[r], "bf16", what=(r, p, layout), spread=spread)
             for r in range(1, t):
                 assert np.array_equal(got[r][:, S], got[0][:, S])
 
@@ -185,9 +200,15 @@ def test_fwd_tc_boundary_tile_mixed(caat, fwd_mode):
     torch().cuda.synchronize()
     assert caat.last_kernel() == "rowpar_fwd_tc"
     got = np.stack([to_f64(o) for o in outs])
-    want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), t, S)
+    Xv, Wv = host_values(X, "bf16"), host_values(Wl, "bf16")
+    want, _ = orc.rowpar_fwd(Xv, Wv, t, S)
+    # an index list of S: the S channels fold the ranks' rounded partials (except
+    # in the MIXED-tile mode of the ":r" schedule, where this bound is just looser)
+    parts, _ = orc.rowpar_fwd(Xv, Wv, t, np.zeros(0, np.int32))
+    spread = np.zeros((N, h))
+    spread[:, S] = np.abs(parts).sum(axis=0)[:, S]
     for r in range(t):
-        check(got[r], want[r], "bf16")
+        check(got[r], want[r], "bf16", spread=spread)
         # per-column check: the non-S half of the mixed tile is this rank's own sum
         check(got[r][:, 300:512], want[r][:, 300:512], "bf16")
 
@@ -206,9 +227,11 @@ def test_fwd_tc_output_guard(caat, fwd_mode):
     assert caat.last_kernel() == "rowpar_fwd_tc"
     for b in bufs:
         assert bool((b[:, h:] == 7.0).all())
-    want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), t, S)
+    Xv, Wv = host_values(X, "bf16"), host_values(Wl, "bf16")
+    want, _ = orc.rowpar_fwd(Xv, Wv, t, S)
+    spread = _spread(Xv, Wv, t, S)
     for r in range(t):
-        check(to_f64(outs[r]), want[r], "bf16")
+        check(to_f64(outs[r]), want[r], "bf16", spread=spread)
 
 
 FULL = [("130m", 0), ("130m", 1), ("1.1b", 0), ("1.1b", 1), ("7b_prefill", 0), ("7b_prefill", 1)]
@@ -249,9 +272,15 @@ def test_fwd_full_size_sampled_rows(caat, wname, li):
             assert caat.device_status() == 0
             assert caat.last_kernel() == "rowpar_fwd_tc"
             want, _ = orc.rowpar_fwd(Xs, Wv, w.t, S)
+            spread = None
+            if layout == 1 and 0 < S.size < w.h:
+                # a random S (index list): the S channels fold the rounded partials
+                parts, _ = orc.rowpar_fwd(Xs, Wv, w.t, np.zeros(0, np.int32))
+                spread = np.zeros(want.shape[1:])
+                spread[:, S] = np.abs(parts).sum(axis=0)[:, S]
             for r in range(w.t):
                 got = to_f64(outs[r][rows.tolist()])
-                check(got, want[r], "bf16", what=(p, layout, r))
+                check(got, want[r], "bf16", what=(p, layout, r), spread=spread)
             full0 = outs[0][:, S.tolist()] if S.size else None
             for r in range(1, w.t):
                 if full0 is not None:
@@ -353,10 +382,10 @@ def test_fwd_decode_parity(caat, t, N, monkeypatch):
     kt = 96 if t <= 8 else 64
     for p in (0.0, 0.5, 1.0):
         for layout in (0, 1):
-            got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=11 * t + N)
+            got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=11 * t + N)
             assert caat.last_kernel() == "rowpar_fwd_decode"
             for r in range(t):
-                check(got[r], want[r], "bf16", what=(r, p, layout))
+                check(got[r], want[r], "bf16", what=(r, p, layout), spread=spread)
             for r in range(1, t):
                 assert np.array_equal(got[r][:, S], got[0][:, S])
 
@@ -368,29 +397,47 @@ def test_fwd_small_n_tensor_core(caat, N, monkeypatch):
     monkeypatch.setenv("CAAT_FWD_SKINNY", "0")
     t, kt, h = 8, 128, 512
     for layout in (0, 1):
-        got, want, S = _fwd_case(caat, t, N, kt * t, h, 0.5, layout, "bf16", "nn", seed=N)
+        got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, 0.5, layout, "bf16", "nn", seed=N)
         assert caat.last_kernel() in ("rowpar_fwd_tc", "rowpar_fwd_decode")
         for r in range(t):
-            check(got[r], want[r], "bf16", what=(r, layout))
+            check(got[r], want[r], "bf16", what=(r, layout), spread=spread)
 
 
 @pytest.mark.parametrize("N,kt", [(1, 96), (8, 96), (300, 64), (2048, 96)])
 def test_fwd_contiguous_null_sel_matches_index_list(caat, N, kt):
-    """sel given as an int n (null pointer: S = first n channels) gives the same
-    bits as the explicit index list, on every forward kernel."""
+    """sel given as an int n (null pointer: S = first n channels) against the
+    explicit index list of the same S, on every forward kernel.  The channels
+    outside S are each rank's own partial, computed alike: the same bits.  On the
+    tile kernel an index list with 0 < |S| < h sums the S channels from the ranks'
+    rounded partials, the size form in fp32 over all of K: there both must match
+    the oracle; the few-token kernels sum in fp32 either way: the same bits."""
     T = torch()
     t, h = 8, 768
     X = ci.normal(1301, (N, kt * t))
     Wl = ci.normal(1302, (kt * t, h), std=0.02)
     Xd, Wd = dev(X, "bf16"), _weight(Wl, "bf16", "nn")
+    Xv, Wv = host_values(X, "bf16"), host_values(Wl, "bf16")
     for s in (0, 100, 384, 768):
-        a = caat.rowpar_linear_fwd(Xd, Wd, t, sel_dev(np.arange(s, dtype=np.int32)))
+        S = np.arange(s, dtype=np.int32)
+        a = caat.rowpar_linear_fwd(Xd, Wd, t, sel_dev(S))
         ka = caat.last_kernel()
         b = caat.rowpar_linear_fwd(Xd, Wd, t, s)
         assert caat.last_kernel() == ka
         T.cuda.synchronize()
         for r in range(t):
-            assert bool((a[r].view(T.int16) == b[r].view(T.int16)).all()), (s, r)
+            assert bool((a[r][:, s:].view(T.int16) == b[r][:, s:].view(T.int16)).all()), (s, r)
+        if ka != "rowpar_fwd_tc" or s in (0, h):
+            for r in range(t):
+                assert bool((a[r].view(T.int16) == b[r].view(T.int16)).all()), (s, r)
+        else:
+            want, _ = orc.rowpar_fwd(Xv, Wv, t, S)
+            parts, _ = orc.rowpar_fwd(Xv, Wv, t, np.zeros(0, np.int32))
+            spread = np.zeros((N, h))
+            spread[:, :s] = np.abs(parts).sum(axis=0)[:, :s]
+            for r in range(t):
+                check(to_f64(a[r]), want[r], "bf16", spread=spread, what=("list", s, r))
+                check(to_f64(b[r]), want[r], "bf16", what=("size", s, r))
+                assert bool((a[r][:, :s] == a[0][:, :s]).all())
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -467,10 +514,10 @@ def test_fwd_skinny_parity(caat, t, N):
     for h, kt in ((1000, 136), (512, 64)):
         for p in (0.0, 0.5, 1.0):
             for layout in (0, 1):
-                got, want, S = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=13 * t + N + h)
+                got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=13 * t + N + h)
                 assert caat.last_kernel() == "rowpar_fwd_skinny_tc"
                 for r in range(t):
-                    check(got[r], want[r], "bf16", what=(h, r, p, layout))
+                    check(got[r], want[r], "bf16", what=(h, r, p, layout), spread=spread)
                 for r in range(1, t):
                     assert np.array_equal(got[r][:, S], got[0][:, S])
 
@@ -479,10 +526,10 @@ def test_fwd_skinny_declines_to_other_kernels(caat):
     """Shapes the swapped-operand kernel does not take still run: t = 16 (above
     the portable cluster size) and k_t < 64 go to the CUDA-core decode kernel."""
     for t, kt in ((16, 64), (8, 32)):
-        got, want, _ = _fwd_case(caat, t, 4, kt * t, 256, 0.5, 1, "bf16", "nn", seed=t + kt)
+        got, want, _, spread = _fwd_case(caat, t, 4, kt * t, 256, 0.5, 1, "bf16", "nn", seed=t + kt)
         assert caat.last_kernel() == "rowpar_fwd_decode"
         for r in range(t):
-            check(got[r], want[r], "bf16")
+            check(got[r], want[r], "bf16", spread=spread)
 
 
 @pytest.mark.parametrize("N", [5, 40])
@@ -511,9 +558,9 @@ def test_fwd_skinny_output_guard(caat, N):
 def test_layer_maximum_rank_count(caat, dtype, t, N, kt, h):
     """t up to 64: forward and both backward placements on the kernels that take it."""
     for p in (0.0, 0.5, 1.0):
-        got, want, S = _fwd_case(caat, t, N, kt * t, h, p, 1, dtype, "nn", seed=t + N)
+        got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, p, 1, dtype, "nn", seed=t + N)
         for r in range(t):
-            check(got[r], want[r], dtype, what=("fwd", r, p))
+            check(got[r], want[r], dtype, what=("fwd", r, p), spread=spread)
         for r in range(1, t):
             assert np.array_equal(got[r][:, S], got[0][:, S])
         for mode in (0, 1):
@@ -527,10 +574,10 @@ def test_layer_tensor_core_rank_limit(caat, t):
     """t = 16 is the largest rank count of the tile kernels (one output tensor map
     per rank); t = 17 falls back to the CUDA-core kernels.  Both match the oracle."""
     N, kt, h = 256, 64, 256
-    got, want, S = _fwd_case(caat, t, N, kt * t, h, 0.5, 1, "bf16", "nn", seed=t)
+    got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, 0.5, 1, "bf16", "nn", seed=t)
     assert caat.last_kernel() == ("rowpar_fwd_tc" if t <= 16 else "rowpar_fwd_simt")
     for r in range(t):
-        check(got[r], want[r], "bf16")
+        check(got[r], want[r], "bf16", spread=spread)
     gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, 0.5, 1, "bf16", 0, "nn", seed=t)
     check(gX, wX, "bf16", bwd=True)
     check(gW, wW, "bf16", bwd=True)
@@ -541,9 +588,9 @@ def test_layer_tensor_core_rank_limit(caat, t):
 def test_layer_degenerate_shapes(caat, dtype, t, N, kt, h):
     """One channel, one token, one element per shard."""
     for p in (0.0, 1.0):
-        got, want, S = _fwd_case(caat, t, N, kt * t, h, p, 0, dtype, "rm", seed=t + h)
+        got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, p, 0, dtype, "rm", seed=t + h)
         for r in range(t):
-            check(got[r], want[r], dtype)
+            check(got[r], want[r], dtype, spread=spread)
         gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, p, 0, dtype, 0, "rm", seed=t + h)
         check(gX, wX, dtype, bwd=True)
         check(gW, wW, dtype, bwd=True)
