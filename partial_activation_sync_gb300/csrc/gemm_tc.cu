@@ -187,6 +187,7 @@ struct FwdParams {
     // shard.  balanced == 0: every tile runs whole, in unit order.
     int balanced;
     int n_whole;
+    int wgt;            // pieces a whole tile's time is worth (1 .. t): the light workers' extra share
     uint8_t nbl[MAX_NB];
     const int32_t *sel;
     int64_t n_sel;
@@ -234,7 +235,7 @@ __device__ __forceinline__ void cursor_init(Cursor &c, const FwdParams &p, int g
     const int rem = nW % G;
     const int light = rem > 0 ? G - rem : 0;
     const int P = num_mg * (p.num_n - p.n_whole) * p.t;
-    const int A = min(P, light * p.t);
+    const int A = min(P, light * p.wgt);
     int q = 0;    // this worker's pieces
     if (light > 0 && g >= rem && g - rem < A) {
         c.phase = 0;
@@ -872,6 +873,11 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         // keeps every tile whole; CAAT_FWD_SCHED=first runs the whole tiles first)
         p.balanced = 0;
         p.n_whole = p.num_n;
+        p.wgt = t;
+        if (const char *e = std::getenv("CAAT_FWD_WGT")) {
+            const int v = std::atoi(e);
+            if (v >= 1 && v <= t) p.wgt = v;
+        }
         const bool rounds_env = sched_env != nullptr && sched_env[0] == 'r';
         // An index list of S with 0 < |S| < h (a random S): its tiles would be MIXED
         // -- per-shard epilogues, the S channels summed in TMEM across shards, and
