@@ -130,18 +130,18 @@ std::atomic<int> g_inject{CAAT_INJECT_NONE};
 #ifndef CAAT_FWD_PAIR_NBUF256
 #define CAAT_FWD_PAIR_NBUF256 1
 #endif
-// ring depth of the single-CTA mode (stages of 16 KB of X + 32 / 24 KB of W)
-#ifndef CAAT_FWD_SINGLE_STAGES
-#define CAAT_FWD_SINGLE_STAGES 4
-#endif
-
-template <int CLN, int BNT>
+// DEEP (single-CTA 192-wide tiles only): 5 ring stages of 40 KB and one staging
+// buffer per epilogue warp instead of 4 stages and two.  Shards of 4 or more
+// k-blocks are fed faster (130M down-proj, k_t = 384: 49.3 -> 46.6 us); shorter
+// shards are bound by their per-shard epilogue, which the second buffer helps
+// (130M out-proj, k_t = 96: 33.5 against 35.2 us).
+template <int CLN, int BNT, bool DEEP = false>
 struct Cfg {
     static constexpr bool PAIR = CLN > 1;
-    static constexpr int STAGES = PAIR ? CAAT_FWD_PAIR_STAGES : CAAT_FWD_SINGLE_STAGES;
+    static constexpr int STAGES = PAIR ? CAAT_FWD_PAIR_STAGES : (BNT < 256 && DEEP ? 5 : 4);
     // staging buffers per epilogue warp: several (bulk stores drain the earlier
     // ones while the next chunk fills one) where shared memory allows
-    static constexpr int NBUF = BNT < 256 ? 2 : (PAIR ? CAAT_FWD_PAIR_NBUF256 : 1);
+    static constexpr int NBUF = BNT < 256 ? (DEEP ? 1 : 2) : (PAIR ? CAAT_FWD_PAIR_NBUF256 : 1);
     static constexpr int B_ROWS = PAIR ? BNT / 2 : BNT;        // W rows (channels) per CTA per stage
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -161,11 +161,12 @@ struct SmemCtl {
     uint32_t bitmap[MAX_H_TC / 32];
 };
 
-template <int CLN, int BNT>
+template <int CLN, int BNT, bool DEEP>
 constexpr size_t smem_bytes()
 {
-    static_assert(Cfg<CLN, BNT>::STAGES <= MAX_STAGES, "ring deeper than the barrier arrays");
-    return 1024 + (size_t)Cfg<CLN, BNT>::STAGES * Cfg<CLN, BNT>::STAGE_BYTES + 4 * Cfg<CLN, BNT>::NBUF * STG_BYTES +
+    using C = Cfg<CLN, BNT, DEEP>;
+    static_assert(C::STAGES <= MAX_STAGES, "ring deeper than the barrier arrays");
+    return 1024 + (size_t)C::STAGES * C::STAGE_BYTES + 4 * C::NBUF * STG_BYTES +
            sizeof(SmemCtl);
 }
 
@@ -350,12 +351,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
 
 // CLN = CTAs per cluster: 1 (one CTA per tile) or 2 (a CTA pair).  Each CTA
 // fetches its own X and W tiles from this GPU's memory; no load is multicast.
-template <int CLN, int BNT>
+template <int CLN, int BNT, bool DEEP>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ YMaps ymaps, const FwdParams p)
 {
-    using C = Cfg<CLN, BNT>;
+    using C = Cfg<CLN, BNT, DEEP>;
     constexpr bool PAIR = C::PAIR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -743,13 +744,13 @@ bool encode_3d(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1, uint
     return encode_tmap(tm, base, 3, dims, strides, box);
 }
 
-template <int CLN, int BNT>
+template <int CLN, int BNT, bool DEEP = false>
 caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMaps &ym, const FwdParams &p,
                        cudaStream_t s)
 {
     constexpr bool PAIR = CLN > 1;
-    auto kern = rowpar_fwd_tc_kernel<CLN, BNT>;
-    constexpr size_t smem = smem_bytes<CLN, BNT>();
+    auto kern = rowpar_fwd_tc_kernel<CLN, BNT, DEEP>;
+    constexpr size_t smem = smem_bytes<CLN, BNT, DEEP>();
     static_assert(smem <= 227 * 1024, "shared memory beyond the per-CTA limit");
     if (prepare_kernel_smem((const void *)kern, (int)smem) != CAAT_OK) return CAAT_ERR_CUDA;
     const int per = CLN;
@@ -914,7 +915,8 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
             return CAAT_ERR_UNSUPPORTED;
         caat_status st;
         if (bn == 192)
-            st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s) : launch_fwd<1, 192>(tmX, tmW, ym, p, s);
+            st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s)
+               : (p.nkb >= 4 ? launch_fwd<1, 192, true>(tmX, tmW, ym, p, s) : launch_fwd<1, 192>(tmX, tmW, ym, p, s));
         else
             st = cln == 2 ? launch_fwd<2, BN>(tmX, tmW, ym, p, s) : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
         if (st == CAAT_OK && pieces_then_reduce) {
