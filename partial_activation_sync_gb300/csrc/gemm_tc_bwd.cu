@@ -48,37 +48,56 @@ namespace {
 
 using namespace tc;
 
-constexpr int BM = 128, BK = 64, STAGES = 4, MAX_BN = 256;
+constexpr int BM = 128, BK = 64, MAX_BN = 256;
+constexpr int MAX_STAGES = 6;
 constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_MAX_BYTES = MAX_BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_MAX_BYTES;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MAX_T_TC = 16;
 constexpr int STG_BYTES = 32 * 128;          // 32 rows x 64 bf16 columns
-constexpr int NBUF = 2;                      // staging buffers per epilogue warp
+constexpr int MAX_NBUF = 2;                  // staging buffers per epilogue warp (at most)
 
 struct TmapArray {
     CUtensorMap m[MAX_T_TC];
 };
 
 struct SmemCtl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t SMEM_BYTES = 1024 + (size_t)STAGES * STAGE_BYTES + 4 * NBUF * STG_BYTES + sizeof(SmemCtl);
+// The ring: stages of A (128 x 64) + B (BN x 64); 4 stages of the widest tiles
+// fit.  Narrower tiles take more stages (BN = 192: 5 stages and one staging
+// buffer per epilogue warp; BN <= 128: 6 stages and two), which keeps more
+// operand bytes in flight -- these short-K GEMMs otherwise wait on their ring.
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+struct Ring {
+    int stages, stage_bytes, nbuf;
+};
+inline Ring ring_for(int BN, bool deep)
+{
+    Ring g;
+    g.stage_bytes = A_BYTES + BN * BK * 2;
+    g.stages = !deep ? 4 : (BN <= 128 ? 6 : (BN <= 192 ? 5 : 4));
+    g.nbuf = (deep && BN > 128 && BN <= 192) ? 1 : 2;
+    return g;
+}
+inline size_t ring_smem(const Ring &g)
+{
+    return 1024 + (size_t)g.stages * g.stage_bytes + 4 * g.nbuf * STG_BYTES + sizeof(SmemCtl);
+}
 
 struct GemmParams {
     int64_t M, Nn, Kk;  // per-rank GEMM
     int t, num_m, num_n, nkb, BN, units;
     int s_blocks;       // 64-channel blocks of the gradient read from the reduced sum (smap)
     int ksplit, kbps;   // K range split in ksplit parts of kbps k-blocks (RED only)
+    int stages, stage_bytes, nbuf;   // the ring (see ring_for)
     uint32_t idesc;
 };
 
@@ -106,13 +125,13 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *staging = base + STAGES * STAGE_BYTES;
-    SmemCtl *ctl = (SmemCtl *)(staging + 4 * NBUF * STG_BYTES);
+    uint8_t *staging = base + p.stages * p.stage_bytes;
+    SmemCtl *ctl = (SmemCtl *)(staging + 4 * p.nbuf * STG_BYTES);
     volatile int *abort = &ctl->abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < p.stages; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
             mbar_init(smem_u32(&ctl->empty[s]), 1);
         }
@@ -153,7 +172,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     }
                     const uint32_t fb = smem_u32(&ctl->full[stage]);
                     mbar_arrive_expect_tx(fb, A_BYTES + b_bytes);
-                    uint8_t *sa = base + stage * STAGE_BYTES;
+                    uint8_t *sa = base + stage * p.stage_bytes;
                     uint8_t *sb = sa + A_BYTES;
                     const int k0 = kb * BK;
                     // gradient channels below s_blocks*64 come from the reduced sum
@@ -173,7 +192,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     }
                     for (int i = 0; i < p.BN / 64; ++i)
                         tma_load_3d(smem_u32(sb + i * 8192), &bmap, fb, n0 + 64 * i, r, k0);
-                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                    if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                 }
             }
         }
@@ -197,7 +216,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                         goto done;
                     }
                     fence_after_sync();
-                    const uint32_t a0 = smem_u32(base + stage * STAGE_BYTES);
+                    const uint32_t a0 = smem_u32(base + stage * p.stage_bytes);
                     const uint32_t b0 = a0 + A_BYTES;
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
@@ -207,7 +226,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                         mma_f16(d, ad, bd, p.idesc, (kb == kb_lo && k == 0) ? 0u : 1u);
                     }
                     mma_commit(smem_u32(&ctl->empty[stage]));
-                    if (++stage == STAGES) { stage = 0; ph ^= 1u; }
+                    if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                 }
                 mma_commit(smem_u32(&ctl->acc_full[b]));
                 ++au;
@@ -247,10 +266,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     for (int hf = 0; hf < 2; ++hf) {
                         const int64_t c0 = n0 + 64 * c64 + 32 * hf;
                         if (c0 >= p.Nn) break;         // same for the whole warp
-                        uint8_t *stg = staging + (q * NBUF + sbuf) * STG_BYTES;
+                        uint8_t *stg = staging + (q * p.nbuf + sbuf) * STG_BYTES;
                         const uint32_t stg_a = smem_u32(stg);
-                        if (++sbuf == NBUF) sbuf = 0;
-                        if (lane == 0) bulk_wait_read1();
+                        if (++sbuf == p.nbuf) sbuf = 0;
+                        if (lane == 0) {
+                            if (p.nbuf > 1) bulk_wait_read1(); else bulk_wait_read0();
+                        }
                         __syncwarp();
                         uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
 #pragma unroll
@@ -278,10 +299,12 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                     w[i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
                     w[16 + i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
                 }
-                uint8_t *stg = staging + (q * NBUF + sbuf) * STG_BYTES;
+                uint8_t *stg = staging + (q * p.nbuf + sbuf) * STG_BYTES;
                 const uint32_t stg_a = smem_u32(stg);
-                if (++sbuf == NBUF) sbuf = 0;
-                if (lane == 0) bulk_wait_read1();   // the store that last used this buffer has read it
+                if (++sbuf == p.nbuf) sbuf = 0;
+                if (lane == 0) {                    // the store that last used this buffer has read it
+                    if (p.nbuf > 1) bulk_wait_read1(); else bulk_wait_read0();
+                }
                 __syncwarp();
                 uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
 #pragma unroll
@@ -333,8 +356,16 @@ caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &smap, cons
     if (p.units <= 0) return CAAT_OK;
     const int grid = p.units < num_sms() ? p.units : num_sms();
     auto kern = grouped_gemm_tc_kernel<A_MN, RED>;
-    if (prepare_kernel_smem((const void *)kern, (int)SMEM_BYTES) != CAAT_OK) return CAAT_ERR_CUDA;
-    kern<<<grid, NUM_THREADS, SMEM_BYTES, s>>>(amaps, smap, bmap, cmap, p);
+    // the ring for this tile width (CAAT_BWD_RING=4 keeps 4 stages at every width)
+    const char *ring_env = std::getenv("CAAT_BWD_RING");
+    const Ring g = ring_for(p.BN, !(ring_env != nullptr && ring_env[0] == '4'));
+    p.stages = g.stages;
+    p.stage_bytes = g.stage_bytes;
+    p.nbuf = g.nbuf;
+    const size_t smem = ring_smem(g);
+    if (smem > SMEM_LIMIT || p.stages > MAX_STAGES) return CAAT_ERR_UNSUPPORTED;
+    if (prepare_kernel_smem((const void *)kern, (int)SMEM_LIMIT) != CAAT_OK) return CAAT_ERR_CUDA;
+    kern<<<grid, NUM_THREADS, smem, s>>>(amaps, smap, bmap, cmap, p);
     note_launch(name);
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }
