@@ -31,7 +31,8 @@
  *    load; or the whole tiles first and the pieces after them, instead of the
  *    pieces in runs around each worker's whole tiles),
  *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
- *    (backward on `stream` only).
+ *    (backward on `stream` only), CAAT_BWD_RING=4 (the backward GEMMs' ring at 4
+ *    stages whatever the tile width).
  *  - "device pointer" = memory the caller allocated on the current CUDA device;
  *    the library never allocates or frees device memory and never keeps a pointer
  *    after the call returns.  Arrays "of t device pointers" are HOST arrays whose
