@@ -11,7 +11,7 @@ of the upstream gradient, dX, dW).  Metric: algorithmic TFLOP/s (2NKh forward,
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl caat|reference]
                   [--workload 7b_prefill|130m|1.1b|7b_decode8|130m_stack]
-                  [--layout contiguous|random] [--p P] [--placement reduce_dout|column]
+                  [--layout contiguous|random] [--p P] [--t T] [--placement reduce_dout|column]
                   [--no-extras] [--no-stack]
 
 Under torchrun (N GPUs) the workload's t ranks are spread over the GPUs, t / N on
@@ -1011,6 +1011,7 @@ def main():
     ap.add_argument("--layout", choices=["contiguous", "random"], default=None,
                     help="channel-set layout (default: the workload's own)")
     ap.add_argument("--p", type=float, default=None, help="synchronized fraction (default: workload's)")
+    ap.add_argument("--t", type=int, default=None, help="tensor-parallel ranks (default: the workload's 8)")
     ap.add_argument("--placement", choices=["reduce_dout", "column"], default="reduce_dout",
                     help="130m_stack: where the backward reduce sits")
     ap.add_argument("--no-extras", action="store_true")
@@ -1036,10 +1037,13 @@ def main():
             print(json.dumps(res), flush=True)
         return
     w = ci.WORKLOADS[args.workload]
-    if args.layout is not None or args.p is not None:
+    if args.layout is not None or args.p is not None or args.t is not None:
         import dataclasses
+        if args.t is not None and (args.t < 1 or any(L.K % args.t for L in w.layers)):
+            ap.error("--t must divide every layer's K")
         w = dataclasses.replace(w, layout=(1 if args.layout == "random" else 0) if args.layout else w.layout,
-                                p=args.p if args.p is not None else w.p)
+                                p=args.p if args.p is not None else w.p,
+                                t=args.t if args.t is not None else w.t)
     if args.impl == "reference":
         res = run_reference(args, w)
     else:
