@@ -53,10 +53,10 @@ STEP_SPIN_CYCLES = 400000
 # capture reports null.  Output lines still dirty in L2 when the kernel ends are
 # not in the count.
 DRAM_TRAFFIC = {
-    ("7b_prefill", "out_proj"): 124.69e6 + 211.19e6,
-    ("7b_prefill", "down_proj"): 360.64e6 + 231.02e6,
-    ("130m", "out_proj"): 14.90e6 + 36.48e6,
-    ("130m", "down_proj"): 82.42e6 + 43.84e6,
+    ("7b_prefill", "out_proj"): 118.22e6 + 208.54e6,
+    ("7b_prefill", "down_proj"): 420.09e6 + 222.17e6,
+    ("130m", "out_proj"): 13.85e6 + 36.25e6,
+    ("130m", "down_proj"): 57.27e6 + 38.95e6,
 }
 
 
