@@ -33,6 +33,13 @@
  *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
  *    (backward on `stream` only), CAAT_BWD_RING=4 (the backward GEMMs' ring at 4
  *    stages whatever the tile width).
+ *  - bf16 layer work that no tensor-core kernel takes (for example a weight that
+ *    is not K-contiguous, a shard width k_t that is not a multiple of 8, more
+ *    than 16 ranks beyond a few tokens, pointers off 16 bytes) returns
+ *    UNSUPPORTED, before anything is launched, unless CAAT_ALLOW_FALLBACK=1 is in
+ *    the environment at the call: then it runs on the CUDA-core (FFMA) kernels,
+ *    correct but one to two orders of magnitude slower.  fp32 always runs there
+ *    (it has no tensor-core path).  Empty work (N, K or h zero) needs no opt-in.
  *  - "device pointer" = memory the caller allocated on the current CUDA device;
  *    the library never allocates or frees device memory and never keeps a pointer
  *    after the call returns.  Arrays "of t device pointers" are HOST arrays whose
@@ -153,7 +160,8 @@ caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, caat_dtype 
  * (fp32 FMA, no TF32).
  * Errors: INVALID_ARG for t outside 1..64, K % t != 0, negative sizes, a stride
  *         or leading dimension smaller than the row it spans, null pointers.
- *         UNSUPPORTED when no kernel takes the layout and alignment given.
+ *         UNSUPPORTED when no kernel takes the layout and alignment given (for
+ *         bf16: no tensor-core kernel, and CAAT_ALLOW_FALLBACK is not 1).
  */
 caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
                                    const void *X, int64_t ldx,
@@ -280,6 +288,8 @@ caat_status caat_rowpar_linear_bwd_noalloc(int t, int64_t N, int64_t K, int64_t 
  *   accumulator the call uses with each other and with every other buffer of the
  *   call); UNSUPPORTED / CUDA as
  *   caat_rowpar_linear_fwd.  sel as there (null = the first n_sel channels).
+ *   The backward computes dW1 before dA: when only dA's product is declined
+ *   (UNSUPPORTED), dW1 and the accumulator may already have been written.
  */
 caat_status caat_colpar_linear_fwd(int t, int64_t N, int64_t h, int64_t K, caat_dtype dt,
                                    const void *const *A, int64_t lda,

@@ -197,6 +197,17 @@ caat_status check_layer_args(int t, int64_t N, int64_t K, int64_t h, caat_dtype 
     return CAAT_OK;
 }
 
+// bf16 work that no tensor-core kernel takes runs on the CUDA cores only when the
+// caller opts in with CAAT_ALLOW_FALLBACK=1: that path is one to two orders of
+// magnitude slower, and a caller should learn of the cliff rather than meet it.
+// fp32 has no tensor-core path (no TF32), so the CUDA-core kernels are its path.
+bool cuda_core_path_allowed(caat_dtype dt)
+{
+    if (dt != CAAT_BF16) return true;
+    const char *e = std::getenv("CAAT_ALLOW_FALLBACK");
+    return e != nullptr && std::strcmp(e, "1") == 0;
+}
+
 }  // namespace
 
 extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64_t h,
@@ -245,6 +256,8 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
         st = launch_rowpar_fwd_decode(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
         if (st != CAAT_ERR_UNSUPPORTED) return st;
     }
+    // K == 0 only writes zeros (an empty sum)
+    if (K > 0 && !cuda_core_path_allowed(dt)) return CAAT_ERR_UNSUPPORTED;
     return launch_rowpar_fwd_simt(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, py, ldy, sel, n_sel, s);
 }
 
@@ -267,6 +280,17 @@ size_t wacc_region_bytes(int64_t K, int64_t h, caat_dtype dt)
 }
 
 
+// Whether the tensor-core GEMMs take the gradient products of rowpar_grads.
+bool grads_on_tensor_cores(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt, const void *X,
+                           int64_t ldx, const void *W, int64_t w_rs, int64_t w_cs, const ConstPtrs &dy,
+                           int64_t ld_dy, void *dX, int64_t lddx, void *dW, int64_t dw_rs, int64_t dw_cs)
+{
+    return dt == CAAT_BF16 && (dX == nullptr || w_rs == 1) && (dW == nullptr || dw_rs == 1) && N > 0 &&
+           h > 0 && K > 0 &&
+           bwd_tc_supported(t, N, K, h, X, dW != nullptr ? ldx : 0, W, dX != nullptr ? w_cs : 0, dy, ld_dy,
+                            dX, dX != nullptr ? lddx : 0, dW, dW != nullptr ? dw_cs : 0);
+}
+
 // dX[:, shard r] = dY_r W_r^T and dW[shard r, :] = X_r^T dY_r for every rank
 // (dY: t pointers [N, h], row stride ld_dy).  A null dX or dW skips that
 // product; X is read only for dW, W only for dX.
@@ -279,10 +303,7 @@ caat_status rowpar_grads(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt, 
     const int64_t es = elem_size(dt);
     const int64_t kt = K / t;
     caat_status st;
-    if (dt == CAAT_BF16 && (dX == nullptr || w_rs == 1) && (dW == nullptr || dw_rs == 1) && N > 0 &&
-        h > 0 &&
-        bwd_tc_supported(t, N, K, h, X, dW != nullptr ? ldx : 0, W, dX != nullptr ? w_cs : 0, dy, ld_dy,
-                         dX, dX != nullptr ? lddx : 0, dW, dW != nullptr ? dw_cs : 0)) {
+    if (grads_on_tensor_cores(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, dy, ld_dy, dX, lddx, dW, dw_rs, dw_cs)) {
         st = launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, ld_dy, dX, lddx, dW, dw_cs, wacc, 0,
                                   nullptr, 0, s);
         if (st != CAAT_ERR_UNSUPPORTED) return st;
@@ -294,6 +315,8 @@ caat_status rowpar_grads(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt, 
             return CAAT_ERR_CUDA;
         return CAAT_OK;
     }
+    // N == 0 only writes zeros into dW (an empty sum)
+    if (N > 0 && !cuda_core_path_allowed(dt)) return CAAT_ERR_UNSUPPORTED;
     if (dX != nullptr) {
         // dX[:, shard r] = dY_r W_r^T : M = N, Nn = kt, Kk = h
         BatchedGemm gx{};
@@ -404,6 +427,18 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
                                           wacc, n_sel, workspace, n_sel, s);
             if (st != CAAT_ERR_UNSUPPORTED) return st;
         }
+    }
+
+    // without the opt-in, refuse bf16 work the tensor cores will not take before
+    // anything is launched (the GEMMs would read the reduced gradient from the
+    // workspace, row stride h)
+    if (dt == CAAT_BF16 && N > 0 && K > 0 && h > 0 && !cuda_core_path_allowed(dt)) {
+        ConstPtrs probe{};
+        for (int r = 0; r < t; ++r)
+            probe.p[r] = reduce ? (const void *)((char *)workspace + need / (size_t)t * (size_t)r) : dOut[r];
+        if (!grads_on_tensor_cores(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, probe, reduce ? h : ld_dout, dX, lddx,
+                                   dW, dw_rs, dw_cs))
+            return CAAT_ERR_UNSUPPORTED;
     }
 
     if (reduce) {
@@ -537,9 +572,10 @@ extern "C" caat_status caat_colpar_linear_bwd(int t, int64_t N, int64_t h, int64
     // dW1 = A_r^T dZ_r per block (the dW product with X = dZ, dY_r = A_r)
     st = rowpar_grads(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, a, lda, nullptr, 0, dW1, dw1_cs, dw1_rs,
                       wacc, sw);
-    if (st != CAAT_OK) return st;
     // dA = PCR_S(dZ_r W1_r^T): the fused row-parallel forward on (dZ, W1^T)
-    st = caat_rowpar_linear_fwd(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, dA, ldda, sel, n_sel, stream);
+    if (st == CAAT_OK)
+        st = caat_rowpar_linear_fwd(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, dA, ldda, sel, n_sel, stream);
+    // the side stream joins back even after an error (a captured fork must join)
     if (side != nullptr &&
         (cudaEventRecord(side->join, sw) != cudaSuccess || cudaStreamWaitEvent(s, side->join, 0) != cudaSuccess))
         return CAAT_ERR_CUDA;

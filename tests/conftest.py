@@ -12,6 +12,15 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
 
 
+@pytest.fixture(autouse=True)
+def _cuda_core_opt_in(request, monkeypatch):
+    """The parity tests also cover the bf16 shapes that only the CUDA-core
+    kernels take, which the library runs only on request; the tests of that
+    refusal remove the variable again."""
+    if "gpu" in request.keywords:
+        monkeypatch.setenv("CAAT_ALLOW_FALLBACK", "1")
+
+
 def pytest_collection_modifyitems(config, items):
     try:
         import torch

@@ -18,6 +18,12 @@ from tests.gpu_helpers import rel_fro, torch
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True)
+def _tensor_cores_only(monkeypatch):
+    """Every layer of the stack takes a tensor-core kernel: no CUDA-core opt-in."""
+    monkeypatch.delenv("CAAT_ALLOW_FALLBACK", raising=False)
+
+
 @pytest.mark.parametrize("placement", ["reduce_dout", "column"])
 def test_stack_loss_and_gradients_match_reference(placement):
     T = torch()
