@@ -13,9 +13,11 @@
 // operands (their n index is contiguous in memory), dY_r^T too, so the MMA reads
 // them with the MN-major shared-memory layout instead of transposing in memory.
 //
-// Same machinery as the forward kernel: TMA into a 4-stage ring (warp 0), one
+// Same machinery as the forward kernel: TMA into a ring of stages (warp 0), one
 // thread issuing tcgen05.mma into two alternating TMEM accumulators (warp 1),
-// four epilogue warps converting to bf16 and storing.  Every wait is bounded.
+// four epilogue warps converting to bf16 and storing.  Above one 128-row block
+// the tiles are 256 rows on a CTA pair (cta_group::2), which halves the operand
+// bytes each SM pulls per FLOP of B.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -87,6 +89,15 @@ inline Ring ring_for(int BN, bool deep)
     g.nbuf = (deep && BN > 128 && BN <= 192) ? 1 : 2;
     return g;
 }
+// CTA pairs: A (128 x 64) + this CTA's half of B (at most 128 x 64) per stage
+inline Ring ring_for_pair()
+{
+    Ring g;
+    g.stage_bytes = A_BYTES + (MAX_BN / 2) * BK * 2;
+    g.stages = 6;
+    g.nbuf = 2;
+    return g;
+}
 inline size_t ring_smem(const Ring &g)
 {
     return 1024 + (size_t)g.stages * g.stage_bytes + 4 * g.nbuf * STG_BYTES + sizeof(SmemCtl);
@@ -94,7 +105,8 @@ inline size_t ring_smem(const Ring &g)
 
 struct GemmParams {
     int64_t M, Nn, Kk;  // per-rank GEMM
-    int t, num_m, num_n, nkb, BN, units;
+    int t, num_m, num_n, nkb, units;
+    int BN;             // column tile width
     int s_blocks;       // 64-channel blocks of the gradient read from the reduced sum (smap)
     int ksplit, kbps;   // K range split in ksplit parts of kbps k-blocks (RED only)
     int stages, stage_bytes, nbuf;   // the ring (see ring_for)
@@ -113,11 +125,43 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// One work unit: rank r, 128-row block mb of this CTA, column tile nb,
+// k-blocks [kb_lo, kb_hi).  With CTA pairs a unit is a 256-row block whose
+// halves are the two CTAs' row blocks.  Units run the K parts of every column
+// tile of a row block, then the next row block, then the next rank: the units
+// dealt to neighbouring workers share their A rows.
+struct Unit {
+    int r, mb, nb, kb_lo, kb_hi;
+};
+
+template <bool PAIR>
+__device__ __forceinline__ Unit decode_unit(int u, const GemmParams &p, uint32_t crank)
+{
+    Unit x;
+    const int num_mu = PAIR ? (p.num_m + 1) / 2 : p.num_m;
+    const int ks = u % p.ksplit;
+    int v = u / p.ksplit;
+    x.nb = v % p.num_n;
+    v /= p.num_n;
+    const int mu = v % num_mu;
+    x.r = v / num_mu;
+    x.mb = PAIR ? 2 * mu + (int)crank : mu;
+    x.kb_lo = ks * p.kbps;
+    x.kb_hi = min(p.nkb, x.kb_lo + p.kbps);
+    return x;
+}
+
 // A_MN: A is MN-major (dW: dY_r^T); otherwise K-major (dX: dY_r).  B is MN-major.
 // RED: the K range is split over several CTAs and each adds its fp32 partial
 // into an fp32 array with a TMA reduce-add (cmap is then an fp32 map);
 // otherwise the tile is rounded to bf16 and stored.
-template <bool A_MN, bool RED>
+// PAIR: a CTA pair (cta_group::2) computes a 256-row tile.  Each CTA loads its
+// own 128 rows of A and its half of the tile's columns of B; both halves land
+// on the even CTA's barriers, whose single thread issues the MMAs for the pair.
+// Each CTA's TMEM then holds its 128 rows of the accumulator, which its own
+// epilogue warps store.  Per SM this halves the B bytes per FLOP.  Pairs take
+// 256-column tiles only: each half is two whole 64-column boxes.
+template <bool A_MN, bool RED, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_constant__ CUtensorMap smap,
                        const __grid_constant__ CUtensorMap bmap, const __grid_constant__ CUtensorMap cmap,
@@ -129,6 +173,8 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
     SmemCtl *ctl = (SmemCtl *)(staging + 4 * p.nbuf * STG_BYTES);
     volatile int *abort = &ctl->abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+    const bool is_leader = crank == 0u;
 
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -137,41 +183,54 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&ctl->acc_full[b]), 1);
-            mbar_init(smem_u32(&ctl->acc_empty[b]), 128);
+            mbar_init(smem_u32(&ctl->acc_empty[b]), PAIR ? 256 : 128);
         }
         ctl->abort = 0;
         fence_mbar_init();
         prefetch_tmap(&bmap);
     }
+    if (PAIR) cluster_sync();        // the peer's barriers exist before anything signals them
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-        tmem_relinquish();
+        if (PAIR) {
+            tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
-    const int per_rank = p.num_m * p.num_n;
-    // unit u -> split ks (fastest), then row block, column block, rank
-    const uint32_t b_bytes = (uint32_t)p.BN * BK * 2;
+    // units are dealt round-robin to the workers (CTAs, or CTA pairs)
+    const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int nworkers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
     if (warp == 0) {
         if (lane == 0) {
             int stage = 0;
             uint32_t ph = 0;
-            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-                const int ks = u % p.ksplit, v = u / p.ksplit;
-                const int r = v / per_rank, rem = v - r * per_rank;
-                const int mb = rem % p.num_m, nb = rem / p.num_m;
-                const int m0 = mb * BM, n0 = nb * p.BN;
-                const int kb_lo = ks * p.kbps, kb_hi = min(p.nkb, kb_lo + p.kbps);
-                for (int kb = kb_lo; kb < kb_hi; ++kb) {
+            for (int u = worker; u < p.units; u += nworkers) {
+                const Unit x = decode_unit<PAIR>(u, p, crank);
+                const int m0 = x.mb * BM;
+                // B columns this CTA loads: all BN, or its half of them
+                const int half = PAIR ? p.BN / 2 : p.BN;
+                const int nc0 = x.nb * p.BN + (int)crank * half;
+                const uint32_t bytes = (uint32_t)(A_BYTES + half * BK * 2);
+                for (int kb = x.kb_lo; kb < x.kb_hi; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, WAIT_LIMIT_NS)) {
                         fail(abort);
                         goto done;
                     }
                     const uint32_t fb = smem_u32(&ctl->full[stage]);
-                    mbar_arrive_expect_tx(fb, A_BYTES + b_bytes);
+                    uint32_t fbar = fb;
+                    if (PAIR) {
+                        fbar = map_to_cta(fb, 0);
+                        if (is_leader) mbar_arrive_expect_tx(fb, 2u * bytes);
+                    } else {
+                        mbar_arrive_expect_tx(fb, bytes);
+                    }
                     uint8_t *sa = base + stage * p.stage_bytes;
                     uint8_t *sb = sa + A_BYTES;
                     const int k0 = kb * BK;
@@ -183,26 +242,31 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
 #pragma unroll
                         for (int i = 0; i < 2; ++i) {
                             const int c = m0 + 64 * i;
-                            if (c < sc) tma_load_2d(smem_u32(sa + 8192 * i), &smap, fb, c, k0);
-                            else tma_load_2d(smem_u32(sa + 8192 * i), &amaps.m[r], fb, c - sc, k0);
+                            const CUtensorMap *am = c < sc ? &smap : &amaps.m[x.r];
+                            const int cc = c < sc ? c : c - sc;
+                            if (PAIR) tma_load_2d_pair(smem_u32(sa + 8192 * i), am, fbar, cc, k0);
+                            else tma_load_2d(smem_u32(sa + 8192 * i), am, fbar, cc, k0);
                         }
                     } else {
-                        if (k0 < sc) tma_load_2d(smem_u32(sa), &smap, fb, k0, m0);
-                        else tma_load_2d(smem_u32(sa), &amaps.m[r], fb, k0 - sc, m0);
+                        const CUtensorMap *am = k0 < sc ? &smap : &amaps.m[x.r];
+                        const int kk = k0 < sc ? k0 : k0 - sc;
+                        if (PAIR) tma_load_2d_pair(smem_u32(sa), am, fbar, kk, m0);
+                        else tma_load_2d(smem_u32(sa), am, fbar, kk, m0);
                     }
-                    for (int i = 0; i < p.BN / 64; ++i)
-                        tma_load_3d(smem_u32(sb + i * 8192), &bmap, fb, n0 + 64 * i, r, k0);
+                    for (int i = 0; i < half / 64; ++i) {      // 64 columns x 64 rows each
+                        if (PAIR) tma_load_3d_pair(smem_u32(sb + i * 8192), &bmap, fbar, nc0 + 64 * i, x.r, k0);
+                        else tma_load_3d(smem_u32(sb + i * 8192), &bmap, fbar, nc0 + 64 * i, x.r, k0);
+                    }
                     if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && is_leader) {
             int stage = 0;
             uint32_t ph = 0, au = 0;
-            for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-                const int ks = u % p.ksplit;
-                const int kb_lo = ks * p.kbps, kb_hi = min(p.nkb, kb_lo + p.kbps);
+            for (int u = worker; u < p.units; u += nworkers) {
+                const Unit x = decode_unit<PAIR>(u, p, crank);
                 const uint32_t b = au & 1u;
                 if (!mbar_wait(smem_u32(&ctl->acc_empty[b]), ((au >> 1) & 1u) ^ 1u, abort, WAIT_LIMIT_NS)) {
                     fail(abort);
@@ -210,7 +274,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                 }
                 fence_after_sync();
                 const uint32_t d = tmem + b * (uint32_t)p.BN;
-                for (int kb = kb_lo; kb < kb_hi; ++kb) {
+                for (int kb = x.kb_lo; kb < x.kb_hi; ++kb) {
                     if (!mbar_wait(smem_u32(&ctl->full[stage]), ph, abort, WAIT_LIMIT_NS)) {
                         fail(abort);
                         goto done;
@@ -223,12 +287,16 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                         const uint64_t ad = A_MN ? desc_sw128(a0 + 2048u * k, 8192u, 1024u)
                                                  : desc_kmajor_sw128(a0 + 32u * k);
                         const uint64_t bd = desc_sw128(b0 + 2048u * k, 8192u, 1024u);
-                        mma_f16(d, ad, bd, p.idesc, (kb == kb_lo && k == 0) ? 0u : 1u);
+                        const uint32_t acc = (kb == x.kb_lo && k == 0) ? 0u : 1u;
+                        if (PAIR) mma_f16_pair(d, ad, bd, p.idesc, acc);
+                        else mma_f16(d, ad, bd, p.idesc, acc);
                     }
-                    mma_commit(smem_u32(&ctl->empty[stage]));
+                    if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), (uint16_t)3u);
+                    else mma_commit(smem_u32(&ctl->empty[stage]));
                     if (++stage == p.stages) { stage = 0; ph ^= 1u; }
                 }
-                mma_commit(smem_u32(&ctl->acc_full[b]));
+                if (PAIR) mma_commit_pair_mc(smem_u32(&ctl->acc_full[b]), (uint16_t)3u);
+                else mma_commit(smem_u32(&ctl->acc_full[b]));
                 ++au;
             }
         }
@@ -237,11 +305,9 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
         const uint32_t lane_off = (uint32_t)(32 * q) << 16;
         uint32_t au = 0;
         int sbuf = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
-            const int v = u / p.ksplit;
-            const int r = v / per_rank, rem = v - r * per_rank;
-            const int mb = rem % p.num_m, nb = rem / p.num_m;
-            const int64_t n0 = (int64_t)nb * p.BN;
+        for (int u = worker; u < p.units; u += nworkers) {
+            const Unit x = decode_unit<PAIR>(u, p, crank);
+            const int64_t n0 = (int64_t)x.nb * p.BN;
             const uint32_t b = au & 1u;
             bool ok = mbar_wait(smem_u32(&ctl->acc_full[b]), (au >> 1) & 1u, abort, WAIT_LIMIT_NS);
             ok = __all_sync(0xffffffffu, ok);
@@ -253,7 +319,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
             const uint32_t tb = tmem + lane_off + b * (uint32_t)p.BN;
             // 32 rows x 64 columns per bulk store; the output map (column within
             // shard, shard, row) clips columns past k_t and rows past M
-            const int y = mb * BM + 32 * q;
+            const int y = x.mb * BM + 32 * q;
             if (RED) {
                 // fp32 partial: 32 rows x 32 columns (128-byte rows) per reduce-add;
                 // 64 columns are read from TMEM under one wait (BN is a multiple of 64)
@@ -281,7 +347,7 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0 && y < p.M) {
-                            tma_reduce_add_3d(&cmap, stg_a, (int)c0, r, y);
+                            tma_reduce_add_3d(&cmap, stg_a, (int)c0, x.r, y);
                             bulk_commit();
                         }
                     }
@@ -313,12 +379,15 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0 && y < p.M) {
-                    tma_store_3d(&cmap, stg_a, (int)c0, r, y);
+                    tma_store_3d(&cmap, stg_a, (int)c0, x.r, y);
                     bulk_commit();
                 }
             }
             fence_before_sync();
-            mbar_arrive(smem_u32(&ctl->acc_empty[b]));
+            // release the accumulator to the MMA issuer (the even CTA's barrier)
+            const uint32_t eb = smem_u32(&ctl->acc_empty[b]);
+            if (PAIR) mbar_arrive_cluster(map_to_cta(eb, 0));
+            else mbar_arrive(eb);
             ++au;
         }
     }
@@ -334,10 +403,12 @@ done:
         }
         __syncthreads();
     }
+    if (PAIR) cluster_sync();        // neither CTA leaves while its peer may still signal it
     if (warp == 1) {
         __syncwarp();
         fence_after_sync();
-        tmem_dealloc(tmem, TMEM_COLS);
+        if (PAIR) tmem_dealloc_pair(tmem, TMEM_COLS);
+        else tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
@@ -349,25 +420,69 @@ int pick_bn(int64_t n)
     return (int)((per + 63) / 64 * 64);
 }
 
-template <bool A_MN, bool RED>
+template <bool A_MN, bool RED, bool PAIR>
 caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &smap, const CUtensorMap &bmap,
                            const CUtensorMap &cmap, GemmParams &p, cudaStream_t s, const char *name)
 {
     if (p.units <= 0) return CAAT_OK;
-    const int grid = p.units < num_sms() ? p.units : num_sms();
-    auto kern = grouped_gemm_tc_kernel<A_MN, RED>;
+    auto kern = grouped_gemm_tc_kernel<A_MN, RED, PAIR>;
     // the ring for this tile width (CAAT_BWD_RING=4 keeps 4 stages at every width)
     const char *ring_env = std::getenv("CAAT_BWD_RING");
-    const Ring g = ring_for(p.BN, !(ring_env != nullptr && ring_env[0] == '4'));
+    const Ring g = PAIR ? ring_for_pair() : ring_for(p.BN, !(ring_env != nullptr && ring_env[0] == '4'));
     p.stages = g.stages;
     p.stage_bytes = g.stage_bytes;
     p.nbuf = g.nbuf;
     const size_t smem = ring_smem(g);
     if (smem > SMEM_LIMIT || p.stages > MAX_STAGES) return CAAT_ERR_UNSUPPORTED;
     if (prepare_kernel_smem((const void *)kern, (int)SMEM_LIMIT) != CAAT_OK) return CAAT_ERR_CUDA;
-    kern<<<grid, NUM_THREADS, smem, s>>>(amaps, smap, bmap, cmap, p);
+    if (!PAIR) {
+        const int grid = p.units < num_sms() ? p.units : num_sms();
+        kern<<<grid, NUM_THREADS, smem, s>>>(amaps, smap, bmap, cmap, p);
+    } else {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int pairs = num_sms() / 2;
+        cfg.gridDim = dim3(2 * pairs);
+        const int active = max_active_clusters((const void *)kern, cfg);
+        if (active < 1) return CAAT_ERR_UNSUPPORTED;
+        if (active < pairs) pairs = active;
+        if (pairs > p.units) pairs = p.units;
+        cfg.gridDim = dim3(2 * pairs);
+        if (cudaLaunchKernelEx(&cfg, kern, amaps, smap, bmap, cmap, p) != cudaSuccess) return CAAT_ERR_CUDA;
+    }
     note_launch(name);
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
+}
+
+// Column tiling of an n-wide GEMM: pick_bn's width for every tile.
+void column_tiles(GemmParams &p, int64_t n, bool pair, bool a_mn)
+{
+    p.BN = pick_bn(n);
+    p.num_n = (int)((n + p.BN - 1) / p.BN);
+    p.idesc = idesc_bf16_f32(pair ? 2 * BM : BM, p.BN, a_mn, true);
+}
+
+// CTA pairs for 256-column tiles (each CTA then loads two whole 64-column boxes
+// of B) when there is more than one 128-row block, unless switched off
+// (CAAT_BWD_PAIR=0).  Narrower tiles stay on single CTAs: 128-column pair
+// tiles run their MMAs at about half the rate per FLOP of 256-column ones, and
+// 192-column tiles would split B into 96-column halves, which the 128-byte
+// swizzle cannot lay out (the 64-byte one can, but measured no faster than
+// single CTAs).
+bool use_pairs(int64_t M, int64_t n)
+{
+    const char *env = std::getenv("CAAT_BWD_PAIR");
+    if (env != nullptr && std::strcmp(env, "0") == 0) return false;
+    return M > BM && pick_bn(n) == MAX_BN;
 }
 
 // fp32 [rows, cols] (row stride lds) -> bf16 (row stride ldd), 8 columns per thread
@@ -390,18 +505,26 @@ f32_rows_to_bf16_kernel(const float *__restrict__ src, int64_t rows, int64_t col
     }
 }
 
-// split of the K range that minimises waves-of-work per split, at least 8
-// k-blocks per part
-int pick_ksplit(int units, int nkb)
+// Split of the K range into k parts of ceil(nkb / k) k-blocks (every part
+// non-empty); units = tiles * parts.
+void set_ksplit(GemmParams &p, int k, int tiles)
 {
-    const int sms = num_sms();
+    p.kbps = (p.nkb + k - 1) / k;
+    p.ksplit = (p.nkb + p.kbps - 1) / p.kbps;
+    p.units = tiles * p.ksplit;
+}
+
+// The split (1..8 parts, at least 8 k-blocks per part) with the fewest
+// waves-of-work over `slots` workers, per part
+void pick_ksplit(GemmParams &p, int tiles, int slots)
+{
     int best = 1;
-    double best_cost = (double)((units + sms - 1) / sms);
-    for (int k = 2; k <= 8 && nkb / k >= 8; ++k) {
-        const double cost = (double)((units * k + sms - 1) / sms) / k;
+    double best_cost = (double)((tiles + slots - 1) / slots);
+    for (int k = 2; k <= 8 && p.nkb / k >= 8; ++k) {
+        const double cost = (double)((tiles * k + slots - 1) / slots) / k;
         if (cost < best_cost - 1e-9) { best = k; best_cost = cost; }
     }
-    return best;
+    set_ksplit(p, best, tiles);
 }
 
 }  // namespace
@@ -466,7 +589,6 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
                                  int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s)
 {
     const int64_t kt = K / t;
-    const int BN = pick_bn(kt);
     if (s_sum < 0 || s_sum > h || s_sum % 64 != 0 || (s_sum > 0 && dsum == nullptr)) return CAAT_ERR_UNSUPPORTED;
     const int64_t h_own = h - s_sum;           // channels read from each rank's own gradient
 
@@ -506,6 +628,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         TmapArray am;
         CUtensorMap sm;
         if (!grad_maps(am, sm, 64, BM)) return CAAT_ERR_UNSUPPORTED;
+        const bool pair = use_pairs(N, kt);
         CUtensorMap bm;
         const uint64_t dims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
         const uint64_t str[2] = {(uint64_t)kt * 2, (uint64_t)ldw * 2};
@@ -515,20 +638,17 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.M = N; p.Nn = kt; p.Kk = h;
         p.t = t;
         p.num_m = (int)((N + BM - 1) / BM);
-        p.num_n = (int)((kt + BN - 1) / BN);
+        column_tiles(p, kt, pair, false);
         p.nkb = (int)((h + BK - 1) / BK);
-        p.BN = BN;
-        p.ksplit = 1;
-        p.kbps = p.nkb;
         p.s_blocks = (int)(s_sum / 64);
-        p.units = t * p.num_m * p.num_n;
-        p.idesc = idesc_bf16_f32(BM, BN, false, true);
+        set_ksplit(p, 1, t * (pair ? (p.num_m + 1) / 2 : p.num_m) * p.num_n);
         CUtensorMap cm;
         const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)N};
         const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)lddx * 2};
         const uint32_t cbox[3] = {64, 1, 32};
         if (!encode_tmap(&cm, dX, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
-        const caat_status st = launch_grouped<false, false>(am, sm, bm, cm, p, s, "rowpar_bwd_dx_tc");
+        const caat_status st = pair ? launch_grouped<false, false, true>(am, sm, bm, cm, p, s, "rowpar_bwd_dx_tc")
+                                    : launch_grouped<false, false, false>(am, sm, bm, cm, p, s, "rowpar_bwd_dx_tc");
         if (st != CAAT_OK) return st;
     }
     if (dW == nullptr) return CAAT_OK;
@@ -537,6 +657,7 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         TmapArray am;
         CUtensorMap sm;
         if (!grad_maps(am, sm, 64, 64)) return CAAT_ERR_UNSUPPORTED;
+        const bool pair = use_pairs(h, kt);
         CUtensorMap bm;
         const uint64_t dims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)N};
         const uint64_t str[2] = {(uint64_t)kt * 2, (uint64_t)ldx * 2};
@@ -546,23 +667,20 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         p.M = h; p.Nn = kt; p.Kk = N;
         p.t = t;
         p.num_m = (int)((h + BM - 1) / BM);
-        p.num_n = (int)((kt + BN - 1) / BN);
+        column_tiles(p, kt, pair, true);
         p.nkb = (int)((N + BK - 1) / BK);
-        p.BN = BN;
-        p.idesc = idesc_bf16_f32(BM, BN, true, true);
         p.s_blocks = (int)(s_sum / 64);
-        const int base_units = t * p.num_m * p.num_n;
-        p.ksplit = wacc != nullptr ? pick_ksplit(base_units, p.nkb) : 1;
-        p.kbps = (p.nkb + p.ksplit - 1) / p.ksplit;
-        p.ksplit = (p.nkb + p.kbps - 1) / p.kbps;
-        p.units = base_units * p.ksplit;
+        const int tiles = t * (pair ? (p.num_m + 1) / 2 : p.num_m) * p.num_n;
+        if (wacc != nullptr) pick_ksplit(p, tiles, pair ? num_sms() / 2 : num_sms());
+        else set_ksplit(p, 1, tiles);
         if (p.ksplit == 1) {
             CUtensorMap cm;
             const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
             const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)ld_dw * 2};
             const uint32_t cbox[3] = {64, 1, 32};
             if (!encode_tmap(&cm, dW, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
-            return launch_grouped<true, false>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc");
+            return pair ? launch_grouped<true, false, true>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc")
+                        : launch_grouped<true, false, false>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc");
         }
         // split over tokens: fp32 partials reduce-added into wacc [h, K], then one
         // rounding to bf16 into dW
@@ -572,7 +690,8 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const uint32_t cbox[3] = {32, 1, 32};
         if (!encode_tmap(&cm, wacc, 3, cdims, cstr, cbox, true)) return CAAT_ERR_UNSUPPORTED;
         if (cudaMemsetAsync(wacc, 0, (size_t)h * (size_t)K * 4, sw) != cudaSuccess) return CAAT_ERR_CUDA;
-        caat_status st = launch_grouped<true, true>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc");
+        caat_status st = pair ? launch_grouped<true, true, true>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc")
+                              : launch_grouped<true, true, false>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc");
         if (st != CAAT_OK) return st;
         const int64_t total = h * (K / 8);
         int64_t blocks = (total + 255) / 256;

@@ -161,6 +161,16 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap, uint32_t bar, int c0,
+                                                 int c1)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(tmap), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // shared::cta address -> shared::cluster address of the same offset in CTA `rank`
 __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank)
 {

@@ -302,9 +302,24 @@ def test_fwd_7b_decode(caat, Nd, li):
         check(to_f64(outs[r]), want[r], "bf16")
 
 
-@pytest.mark.parametrize("t,N,kt,h", TC_SHAPES)
+@pytest.fixture(params=["pair", "single"])
+def bwd_cta(request, monkeypatch):
+    """The backward GEMMs as CTA pairs (256 x 256 tiles, the default for
+    256-column tiles above one 128-row block) or as single CTAs (CAAT_BWD_PAIR=0)."""
+    monkeypatch.setenv("CAAT_BWD_PAIR", "1" if request.param == "pair" else "0")
+    return request.param
+
+
+# shapes whose backward tiles are 256 columns wide (CTA pairs by default):
+# k_t = 256 with ragged rows (N = 300: the second pair's odd CTA reads only
+# zero fill) and ragged channels (h = 264), and k_t = 480 (two tiles, the last
+# one 224 columns)
+BWD_PAIR_SHAPES = [(2, 300, 256, 264), (4, 512, 480, 768)]
+
+
+@pytest.mark.parametrize("t,N,kt,h", TC_SHAPES + BWD_PAIR_SHAPES)
 @pytest.mark.parametrize("mode", [0, 1])
-def test_bwd_tc_parity(caat, t, N, kt, h, mode):
+def test_bwd_tc_parity(caat, t, N, kt, h, mode, bwd_cta):
     for p in (0.0, 1.0 / h, 0.5, 0.75, 1.0 - 1.0 / h, 1.0):
         gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, p, 1, "bf16", mode, "nn", seed=3 * t + h)
         assert caat.last_kernel() == "rowpar_bwd_dw_tc"
@@ -459,8 +474,8 @@ def test_pcr_contiguous_null_sel_bitexact(caat, dtype):
 
 
 @pytest.mark.parametrize("s", [0, 64, 384, 448, 768, 100])
-@pytest.mark.parametrize("kt", [96, 384])
-def test_bwd_contiguous_reduce_once(caat, s, kt):
+@pytest.mark.parametrize("kt", [96, 256, 384])
+def test_bwd_contiguous_reduce_once(caat, s, kt, bwd_cta):
     """Contiguous S given as an int: with |S| a multiple of 64 the backward reduces
     only the S channels once (the GEMMs read the other channels straight from each
     rank's gradient); other sizes take the materialising path.  Both match the
