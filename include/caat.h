@@ -232,11 +232,10 @@ caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h, caat_
  *    workspace instead).  CAAT_BWD_NO_REDUCE, an empty S or t == 1 need no
  *    scratch.  When the rest of the array also holds the optional fp32 dW
  *    accumulator (h * K * 4 bytes), it is used for it as well.
- *  - The first call on a device that needs the scratch looks up the array's device
- *    address (cudaGetSymbolAddress) with that device current and keeps it for the
- *    life of the process; make that first call before any stream capture.  The
- *    kept address does not survive cudaDeviceReset (the array may then move):
- *    a process that resets a device must not call this entry point on it again.
+ *  - Every call that needs the scratch looks up the array's device address
+ *    (cudaGetSymbolAddress, no allocation) on the current device, so the call
+ *    stays valid after a cudaDeviceReset has moved the array.  The first call on
+ *    a device loads the array with the module: make it before any stream capture.
  *  - All calls in the process share the one array, which keeps the last call's
  *    contents.  Calls whose work overlaps on the GPU (different streams, or other
  *    host threads, without ordering between them) race on it and corrupt each

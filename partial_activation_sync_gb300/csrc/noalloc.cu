@@ -7,33 +7,21 @@
 // process that fixes its memory budget when it starts.  For them this file holds
 // a file-scope device array of CAAT_NOALLOC_SCRATCH_BYTES; every GPU that loads
 // the library keeps it until the process exits.
-#include <mutex>
-
 #include "caat_internal.h"
 
 namespace {
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[CAAT_NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[128];   // device address of g_noalloc_scratch, per device ordinal
-
 // In host code the array's name is a host-side shadow, not a device address;
-// the device address comes from the runtime, once per device, with that device
-// current.
+// the device address comes from the runtime for the current device.  It is
+// looked up on every call (no allocation, a few microseconds at most), so a
+// device reset that reloads the module and moves the array leaves nothing stale.
 caat_status scratch_address(void **out)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return CAAT_ERR_CUDA;
-    if (dev < 0 || dev >= 128) return CAAT_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
-            return CAAT_ERR_CUDA;
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return CAAT_ERR_CUDA;
+    *out = p;
     return CAAT_OK;
 }
 
