@@ -15,7 +15,8 @@ import numpy as np
 import pytest
 
 import caat_inputs as ci
-from tests.gpu_helpers import TOL, dev, rel_fro, sel_dev, to_f64, torch
+from oracle import oracle as orc
+from tests.gpu_helpers import TOL, check, dev, host_values, rel_fro, sel_dev, to_f64, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -74,6 +75,11 @@ def test_noalloc_matches_workspace_entry_point_twice(dtype, t, N, K, h):
         assert caat.device_status() == 0
         assert rel_fro(to_f64(dX), to_f64(dX_ref)) <= TOL[dtype], call
         assert rel_fro(to_f64(dWst.t()), to_f64(dW_ref)) <= TOL[dtype], call
+        # and both against the oracle
+        wX, wW = orc.rowpar_bwd(host_values(X, dtype), host_values(Wl, dtype),
+                                np.stack([host_values(G[r], dtype) for r in range(t)]), t, S, 0)
+        check(to_f64(dX), wX, dtype, bwd=True, what=("dX", call))
+        check(to_f64(dWst.t()), wW, dtype, bwd=True, what=("dW", call))
 
 
 # Shapes whose scratch also holds the fp32 dW accumulator, so the token-split dW
@@ -110,6 +116,11 @@ def test_noalloc_accumulator_paths_match_twice(mode, sel_kind):
         assert caat.device_status() == 0
         assert rel_fro(to_f64(dX), to_f64(dX_ref)) <= TOL["bf16"], call
         assert rel_fro(to_f64(dWst.t()), to_f64(dW_ref)) <= TOL["bf16"], call
+        S = np.arange(sel, dtype=np.int32) if isinstance(sel, int) else sel.cpu().numpy()
+        wX, wW = orc.rowpar_bwd(host_values(X, "bf16"), host_values(Wl, "bf16"),
+                                np.stack([host_values(G[r], "bf16") for r in range(t)]), t, S, mode)
+        check(to_f64(dX), wX, "bf16", bwd=True, what=("dX", call))
+        check(to_f64(dWst.t()), wW, "bf16", bwd=True, what=("dW", call))
 
 
 def test_noalloc_rejects_sizes_beyond_the_scratch():
