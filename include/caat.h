@@ -156,7 +156,8 @@ caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, caat_dtype 
  * sel: device int32[n_sel], ascending and unique (S); or null for the contiguous
  *      S = {0, ..., n_sel-1}.  With the contiguous form and n_sel a multiple of 64,
  *      the backward reduces only the S channels, once, instead of materialising
- *      every rank's reduced gradient.
+ *      every rank's reduced gradient.  An index list of all h channels can only be
+ *      {0, ..., h-1} and takes the contiguous paths.
  * Precision: bf16 in, fp32 accumulate, one rounding to bf16; or fp32 throughout
  * (fp32 FMA, no TF32).
  * Errors: INVALID_ARG for t outside 1..64, K % t != 0, negative sizes, a stride

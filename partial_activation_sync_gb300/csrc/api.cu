@@ -171,11 +171,21 @@ extern "C" caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, 
             if (!in_place && overlap(so, span_of(in[q], N, h, ld_in, es))) return CAAT_ERR_INVALID_ARG;
         }
     }
+    if (sel != nullptr && n_sel == h) sel = nullptr;   // S = every channel: {0, ..., h-1}
     return launch_pcr(t, N, h, dt, pin, ld_in, pout, ld_out, in_place, sel, n_sel,
                       (cudaStream_t)stream);
 }
 
 namespace {
+
+// An index list of S is ascending and unique in [0, h): with h entries it can
+// only be {0, ..., h-1}, the contiguous S of full size (the plain all-reduce).
+// The calls then take the contiguous paths, which need no bitmap and, in the
+// backward, reduce the gradient once instead of materialising it per rank.
+inline const int32_t *all_channels(const int32_t *sel, int64_t n_sel, int64_t h)
+{
+    return (sel != nullptr && n_sel == h) ? nullptr : sel;
+}
 
 caat_status check_layer_args(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
                              const void *X, int64_t ldx, const void *W, int64_t w_rs,
@@ -235,6 +245,7 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
             return CAAT_ERR_INVALID_ARG;
     }
     if (N == 0 || h == 0) return CAAT_OK;
+    sel = all_channels(sel, n_sel, h);
     const cudaStream_t s = (cudaStream_t)stream;
     if (dt == CAAT_BF16 && w_rs == 1 && K > 0) {
         // a few tokens: the swapped-operand tensor-core kernel (one cluster of
@@ -408,6 +419,7 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
         }
     }
 
+    sel = all_channels(sel, n_sel, h);
     const cudaStream_t s = (cudaStream_t)stream;
     ConstPtrs dy{};
     int64_t ld_dy = ld_dout;
