@@ -33,7 +33,10 @@
  *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
  *    (backward on `stream` only), CAAT_BWD_RING=4 (the backward GEMMs' ring at 4
  *    stages whatever the tile width; single CTAs only), CAAT_BWD_PAIR=0 (the
- *    backward GEMMs on single CTAs instead of CTA pairs).
+ *    backward GEMMs on single CTAs instead of CTA pairs), CAAT_PDL=0 (the
+ *    few-token kernel launched plainly instead of as a programmatic dependent of
+ *    the previous launch in the stream, whose CTAs may then be set up while that
+ *    launch finishes; the kernel waits for it before it touches memory).
  *  - bf16 layer work that no tensor-core kernel takes (for example a weight that
  *    is not K-contiguous, a shard width k_t that is not a multiple of 8, more
  *    than 16 ranks beyond a few tokens, pointers off 16 bytes) returns

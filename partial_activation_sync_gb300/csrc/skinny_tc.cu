@@ -22,6 +22,9 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "caat_internal.h"
 #include "tc_ptx.cuh"
 
@@ -172,6 +175,12 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
+    // Launched as a programmatic dependent, this grid may have started while the
+    // previous one in the stream was still running: nothing above touched global
+    // memory (the tensor maps are launch parameters).  Wait for it before the
+    // first load or store, then let the next grid start its own setup.
+    griddep_wait();
+    griddep_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -359,7 +368,7 @@ caat_status launch_nt(const CUtensorMap &tmX, const CUtensorMap &tmW, const Skin
     constexpr size_t smem = skinny_smem<NT>();
     if (prepare_kernel_smem((const void *)kern, (int)smem) != CAAT_OK) return CAAT_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)p.t;
     attr[0].val.clusterDim.y = 1;
@@ -371,6 +380,15 @@ caat_status launch_nt(const CUtensorMap &tmX, const CUtensorMap &tmW, const Skin
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (max_active_clusters((const void *)kern, cfg) < 1) return CAAT_ERR_UNSUPPORTED;
+    // A programmatic dependent of the previous launch in the stream (CAAT_PDL=0:
+    // a plain launch): its CTAs may be set up while that grid finishes; the
+    // kernel waits for it before touching memory.
+    const char *pdl_env = std::getenv("CAAT_PDL");
+    if (pdl_env == nullptr || std::strcmp(pdl_env, "0") != 0) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     if (cudaLaunchKernelEx(&cfg, kern, tmX, tmW, p) != cudaSuccess) return CAAT_ERR_CUDA;
     note_launch("rowpar_fwd_skinny_tc");
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;

@@ -171,6 +171,17 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void *tmap,
         : "memory");
 }
 
+// Programmatic dependent launch.  griddep_wait: wait until the grids this one
+// depends on have completed and their memory operations are visible (returns at
+// once when the launch has no such dependency).  griddep_launch_dependents: let
+// the next grid in the stream, if it was launched as a programmatic dependent,
+// start its own setup now.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // shared::cta address -> shared::cluster address of the same offset in CTA `rank`
 __device__ __forceinline__ uint32_t map_to_cta(uint32_t addr, uint32_t rank)
 {

@@ -90,3 +90,51 @@ def test_colpar_backward_replays_from_a_graph(caat):
     assert caat.device_status() == 0
     assert bool((dA.view(T.int16) == rA.view(T.int16)).all())
     assert rel_fro(to_f64(dW1), to_f64(rW)) <= 1e-3
+
+
+@pytest.mark.parametrize("N", [1, 8, 64])
+@pytest.mark.parametrize("graph", [False, True])
+def test_few_token_chain_with_programmatic_launch(caat, N, graph, monkeypatch):
+    """The few-token kernel is launched as a programmatic dependent of the
+    previous launch (its CTAs may start while that grid finishes; it waits for it
+    before touching memory).  A chain of dependent calls -- each call's X is the
+    previous call's rank-0 output -- must give the same bits with and without
+    that launch mode, one call after another and replayed from a graph."""
+    T = torch()
+    t, h = 8, 512
+    K = h
+    depth = 6
+    Ws = [dev(np.ascontiguousarray(ci.normal(1700 + i, (K, h), std=0.05).T), "bf16").t() for i in range(depth)]
+    X0 = dev(ci.normal(1699, (N, K)), "bf16")
+    outs = [[T.empty((N, h), dtype=T.bfloat16, device="cuda") for _ in range(t)] for _ in range(depth)]
+
+    def chain():
+        x = X0
+        for i in range(depth):
+            caat.rowpar_linear_fwd(x, Ws[i], t, h // 2, outs=outs[i])
+            x = outs[i][0]
+
+    def run():
+        for o in outs:
+            for y in o:
+                y.fill_(float("nan"))
+        if graph:
+            g = _capture(T, chain)
+            for o in outs:
+                for y in o:
+                    y.fill_(float("nan"))
+            g.replay()
+        else:
+            chain()
+        T.cuda.synchronize()
+        assert caat.last_kernel() == "rowpar_fwd_skinny_tc" or graph
+        return [[y.view(T.int16).cpu().numpy().copy() for y in o] for o in outs]
+
+    monkeypatch.setenv("CAAT_PDL", "0")
+    plain = run()
+    monkeypatch.setenv("CAAT_PDL", "1")
+    pdl = run()
+    for i in range(depth):
+        for r in range(t):
+            np.testing.assert_array_equal(pdl[i][r], plain[i][r], err_msg="call %d rank %d" % (i, r))
+    assert caat.device_status() == 0
