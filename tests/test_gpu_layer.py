@@ -327,6 +327,40 @@ def test_bwd_tc_parity(caat, t, N, kt, h, mode, bwd_cta):
         check(gW, wW, "bf16", bwd=True, what=("dW", p))
 
 
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("sel_kind", ["random", "contiguous_list", "contiguous_size"])
+def test_bwd_token_split_parity(caat, mode, sel_kind, bwd_cta):
+    """dW split over tokens: fp32 reduce-adds of the parts into the workspace's
+    accumulator, then one rounding.  N = 2048 tokens are 32 k-blocks, which the
+    split cuts into parts; k_t = 256 makes the column tiles 256 wide, so the
+    default runs both GEMMs on CTA pairs; h = 520 leaves a pair whose odd CTA reads
+    only zero fill.  S as a random index list, the contiguous S as a list, and the
+    contiguous S by its size (the sum of the S channels formed once)."""
+    T = torch()
+    t, N, kt, h = 4, 2048, 256, 520
+    K = kt * t
+    X = ci.normal(1901, (N, K))
+    Wl = ci.normal(1902, (K, h), std=0.02)
+    G = ci.normal(1903, (t, N, h))
+    if sel_kind == "contiguous_size":
+        S = np.arange(256, dtype=np.int32)   # |S| a multiple of 64: the sum formed once
+        sel = 256
+    else:
+        layout = caat.CAAT_S_RANDOM if sel_kind == "random" else caat.CAAT_S_CONTIGUOUS
+        S = caat.select_channels(h, 0.5, layout, 1904)
+        sel = sel_dev(S)
+    Xd, Wd = dev(X, "bf16"), _weight(Wl, "bf16", "nn")
+    Gd = [dev(G[r], "bf16") for r in range(t)]
+    dX, dW = caat.rowpar_linear_bwd(Xd, Wd, Gd, t, sel, mode)
+    T.cuda.synchronize()
+    assert caat.device_status() == 0
+    assert caat.last_kernel() == "rowpar_bwd_dw_tc"
+    wX, wW = orc.rowpar_bwd(host_values(X, "bf16"), host_values(Wl, "bf16"),
+                            np.stack([host_values(G[r], "bf16") for r in range(t)]), t, S, mode)
+    check(to_f64(dX), wX, "bf16", bwd=True, what="dX")
+    check(to_f64(dW), wW, "bf16", bwd=True, what="dW")
+
+
 BWD_FULL = ([("130m", li, 0, 0.5, lay) for li in (0, 1) for lay in (0, 1)]
             + [("1.1b", li, 0, p, lay) for li in (0, 1) for p in (0.0, 0.25, 0.5, 0.75, 1.0)
                for lay in (0, 1)]
