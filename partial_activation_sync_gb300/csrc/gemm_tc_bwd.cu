@@ -58,7 +58,6 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 constexpr int MAX_T_TC = 16;
 constexpr int STG_BYTES = 32 * 128;          // 32 rows x 64 bf16 columns
-constexpr int MAX_NBUF = 2;                  // staging buffers per epilogue warp (at most)
 
 struct TmapArray {
     CUtensorMap m[MAX_T_TC];
