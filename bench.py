@@ -724,8 +724,27 @@ def run_extras(torch, caat, device, peaks, args):
             sec_g = _time_call(torch, graph.replay, 10, flush) / nsets
             rec.update({"graph_us": round(sec_g * 1e6, 2), "graph_GB/s": round(byt / sec_g / 1e9, 1),
                         "graph_frac_hbm": round(byt / sec_g / 1e9 / peaks["hbm"], 4)})
+            # the same graph with the inference opt-in CAAT_PDL_WEIGHTS=1 (no launch
+            # writes the weights, so each call may start streaming them before the
+            # previous call has finished)
+            prev = os.environ.get("CAAT_PDL_WEIGHTS")
+            os.environ["CAAT_PDL_WEIGHTS"] = "1"
+            try:
+                graph_w = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph_w):
+                    for Wk in Wsets:
+                        caat.rowpar_linear_fwd(X, Wk.t(), w.t, sel, outs=Ys)
+            finally:
+                if prev is None:
+                    os.environ.pop("CAAT_PDL_WEIGHTS", None)
+                else:
+                    os.environ["CAAT_PDL_WEIGHTS"] = prev
+            graph_w.replay()
+            sec_w = _time_call(torch, graph_w.replay, 10, flush) / nsets
+            rec.update({"graph_static_weights_us": round(sec_w * 1e6, 2),
+                        "graph_static_weights_frac_hbm": round(byt / sec_w / 1e9 / peaks["hbm"], 4)})
             out["7b_decode_N%d_%s" % (Nd, L.name)] = rec
-            del X, Ys, graph
+            del X, Ys, graph, graph_w
         del Wsets, Wst
     # column-parallel layer at the 130M MLP up-projection (N = 8192, h = 768,
     # FFN 3072, t = 8, p = 0.5): forward, and the backward with the partial reduce

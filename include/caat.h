@@ -37,6 +37,11 @@
  *    few-token kernel launched plainly instead of as a programmatic dependent of
  *    the previous launch in the stream, whose CTAs may then be set up while that
  *    launch finishes; the kernel waits for it before it touches memory).
+ *  - CAAT_PDL_WEIGHTS=1 is an opt-in for inference with static weights: the
+ *    few-token kernel then reads the weight tiles of its first ring stages before
+ *    waiting for the previous launch in the stream (X, S and the outputs still
+ *    wait).  Set it only when no kernel launched right before a call writes that
+ *    call's weights; otherwise the call may read stale weights.
  *  - bf16 layer work that no tensor-core kernel takes (for example a weight that
  *    is not K-contiguous, a shard width k_t that is not a multiple of 8, more
  *    than 16 ranks beyond a few tokens, pointers off 16 bytes) returns

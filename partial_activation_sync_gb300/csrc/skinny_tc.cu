@@ -73,6 +73,7 @@ struct SkinnyParams {
     int vec;                                 // outputs take 16-byte stores (aligned rows)
     const int32_t *sel;
     int64_t n_sel;
+    int prefetch_w;                          // weight tiles of the first stages before the wait
 };
 
 template <int NT>
@@ -178,8 +179,11 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     // Launched as a programmatic dependent, this grid may have started while the
     // previous one in the stream was still running: nothing above touched global
     // memory (the tensor maps are launch parameters).  Wait for it before the
-    // first load or store, then let the next grid start its own setup.
-    griddep_wait();
+    // first load or store, then let the next grid start its own setup.  With
+    // prefetch_w the producer thread waits later, after it has issued the weight
+    // tiles of the first ring stages (the caller guarantees that the previous
+    // launch does not write the weights); the rest of warp 0 touches no memory.
+    if (!(p.prefetch_w != 0 && warp == 0)) griddep_wait();
     griddep_launch_dependents();
 
     if (warp == 0) {
@@ -187,7 +191,24 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
         if (lane == 0) {
             int stage = 0;
             uint32_t ph = 0;
-            for (int kb = 0; kb < p.nkb; ++kb) {
+            int kb0 = 0;
+            if (p.prefetch_w != 0) {
+                // the first pass over the ring needs no empty-slot wait: weight
+                // tiles now, then (after the previous grid) the token tiles
+                const int pre = p.nkb < STAGES ? p.nkb : STAGES;
+                for (int kb = 0; kb < pre; ++kb) {
+                    const uint32_t fb = smem_u32(&ctl->full[kb]);
+                    mbar_arrive_expect_tx(fb, TX);
+                    tma_load_3d(smem_u32(smW + kb * W_BYTES), &tmW, fb, kb * BK, r, (int)c0);
+                }
+                griddep_wait();
+                for (int kb = 0; kb < pre; ++kb)
+                    tma_load_3d(smem_u32(smX + kb * XB), &tmX, smem_u32(&ctl->full[kb]), kb * BK, r, 0);
+                kb0 = pre;
+                stage = pre % STAGES;
+                ph = pre == STAGES ? 1u : 0u;
+            }
+            for (int kb = kb0; kb < p.nkb; ++kb) {
                 if (!mbar_wait(smem_u32(&ctl->empty[stage]), ph ^ 1u, abort, WAIT_LIMIT_NS)) {
                     fail(abort);
                     break;
@@ -433,6 +454,8 @@ caat_status launch_rowpar_fwd_skinny(int t, int64_t N, int64_t K, int64_t h, con
     p.nkb = (int)((kt + BK - 1) / BK);
     p.sel = sel;
     p.n_sel = n_sel;
+    const char *pw_env = std::getenv("CAAT_PDL_WEIGHTS");
+    p.prefetch_w = pw_env != nullptr && std::strcmp(pw_env, "1") == 0;
     const int64_t num_cb = (h + CH - 1) / CH;
     if (num_cb * t > INT32_MAX) return CAAT_ERR_UNSUPPORTED;
     switch (nt) {

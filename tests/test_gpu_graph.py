@@ -99,7 +99,10 @@ def test_few_token_chain_with_programmatic_launch(caat, N, graph, monkeypatch):
     previous launch (its CTAs may start while that grid finishes; it waits for it
     before touching memory).  A chain of dependent calls -- each call's X is the
     previous call's rank-0 output -- must give the same bits with and without
-    that launch mode, one call after another and replayed from a graph."""
+    that launch mode, one call after another and replayed from a graph.  With
+    CAAT_PDL_WEIGHTS=1 the weight tiles of the first ring stages are read before
+    the wait: the chain's weights are written by nothing, so that is allowed, and
+    X still waits for the call that produced it."""
     T = torch()
     t, h = 8, 512
     K = h
@@ -134,7 +137,10 @@ def test_few_token_chain_with_programmatic_launch(caat, N, graph, monkeypatch):
     plain = run()
     monkeypatch.setenv("CAAT_PDL", "1")
     pdl = run()
+    monkeypatch.setenv("CAAT_PDL_WEIGHTS", "1")
+    early_w = run()
     for i in range(depth):
         for r in range(t):
             np.testing.assert_array_equal(pdl[i][r], plain[i][r], err_msg="call %d rank %d" % (i, r))
+            np.testing.assert_array_equal(early_w[i][r], plain[i][r], err_msg="weights early: call %d rank %d" % (i, r))
     assert caat.device_status() == 0
