@@ -50,15 +50,20 @@ using namespace tc;
 
 constexpr int CH = 128;                      // channels per CTA (MMA M)
 constexpr int BK = 64;                       // k per stage (one 128-byte swizzled row)
-constexpr int STAGES = 4;
+constexpr int MAX_STAGES = 6;
+// Ring depth by token tile: as deep as lets two CTAs share an SM (the 7B layers
+// launch 256 CTAs on 152 SMs): 6 stages of 18 KB at NT = 16, 5 of 20 KB at 32,
+// 4 of 24 KB at 64.
+template <int NT>
+__host__ __device__ constexpr int stages() { return NT <= 16 ? 6 : (NT <= 32 ? 5 : 4); }
 constexpr int NUM_THREADS = 192;
 constexpr int W_BYTES = CH * BK * 2;         // 16 KB
 constexpr int MAX_T_SKINNY = 8;              // portable cluster size
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 struct SkinnyCtl {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[MAX_STAGES];
+    uint64_t empty[MAX_STAGES];
     uint64_t acc_full;
     uint32_t tmem_base;
     int abort;
@@ -82,7 +87,7 @@ __host__ __device__ constexpr int x_bytes() { return NT * BK * 2; }
 template <int NT>
 constexpr size_t skinny_smem()
 {
-    return 1024 + (size_t)STAGES * (W_BYTES + x_bytes<NT>()) + sizeof(SkinnyCtl);
+    return 1024 + (size_t)stages<NT>() * (W_BYTES + x_bytes<NT>()) + sizeof(SkinnyCtl);
 }
 
 __device__ __forceinline__ void fail(volatile int *abort)
@@ -139,6 +144,7 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                          const SkinnyParams p)
 {
     constexpr int XB = x_bytes<NT>();
+    constexpr int STAGES = stages<NT>();
     constexpr uint32_t TX = W_BYTES + XB;
     constexpr uint32_t TMEM_COLS = NT < 32 ? 32 : NT;
     constexpr uint32_t IDESC = idesc_bf16_f32(CH, NT);
@@ -387,6 +393,8 @@ caat_status launch_nt(const CUtensorMap &tmX, const CUtensorMap &tmW, const Skin
 {
     auto kern = rowpar_fwd_skinny_kernel<NT>;
     constexpr size_t smem = skinny_smem<NT>();
+    static_assert(2 * (smem + 1024) <= 228 * 1024, "two CTAs per SM (1 KB reserved each)");
+    static_assert((size_t)NT * CH * 4 <= (size_t)stages<NT>() * W_BYTES, "partials fit in the ring");
     if (prepare_kernel_smem((const void *)kern, (int)smem) != CAAT_OK) return CAAT_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
