@@ -82,7 +82,8 @@ def test_colpar_small_shapes(caat, dtype, t, N, h, kt, wl):
 
 
 @pytest.mark.parametrize("t,N,h,K", [(8, 256, 768, 2304), (8, 300, 768, 3072), (3, 200, 520, 408),
-                                     (4, 130, 256, 256)])
+                                     (4, 130, 256, 256),
+                                     (4, 384, 520, 1024)])   # k_t = 256: the GEMMs on CTA pairs
 @pytest.mark.parametrize("p,layout", [(0.5, 0), (0.5, 1), (0.0, 0), (1.0, 0)])
 def test_colpar_tensor_core_shapes(caat, t, N, h, K, p, layout):
     got, want, S, kernels = _run(caat, t, N, h, K, p, layout, "bf16", "rm", seed=N)

@@ -312,9 +312,9 @@ def bwd_cta(request, monkeypatch):
 
 # shapes whose backward tiles are 256 columns wide (CTA pairs by default):
 # k_t = 256 with ragged rows (N = 300: the second pair's odd CTA reads only
-# zero fill) and ragged channels (h = 264), and k_t = 480 (two tiles, the last
-# one 224 columns)
-BWD_PAIR_SHAPES = [(2, 300, 256, 264), (4, 512, 480, 768)]
+# zero fill) and ragged channels (h = 264), k_t = 480 (two tiles, the last one
+# 224 columns), and the most ranks the tensor-core backward takes (t = 16)
+BWD_PAIR_SHAPES = [(2, 300, 256, 264), (4, 512, 480, 768), (16, 256, 256, 512)]
 
 
 @pytest.mark.parametrize("t,N,kt,h", TC_SHAPES + BWD_PAIR_SHAPES)
