@@ -644,3 +644,22 @@ def test_layer_degenerate_shapes(caat, dtype, t, N, kt, h):
         gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, p, 0, dtype, 0, "rm", seed=t + h)
         check(gX, wX, dtype, bwd=True)
         check(gW, wW, dtype, bwd=True)
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+def test_fwd_bwd_largest_h(caat, layout, fwd_mode):
+    """The largest channel count the tensor-core forward takes (h = 32768: a
+    1024-word S bitmap, 128 channel blocks of 256 -- h is no multiple of 192, so
+    the 192-wide modes run 256-wide tiles), random and contiguous S, in every
+    forward mode; and the backward in both placements."""
+    t, N, kt, h = 2, 256, 64, 32768
+    got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, 0.5, layout, "bf16", "nn", seed=31)
+    assert caat.last_kernel() == "rowpar_fwd_tc"
+    for r in range(t):
+        check(got[r], want[r], "bf16", what=r, spread=spread)
+    if fwd_mode != "2":
+        return                      # the backward does not depend on the forward mode
+    for mode in (0, 1):
+        gX, gW, wX, wW = _bwd_case(caat, t, N, kt * t, h, 0.5, layout, "bf16", mode, seed=32)
+        check(gX, wX, "bf16", bwd=True, what=("dX", mode))
+        check(gW, wW, "bf16", bwd=True, what=("dW", mode))
