@@ -156,6 +156,7 @@ TC_FWD_SHAPES = TC_SHAPES + [
     (4, 200, 64, 192),      # the smallest h: one 192-wide tile
     (3, 260, 128, 576),     # 192-wide tiles: three per row block
     (2, 300, 256, 384),     # 192-wide tiles with shards of 4 k-blocks: the deeper ring
+    (16, 256, 64, 512),     # the most ranks the tile kernel takes (one tensor map each)
 ]
 
 
