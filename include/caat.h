@@ -34,9 +34,10 @@
  *    (backward on `stream` only), CAAT_BWD_RING=4 (the backward GEMMs' ring at 4
  *    stages whatever the tile width; single CTAs only), CAAT_BWD_PAIR=0 (the
  *    backward GEMMs on single CTAs instead of CTA pairs), CAAT_PDL=0 (the
- *    few-token kernel launched plainly instead of as a programmatic dependent of
- *    the previous launch in the stream, whose CTAs may then be set up while that
- *    launch finishes; the kernel waits for it before it touches memory).
+ *    few-token forward and the standalone reduce launched plainly instead of as
+ *    programmatic dependents of the previous launch in the stream, whose blocks
+ *    may then start while that launch finishes; they wait for it before they
+ *    touch memory).
  *  - CAAT_PDL_WEIGHTS=1 is an opt-in for inference with static weights: the
  *    few-token kernel then reads the weight tiles of its first ring stages before
  *    waiting for the previous launch in the stream (X, S and the outputs still

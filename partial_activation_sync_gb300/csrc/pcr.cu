@@ -13,14 +13,23 @@
 // list at block start.
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+#include <cstring>
+
 #include "caat_internal.h"
 
 namespace caat {
 namespace {
 
+// The reduce kernels are launched as programmatic dependents of the previous
+// launch in the stream (see launch_dependent): a block may start while that
+// grid finishes, so it waits for it before its first access to global memory
+// (the index list of S, then the inputs), and then lets the next grid start.
 __device__ __forceinline__ void build_bitmap(uint32_t *bm, int64_t h, const int32_t *sel,
                                              int64_t n_sel)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t words = (h + 31) >> 5;
     if (sel == nullptr) {   // S = {0, ..., n_sel-1}
         for (int64_t w = threadIdx.x; w < words; w += blockDim.x) {
@@ -253,13 +262,36 @@ pcr_colsum_kernel(int t, int64_t N, int64_t s, ConstPtrs in, int64_t ld_in, uint
     }
 }
 
+// A launch as a programmatic dependent of the previous launch in the stream
+// (CAAT_PDL=0: a plain launch).  The kernel waits for that launch before it
+// touches memory, so only its start-up overlaps the previous grid's end.
+template <typename... Params, typename... Args>
+void launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                      Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    const char *env = std::getenv("CAAT_PDL");
+    if (env == nullptr || std::strcmp(env, "0") != 0) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    (void)cudaLaunchKernelEx(&cfg, kern, args...);   // errors are read by the caller
+}
+
 template <int TT, bool BF16, bool INPLACE>
 void launch_vec(dim3 grid, dim3 block, size_t smem, cudaStream_t s, int t, int64_t N, int64_t h,
                 const ConstPtrs &in, int64_t ld_in, const MutPtrs &out, int64_t ld_out,
                 const int32_t *sel, int64_t n_sel)
 {
-    pcr_vec_kernel<TT, BF16, INPLACE><<<grid, block, smem, s>>>(t, N, h, in, ld_in, out, ld_out,
-                                                                sel, n_sel);
+    launch_dependent(pcr_vec_kernel<TT, BF16, INPLACE>, grid, block, smem, s, t, N, h, in, ld_in, out, ld_out,
+                     sel, n_sel);
 }
 
 template <bool BF16, bool INPLACE>
@@ -341,11 +373,11 @@ caat_status launch_pcr(int t, int64_t N, int64_t h, caat_dtype dt, const ConstPt
         note_launch("pcr_vec");
     } else {
         if (bf16) {
-            if (in_place) pcr_scalar_kernel<true, true><<<grid, block, smem, s>>>(t, N, h, in, ld_in, out, ld_out, sel, n_sel);
-            else pcr_scalar_kernel<true, false><<<grid, block, smem, s>>>(t, N, h, in, ld_in, out, ld_out, sel, n_sel);
+            if (in_place) launch_dependent(pcr_scalar_kernel<true, true>, grid, block, smem, s, t, N, h, in, ld_in, out, ld_out, sel, n_sel);
+            else launch_dependent(pcr_scalar_kernel<true, false>, grid, block, smem, s, t, N, h, in, ld_in, out, ld_out, sel, n_sel);
         } else {
-            if (in_place) pcr_scalar_kernel<false, true><<<grid, block, smem, s>>>(t, N, h, in, ld_in, out, ld_out, sel, n_sel);
-            else pcr_scalar_kernel<false, false><<<grid, block, smem, s>>>(t, N, h, in, ld_in, out, ld_out, sel, n_sel);
+            if (in_place) launch_dependent(pcr_scalar_kernel<false, true>, grid, block, smem, s, t, N, h, in, ld_in, out, ld_out, sel, n_sel);
+            else launch_dependent(pcr_scalar_kernel<false, false>, grid, block, smem, s, t, N, h, in, ld_in, out, ld_out, sel, n_sel);
         }
         note_launch("pcr_scalar");
     }

@@ -144,3 +144,49 @@ def test_few_token_chain_with_programmatic_launch(caat, N, graph, monkeypatch):
             np.testing.assert_array_equal(pdl[i][r], plain[i][r], err_msg="call %d rank %d" % (i, r))
             np.testing.assert_array_equal(early_w[i][r], plain[i][r], err_msg="weights early: call %d rank %d" % (i, r))
     assert caat.device_status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("graph", [False, True])
+def test_reduce_chain_with_programmatic_launch(caat, dtype, graph, monkeypatch):
+    """The standalone reduce is launched as a programmatic dependent of the
+    previous launch and waits for it before reading.  A chain of reduces, each
+    reading the previous one's outputs (alternating two buffer sets, with a random
+    S so that both kinds of channel move), must give the same bits with and
+    without that launch mode, one call after another and replayed from a graph."""
+    T = torch()
+    t, N, h, depth = 4, 256, 768, 6
+    S = caat.select_channels(h, 0.5, caat.CAAT_S_RANDOM, 77)
+    sel = T.from_numpy(S).cuda()
+    src = [dev(ci.normal(2300 + r, (N, h)), dtype) for r in range(t)]
+    bufs = [[T.empty_like(src[0]) for _ in range(t)] for _ in range(2)]
+
+    def chain():
+        x = src
+        for i in range(depth):
+            caat.partial_channel_reduce(x, sel, outs=bufs[i % 2])
+            x = bufs[i % 2]
+
+    def run():
+        for b in bufs:
+            for y in b:
+                y.fill_(float("nan"))
+        if graph:
+            g = _capture(T, chain)
+            for b in bufs:
+                for y in b:
+                    y.fill_(float("nan"))
+            g.replay()
+        else:
+            chain()
+        T.cuda.synchronize()
+        return [[y.view(T.int16 if dtype == "bf16" else T.int32).cpu().numpy().copy() for y in b] for b in bufs]
+
+    monkeypatch.setenv("CAAT_PDL", "0")
+    plain = run()
+    monkeypatch.setenv("CAAT_PDL", "1")
+    pdl = run()
+    for j in range(2):
+        for r in range(t):
+            np.testing.assert_array_equal(pdl[j][r], plain[j][r], err_msg="buffer %d rank %d" % (j, r))
+    assert caat.device_status() == 0
