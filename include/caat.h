@@ -38,6 +38,12 @@
  *    programmatic dependents of the previous launch in the stream, whose blocks
  *    may then start while that launch finishes; they wait for it before they
  *    touch memory).
+ *  - CAAT_CHECK_SEL=1 (a debug switch) checks every index list of S: the list is
+ *    copied to the host on the call's stream, which is synchronised, and must be
+ *    ascending, unique and inside [0, h), else the call returns INVALID_ARG
+ *    before anything is launched.  Without it the list is trusted (an invalid
+ *    list gives undefined channel sets).  The check is skipped while the stream
+ *    is being captured into a graph.
  *  - CAAT_PDL_WEIGHTS=1 is an opt-in for inference with static weights: the
  *    few-token kernel then reads the weight tiles of its first ring stages before
  *    waiting for the previous launch in the stream (X, S and the outputs still

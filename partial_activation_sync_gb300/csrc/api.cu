@@ -3,6 +3,7 @@
 #include <cstring>
 #include <initializer_list>
 #include <mutex>
+#include <vector>
 
 #include "caat_internal.h"
 
@@ -14,6 +15,29 @@ thread_local uint64_t t_launches = 0;
 int g_sms[128];
 std::mutex g_mu;
 }  // namespace
+
+// Debug check of an index list of S (CAAT_CHECK_SEL=1): the list is copied to
+// the host on the call's stream, which is then synchronised, and must be
+// ascending, unique and inside [0, h).  Skipped while the stream is being
+// captured (a synchronising copy cannot be captured) and for the contiguous form.
+caat_status check_sel_debug(const int32_t *sel, int64_t n_sel, int64_t h, cudaStream_t s)
+{
+    const char *env = std::getenv("CAAT_CHECK_SEL");
+    if (env == nullptr || std::strcmp(env, "1") != 0 || sel == nullptr || n_sel <= 0) return CAAT_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return CAAT_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return CAAT_OK;
+    std::vector<int32_t> host((size_t)n_sel);
+    if (cudaMemcpyAsync(host.data(), sel, (size_t)n_sel * sizeof(int32_t), cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return CAAT_ERR_CUDA;
+    for (int64_t i = 0; i < n_sel; ++i) {
+        if (host[(size_t)i] < 0 || host[(size_t)i] >= h) return CAAT_ERR_INVALID_ARG;
+        if (i > 0 && host[(size_t)i] <= host[(size_t)i - 1]) return CAAT_ERR_INVALID_ARG;
+    }
+    return CAAT_OK;
+}
 
 void note_launch(const char *kernel_name, int launches)
 {
@@ -150,6 +174,7 @@ extern "C" caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, 
     if (t < 1 || t > CAAT_MAX_T || N < 0 || h < 0 || !valid_dtype(dt)) return CAAT_ERR_INVALID_ARG;
     if (in == nullptr || out == nullptr) return CAAT_ERR_INVALID_ARG;
     if (ld_in < h || ld_out < h || n_sel < 0 || n_sel > h) return CAAT_ERR_INVALID_ARG;
+    if (const caat_status cs = check_sel_debug(sel, n_sel, h, (cudaStream_t)stream)) return cs;
     const int64_t es = elem_size(dt);
     ConstPtrs pin{};
     MutPtrs pout{};
@@ -229,6 +254,7 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
 {
     caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, sel, n_sel);
     if (st != CAAT_OK) return st;
+    if ((st = check_sel_debug(sel, n_sel, h, (cudaStream_t)stream)) != CAAT_OK) return st;
     if (Y == nullptr || ldy < h) return CAAT_ERR_INVALID_ARG;
     const int64_t es = elem_size(dt);
     MutPtrs py{};
@@ -379,6 +405,7 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
 {
     caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, sel, n_sel);
     if (st != CAAT_OK) return st;
+    if ((st = check_sel_debug(sel, n_sel, h, (cudaStream_t)stream)) != CAAT_OK) return st;
     if (mode != CAAT_BWD_REDUCE_DOUT && mode != CAAT_BWD_NO_REDUCE) return CAAT_ERR_INVALID_ARG;
     if (dOut == nullptr || ld_dout < h || lddx < K) return CAAT_ERR_INVALID_ARG;
     if (N > 0 && K > 0 && dX == nullptr) return CAAT_ERR_INVALID_ARG;
@@ -531,6 +558,7 @@ extern "C" caat_status caat_colpar_linear_bwd(int t, int64_t N, int64_t h, int64
 {
     caat_status st = check_layer_args(t, N, K, h, dt, dZ, ldz, W1, w1_cs, w1_rs, sel, n_sel);
     if (st != CAAT_OK) return st;
+    if ((st = check_sel_debug(sel, n_sel, h, (cudaStream_t)stream)) != CAAT_OK) return st;
     st = check_colpar_inputs(t, N, h, A, lda);
     if (st != CAAT_OK) return st;
     if (dA == nullptr || ldda < h) return CAAT_ERR_INVALID_ARG;

@@ -80,6 +80,10 @@ caat_status launch_rowpar_fwd_decode(int t, int64_t N, int64_t K, int64_t h, con
                                      const void *W, int64_t ldw, const MutPtrs &Y, int64_t ldy,
                                      const int32_t *sel, int64_t n_sel, cudaStream_t s);
 
+// Debug check of an index list of S (api.cu): ascending, unique, in [0, h);
+// active only with CAAT_CHECK_SEL=1.
+caat_status check_sel_debug(const int32_t *sel, int64_t n_sel, int64_t h, cudaStream_t s);
+
 // Tensor map for TMA (gemm_tc.cu): 128-byte swizzle, zero fill out of bounds;
 // bf16 elements unless f32.
 bool encode_tmap(CUtensorMap *tm, const void *base, int rank, const uint64_t *dims,

@@ -167,6 +167,7 @@ extern "C" caat_status caat_pcr_pack(int64_t N, int64_t h, caat_dtype dt, const 
     if (N < 0 || h < 0 || n_sel < 0 || n_sel > h || ldy < h || ldp < n_sel) return CAAT_ERR_INVALID_ARG;
     if (dt != CAAT_F32 && dt != CAAT_BF16) return CAAT_ERR_INVALID_ARG;
     if (N == 0 || n_sel == 0) return CAAT_OK;
+    if (const caat_status cs = check_sel_debug(sel, n_sel, h, (cudaStream_t)stream)) return cs;
     if (Y == nullptr || P == nullptr) return CAAT_ERR_INVALID_ARG;
     const int64_t es = dt == CAAT_BF16 ? 2 : 4;
     if (overlap(span_rows(P, N, n_sel, ldp, es), span_rows(Y, N, h, ldy, es)) ||
@@ -200,6 +201,7 @@ extern "C" caat_status caat_pcr_unpack(int64_t N, int64_t h, caat_dtype dt, cons
     if (dt != CAAT_F32 && dt != CAAT_BF16) return CAAT_ERR_INVALID_ARG;
     if (n_out < 1 || n_out > CAAT_MAX_T || Y == nullptr) return CAAT_ERR_INVALID_ARG;
     if (N == 0 || n_sel == 0) return CAAT_OK;
+    if (const caat_status cs = check_sel_debug(sel, n_sel, h, (cudaStream_t)stream)) return cs;
     if (P == nullptr) return CAAT_ERR_INVALID_ARG;
     const int64_t es = dt == CAAT_BF16 ? 2 : 4;
     MutPtrs y{};

@@ -4,7 +4,8 @@ bf16 work that no tensor-core kernel takes -- 17 ranks at prefill size, a
 row-major weight -- is refused with UNSUPPORTED, before anything is launched,
 unless CAAT_ALLOW_FALLBACK=1 is in the environment.  fp32 (no tensor-core path)
 and empty work need no opt-in.  The conftest sets the variable for every GPU
-test; these tests remove it."""
+test; these tests remove it.  Also here: the other opt-in check of the
+arguments, CAAT_CHECK_SEL=1, which validates an index list of S."""
 import numpy as np
 import pytest
 
@@ -146,5 +147,38 @@ def test_tensor_core_shapes_need_no_opt_in(no_opt_in):
     assert caat.last_kernel() != "rowpar_fwd_simt"
     caat.rowpar_linear_bwd(Xd, Wd, [dev(G[r], "bf16") for r in range(t)], t, sel_dev(S))
     assert caat.last_kernel() != "batched_gemm_simt"
+    T.cuda.synchronize()
+    assert caat.device_status() == 0
+
+
+@pytest.mark.parametrize("bad", ["duplicate", "unsorted", "out_of_range"])
+def test_index_list_debug_check(bad, monkeypatch):
+    """CAAT_CHECK_SEL=1 validates an index list of S on the host (ascending,
+    unique, inside [0, h)) before anything is launched; a valid list passes."""
+    import partial_activation_sync_gb300 as caat
+    T = torch()
+    t, N, K, h = 4, 128, 256, 256
+    X = dev(ci.normal(21, (N, K)), "bf16")
+    Wd = dev(np.ascontiguousarray(ci.normal(22, (K, h), std=0.02).T), "bf16").t()
+    S = np.arange(0, h, 2, dtype=np.int32)
+    if bad == "duplicate":
+        S[5] = S[4]
+    elif bad == "unsorted":
+        S[[3, 4]] = S[[4, 3]]
+    else:
+        S[-1] = h
+    monkeypatch.setenv("CAAT_CHECK_SEL", "1")
+    outs = _nan_outs(t, N, h, T.bfloat16)
+    n0 = caat.launch_count()
+    with pytest.raises(caat.CaatError) as e:
+        caat.rowpar_linear_fwd(X, Wd, t, sel_dev(S), outs=outs)
+    assert e.value.status == 1                       # CAAT_ERR_INVALID_ARG
+    with pytest.raises(caat.CaatError) as e:
+        caat.partial_channel_reduce(outs, sel_dev(S))
+    assert e.value.status == 1
+    T.cuda.synchronize()
+    assert caat.launch_count() == n0 and _untouched(outs)
+    good = np.arange(0, h, 2, dtype=np.int32)
+    caat.rowpar_linear_fwd(X, Wd, t, sel_dev(good), outs=outs)
     T.cuda.synchronize()
     assert caat.device_status() == 0
