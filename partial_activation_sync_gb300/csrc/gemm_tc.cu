@@ -135,13 +135,18 @@ std::atomic<int> g_inject{CAAT_INJECT_NONE};
 // k-blocks are fed faster (130M down-proj, k_t = 384: 49.3 -> 46.6 us); shorter
 // shards are bound by their per-shard epilogue, which the second buffer helps
 // (130M out-proj, k_t = 96: 33.5 against 35.2 us).
-template <int CLN, int BNT, bool DEEP = false>
+// STG2 (CTA pairs with 256-wide tiles): two staging buffers per epilogue warp
+// instead of CAAT_FWD_PAIR_NBUF256, taken when the S bitmap of the call leaves
+// room for them next to the 6-stage ring (h up to about 15,000 channels).  A
+// bulk store then drains one buffer while the next chunk fills the other (7B
+// prefill out-proj: 115 -> 112 us).
+template <int CLN, int BNT, bool DEEP = false, bool STG2 = false>
 struct Cfg {
     static constexpr bool PAIR = CLN > 1;
     static constexpr int STAGES = PAIR ? CAAT_FWD_PAIR_STAGES : (BNT < 256 && DEEP ? 5 : 4);
     // staging buffers per epilogue warp: several (bulk stores drain the earlier
     // ones while the next chunk fills one) where shared memory allows
-    static constexpr int NBUF = BNT < 256 ? (DEEP ? 1 : 2) : (PAIR ? CAAT_FWD_PAIR_NBUF256 : 1);
+    static constexpr int NBUF = BNT < 256 ? (DEEP ? 1 : 2) : (PAIR ? (STG2 ? 2 : CAAT_FWD_PAIR_NBUF256) : 1);
     static constexpr int B_ROWS = PAIR ? BNT / 2 : BNT;        // W rows (channels) per CTA per stage
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -158,17 +163,19 @@ struct SmemCtl {
     uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort;
-    uint32_t bitmap[MAX_H_TC / 32];
+    // followed in shared memory by the S bitmap: ceil(h / 32) words
 };
 
-template <int CLN, int BNT, bool DEEP>
+// shared memory of a mode without the S bitmap (which takes ceil(h / 32) words more)
+template <int CLN, int BNT, bool DEEP, bool STG2>
 constexpr size_t smem_bytes()
 {
-    using C = Cfg<CLN, BNT, DEEP>;
+    using C = Cfg<CLN, BNT, DEEP, STG2>;
     static_assert(C::STAGES <= MAX_STAGES, "ring deeper than the barrier arrays");
     return 1024 + (size_t)C::STAGES * C::STAGE_BYTES + 4 * C::NBUF * STG_BYTES +
            sizeof(SmemCtl);
 }
+constexpr size_t bitmap_bytes(int64_t h) { return (size_t)((h + 31) / 32) * 4; }
 
 struct YMaps {
     CUtensorMap m[MAX_T_TC];   // rank r's output [N, h], box 64 channels x 32 rows
@@ -351,12 +358,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
 
 // CLN = CTAs per cluster: 1 (one CTA per tile) or 2 (a CTA pair).  Each CTA
 // fetches its own X and W tiles from this GPU's memory; no load is multicast.
-template <int CLN, int BNT, bool DEEP>
+template <int CLN, int BNT, bool DEEP, bool STG2>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ YMaps ymaps, const FwdParams p)
 {
-    using C = Cfg<CLN, BNT, DEEP>;
+    using C = Cfg<CLN, BNT, DEEP, STG2>;
     constexpr bool PAIR = C::PAIR;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -364,6 +371,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     uint8_t *smB = base + C::STAGES * A_BYTES;
     uint8_t *staging = base + C::STAGES * C::STAGE_BYTES;
     SmemCtl *ctl = (SmemCtl *)(staging + 4 * C::NBUF * STG_BYTES);
+    uint32_t *bitmap = reinterpret_cast<uint32_t *>(ctl + 1);
     volatile int *abort = &ctl->abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -372,7 +380,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     const uint32_t leader = crank & ~1u;                    // even CTA of this CTA's pair
     const bool is_leader = crank == leader;
 
-    for (int64_t w = tid; w < words; w += NUM_THREADS) ctl->bitmap[w] = 0u;
+    for (int64_t w = tid; w < words; w += NUM_THREADS) bitmap[w] = 0u;
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
@@ -411,7 +419,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         if (p.sel == nullptr) {      // S = {0, ..., n_sel-1}
             for (int64_t w = e; w < words; w += NB) {
                 const int64_t lo = w * 32;
-                ctl->bitmap[w] = p.n_sel >= lo + 32 ? 0xffffffffu
+                bitmap[w] = p.n_sel >= lo + 32 ? 0xffffffffu
                                : (p.n_sel <= lo ? 0u : ((1u << (p.n_sel - lo)) - 1u));
             }
         } else {
@@ -421,7 +429,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                 for (int u = 0; u < 8; ++u) v[u] = i0 + NB * u < p.n_sel ? __ldg(p.sel + i0 + NB * u) : -1;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
-                    if (v[u] >= 0 && v[u] < p.h) atomicOr(&ctl->bitmap[v[u] >> 5], 1u << (v[u] & 31));
+                    if (v[u] >= 0 && v[u] < p.h) atomicOr(&bitmap[v[u] >> 5], 1u << (v[u] & 31));
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(NB) : "memory");   // warps 1..5
@@ -488,7 +496,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
             Work wk;
             while (next_work(cur, p, worker, nworkers, num_mg, wk)) {
                 const int nb = wk.nb;
-                const int cls = wk.piece ? (int)NO_S : tile_class<BNT>(ctl->bitmap, (int64_t)nb * BNT, p.h, p.t);
+                const int cls = wk.piece ? (int)NO_S : tile_class<BNT>(bitmap, (int64_t)nb * BNT, p.h, p.t);
                 for (int r = wk.r0; r < wk.r1; ++r) {
                     const bool starts = cls != FULL_S || r == 0;
                     const bool ends = cls != FULL_S || r == p.t - 1;
@@ -544,7 +552,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
             const int mb = wk.mg * CLN + (int)crank;
             const int nb = wk.nb;
             const int64_t n0 = (int64_t)nb * BNT;
-            const int cls = wk.piece ? (int)NO_S : tile_class<BNT>(ctl->bitmap, n0, p.h, p.t);
+            const int cls = wk.piece ? (int)NO_S : tile_class<BNT>(bitmap, n0, p.h, p.t);
             for (int r = wk.r0; r < wk.r1; ++r) {
                 if (cls == FULL_S && r != p.t - 1) continue;
                 const uint32_t b = au & 1u;
@@ -582,7 +590,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                         }
                         if (zero_nons) {
                             // keep the S channels accumulating, clear the others
-                            const uint32_t m0 = ctl->bitmap[c0 >> 5], m1 = ctl->bitmap[(c0 >> 5) + 1];
+                            const uint32_t m0 = bitmap[c0 >> 5], m1 = bitmap[(c0 >> 5) + 1];
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
                                 v0[j] = ((m0 >> j) & 1u) ? v0[j] : 0u;
@@ -628,7 +636,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                     for (int c64 = 0; c64 < BNT / 64; ++c64) {
                         const int64_t c0 = n0 + 64 * c64;
                         if (c0 >= p.h) break;
-                        const uint32_t m0 = ctl->bitmap[c0 >> 5], m1 = ctl->bitmap[(c0 >> 5) + 1];
+                        const uint32_t m0 = bitmap[c0 >> 5], m1 = bitmap[(c0 >> 5) + 1];
                         uint32_t w[32], ws[32];
                         {
                             uint32_t v[32], u[32];
@@ -744,14 +752,16 @@ bool encode_3d(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1, uint
     return encode_tmap(tm, base, 3, dims, strides, box);
 }
 
-template <int CLN, int BNT, bool DEEP = false>
+template <int CLN, int BNT, bool DEEP = false, bool STG2 = false>
 caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMaps &ym, const FwdParams &p,
                        cudaStream_t s)
 {
     constexpr bool PAIR = CLN > 1;
-    auto kern = rowpar_fwd_tc_kernel<CLN, BNT, DEEP>;
-    constexpr size_t smem = smem_bytes<CLN, BNT, DEEP>();
-    static_assert(smem <= 227 * 1024, "shared memory beyond the per-CTA limit");
+    auto kern = rowpar_fwd_tc_kernel<CLN, BNT, DEEP, STG2>;
+    static_assert(smem_bytes<CLN, BNT, DEEP, STG2>() + bitmap_bytes(192) <= 227 * 1024,
+                  "shared memory beyond the per-CTA limit");
+    const size_t smem = smem_bytes<CLN, BNT, DEEP, STG2>() + bitmap_bytes(p.h);
+    if (smem > 227 * 1024) return CAAT_ERR_UNSUPPORTED;
     if (prepare_kernel_smem((const void *)kern, (int)smem) != CAAT_OK) return CAAT_ERR_CUDA;
     const int per = CLN;
     const int num_mg = (p.num_m + CLN - 1) / CLN;
@@ -917,8 +927,15 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         if (bn == 192)
             st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s)
                : (p.nkb >= 4 ? launch_fwd<1, 192, true>(tmX, tmW, ym, p, s) : launch_fwd<1, 192>(tmX, tmW, ym, p, s));
-        else
-            st = cln == 2 ? launch_fwd<2, BN>(tmX, tmW, ym, p, s) : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
+        else if (cln == 2) {
+            // two staging buffers where the bitmap leaves room (CAAT_FWD_PAIR_STG=1: one)
+            const char *stg_env = std::getenv("CAAT_FWD_PAIR_STG");
+            const bool stg2 = smem_bytes<2, BN, false, true>() + bitmap_bytes(h) <= 227 * 1024 &&
+                              !(stg_env != nullptr && stg_env[0] == '1');
+            st = stg2 ? launch_fwd<2, BN, false, true>(tmX, tmW, ym, p, s) : launch_fwd<2, BN>(tmX, tmW, ym, p, s);
+        } else {
+            st = launch_fwd<1, BN>(tmX, tmW, ym, p, s);
+        }
         if (st == CAAT_OK && pieces_then_reduce) {
             ConstPtrs yin{};
             for (int r = 0; r < t; ++r) yin.p[r] = Y.p[r];
