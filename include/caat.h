@@ -30,8 +30,8 @@
  *    cutting the tiles outside S into per-shard pieces that even out the SMs'
  *    load; or the whole tiles first and the pieces after them, instead of the
  *    pieces in runs around each worker's whole tiles),
- *    CAAT_FWD_PAIR_STG=1 (one staging buffer per epilogue warp in the pair mode's
- *    256-wide tiles instead of two where shared memory allows),
+ *    CAAT_FWD_STG=1 (one staging buffer per epilogue warp in the 256-wide tiles
+ *    instead of two where shared memory allows),
  *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
  *    (backward on `stream` only), CAAT_BWD_RING=4 (the backward GEMMs' ring at 4
  *    stages whatever the tile width; single CTAs only), CAAT_BWD_PAIR=0 (the

@@ -135,18 +135,18 @@ std::atomic<int> g_inject{CAAT_INJECT_NONE};
 // k-blocks are fed faster (130M down-proj, k_t = 384: 49.3 -> 46.6 us); shorter
 // shards are bound by their per-shard epilogue, which the second buffer helps
 // (130M out-proj, k_t = 96: 33.5 against 35.2 us).
-// STG2 (CTA pairs with 256-wide tiles): two staging buffers per epilogue warp
-// instead of CAAT_FWD_PAIR_NBUF256, taken when the S bitmap of the call leaves
-// room for them next to the 6-stage ring (h up to about 15,000 channels).  A
-// bulk store then drains one buffer while the next chunk fills the other (7B
-// prefill out-proj: 115 -> 112 us).
+// STG2 (256-wide tiles): two staging buffers per epilogue warp instead of one,
+// taken when the S bitmap of the call leaves room for them next to the ring (6
+// stages of 32 KB for CTA pairs, 4 of 48 KB for single CTAs; h up to about
+// 15,000 channels).  A bulk store then drains one buffer while the next chunk
+// fills the other (7B prefill out-proj: 114 -> 111 us).
 template <int CLN, int BNT, bool DEEP = false, bool STG2 = false>
 struct Cfg {
     static constexpr bool PAIR = CLN > 1;
     static constexpr int STAGES = PAIR ? CAAT_FWD_PAIR_STAGES : (BNT < 256 && DEEP ? 5 : 4);
     // staging buffers per epilogue warp: several (bulk stores drain the earlier
     // ones while the next chunk fills one) where shared memory allows
-    static constexpr int NBUF = BNT < 256 ? (DEEP ? 1 : 2) : (PAIR ? (STG2 ? 2 : CAAT_FWD_PAIR_NBUF256) : 1);
+    static constexpr int NBUF = BNT < 256 ? (DEEP ? 1 : 2) : (STG2 ? 2 : (PAIR ? CAAT_FWD_PAIR_NBUF256 : 1));
     static constexpr int B_ROWS = PAIR ? BNT / 2 : BNT;        // W rows (channels) per CTA per stage
     static constexpr int B_BYTES = B_ROWS * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -927,14 +927,17 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         if (bn == 192)
             st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s)
                : (p.nkb >= 4 ? launch_fwd<1, 192, true>(tmX, tmW, ym, p, s) : launch_fwd<1, 192>(tmX, tmW, ym, p, s));
-        else if (cln == 2) {
-            // two staging buffers where the bitmap leaves room (CAAT_FWD_PAIR_STG=1: one)
-            const char *stg_env = std::getenv("CAAT_FWD_PAIR_STG");
-            const bool stg2 = smem_bytes<2, BN, false, true>() + bitmap_bytes(h) <= 227 * 1024 &&
-                              !(stg_env != nullptr && stg_env[0] == '1');
-            st = stg2 ? launch_fwd<2, BN, false, true>(tmX, tmW, ym, p, s) : launch_fwd<2, BN>(tmX, tmW, ym, p, s);
-        } else {
-            st = launch_fwd<1, BN>(tmX, tmW, ym, p, s);
+        else {
+            // two staging buffers where the bitmap leaves room (CAAT_FWD_STG=1: one)
+            const char *stg_env = std::getenv("CAAT_FWD_STG");
+            const bool one = stg_env != nullptr && stg_env[0] == '1';
+            if (cln == 2) {
+                const bool stg2 = !one && smem_bytes<2, BN, false, true>() + bitmap_bytes(h) <= 227 * 1024;
+                st = stg2 ? launch_fwd<2, BN, false, true>(tmX, tmW, ym, p, s) : launch_fwd<2, BN>(tmX, tmW, ym, p, s);
+            } else {
+                const bool stg2 = !one && smem_bytes<1, BN, false, true>() + bitmap_bytes(h) <= 227 * 1024;
+                st = stg2 ? launch_fwd<1, BN, false, true>(tmX, tmW, ym, p, s) : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
+            }
         }
         if (st == CAAT_OK && pieces_then_reduce) {
             ConstPtrs yin{};
