@@ -163,7 +163,8 @@ struct SmemCtl {
     uint64_t acc_empty[2];
     uint32_t tmem_base;
     int abort;
-    // followed in shared memory by the S bitmap: ceil(h / 32) words
+    // followed in shared memory by the S bitmap: ceil(h / 32) words and two
+    // zero words after them (the epilogue reads a chunk's two words at once)
 };
 
 // shared memory of a mode without the S bitmap (which takes ceil(h / 32) words more)
@@ -175,7 +176,7 @@ constexpr size_t smem_bytes()
     return 1024 + (size_t)C::STAGES * C::STAGE_BYTES + 4 * C::NBUF * STG_BYTES +
            sizeof(SmemCtl);
 }
-constexpr size_t bitmap_bytes(int64_t h) { return (size_t)((h + 31) / 32) * 4; }
+constexpr size_t bitmap_bytes(int64_t h) { return (size_t)((h + 31) / 32 + 2) * 4; }
 
 struct YMaps {
     CUtensorMap m[MAX_T_TC];   // rank r's output [N, h], box 64 channels x 32 rows
@@ -380,7 +381,7 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     const uint32_t leader = crank & ~1u;                    // even CTA of this CTA's pair
     const bool is_leader = crank == leader;
 
-    for (int64_t w = tid; w < words; w += NUM_THREADS) bitmap[w] = 0u;
+    for (int64_t w = tid; w < words + 2; w += NUM_THREADS) bitmap[w] = 0u;
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(smem_u32(&ctl->full[s]), 1);
