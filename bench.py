@@ -53,10 +53,10 @@ STEP_SPIN_CYCLES = 400000
 # capture reports null.  Output lines still dirty in L2 when the kernel ends are
 # not in the count.
 DRAM_TRAFFIC = {
-    ("7b_prefill", "out_proj"): 118.22e6 + 208.54e6,
-    ("7b_prefill", "down_proj"): 420.09e6 + 222.17e6,
-    ("130m", "out_proj"): 13.85e6 + 36.25e6,
-    ("130m", "down_proj"): 57.27e6 + 38.95e6,
+    ("7b_prefill", "out_proj"): 117.97e6 + 208.75e6,
+    ("7b_prefill", "down_proj"): 421.03e6 + 222.59e6,
+    ("130m", "out_proj"): 13.85e6 + 36.34e6,
+    ("130m", "down_proj"): 56.79e6 + 38.50e6,
 }
 
 
