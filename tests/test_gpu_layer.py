@@ -556,12 +556,14 @@ def test_bwd_contiguous_reduce_once_wide(caat, s):
     check(to_f64(dW), wW, "bf16", bwd=True)
 
 
-@pytest.mark.parametrize("t", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("t", [1, 2, 3, 4, 5, 7, 8])
 @pytest.mark.parametrize("N", [1, 3, 8, 15, 16, 17, 33, 48, 64])
 def test_fwd_skinny_parity(caat, t, N):
     """Few tokens (N <= 64, t <= 8): the swapped-operand tensor-core kernel, one
     cluster of t shard-CTAs per 128-channel block; ragged channel blocks (h = 1000)
-    and ragged shards (k_t = 136: the last 64-wide k block is part zero fill)."""
+    and ragged shards (k_t = 136: the last 64-wide k block is part zero fill).
+    t = 3, 5, 7 give the CTAs channel slices of the S sum (128 / t channels)
+    that are neither equal nor multiples of the 8-channel store."""
     for h, kt in ((1000, 136), (512, 64)):
         for p in (0.0, 0.5, 1.0):
             for layout in (0, 1):
