@@ -23,12 +23,24 @@ say where it sits):
 """
 import math
 
+import numpy as np
 import torch
+
+
+def in_s(h, s, dtype):
+    """Membership of the h channels in S as 0/1 of the given dtype.  S is a subset
+    of the channels (Introduction, partial channel-reduce): an int s stands for the
+    first s channels, an integer array for the listed channels."""
+    if isinstance(s, (int, np.integer)):
+        return (torch.arange(h) < int(s)).to(dtype)
+    m = torch.zeros(h, dtype=dtype)
+    m[torch.as_tensor(np.asarray(s, dtype=np.int64))] = 1
+    return m
 
 
 def rowpar_pcr(X, W, t, s):
     """X [N, K], W [K, h]; rank r's partial sum X_r W_r over shard r of K; the
-    first s channels summed over ranks in rank order, the rest rank-local.
+    channels of S (see in_s) summed over ranks in rank order, the rest rank-local.
     Returns [t, N, h]."""
     K = X.shape[1]
     kt = K // t
@@ -36,8 +48,7 @@ def rowpar_pcr(X, W, t, s):
     total = parts[0]
     for r in range(1, t):
         total = total + parts[r]
-    h = W.shape[1]
-    inS = (torch.arange(h) < s).to(X.dtype)
+    inS = in_s(W.shape[1], s, X.dtype)
     return torch.stack([inS * total + (1 - inS) * parts[r] for r in range(t)])
 
 
@@ -68,7 +79,7 @@ class RowNoReduce(torch.autograd.Function):
 class ColReduce(torch.autograd.Function):
     """Column-parallel layer: A [t, N, h] (rank r's own input), W1 [h, K];
     Z[:, block r] = A_r W1[:, block r].  Backward: the input gradient of rank r is
-    P_r = dZ_r W1_r^T, reduced over the first s channels (left fold in rank order,
+    P_r = dZ_r W1_r^T, reduced over the channels of S (left fold in rank order,
     the sum given to every rank); the rest stay each rank's own."""
 
     @staticmethod
@@ -86,7 +97,7 @@ class ColReduce(torch.autograd.Function):
         total = P[0]
         for r in range(1, t):
             total = total + P[r]
-        inS = (torch.arange(W1.shape[0]) < s).to(A.dtype)
+        inS = in_s(W1.shape[0], s, A.dtype)
         dA = torch.stack([inS * total + (1 - inS) * P[r] for r in range(t)])
         dW1 = torch.cat([A[r].t() @ dZ[:, b] for r, b in enumerate(bl)], dim=1)
         return dA, dW1, None, None

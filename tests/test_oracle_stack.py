@@ -162,3 +162,58 @@ def test_column_layer_matches_c_oracle():
         wA, wW = orc.colpar_bwd(A.detach().numpy(), W1.detach().numpy(), dZ.numpy(), t, np.arange(s))
         np.testing.assert_allclose(A.grad.numpy(), wA, rtol=1e-12, atol=1e-12)
         np.testing.assert_allclose(W1.grad.numpy(), wW, rtol=1e-12, atol=1e-12)
+
+
+def test_rowpar_pcr_index_list_matches_c_oracle():
+    # S as a list of channels (a seeded random subset): the same sums as the C oracle
+    g = _r(11)
+    rng = np.random.default_rng(12)
+    for t, N, K, h, s in [(2, 5, 8, 7, 3), (4, 3, 16, 12, 5), (8, 2, 64, 24, 12)]:
+        S = np.sort(rng.permutation(h)[:s]).astype(np.int32)
+        X = torch.randn(N, K, generator=g, dtype=torch.float64)
+        W = torch.randn(K, h, generator=g, dtype=torch.float64)
+        got = ost.rowpar_pcr(X, W, t, S).numpy()
+        want, _ = orc.rowpar_fwd(X.numpy(), W.numpy(), t, S)
+        np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-12)
+        # channels outside S keep the rank's own partial: they differ between ranks
+        out = np.setdiff1d(np.arange(h), S)
+        assert np.abs(got[0][:, out] - got[1][:, out]).max() > 1e-6
+
+
+def _relabel(params, perm):
+    """The stack's parameters with the residual-stream channels renamed: new channel
+    j is old channel perm[j].  Every h-indexed axis moves: the embedding's columns,
+    the norms' gains and biases, and the rows of the four weights (QKV and MLP-up
+    read the stream, out- and down-projection write it)."""
+    out = {}
+    for k, v in params.items():
+        leaf = k.split(".")[-1]
+        if k == "emb":
+            out[k] = v[:, perm]
+        elif leaf in ("weight", "bias"):
+            out[k] = v[perm]
+        else:
+            out[k] = v[perm, :]
+    return out
+
+
+@pytest.mark.parametrize("placement", ["reduce_dout", "column"])
+def test_random_set_equals_contiguous_set_after_relabelling(placement):
+    # Every op of the block either acts channel-wise on the stream (norm gains,
+    # residual adds, the partial reduce) or sums over all its channels (norm
+    # statistics, the QKV / MLP-up contractions), so renaming the channels -- S
+    # first -- leaves the loss unchanged and renames the gradients the same way.
+    t, heads, layers, h = 2, 2, 2, 8
+    params = _tiny_params(layers=layers)
+    tokens = torch.tensor([[1, 5, 3, 9], [2, 2, 7, 0]])
+    S = np.array([1, 4, 6], dtype=np.int32)
+    perm = np.concatenate([S, np.setdiff1d(np.arange(h), S)])
+    L_r, g_r = ost.loss_and_grads(params, tokens, t, heads, layers, S, placement)
+    L_c, g_c = ost.loss_and_grads(_relabel(params, perm), tokens, t, heads, layers, len(S), placement)
+    assert abs(L_r - L_c) <= 1e-12 * abs(L_r)
+    g_rp = _relabel(g_r, perm)
+    for k in params:
+        torch.testing.assert_close(g_c[k], g_rp[k], rtol=1e-9, atol=1e-12)
+    # and the random set is not the contiguous one: the loss differs without the renaming
+    L_x, _ = ost.loss_and_grads(params, tokens, t, heads, layers, len(S), placement)
+    assert abs(L_x - L_r) > 1e-9
