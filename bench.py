@@ -772,10 +772,14 @@ def run_extras(torch, caat, device, peaks, args):
     torch.cuda.empty_cache()
     # the full 130M CAAT-Net training step (forward, backward, AdamW), both
     # placements of the backward reduce
+    # (and, default placement, with a seeded random S: the layers given its index
+    # list, then the same model relabelled so that S comes first)
     if not args.no_stack:
-        for placement in ("reduce_dout", "column"):
-            r = stack_rate(placement, steps=5, warmup=3)
-            out["130m_stack_" + placement] = {
+        for placement, layout, relabel in (("reduce_dout", "contiguous", False), ("column", "contiguous", False),
+                                           ("reduce_dout", "random", False), ("reduce_dout", "random", True)):
+            r = stack_rate(placement, steps=5, warmup=3, layout=layout, relabel=relabel)
+            key = "130m_stack_" + placement + ("" if layout == "contiguous" else "_random_S")
+            out[key + ("_relabelled" if relabel else "")] = {
                 "tokens/s": r["value"], "ms_per_step": r["ms_per_step"],
                 "gpu_launches_per_step": r["gpu_launches"] // 5, "loss_last": r["loss_last"]}
             torch.cuda.empty_cache()
@@ -946,25 +950,29 @@ STACK_METRIC = "130M CAAT-Net training step tokens/s (t=8 emulated ranks, p=0.5)
 
 def run_stack(args):
     """The full 130M block stack as the step (see stack_rate), with clocks and e2e."""
-    return stack_rate(args.placement, args.steps, args.warmup, full=True)
+    return stack_rate(args.placement, args.steps, args.warmup, full=True, layout=args.layout or "contiguous")
 
 
-def stack_rate(placement, steps, warmup, full=False):
+def stack_rate(placement, steps, warmup, full=False, layout="contiguous", relabel=False):
     """The full 130M block stack, one training step = forward, backward, AdamW:
     12 layers, 16 heads, h = 768, FFN 3072, RoPE, sequence 1024, batch 8, t = 8
     emulated ranks, p = 0.5; token ids uniform over a 32000 vocabulary; random
     N(0, 0.02) weights.  The two row-parallel layers of every block run the fused
     kernels (with --placement column, the column-parallel layers' backward with the
-    partial reduce too); attention, norms, embedding and loss are PyTorch ops."""
+    partial reduce too); attention, norms, embedding and loss are PyTorch ops.
+    layout "random": S a seeded random subset (index lists in the layers);
+    relabel: that model after relabel_channels (S first, passed by size)."""
     import torch
     import partial_activation_sync_gb300 as caat
-    from partial_activation_sync_gb300.caatnet import CAATNet, train_step
+    from partial_activation_sync_gb300.caatnet import CAATNet, relabel_channels, train_step
     torch.cuda.set_device(0)
     torch.manual_seed(5)
     vocab, batch, seq = 32000, 8, 1024
     model = CAATNet(vocab=vocab, h=768, heads=16, layers=12, ffn=3072, t=8, p=0.5, seq=seq,
-                    placement=placement)
+                    placement=placement, layout=layout, seed=4003)
     model = model.cuda().to(torch.bfloat16)
+    if relabel:
+        model, _ = relabel_channels(model)
     opt = torch.optim.AdamW(model.parameters(), lr=6e-4, fused=True)
     rng = np.random.default_rng(5005)
     host_tok = [torch.from_numpy(rng.integers(0, vocab, (batch, seq))).pin_memory()
@@ -1011,7 +1019,7 @@ def stack_rate(placement, steps, warmup, full=False):
             "data": "synthetic (token ids uniform over 32000, N(0,0.02) weights)",
             "config": {"workload": "130m_stack", "layers": 12, "heads": 16, "h": 768, "ffn": 3072,
                        "seq": seq, "batch": batch, "t": 8, "p": 0.5, "optimizer": "AdamW (fused)",
-                       "placement": placement,
+                       "placement": placement, "S": layout + (" (relabelled)" if relabel else ""),
                        "l2": "working set far above L2"},
             "gpu_launches": int(launches), "clocks": clk,
             "loss_last": round(float(out.item()), 4),

@@ -29,15 +29,23 @@ Readings where the pages are silent:
 The row-parallel and column-parallel layers run in this library's kernels;
 attention, norms, GELU, embedding and loss are PyTorch ops of the harness.  Column-parallel weights are stored [h, K] with column
 block r owned by rank r (K contiguous: the layout the library's kernels take).
-"""
-import math
 
+S is the first round(p h) channels by default, or a seeded random subset
+(layout="random"), which the layers receive as an index list.  A random S costs
+the layers a pass over their outputs (the forward) and over the upstream gradient
+(the backward) that a contiguous S does not.  relabel_channels() removes that
+cost: it renames the residual stream's channels so that S comes first, which
+gives a model with a contiguous S that computes the same loss.
+"""
+
+import numpy as np
 import torch
 import torch.nn as nn
 import torch.nn.functional as F
 
-from . import (CAAT_BWD_NO_REDUCE, CAAT_BWD_REDUCE_DOUT, colpar_linear_bwd, colpar_linear_fwd,
-               rowpar_linear_bwd, rowpar_linear_fwd)
+from . import (CAAT_BWD_NO_REDUCE, CAAT_BWD_REDUCE_DOUT, CAAT_S_CONTIGUOUS, CAAT_S_RANDOM,
+               colpar_linear_bwd, colpar_linear_fwd, rowpar_linear_bwd, rowpar_linear_fwd,
+               select_channels)
 
 
 class RowParallelPCR(torch.autograd.Function):
@@ -102,10 +110,10 @@ PLACEMENTS = ("reduce_dout", "column")
 
 
 class Block(nn.Module):
-    def __init__(self, h, heads, ffn, t, sel, std=0.02, placement="reduce_dout"):
+    def __init__(self, h, heads, ffn, t, std=0.02, placement="reduce_dout"):
         super().__init__()
         assert heads % t == 0 and ffn % t == 0 and h % heads == 0 and placement in PLACEMENTS
-        self.h, self.heads, self.ffn, self.t, self.sel = h, heads, ffn, t, sel
+        self.h, self.heads, self.ffn, self.t = h, heads, ffn, t
         self.placement = placement
         self.hd = h // heads
         self.ln1 = nn.LayerNorm(h)
@@ -117,45 +125,62 @@ class Block(nn.Module):
         self.wo = nn.Parameter(torch.randn(h, h) * std)
         self.w2 = nn.Parameter(torch.randn(h, ffn) * std)
 
-    def _colpar(self, a, W1):
+    def _colpar(self, a, W1, sel):
         """[t, N, h] -> [t, N, K/t]: rank r's input times its column block, in the
         library's column-parallel kernels.  Placement "column" reduces the input
         gradient over S; the default placement reduces nothing there (an empty S:
         each rank's input gradient is its own dZ_r W1_r^T)."""
         t, N, h = a.shape
         kt = W1.shape[1] // t
-        sel = self.sel if self.placement == "column" else 0
+        sel = sel if self.placement == "column" else 0
         return ColParallelPCR.apply(a, W1, t, sel).view(N, t, kt).transpose(0, 1)
 
-    def forward(self, x, cos, sin, batch, seq):
+    def forward(self, x, cos, sin, batch, seq, sel):
+        """x [t, N, h]: the ranks' residual streams; sel: S (a channel count or a
+        device index tensor)."""
         t, N, h = x.shape
         hpr = self.heads // t                              # heads per rank
         mode = CAAT_BWD_NO_REDUCE if self.placement == "column" else CAAT_BWD_REDUCE_DOUT
-        qkv = self._colpar(self.ln1(x), self.wqkv)         # [t, N, 3 h/t]
+        qkv = self._colpar(self.ln1(x), self.wqkv, sel)    # [t, N, 3 h/t]
         qkv = qkv.reshape(t, batch, seq, 3, hpr, self.hd).permute(3, 0, 1, 4, 2, 5)
         q, k, v = (z.reshape(t * batch, hpr, seq, self.hd) for z in qkv)
         q, k = apply_rope(q, cos, sin), apply_rope(k, cos, sin)
         o = F.scaled_dot_product_attention(q, k, v, is_causal=True)   # [t*B, hpr, S, hd]
         o = o.view(t, batch, hpr, seq, self.hd).permute(1, 3, 0, 2, 4).reshape(N, h)
-        x = x + RowParallelPCR.apply(o, self.wo.t(), t, self.sel, mode)
-        u = F.gelu(self._colpar(self.ln2(x), self.w1))     # [t, N, ffn/t]
+        x = x + RowParallelPCR.apply(o, self.wo.t(), t, sel, mode)
+        u = F.gelu(self._colpar(self.ln2(x), self.w1, sel))   # [t, N, ffn/t]
         u = u.transpose(0, 1).reshape(N, self.ffn)         # column block r = rank r
-        return x + RowParallelPCR.apply(u, self.w2.t(), t, self.sel, mode)
+        return x + RowParallelPCR.apply(u, self.w2.t(), t, sel, mode)
 
 
 class CAATNet(nn.Module):
-    """Token ids [batch, seq] -> mean next-token cross-entropy."""
+    """Token ids [batch, seq] -> mean next-token cross-entropy.
+
+    layout "contiguous": S = the first round(p h) channels, passed to the layers by
+    its size; "random": a seeded random subset of that size, passed as an index
+    list (kept as an int32 buffer that moves with the model)."""
 
     def __init__(self, vocab=32000, h=768, heads=16, layers=12, ffn=3072, t=8, p=0.5, seq=1024,
-                 std=0.02, placement="reduce_dout"):
+                 std=0.02, placement="reduce_dout", layout="contiguous", seed=0):
         super().__init__()
+        assert layout in ("contiguous", "random")
         self.t, self.h, self.heads, self.seq = t, h, heads, seq
         self.placement = placement
-        self.n_sel = int(math.floor(p * h + 0.5))          # contiguous S = first n_sel channels
+        kind = CAAT_S_RANDOM if layout == "random" else CAAT_S_CONTIGUOUS
+        self.S = select_channels(h, p, kind, seed)         # sorted channel indices of S
+        self.n_sel = int(self.S.size)
+        # an index list only where it says more than a count: 0 < |S| < h and not
+        # the first |S| channels
+        contiguous = bool(np.array_equal(self.S, np.arange(self.n_sel)))
+        self.register_buffer("sel_idx", None if contiguous else torch.from_numpy(self.S.copy()),
+                             persistent=False)
         self.emb = nn.Parameter(torch.randn(vocab, h) * std)
-        self.blocks = nn.ModuleList([Block(h, heads, ffn, t, self.n_sel, std, placement)
-                                     for _ in range(layers)])
+        self.blocks = nn.ModuleList([Block(h, heads, ffn, t, std, placement) for _ in range(layers)])
         self.ln_f = nn.LayerNorm(h)
+
+    def sel(self):
+        """S as the layers take it: the index buffer, or the count of a contiguous S."""
+        return self.sel_idx if self.sel_idx is not None else self.n_sel
 
     def forward(self, tokens):
         batch, seq = tokens.shape
@@ -163,13 +188,56 @@ class CAATNet(nn.Module):
         x0 = F.embedding(tokens.reshape(N), self.emb)      # [N, h], identical on every rank
         x = x0.unsqueeze(0).expand(self.t, N, self.h).contiguous()
         cos, sin = rope_tables(seq, self.h // self.heads, x.device, x.dtype)
+        sel = self.sel()
         for blk in self.blocks:
-            x = blk(x, cos, sin, batch, seq)
+            x = blk(x, cos, sin, batch, seq, sel)
         z = self.ln_f(x.mean(dim=0))                       # the reduction the loss needs
         logits = z @ self.emb.t()                          # tied LM head
         tgt = tokens.reshape(batch, seq)[:, 1:].reshape(-1)
         logits = logits.view(batch, seq, -1)[:, :-1].reshape(-1, logits.shape[-1])
         return F.cross_entropy(logits.float(), tgt)
+
+
+def channel_order(S, h):
+    """The renaming that puts S first: new channel j is old channel perm[j] (S in
+    ascending order, then the other channels in ascending order)."""
+    S = np.asarray(S, dtype=np.int64)
+    return np.concatenate([S, np.setdiff1d(np.arange(h), S)])
+
+
+@torch.no_grad()
+def relabel_channels(model):
+    """A model with a contiguous S (the first |S| channels) that computes the same
+    loss as ``model`` with its S, and its gradients renamed.
+
+    Every op of a block acts on the residual stream either channel by channel (the
+    norms' gains and biases, the residual adds, the partial reduce) or by summing
+    over all its channels (the norms' statistics, the QKV and MLP-up
+    contractions), so renaming the channels commutes with the model.  What moves is
+    every axis indexed by a stream channel: the embedding's columns (also the tied
+    LM head), the norms' gains and biases, and the rows of the four weights (QKV
+    and MLP-up read the stream, out- and down-projection write it).  Only the
+    order of floating-point sums over channels changes.  Returns (new model, perm)
+    with new channel j = old channel perm[j]."""
+    blk0 = model.blocks[0]
+    new = CAATNet(vocab=model.emb.shape[0], h=model.h, heads=model.heads, layers=len(model.blocks),
+                  ffn=blk0.ffn, t=model.t, p=model.n_sel / model.h, seq=model.seq,
+                  placement=model.placement, layout="contiguous")
+    assert new.n_sel == model.n_sel
+    new = new.to(device=model.emb.device, dtype=model.emb.dtype)
+    perm = channel_order(model.S, model.h)
+    ix = torch.from_numpy(perm).to(model.emb.device)
+    src = dict(model.named_parameters())
+    for name, p in new.named_parameters():
+        q = src[name]
+        leaf = name.split(".")[-1]
+        if name == "emb":
+            p.copy_(q[:, ix])
+        elif leaf in ("weight", "bias"):
+            p.copy_(q[ix])
+        else:
+            p.copy_(q[ix, :])
+    return new, perm
 
 
 def train_step(model, opt, tokens):

@@ -24,28 +24,67 @@ def _tensor_cores_only(monkeypatch):
     monkeypatch.delenv("CAAT_ALLOW_FALLBACK", raising=False)
 
 
-@pytest.mark.parametrize("placement", ["reduce_dout", "column"])
-def test_stack_loss_and_gradients_match_reference(placement):
+def _run(model, tokens):
+    """Loss (float) and gradients (float64, CPU) of one forward + backward."""
     T = torch()
-    from oracle import stack as ost
-    from partial_activation_sync_gb300.caatnet import CAATNet
     import partial_activation_sync_gb300 as caat
-    T.manual_seed(1234)
-    t, heads, layers, seq, batch, vocab = 8, 16, 2, 64, 2, 1024
-    model = CAATNet(vocab=vocab, h=768, heads=heads, layers=layers, ffn=3072, t=t, p=0.5, seq=seq,
-                    placement=placement)
-    model = model.cuda().to(T.bfloat16)
-    tokens = T.from_numpy(np.random.default_rng(7).integers(0, vocab, (batch, seq))).cuda()
+    model.zero_grad(set_to_none=True)
     loss = model(tokens)
     loss.backward()
     T.cuda.synchronize()
     assert caat.device_status() == 0
+    return float(loss.detach()), {n: p.grad.double().cpu().numpy() for n, p in model.named_parameters()}
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "random"])
+@pytest.mark.parametrize("placement", ["reduce_dout", "column"])
+def test_stack_loss_and_gradients_match_reference(placement, layout):
+    """S contiguous (the layers get its size) or a seeded random subset (the
+    layers get an index list); the reference takes the same S."""
+    T = torch()
+    from oracle import stack as ost
+    from partial_activation_sync_gb300.caatnet import CAATNet
+    T.manual_seed(1234)
+    t, heads, layers, seq, batch, vocab = 8, 16, 2, 64, 2, 1024
+    model = CAATNet(vocab=vocab, h=768, heads=heads, layers=layers, ffn=3072, t=t, p=0.5, seq=seq,
+                    placement=placement, layout=layout, seed=31)
+    model = model.cuda().to(T.bfloat16)
+    assert (model.sel_idx is None) == (layout == "contiguous")
+    tokens = T.from_numpy(np.random.default_rng(7).integers(0, vocab, (batch, seq))).cuda()
+    got_L, got_g = _run(model, tokens)
     params = {n: p.detach().double().cpu() for n, p in model.named_parameters()}
-    L, grads = ost.loss_and_grads(params, tokens.cpu(), t, heads, layers, model.n_sel, placement)
-    assert abs(float(loss.detach()) - L) <= 1e-3 * abs(L), (float(loss.detach()), L)
-    for name, p in model.named_parameters():
-        g = p.grad.double().cpu().numpy()
-        assert rel_fro(g, grads[name].numpy()) <= 2e-2, name
+    s = model.n_sel if layout == "contiguous" else model.S
+    L, grads = ost.loss_and_grads(params, tokens.cpu(), t, heads, layers, s, placement)
+    assert abs(got_L - L) <= 1e-3 * abs(L), (got_L, L)
+    for name in got_g:
+        assert rel_fro(got_g[name], grads[name].numpy()) <= 2e-2, name
+
+
+@pytest.mark.parametrize("placement", ["reduce_dout", "column"])
+def test_relabelled_model_matches_random_set(placement):
+    """relabel_channels: the model with a random S and its relabelled copy (S the
+    first |S| channels, passed by size) give the same loss, and the same gradients
+    once renamed, within the bounds above (the two run different kernels, so they
+    round differently)."""
+    T = torch()
+    from partial_activation_sync_gb300.caatnet import CAATNet, relabel_channels
+    T.manual_seed(77)
+    t, heads, layers, seq, batch, vocab = 8, 16, 2, 64, 2, 1024
+    model = CAATNet(vocab=vocab, h=768, heads=heads, layers=layers, ffn=3072, t=t, p=0.5, seq=seq,
+                    placement=placement, layout="random", seed=5).cuda().to(T.bfloat16)
+    relab, perm = relabel_channels(model)
+    assert relab.sel_idx is None and relab.n_sel == model.n_sel
+    assert np.array_equal(np.sort(perm[:model.n_sel]), model.S)
+    tokens = T.from_numpy(np.random.default_rng(8).integers(0, vocab, (batch, seq))).cuda()
+    L_r, g_r = _run(model, tokens)
+    L_c, g_c = _run(relab, tokens)
+    assert abs(L_r - L_c) <= 1e-3 * abs(L_r), (L_r, L_c)
+    for name, g in g_r.items():
+        if name == "emb":
+            g = g[:, perm]
+        else:
+            g = g[perm]          # gains, biases and the four weights: rows
+        assert rel_fro(g_c[name], g) <= 2e-2, name
 
 
 @pytest.mark.parametrize("placement", ["reduce_dout", "column"])
