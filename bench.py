@@ -688,6 +688,52 @@ def run_extras(torch, caat, device, peaks, args):
             "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4),
             "us": round(sec * 1e6, 1), "kernel": caat.last_kernel()}
         del X, Wst, Ys
+    # compact outputs (the S channels, the same on every rank, stored once): the 7B
+    # prefill forward and the 130M layers' forward + backward, p = 0.5 contiguous
+    n_sel = int(caat.select_channels(w.h, w.p).size)
+    for li, L in enumerate(w.layers):
+        X = torch.randn((w.N, L.K), device=device).to(torch.bfloat16)
+        Wst = (torch.randn((w.h, L.K), device=device) * 0.02).to(torch.bfloat16)
+        YS = torch.empty((w.N, n_sel), dtype=torch.bfloat16, device=device)
+        YN = [torch.empty((w.N, w.h - n_sel), dtype=torch.bfloat16, device=device) for _ in range(w.t)]
+        fn = lambda: caat.rowpar_linear_fwd_compact(X, Wst.t(), w.t, n_sel, YS=YS, YN=YN)  # noqa: E731
+        fn()
+        sec = _time_call(torch, fn, 10, flush)
+        tf = 2.0 * w.N * L.K * w.h / sec / 1e12
+        out["7b_prefill_compact_fwd_" + L.name] = {
+            "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4), "us": round(sec * 1e6, 1),
+            "MB_written": round(2.0 * w.N * (n_sel + w.t * (w.h - n_sel)) / 1e6, 1), "kernel": caat.last_kernel()}
+        del X, Wst, YS, YN
+    w130c = ci.WORKLOADS["130m"]
+    ns130 = int(caat.select_channels(w130c.h, w130c.p).size)
+    lay = []
+    for L in w130c.layers:
+        d = {"X": torch.randn((w130c.N, L.K), device=device).to(torch.bfloat16),
+             "W": (torch.randn((w130c.h, L.K), device=device) * 0.02).to(torch.bfloat16).t(),
+             "YS": torch.empty((w130c.N, ns130), dtype=torch.bfloat16, device=device),
+             "YN": [torch.empty((w130c.N, w130c.h - ns130), dtype=torch.bfloat16, device=device)
+                    for _ in range(w130c.t)],
+             "dYS": torch.randn((w130c.N, ns130), device=device).to(torch.bfloat16),
+             "dYN": [torch.randn((w130c.N, w130c.h - ns130), device=device).to(torch.bfloat16)
+                     for _ in range(w130c.t)],
+             "dX": torch.empty((w130c.N, L.K), dtype=torch.bfloat16, device=device),
+             "dW": torch.empty((w130c.h, L.K), dtype=torch.bfloat16, device=device).t(),
+             "ws": torch.empty(caat.rowpar_linear_bwd_workspace(w130c.t, w130c.N, L.K, w130c.h, caat.CAAT_BF16,
+                                                                caat.CAAT_BWD_NO_REDUCE),
+                               dtype=torch.uint8, device=device)}
+        lay.append(d)
+
+    def step_compact():
+        for d in lay:
+            caat.rowpar_linear_fwd_compact(d["X"], d["W"], w130c.t, ns130, YS=d["YS"], YN=d["YN"])
+            caat.rowpar_linear_bwd_compact(d["X"], d["W"], d["dYS"], d["dYN"], w130c.t, dX=d["dX"], dW=d["dW"],
+                                           workspace=d["ws"])
+    step_compact()
+    sec = _time_call(torch, step_compact, 10, flush)
+    fl = sum(6.0 * w130c.N * L.K * w130c.h for L in w130c.layers)
+    out["130m_step_compact"] = {"TFLOP/s": round(fl / sec / 1e12, 1), "ms": round(sec * 1e3, 4),
+                                "frac_bf16": round(fl / sec / 1e12 / peaks["bf16"], 4)}
+    del lay
     # 7B decode: N in {1, 8, 64} tokens, p = 0.5, contiguous S -- weight streaming (HBM
     # bound).  Each call alone (CUDA events around one launch, so the launch latency
     # is in the time), and per call inside a CUDA graph that runs the layer for 8

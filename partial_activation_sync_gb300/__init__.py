@@ -250,6 +250,81 @@ def rowpar_linear_bwd(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
     return dX, dW
 
 
+# ------------------------------------------------- compact outputs
+
+def rowpar_linear_fwd_compact(X, W, t: int, n_sel: int, YS=None, YN=None, stream=None):
+    """The fused layer with the outputs in compact form, for the contiguous
+    S = {0, ..., n_sel-1}: YS [N, n_sel] holds the S channels once (the same on
+    every rank), YN[r] [N, h - n_sel] rank r's other channels.  Returns (YS, YN)."""
+    torch = _torch()
+    N, K = X.shape
+    h = W.shape[1]
+    n_sel = int(n_sel)
+    ldx = _rowmajor(X, "X")
+    w_rs, w_cs = _weight_strides(W, K, h)
+    if W.dtype != X.dtype:
+        raise TypeError("caat: X and W must share a dtype")
+    if not 0 <= n_sel <= h:
+        raise ValueError("caat: n_sel must lie in [0, h]")
+    if YS is None:
+        YS = torch.empty((N, n_sel), dtype=X.dtype, device=X.device)
+    if YN is None:
+        YN = [torch.empty((N, h - n_sel), dtype=X.dtype, device=X.device) for _ in range(t)]
+    if len(YN) != t:
+        raise ValueError("caat: need t tensors YN")
+    _check_like(YS, (N, n_sel), X.dtype, "YS")
+    ldys = _rowmajor(YS, "YS") if YS.numel() else n_sel
+    ldyn = _same_layout(YN, (N, h - n_sel), "YN") if h > n_sel and N > 0 else h - n_sel
+    st = _lib.load().caat_rowpar_linear_fwd_compact(
+        int(t), N, K, h, _dtype_code(X), ctypes.c_void_p(X.data_ptr()), ldx,
+        ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
+        ctypes.c_void_p(YS.data_ptr()), ldys, _lib.ptr_array([y.data_ptr() for y in YN]), ldyn,
+        n_sel, _stream_ptr(stream, X))
+    _check(st, "caat_rowpar_linear_fwd_compact")
+    return YS, YN
+
+
+def rowpar_linear_bwd_compact(X, W, dYS, dYN, t: int, dX=None, dW=None, workspace=None, stream=None):
+    """Gradients of ``rowpar_linear_fwd_compact``: dYS [N, n_sel] (the gradient at
+    YS, already summed over the ranks), dYN t tensors [N, h - n_sel].  Returns
+    (dX [N, K], dW logical [K, h] in W's layout when allocated here).  workspace:
+    optional fp32 dW accumulator (allocated here when None)."""
+    torch = _torch()
+    N, K = X.shape
+    h = W.shape[1]
+    n_sel = int(dYS.shape[1])
+    ldx = _rowmajor(X, "X")
+    w_rs, w_cs = _weight_strides(W, K, h)
+    if W.dtype != X.dtype or dYS.dtype != X.dtype:
+        raise TypeError("caat: X, W and the gradients must share a dtype")
+    if len(dYN) != t:
+        raise ValueError("caat: need t tensors dYN")
+    _check_like(dYS, (N, n_sel), X.dtype, "dYS")
+    lddys = _rowmajor(dYS, "dYS") if dYS.numel() else n_sel
+    lddyn = _same_layout(dYN, (N, h - n_sel), "dYN") if h > n_sel and N > 0 else h - n_sel
+    if dX is None:
+        dX = torch.empty((N, K), dtype=X.dtype, device=X.device)
+    _check_like(dX, (N, K), X.dtype, "dX")
+    lddx = _rowmajor(dX, "dX")
+    if dW is None:
+        dW = torch.empty((h, K), dtype=X.dtype, device=X.device).t()
+    _check_like(dW, (K, h), X.dtype, "dW")
+    dw_rs, dw_cs = _weight_strides(dW, K, h)
+    dt = _dtype_code(X)
+    if workspace is None:
+        need = rowpar_linear_bwd_workspace(t, N, K, h, dt, CAAT_BWD_NO_REDUCE)
+        if need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
+    wp, wb = _workspace(workspace)
+    st = _lib.load().caat_rowpar_linear_bwd_compact(
+        int(t), N, K, h, dt, ctypes.c_void_p(X.data_ptr()), ldx,
+        ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
+        ctypes.c_void_p(dYS.data_ptr()), lddys, _lib.ptr_array([g.data_ptr() for g in dYN]), lddyn,
+        ctypes.c_void_p(dX.data_ptr()), lddx, ctypes.c_void_p(dW.data_ptr()), dw_rs, dw_cs,
+        n_sel, wp, wb, _stream_ptr(stream, X))
+    _check(st, "caat_rowpar_linear_bwd_compact")
+    return dX, dW
+
 # ------------------------------------------------- column-parallel layer
 
 def _rank_inputs(A, t: int, h: int, name: str):

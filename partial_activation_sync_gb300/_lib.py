@@ -19,6 +19,8 @@ EXPORTS = (
     "caat_rowpar_linear_bwd_workspace",
     "caat_rowpar_linear_bwd",
     "caat_rowpar_linear_bwd_noalloc",
+    "caat_rowpar_linear_fwd_compact",
+    "caat_rowpar_linear_bwd_compact",
     "caat_colpar_linear_fwd",
     "caat_colpar_linear_bwd_workspace",
     "caat_colpar_linear_bwd",
@@ -68,6 +70,16 @@ def load(path: str = None) -> ctypes.CDLL:
                                                  _c_pp, _c_i64, _c_p, _c_i64, _c_p, _c_i64, _c_i64,
                                                  _c_p, _c_i64, ctypes.c_int, _c_p]
     L.caat_rowpar_linear_bwd_noalloc.restype = ctypes.c_int
+    L.caat_rowpar_linear_fwd_compact.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
+                                                 _c_p, _c_i64, _c_p, _c_i64, _c_i64,
+                                                 _c_p, _c_i64, _c_pp, _c_i64, _c_i64, _c_p]
+    L.caat_rowpar_linear_fwd_compact.restype = ctypes.c_int
+    L.caat_rowpar_linear_bwd_compact.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
+                                                 _c_p, _c_i64, _c_p, _c_i64, _c_i64,
+                                                 _c_p, _c_i64, _c_pp, _c_i64,
+                                                 _c_p, _c_i64, _c_p, _c_i64, _c_i64,
+                                                 _c_i64, _c_p, ctypes.c_size_t, _c_p]
+    L.caat_rowpar_linear_bwd_compact.restype = ctypes.c_int
     L.caat_colpar_linear_fwd.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
                                          _c_pp, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_p]
     L.caat_colpar_linear_fwd.restype = ctypes.c_int

@@ -500,6 +500,123 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
 }
 
 
+// ------------------------------------------------- compact outputs
+// The t outputs with the S channels (the same on every rank) stored once:
+// YS [N, n_sel] and YN[r] [N, h - n_sel] for the contiguous S = {0..n_sel-1}.
+
+extern "C" caat_status caat_rowpar_linear_fwd_compact(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                                      const void *X, int64_t ldx,
+                                                      const void *W, int64_t w_rs, int64_t w_cs,
+                                                      void *YS, int64_t ldys, void *const *YN, int64_t ldyn,
+                                                      int64_t n_sel, caat_stream_t stream)
+{
+    caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, nullptr, n_sel);
+    if (st != CAAT_OK) return st;
+    const int64_t h_own = h - n_sel;
+    if (N > 0 && n_sel > 0 && (YS == nullptr || ldys < n_sel)) return CAAT_ERR_INVALID_ARG;
+    if (N > 0 && h_own > 0 && (YN == nullptr || ldyn < h_own)) return CAAT_ERR_INVALID_ARG;
+    const int64_t es = elem_size(dt);
+    MutPtrs py{};
+    if (h_own > 0)
+        for (int r = 0; r < t; ++r) {
+            if (N > 0 && YN[r] == nullptr) return CAAT_ERR_INVALID_ARG;
+            py.p[r] = YN[r];
+        }
+    {
+        const Span sx = span_of(X, N, K, ldx, es), sw = span_strided(W, K, h, w_rs, w_cs, es);
+        const Span ss = span_of(YS, N, n_sel, ldys, es);
+        if (overlap(ss, sx) || overlap(ss, sw)) return CAAT_ERR_INVALID_ARG;
+        for (int r = 0; h_own > 0 && r < t; ++r) {
+            const Span so = span_of(YN[r], N, h_own, ldyn, es);
+            if (overlap(so, ss) || overlap(so, sx) || overlap(so, sw)) return CAAT_ERR_INVALID_ARG;
+            for (int q = r + 1; q < t; ++q)
+                if (overlap(so, span_of(YN[q], N, h_own, ldyn, es))) return CAAT_ERR_INVALID_ARG;
+        }
+    }
+    if (N == 0 || h == 0) return CAAT_OK;
+    if (n_sel % 64 != 0 || dt != CAAT_BF16 || w_rs != 1) return CAAT_ERR_UNSUPPORTED;
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (K == 0) {
+        // empty sums: zeros
+        if (n_sel > 0 && cudaMemset2DAsync(YS, (size_t)(ldys * es), 0, (size_t)(n_sel * es), (size_t)N, s) != cudaSuccess)
+            return CAAT_ERR_CUDA;
+        for (int r = 0; h_own > 0 && r < t; ++r)
+            if (cudaMemset2DAsync(YN[r], (size_t)(ldyn * es), 0, (size_t)(h_own * es), (size_t)N, s) != cudaSuccess)
+                return CAAT_ERR_CUDA;
+        return CAAT_OK;
+    }
+    // with no S channel the compact form is the plain one (YN[r] = Y[r])
+    return launch_rowpar_fwd_tc(t, N, K, h, X, ldx, W, w_cs, py, ldyn, nullptr, n_sel, s,
+                                n_sel > 0 ? YS : nullptr, ldys);
+}
+
+extern "C" caat_status caat_rowpar_linear_bwd_compact(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                                      const void *X, int64_t ldx,
+                                                      const void *W, int64_t w_rs, int64_t w_cs,
+                                                      const void *dYS, int64_t lddys,
+                                                      const void *const *dYN, int64_t lddyn,
+                                                      void *dX, int64_t lddx,
+                                                      void *dW, int64_t dw_rs, int64_t dw_cs,
+                                                      int64_t n_sel, void *workspace, size_t ws_bytes,
+                                                      caat_stream_t stream)
+{
+    caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, nullptr, n_sel);
+    if (st != CAAT_OK) return st;
+    const int64_t h_own = h - n_sel;
+    if (N > 0 && n_sel > 0 && (dYS == nullptr || lddys < n_sel)) return CAAT_ERR_INVALID_ARG;
+    if (N > 0 && h_own > 0 && (dYN == nullptr || lddyn < h_own)) return CAAT_ERR_INVALID_ARG;
+    if (lddx < K || (N > 0 && K > 0 && dX == nullptr)) return CAAT_ERR_INVALID_ARG;
+    if (K > 0 && h > 0) {
+        if (dW == nullptr || dw_rs < 1 || dw_cs < 1) return CAAT_ERR_INVALID_ARG;
+        const bool ok = (dw_cs == 1 && dw_rs >= h) || (dw_rs == 1 && dw_cs >= K) ||
+                        (dw_rs >= h * dw_cs) || (dw_cs >= K * dw_rs);
+        if (!ok) return CAAT_ERR_INVALID_ARG;
+    }
+    ConstPtrs dy{};
+    if (h_own > 0)
+        for (int r = 0; r < t; ++r) {
+            if (N > 0 && dYN[r] == nullptr) return CAAT_ERR_INVALID_ARG;
+            dy.p[r] = dYN[r];
+        }
+    const int64_t es = elem_size(dt);
+    float *wacc = nullptr;
+    if (workspace != nullptr && ((uintptr_t)workspace & 255) == 0 && ws_bytes >= wacc_region_bytes(K, h, dt) &&
+        wacc_region_bytes(K, h, dt) > 0)
+        wacc = (float *)workspace;
+    {
+        const Span w_dx = span_of(dX, N, K, lddx, es);
+        const Span w_dw = span_strided(dW, K, h, dw_rs, dw_cs, es);
+        const Span w_ws = span_bytes(workspace, wacc != nullptr ? wacc_region_bytes(K, h, dt) : 0);
+        const Span outs[3] = {w_dx, w_dw, w_ws};
+        if (overlap(w_dx, w_dw) || overlap(w_dx, w_ws) || overlap(w_dw, w_ws)) return CAAT_ERR_INVALID_ARG;
+        for (const Span &o : outs) {
+            if (overlap(o, span_of(X, N, K, ldx, es)) || overlap(o, span_strided(W, K, h, w_rs, w_cs, es)) ||
+                overlap(o, span_of(dYS, N, n_sel, lddys, es)))
+                return CAAT_ERR_INVALID_ARG;
+            for (int r = 0; h_own > 0 && r < t; ++r)
+                if (overlap(o, span_of(dYN[r], N, h_own, lddyn, es))) return CAAT_ERR_INVALID_ARG;
+        }
+    }
+    if (K == 0) return CAAT_OK;                      // dX has no columns, dW no rows
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (h == 0) {                                    // no channels: dX = 0
+        if (N > 0 && cudaMemset2DAsync(dX, (size_t)(lddx * es), 0, (size_t)(K * es), (size_t)N, s) != cudaSuccess)
+            return CAAT_ERR_CUDA;
+        return CAAT_OK;
+    }
+    if (n_sel % 64 != 0 || dt != CAAT_BF16 || w_rs != 1 || dw_rs != 1) return CAAT_ERR_UNSUPPORTED;
+    if (N == 0) {                                    // empty sums over tokens: dW = 0 ([h, K] storage)
+        if (cudaMemset2DAsync(dW, (size_t)(dw_cs * es), 0, (size_t)(K * es), (size_t)h, s) != cudaSuccess)
+            return CAAT_ERR_CUDA;
+        return CAAT_OK;
+    }
+    if (!bwd_tc_supported(t, N, K, h, X, ldx, W, w_cs, dy, lddyn, dX, lddx, dW, dw_cs) ||
+        (n_sel > 0 && ((uintptr_t)dYS % 16 != 0 || lddys % 8 != 0)))
+        return CAAT_ERR_UNSUPPORTED;
+    return launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, lddyn, dX, lddx, dW, dw_cs, wacc, n_sel,
+                                n_sel > 0 ? dYS : nullptr, lddys, s, true);
+}
+
 // ------------------------------------------------- column-parallel layer
 // The column-parallel layer is the row-parallel one seen through W = W1^T
 // (logical [K, h], strides (w1_cs, w1_rs)): its forward is the dX product of the

@@ -69,10 +69,14 @@ caat_status launch_rowpar_fwd_skinny(int t, int64_t N, int64_t K, int64_t h, con
                                      const void *W, int64_t ldw, const MutPtrs &Y, int64_t ldy,
                                      const int32_t *sel, int64_t n_sel, cudaStream_t s);
 
+// YS == nullptr: the t outputs Y [N, h].  Otherwise the compact outputs (a
+// contiguous S, sel == nullptr, n_sel a multiple of 64): YS [N, n_sel] (row
+// stride ldys) once and Y = YN, t outputs [N, h - n_sel] (row stride ldy).
 caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h,
                                  const void *X, int64_t ldx, const void *W, int64_t ldw,
                                  const MutPtrs &Y, int64_t ldy,
-                                 const int32_t *sel, int64_t n_sel, cudaStream_t s);
+                                 const int32_t *sel, int64_t n_sel, cudaStream_t s,
+                                 void *YS = nullptr, int64_t ldys = 0);
 
 // ---- few-token (decode) forward on the CUDA cores (decode.cu): 1 <= N <= 64,
 // t in {1, 2, 4, 8, 16, 32}, bf16, W in the nn.Linear layout (row stride ldw).
@@ -97,7 +101,9 @@ bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int
 // wacc: fp32 scratch of h * K floats for a split reduction over tokens in dW
 // (null: no split).  s_sum > 0: channels [0, s_sum) of every rank's gradient
 // are read from the one reduced buffer dsum [N, s_sum] (row stride ld_dsum) and
-// channels [s_sum, h) from dY_r; s_sum must be a multiple of 64.
+// channels [s_sum, h) from dY_r; s_sum must be a multiple of 64.  own_compact:
+// dY_r holds only channels [s_sum, h), at columns 0 .. h - s_sum - 1 (the compact
+// form); otherwise dY_r is [N, h] and its first s_sum channels are not read.
 // per host thread and device: a second stream and a fork / join event pair for
 // running independent parts of one call side by side (null: stay on `main`)
 struct SideStream {
@@ -109,6 +115,7 @@ SideStream *side_stream(cudaStream_t main);
 caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
                                  void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
-                                 int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s);
+                                 int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s,
+                                 bool own_compact = false);
 
 }  // namespace caat

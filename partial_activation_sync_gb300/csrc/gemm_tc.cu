@@ -23,6 +23,13 @@
 // Two fp32 accumulators (256 TMEM columns apart; all 512 columns allocated)
 // alternate, so the epilogue of one accumulation overlaps the MMAs of the next.
 //
+// Compact outputs (a contiguous S of a multiple of 64 channels): the S channels
+// are written once, to YS [N, |S|], and rank r's other channels to YN[r]
+// [N, h - |S|].  Every 64-channel chunk is then all in S or all outside it: a
+// FULL_S tile stores each chunk once, a NO_S tile at its column minus |S|, and a
+// MIXED tile skips its S chunks until the last shard, which stores their sums to
+// YS (no per-rank stores of the sums).
+//
 // Warp roles: warp 0 lane 0 issues TMA loads into a 4-stage ring, warp 1 lane 0
 // issues the MMAs (warp 1 also owns the TMEM allocation), warps 2..5 drain TMEM
 // (each warp reads the 32 TMEM lanes its rank within the warp quad may access).
@@ -179,7 +186,8 @@ constexpr size_t smem_bytes()
 constexpr size_t bitmap_bytes(int64_t h) { return (size_t)((h + 31) / 32 + 2) * 4; }
 
 struct YMaps {
-    CUtensorMap m[MAX_T_TC];   // rank r's output [N, h], box 64 channels x 32 rows
+    CUtensorMap m[MAX_T_TC];   // rank r's output [N, h] (compact: [N, h - |S|]), box 64 channels x 32 rows
+    CUtensorMap s;             // compact outputs: the S channels [N, |S|], same box
 };
 
 constexpr int MAX_NB = (MAX_H_TC + 191) / 192;   // channel blocks at the narrowest tile
@@ -359,7 +367,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_f32, uint32_t hi_f32
 
 // CLN = CTAs per cluster: 1 (one CTA per tile) or 2 (a CTA pair).  Each CTA
 // fetches its own X and W tiles from this GPU's memory; no load is multicast.
-template <int CLN, int BNT, bool DEEP, bool STG2>
+// COMPACT: the compact outputs (ymaps.s and the shifted ymaps.m), a separate
+// instantiation so that the plain epilogue carries none of its branches.
+template <int CLN, int BNT, bool DEEP, bool STG2, bool COMPACT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ YMaps ymaps, const FwdParams p)
@@ -600,6 +610,8 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             tmem_st32(tb + 64u * c64, v0);
                             tmem_st32(tb + 64u * c64 + 32u, v1);
                         }
+                        // compact outputs: a MIXED shard's S chunks are still summing
+                        if (COMPACT && cls == MIXED && c0 < p.n_sel) continue;
                         // the buffer to fill: every earlier bulk group but the last has
                         // read its staging (the last one read the other buffer)
                         uint8_t *stgc = stg + sbuf * STG_BYTES;
@@ -616,10 +628,15 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                         __syncwarp();
                         if (y < p.N) {                     // same for the whole warp
                             if (lane == 0) {
-                                if (cls == FULL_S) {
-                                    for (int rr = 0; rr < p.t; ++rr) tma_store_2d(&ymaps.m[rr], stgc_a, (int)c0, y);
+                                if (COMPACT && c0 < p.n_sel) {
+                                    tma_store_2d(&ymaps.s, stgc_a, (int)c0, y);     // the sum, once
                                 } else {
-                                    tma_store_2d(&ymaps.m[r], stgc_a, (int)c0, y);
+                                    const int xc = COMPACT ? (int)(c0 - p.n_sel) : (int)c0;
+                                    if (cls == FULL_S) {
+                                        for (int rr = 0; rr < p.t; ++rr) tma_store_2d(&ymaps.m[rr], stgc_a, xc, y);
+                                    } else {
+                                        tma_store_2d(&ymaps.m[r], stgc_a, xc, y);
+                                    }
                                 }
                                 bulk_commit();
                             }
@@ -661,6 +678,25 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             }
                         }
                         uint4 *rowp = reinterpret_cast<uint4 *>(stg + lane * 128);
+                        if (COMPACT) {
+                            // an S chunk: its sums, once, to YS; any other chunk: rank
+                            // t-1's own partials (w, no S channel in it) to YN[t-1]
+                            const bool sch = c0 < p.n_sel;
+                            if (lane == 0) bulk_wait_read0();
+                            __syncwarp();
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                rowp[j ^ (lane & 7)] = sch ? make_uint4(ws[4 * j], ws[4 * j + 1], ws[4 * j + 2], ws[4 * j + 3])
+                                                           : make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0 && y < p.N) {
+                                if (sch) tma_store_2d(&ymaps.s, stg_a, (int)c0, y);
+                                else tma_store_2d(&ymaps.m[p.t - 1], stg_a, (int)(c0 - p.n_sel), y);
+                                bulk_commit();
+                            }
+                            continue;
+                        }
                         if (lane == 0) bulk_wait_read0();
                         __syncwarp();
 #pragma unroll
@@ -753,12 +789,12 @@ bool encode_3d(CUtensorMap *tm, const void *base, uint64_t d0, uint64_t d1, uint
     return encode_tmap(tm, base, 3, dims, strides, box);
 }
 
-template <int CLN, int BNT, bool DEEP = false, bool STG2 = false>
-caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMaps &ym, const FwdParams &p,
-                       cudaStream_t s)
+template <int CLN, int BNT, bool DEEP, bool STG2, bool COMPACT>
+caat_status launch_fwd_v(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMaps &ym, const FwdParams &p,
+                         cudaStream_t s)
 {
     constexpr bool PAIR = CLN > 1;
-    auto kern = rowpar_fwd_tc_kernel<CLN, BNT, DEEP, STG2>;
+    auto kern = rowpar_fwd_tc_kernel<CLN, BNT, DEEP, STG2, COMPACT>;
     static_assert(smem_bytes<CLN, BNT, DEEP, STG2>() + bitmap_bytes(192) <= 227 * 1024,
                   "shared memory beyond the per-CTA limit");
     const size_t smem = smem_bytes<CLN, BNT, DEEP, STG2>() + bitmap_bytes(p.h);
@@ -794,15 +830,26 @@ caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMa
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }
 
+template <int CLN, int BNT, bool DEEP = false, bool STG2 = false>
+caat_status launch_fwd(const CUtensorMap &tmX, const CUtensorMap &tmW, const YMaps &ym, const FwdParams &p,
+                       cudaStream_t s, bool compact)
+{
+    return compact ? launch_fwd_v<CLN, BNT, DEEP, STG2, true>(tmX, tmW, ym, p, s)
+                   : launch_fwd_v<CLN, BNT, DEEP, STG2, false>(tmX, tmW, ym, p, s);
+}
+
 }  // namespace
 
 caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const MutPtrs &Y, int64_t ldy,
-                                 const int32_t *sel, int64_t n_sel, cudaStream_t s)
+                                 const int32_t *sel, int64_t n_sel, cudaStream_t s, void *YS, int64_t ldys)
 {
     const int64_t kt = K / t;
+    const bool compact = YS != nullptr;
     // shapes and alignments this kernel takes; anything else goes to another kernel
     if (kt < BK || kt % 8 != 0 || ldx % 8 != 0 || ldw % 8 != 0 || ldy % 8 != 0) return CAAT_ERR_UNSUPPORTED;
+    if (compact && (sel != nullptr || n_sel % 64 != 0 || ldys % 8 != 0 || (uintptr_t)YS % 16 != 0))
+        return CAAT_ERR_UNSUPPORTED;
     // (h < 256 only as 192-wide single-CTA tiles)
     if (h % 8 != 0 || h < (h % 192 == 0 ? 192 : BN) || h > MAX_H_TC || N < 16 || N > (int64_t)INT32_MAX)
         return CAAT_ERR_UNSUPPORTED;
@@ -811,11 +858,20 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     for (int r = 0; r < t; ++r)
         if ((uintptr_t)Y.p[r] % 16 != 0) return CAAT_ERR_UNSUPPORTED;
     YMaps ym;
+    const int64_t h_out = compact ? h - n_sel : h;     // channels of each rank's own output
     for (int r = 0; r < t; ++r) {
-        const uint64_t dims[2] = {(uint64_t)h, (uint64_t)N};
+        if (h_out == 0) { ym.m[r] = CUtensorMap{}; continue; }   // (never stored to)
+        const uint64_t dims[2] = {(uint64_t)h_out, (uint64_t)N};
         const uint64_t str[1] = {(uint64_t)ldy * 2};
         const uint32_t box[2] = {64, 32};
         if (!encode_tmap(&ym.m[r], Y.p[r], 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
+    }
+    ym.s = CUtensorMap{};
+    if (compact && n_sel > 0) {
+        const uint64_t dims[2] = {(uint64_t)n_sel, (uint64_t)N};
+        const uint64_t str[1] = {(uint64_t)ldys * 2};
+        const uint32_t box[2] = {64, 32};
+        if (!encode_tmap(&ym.s, YS, 2, dims, str, box)) return CAAT_ERR_UNSUPPORTED;
     }
     // CTAs per cluster: a CTA pair when there are at least two 128-row blocks,
     // else one CTA per tile.  Short shards (k_t <= 384) make the t output copies
@@ -926,18 +982,21 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
             return CAAT_ERR_UNSUPPORTED;
         caat_status st;
         if (bn == 192)
-            st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s)
-               : (p.nkb >= 4 ? launch_fwd<1, 192, true>(tmX, tmW, ym, p, s) : launch_fwd<1, 192>(tmX, tmW, ym, p, s));
+            st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s, compact)
+               : (p.nkb >= 4 ? launch_fwd<1, 192, true>(tmX, tmW, ym, p, s, compact)
+                             : launch_fwd<1, 192>(tmX, tmW, ym, p, s, compact));
         else {
             // two staging buffers where the bitmap leaves room (CAAT_FWD_STG=1: one)
             const char *stg_env = std::getenv("CAAT_FWD_STG");
             const bool one = stg_env != nullptr && stg_env[0] == '1';
             if (cln == 2) {
                 const bool stg2 = !one && smem_bytes<2, BN, false, true>() + bitmap_bytes(h) <= 227 * 1024;
-                st = stg2 ? launch_fwd<2, BN, false, true>(tmX, tmW, ym, p, s) : launch_fwd<2, BN>(tmX, tmW, ym, p, s);
+                st = stg2 ? launch_fwd<2, BN, false, true>(tmX, tmW, ym, p, s, compact)
+                          : launch_fwd<2, BN>(tmX, tmW, ym, p, s, compact);
             } else {
                 const bool stg2 = !one && smem_bytes<1, BN, false, true>() + bitmap_bytes(h) <= 227 * 1024;
-                st = stg2 ? launch_fwd<1, BN, false, true>(tmX, tmW, ym, p, s) : launch_fwd<1, BN>(tmX, tmW, ym, p, s);
+                st = stg2 ? launch_fwd<1, BN, false, true>(tmX, tmW, ym, p, s, compact)
+                          : launch_fwd<1, BN>(tmX, tmW, ym, p, s, compact);
             }
         }
         if (st == CAAT_OK && pieces_then_reduce) {

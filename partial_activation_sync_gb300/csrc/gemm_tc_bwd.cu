@@ -585,21 +585,24 @@ bool bwd_tc_supported(int t, int64_t N, int64_t K, int64_t h, const void *X, int
 caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
                                  void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
-                                 int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s)
+                                 int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s,
+                                 bool own_compact)
 {
     const int64_t kt = K / t;
     if (s_sum < 0 || s_sum > h || s_sum % 64 != 0 || (s_sum > 0 && dsum == nullptr)) return CAAT_ERR_UNSUPPORTED;
     const int64_t h_own = h - s_sum;           // channels read from each rank's own gradient
 
-    // A-operand maps: rank r's gradient from channel s_sum on (each rank), and the
-    // reduced sum of channels [0, s_sum) (box shapes differ between dX and dW)
+    // A-operand maps: rank r's gradient from channel s_sum on (each rank; in the
+    // compact form its columns start there), and the reduced sum of channels
+    // [0, s_sum) (box shapes differ between dX and dW)
     auto grad_maps = [&](TmapArray &am, CUtensorMap &sm, uint32_t box0, uint32_t box1) -> bool {
         for (int r = 0; r < t; ++r) {
             if (h_own == 0) { am.m[r] = CUtensorMap{}; continue; }
             const uint64_t dims[2] = {(uint64_t)h_own, (uint64_t)N};
             const uint64_t str[1] = {(uint64_t)ld_dy * 2};
             const uint32_t box[2] = {box0, box1};
-            if (!encode_tmap(&am.m[r], (const uint16_t *)dY.p[r] + s_sum, 2, dims, str, box)) return false;
+            const uint16_t *own = (const uint16_t *)dY.p[r] + (own_compact ? 0 : s_sum);
+            if (!encode_tmap(&am.m[r], own, 2, dims, str, box)) return false;
         }
         if (s_sum == 0) { sm = am.m[0]; return true; }
         const uint64_t dims[2] = {(uint64_t)s_sum, (uint64_t)N};

@@ -147,6 +147,37 @@ def test_layer_rejects_bad_args_without_launch(lib):
              sel, 2, 0, ws, 768, None) == 1
 
 
+def test_compact_layer_rejects_bad_args_without_launch(lib):
+    # compact outputs: YS [4, n_sel] and YN[r] [4, 8 - n_sel]; fake device pointers,
+    # every case returns before anything touches the device
+    X, W, YS, Y0, Y1 = 1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20
+    f = lib.caat_rowpar_linear_fwd_compact
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, 2, None) == 2   # n_sel % 64
+    assert f(2, 4, 8, 8, 0, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, 2, None) == 2   # fp32
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 1, _ptrs([Y0, Y1]), 6, 2, None) == 1   # ldys < n_sel
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 5, 2, None) == 1   # ldyn < h - n_sel
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, None, 2, _ptrs([Y0, Y1]), 6, 2, None) == 1  # no YS
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, YS + 8]), 6, 2, None) == 1   # YN over YS
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y0 + 4]), 6, 2, None) == 1   # YN overlap
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, X + 2, 2, _ptrs([Y0, Y1]), 6, 2, None) == 1    # YS over X
+    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, 9, None) == 1       # n_sel > h
+    g = lib.caat_rowpar_linear_bwd_compact
+    dX, dW = 6 << 20, 7 << 20
+    ok = (2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, dX, 8, dW, 1, 8, 2, None, 0, None)
+    assert g(*ok) == 2                                                             # n_sel % 64
+    bad = list(ok); bad[11] = 1
+    assert g(*bad) == 1                                                            # lddys < n_sel
+    bad = list(ok); bad[13] = 5
+    assert g(*bad) == 1                                                            # lddyn < h - n_sel
+    bad = list(ok); bad[14] = YS + 4
+    assert g(*bad) == 1                                                            # dX over dYS
+    bad = list(ok); bad[16] = Y1 + 8
+    assert g(*bad) == 1                                                            # dW over a dYN
+    bad = list(ok); bad[16] = dX + 16
+    assert g(*bad) == 1                                                            # dX and dW overlap
+    bad = list(ok); bad[12] = None
+    assert g(*bad) == 1                                                            # no dYN
+
 def test_colpar_rejects_bad_args_without_launch(lib):
     A0, A1, W1, Z = 1 << 20, 2 << 20, 3 << 20, 4 << 20
     sel = ctypes.c_void_p(5 << 20)
