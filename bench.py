@@ -157,6 +157,32 @@ class LayerData:
         self.flops_bwd = 4.0 * w.N * L.K * w.h if w.backward else 0.0
         self.bytes_fwd = 2.0 * (w.N * L.K + L.K * w.h + w.t * w.N * w.h)
 
+    def make_compact(self, torch, w, S, device):
+        """Compact outputs (the S channels once, YS, and each rank's others, YN[r])
+        in place of Y, and the gradient in the same form: dYS = the sum over ranks
+        of G_r on S, dYN[r] = G_r outside S (device tensors and host words)."""
+        bf = torch.bfloat16
+        U = np.setdiff1d(np.arange(w.h), S)
+        ns = int(S.size)
+        self.Y = None
+        self.YS = torch.empty((w.N, ns), dtype=bf, device=device)
+        self.YN = [torch.empty((w.N, w.h - ns), dtype=bf, device=device) for _ in range(w.t)]
+        self.bytes_fwd = 2.0 * (w.N * self.K + self.K * w.h + w.N * ns + w.t * w.N * (w.h - ns))
+        if self.G_host is None:
+            return
+        G = [ci.words_to_f32(g) for g in self.G_host]
+        gs = np.zeros((w.N, ns), dtype=np.float32)
+        for g in G:
+            gs += g[:, S]
+        self.dYS_host = ci.bf16_words(gs)
+        self.dYN_host = [ci.bf16_words(np.ascontiguousarray(g[:, U])) for g in G]
+
+        def dev(a):
+            return torch.from_numpy(a.view(np.int16)).to(device).view(bf)
+        self.dYS = dev(self.dYS_host)
+        self.dYN = [dev(a) for a in self.dYN_host]
+        self.G = None
+
 
 def job_rate(dist, device, ms_local, flops_per_step, steps):
     """Whole-job time and throughput of a weak-scaling run: every rank did
@@ -194,14 +220,24 @@ class LayerStep:
     then its backward when the workload trains), recording an event before each
     call and one after the last."""
 
-    def __init__(self, torch, caat, w, device):
+    def __init__(self, torch, caat, w, device, compact=False):
         self.torch, self.caat, self.w = torch, caat, w
+        self.compact = compact
         S = caat.select_channels(w.h, w.p, w.layout, w.seeds()["perm"])
         # a contiguous S is passed by its size (the library's null-index form)
         self.sel = int(S.size) if w.layout == 0 else torch.from_numpy(S).to(device)
         self.layers = [LayerData(torch, w, i, device) for i in range(len(w.layers))]
         ws_bytes = max([caat.rowpar_linear_bwd_workspace(w.t, w.N, L.K, w.h, 1, 0) for L in w.layers] + [256])
         self.ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+        self.wsf = self.ws
+        if compact:
+            idx = w.layout != 0 and 0 < S.size < w.h
+            for L in self.layers:
+                L.make_compact(torch, w, S, device)
+            self.wsf = torch.empty(max([caat.rowpar_linear_compact_workspace(w.t, w.N, L.K, w.h, 1, idx, False)
+                                        for L in w.layers] + [256]), dtype=torch.uint8, device=device)
+            self.ws = torch.empty(max([caat.rowpar_linear_compact_workspace(w.t, w.N, L.K, w.h, 1, idx, True)
+                                       for L in w.layers] + [256]), dtype=torch.uint8, device=device)
         self.names = []
         for L in self.layers:
             self.names.append("fwd_" + L.name)
@@ -215,12 +251,19 @@ class LayerStep:
         for L in self.layers:
             if evs is not None:
                 evs[k].record(stream); k += 1
-            caat.rowpar_linear_fwd(L.X, L.W, w.t, self.sel, outs=L.Y)
+            if self.compact:
+                caat.rowpar_linear_fwd_compact(L.X, L.W, w.t, self.sel, YS=L.YS, YN=L.YN, workspace=self.wsf)
+            else:
+                caat.rowpar_linear_fwd(L.X, L.W, w.t, self.sel, outs=L.Y)
             if w.backward:
                 if evs is not None:
                     evs[k].record(stream); k += 1
-                caat.rowpar_linear_bwd(L.X, L.W, L.G, w.t, self.sel, caat.CAAT_BWD_REDUCE_DOUT,
-                                       dX=L.dX, dW=L.dW, workspace=self.ws)
+                if self.compact:
+                    caat.rowpar_linear_bwd_compact(L.X, L.W, L.dYS, L.dYN, w.t, sel=self.sel, dX=L.dX, dW=L.dW,
+                                                   workspace=self.ws)
+                else:
+                    caat.rowpar_linear_bwd(L.X, L.W, L.G, w.t, self.sel, caat.CAAT_BWD_REDUCE_DOUT,
+                                           dX=L.dX, dW=L.dW, workspace=self.ws)
         if evs is not None:
             evs[k].record(stream)
 
@@ -369,7 +412,8 @@ def roofline_of(ls, per_call, steps, peaks, kernel_name):
         roof["peak_kind"] = "copy bandwidth (read + write)"
     roof["peak_source"] = "of measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "of fallback"
     # DRAM counters exist for the one-GPU launch configuration only
-    roof["traffic"] = DRAM_TRAFFIC.get((w.name, Ld.name)) if isinstance(ls, LayerStep) else None
+    roof["traffic"] = (DRAM_TRAFFIC.get((w.name, Ld.name))
+                       if isinstance(ls, LayerStep) and not ls.compact else None)
     roof["algorithmic_per_launch"] = {"flops": Ld.flops_fwd, "bytes": Ld.bytes_fwd}
     roof["us_per_launch"] = round(t_dom * 1e6, 2)
     return roof
@@ -384,7 +428,8 @@ def run_gpu(args, w):
     # one GPU: the t ranks emulated in its memory; several: the ranks spread over
     # the GPUs, with the partial channel-reduce across them (strong scaling: the
     # layer is the same whatever the GPU count)
-    ls = LayerStep(torch, caat, w, device) if world == 1 else TPStep(torch, caat, w, device, rank, world)
+    compact = bool(args.compact) and world == 1      # the compact outputs are a one-GPU form
+    ls = LayerStep(torch, caat, w, device, compact) if world == 1 else TPStep(torch, caat, w, device, rank, world)
     clocks = ClockSampler(device.index)
     per_call, launches, clk = time_steps(torch, caat, ls, args.steps, args.warmup, device, dist, clocks)
     kernel_name = caat.last_kernel()
@@ -403,6 +448,8 @@ def run_gpu(args, w):
         "config": {"workload": w.name, "t": w.t, "N": w.N, "h": w.h,
                    "layers": {L.name: L.K for L in ls.layers}, "p": w.p,
                    "S": "contiguous" if w.layout == 0 else "random",
+                   "outputs": ("compact: the S channels once [N, |S|] + each rank's other channels "
+                               "[N, h - |S|]" if compact else "t full rank outputs [N, h]"),
                    "fwd_and_bwd": bool(w.backward),
                    "l2": "flushed between timed steps by reading a 2x L2 buffer (untimed)",
                    "timing": "CUDA events around each call of a step; an untimed spin kernel before "
@@ -419,7 +466,8 @@ def run_gpu(args, w):
 
     # end to end through the public API with host buffers (pinned), per step
     if world == 1:
-        result["e2e"] = run_e2e(torch, caat, w, ls.layers, ls.sel, ls.ws, args, device, dist)
+        result["e2e"] = run_e2e(torch, caat, w, ls.layers, ls.sel, ls.ws, args, device, dist,
+                                compact=compact, wsf=ls.wsf)
     else:
         result["e2e"] = run_e2e_tp(torch, ls, args, device, dist)
     del ls
@@ -434,10 +482,12 @@ def run_gpu(args, w):
     return result if rank == 0 else None
 
 
-def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
+def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist, compact=False, wsf=None):
     """End to end through the public API with host buffers: every step copies its
     inputs (X and the t upstream gradients of every layer) from pinned host memory
     and reads its results (dX and dW; without a backward, all t rank outputs) back.
+    compact: the compact calls, whose outputs (and gradients) hold the S channels
+    once: YS and the t YN[r] come back, dYS and the t dYN[r] go in.
 
     The copies run on their own streams and overlap the compute of the neighbouring
     steps: step i+1's inputs go in while step i computes, and step i-1's results come
@@ -447,19 +497,27 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
     h2d_s = torch.cuda.Stream(device=device)
     d2h_s = torch.cuda.Stream(device=device)
     hostX = [torch.from_numpy(L.X_host.view(np.int16)).pin_memory() for L in layers]
-    hostG = [[torch.from_numpy(g.view(np.int16)).pin_memory() for g in L.G_host]
-             if w.backward else [] for L in layers]
+    if compact:
+        # [dYS, dYN[0], ..., dYN[t-1]] per layer
+        hostG = [[torch.from_numpy(a.view(np.int16)).pin_memory() for a in [L.dYS_host] + L.dYN_host]
+                 if w.backward else [] for L in layers]
+    else:
+        hostG = [[torch.from_numpy(g.view(np.int16)).pin_memory() for g in L.G_host]
+                 if w.backward else [] for L in layers]
 
     def dev_set(own):
         """One device buffer set per layer: the layer's own buffers, or fresh ones."""
         out = []
         for L in layers:
+            # the device gradients in the order of hostG; the outputs that come back
+            G = ([L.dYS] + L.dYN if w.backward else []) if compact else (L.G or [])
+            Y = [L.YS] + L.YN if compact else L.Y
             if own:
-                out.append({"X": L.X, "G": L.G, "Y": L.Y, "dX": L.dX, "dW": L.dW, "dWs": L.dWstore})
+                out.append({"X": L.X, "G": G, "Y": Y, "dX": L.dX, "dW": L.dW, "dWs": L.dWstore})
                 continue
             dWs = torch.empty_like(L.dWstore)
-            out.append({"X": torch.empty_like(L.X), "G": [torch.empty_like(g) for g in (L.G or [])],
-                        "Y": [torch.empty_like(y) for y in L.Y], "dX": torch.empty_like(L.dX),
+            out.append({"X": torch.empty_like(L.X), "G": [torch.empty_like(g) for g in G],
+                        "Y": [torch.empty_like(y) for y in Y], "dX": torch.empty_like(L.dX),
                         "dW": dWs.t(),
                         "dWs": dWs})
         return out
@@ -467,14 +525,14 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
     sets = [dev_set(True), dev_set(False)]
     outs = [[{"dX": torch.empty(L.dX.shape, dtype=torch.int16).pin_memory(),
               "dW": torch.empty(L.dWstore.shape, dtype=torch.int16).pin_memory(),
-              "Y": ([torch.empty(y.shape, dtype=torch.int16).pin_memory() for y in L.Y]
-                    if not w.backward else [])} for L in layers]
+              "Y": ([torch.empty(y.shape, dtype=torch.int16).pin_memory() for y in sets[0][li]["Y"]]
+                    if not w.backward else [])} for li, L in enumerate(layers)]
             for _ in range(2)]
     h2d = sum(x.numel() * 2 for x in hostX) + sum(g.numel() * 2 for gs in hostG for g in gs)
     if w.backward:
         d2h = sum(L.dX.numel() * 2 + L.dWstore.numel() * 2 for L in layers)
     else:
-        d2h = sum(y.numel() * 2 for L in layers for y in L.Y)
+        d2h = sum(y.numel() * 2 for st in sets[0] for y in st["Y"])
     in_ready = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
     out_done = [torch.cuda.Event() for _ in range(2)]
@@ -495,6 +553,12 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
             comp.wait_event(out_done[j])                # step i-2's results have been read
         for li in range(len(layers)):
             L, B = layers[li], S[li]
+            if compact:
+                caat.rowpar_linear_fwd_compact(B["X"], L.W, w.t, sel, YS=B["Y"][0], YN=B["Y"][1:], workspace=wsf)
+                if w.backward:
+                    caat.rowpar_linear_bwd_compact(B["X"], L.W, B["G"][0], B["G"][1:], w.t, sel=sel, dX=B["dX"],
+                                                   dW=B["dW"], workspace=ws)
+                continue
             caat.rowpar_linear_fwd(B["X"], L.W, w.t, sel, outs=B["Y"])
             if w.backward:
                 caat.rowpar_linear_bwd(B["X"], L.W, B["G"], w.t, sel, caat.CAAT_BWD_REDUCE_DOUT,
@@ -508,7 +572,7 @@ def run_e2e(torch, caat, w, layers, sel, ws, args, device, dist):
                     O[li]["dX"].copy_(B["dX"].view(torch.int16), non_blocking=True)
                     O[li]["dW"].copy_(B["dWs"].view(torch.int16), non_blocking=True)
                 else:
-                    for r in range(w.t):
+                    for r in range(len(B["Y"])):
                         O[li]["Y"][r].copy_(B["Y"][r].view(torch.int16), non_blocking=True)
             out_done[j].record(d2h_s)
 
@@ -609,6 +673,46 @@ def _time_call(torch, fn, reps, flush=None):
     return statistics.median(a.elapsed_time(b) for a, b in ts) * 1e-3
 
 
+def _compact_step(torch, caat, w, device, flush, peaks, random_s):
+    """Forward + backward of the workload's layers with compact outputs (S stored
+    once; the gradient at it already summed over the ranks), p = w.p.  Returns
+    TFLOP/s (6 N K h per layer) and ms per step, median of 10, L2 flushed."""
+    S = caat.select_channels(w.h, w.p, caat.CAAT_S_RANDOM if random_s else caat.CAAT_S_CONTIGUOUS,
+                             w.seeds()["perm"])
+    ns = int(S.size)
+    sel = torch.from_numpy(S).to(device) if random_s else ns
+    lay = []
+    for L in w.layers:
+        lay.append({
+            "X": torch.randn((w.N, L.K), device=device).to(torch.bfloat16),
+            "W": (torch.randn((w.h, L.K), device=device) * 0.02).to(torch.bfloat16).t(),
+            "YS": torch.empty((w.N, ns), dtype=torch.bfloat16, device=device),
+            "YN": [torch.empty((w.N, w.h - ns), dtype=torch.bfloat16, device=device) for _ in range(w.t)],
+            "dYS": torch.randn((w.N, ns), device=device).to(torch.bfloat16),
+            "dYN": [torch.randn((w.N, w.h - ns), device=device).to(torch.bfloat16) for _ in range(w.t)],
+            "dX": torch.empty((w.N, L.K), dtype=torch.bfloat16, device=device),
+            "dW": torch.empty((w.h, L.K), dtype=torch.bfloat16, device=device).t(),
+            "wsf": torch.empty(max(caat.rowpar_linear_compact_workspace(w.t, w.N, L.K, w.h, caat.CAAT_BF16,
+                                                                        random_s, False), 1),
+                               dtype=torch.uint8, device=device),
+            "wsb": torch.empty(caat.rowpar_linear_compact_workspace(w.t, w.N, L.K, w.h, caat.CAAT_BF16,
+                                                                    random_s, True),
+                               dtype=torch.uint8, device=device)})
+
+    def step():
+        for d in lay:
+            caat.rowpar_linear_fwd_compact(d["X"], d["W"], w.t, sel, YS=d["YS"], YN=d["YN"], workspace=d["wsf"])
+            caat.rowpar_linear_bwd_compact(d["X"], d["W"], d["dYS"], d["dYN"], w.t, sel=sel, dX=d["dX"],
+                                           dW=d["dW"], workspace=d["wsb"])
+    step()
+    sec = _time_call(torch, step, 10, flush)
+    fl = sum(6.0 * w.N * L.K * w.h for L in w.layers)
+    del lay
+    torch.cuda.empty_cache()
+    return {"TFLOP/s": round(fl / sec / 1e12, 1), "ms": round(sec * 1e3, 4),
+            "frac_bf16": round(fl / sec / 1e12 / peaks["bf16"], 4), "S": "random" if random_s else "contiguous"}
+
+
 def run_extras(torch, caat, device, peaks, args):
     """Side measurements next to the headline step: the 130M-shaped training step
     (forward and backward of both row-parallel layers) with its own roofline, the
@@ -704,36 +808,12 @@ def run_extras(torch, caat, device, peaks, args):
             "TFLOP/s": round(tf, 1), "frac_bf16": round(tf / peaks["bf16"], 4), "us": round(sec * 1e6, 1),
             "MB_written": round(2.0 * w.N * (n_sel + w.t * (w.h - n_sel)) / 1e6, 1), "kernel": caat.last_kernel()}
         del X, Wst, YS, YN
-    w130c = ci.WORKLOADS["130m"]
-    ns130 = int(caat.select_channels(w130c.h, w130c.p).size)
-    lay = []
-    for L in w130c.layers:
-        d = {"X": torch.randn((w130c.N, L.K), device=device).to(torch.bfloat16),
-             "W": (torch.randn((w130c.h, L.K), device=device) * 0.02).to(torch.bfloat16).t(),
-             "YS": torch.empty((w130c.N, ns130), dtype=torch.bfloat16, device=device),
-             "YN": [torch.empty((w130c.N, w130c.h - ns130), dtype=torch.bfloat16, device=device)
-                    for _ in range(w130c.t)],
-             "dYS": torch.randn((w130c.N, ns130), device=device).to(torch.bfloat16),
-             "dYN": [torch.randn((w130c.N, w130c.h - ns130), device=device).to(torch.bfloat16)
-                     for _ in range(w130c.t)],
-             "dX": torch.empty((w130c.N, L.K), dtype=torch.bfloat16, device=device),
-             "dW": torch.empty((w130c.h, L.K), dtype=torch.bfloat16, device=device).t(),
-             "ws": torch.empty(caat.rowpar_linear_bwd_workspace(w130c.t, w130c.N, L.K, w130c.h, caat.CAAT_BF16,
-                                                                caat.CAAT_BWD_NO_REDUCE),
-                               dtype=torch.uint8, device=device)}
-        lay.append(d)
-
-    def step_compact():
-        for d in lay:
-            caat.rowpar_linear_fwd_compact(d["X"], d["W"], w130c.t, ns130, YS=d["YS"], YN=d["YN"])
-            caat.rowpar_linear_bwd_compact(d["X"], d["W"], d["dYS"], d["dYN"], w130c.t, dX=d["dX"], dW=d["dW"],
-                                           workspace=d["ws"])
-    step_compact()
-    sec = _time_call(torch, step_compact, 10, flush)
-    fl = sum(6.0 * w130c.N * L.K * w130c.h for L in w130c.layers)
-    out["130m_step_compact"] = {"TFLOP/s": round(fl / sec / 1e12, 1), "ms": round(sec * 1e3, 4),
-                                "frac_bf16": round(fl / sec / 1e12 / peaks["bf16"], 4)}
-    del lay
+    out["130m_step_compact"] = _compact_step(torch, caat, ci.WORKLOADS["130m"], device, flush, peaks, False)
+    # the 1.1B layers, S contiguous and a seeded random S (index lists: W's channels
+    # renamed S-first once per call, dW's rows put back)
+    for rnd in (False, True):
+        out["1.1b_step_compact_" + ("random_S" if rnd else "contiguous_S")] = _compact_step(
+            torch, caat, ci.WORKLOADS["1.1b"], device, flush, peaks, rnd)
     # 7B decode: N in {1, 8, 64} tokens, p = 0.5, contiguous S -- weight streaming (HBM
     # bound).  Each call alone (CUDA events around one launch, so the launch latency
     # is in the time), and per call inside a CUDA graph that runs the layer for 8
@@ -1084,6 +1164,8 @@ def main():
     ap.add_argument("--layout", choices=["contiguous", "random"], default=None,
                     help="channel-set layout (default: the workload's own)")
     ap.add_argument("--p", type=float, default=None, help="synchronized fraction (default: workload's)")
+    ap.add_argument("--compact", action="store_true",
+                    help="layer workloads with compact outputs: the S channels stored once (one GPU)")
     ap.add_argument("--t", type=int, default=None, help="tensor-parallel ranks (default: the workload's 8)")
     ap.add_argument("--placement", choices=["reduce_dout", "column"], default="reduce_dout",
                     help="130m_stack: where the backward reduce sits")

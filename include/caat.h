@@ -236,31 +236,39 @@ caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64_t h, caat_
  *
  * Paper: Introduction (PCR: every rank gets the sum on S and keeps its own
  * partial elsewhere).  With the t ranks' outputs in one GPU's memory the t copies
- * of the S channels carry nothing beyond one of them.  For the contiguous
- * S = {0, ..., n_sel-1} this call writes
- *   YS[n, j]    = Y[r][n, j]            for j <  n_sel       (the same for every r)
- *   YN[r][n, j] = Y[r][n, n_sel + j]    for j <  h - n_sel
- * with Y[r] as defined for caat_rowpar_linear_fwd: N*n_sel + t*N*(h-n_sel)
- * elements written instead of t*N*h.  (An index list of S becomes this form by
- * renaming the channels so that S comes first: W's channels permuted, and the
- * consumer of the outputs renamed likewise.)
+ * of the S channels carry nothing beyond one of them.  With S = {s_0 < s_1 < ...}
+ * and its complement {u_0 < u_1 < ...} this call writes
+ *   YS[n, j]    = Y[r][n, s_j]      (the same for every r)
+ *   YN[r][n, j] = Y[r][n, u_j]
+ * with Y[r] as defined for caat_rowpar_linear_fwd: N*|S| + t*N*(h-|S|) elements
+ * written instead of t*N*h.
  * YS:    device [N, n_sel], row stride ldys (unused when n_sel == 0).
  * YN:    host array of t device pointers, each [N, h - n_sel], row stride ldyn
- *        (unused when n_sel == h).  No output may overlap another, X or W.
- * n_sel: |S| in [0, h]; a multiple of 64 (else UNSUPPORTED), so that every
+ *        (unused when n_sel == h).  No output may overlap another, X, W, sel or
+ *        the workspace.
+ * sel, n_sel: S as for caat_rowpar_linear_fwd (null: the first n_sel channels).
+ *        n_sel must be a multiple of 64 (else UNSUPPORTED), so that every
  *        64-channel chunk of a tile lies in S or outside it.
+ * workspace: required only for an index list with 0 < n_sel < h: a copy of W
+ *        with its channels in the order "S first" (which makes S contiguous for
+ *        the kernel), h*K*2 bytes, 256-byte aligned;
+ *        caat_rowpar_linear_compact_workspace(..., index_list = 1, backward = 0)
+ *        gives the size.  Else it may be null.  The copy costs one read and one
+ *        write of W per call.
  * Kernel: the tensor-core tile kernel only: bf16, W in the nn.Linear layout
  *        (w_rs == 1), N >= 16, k_t >= 64 and a multiple of 8, 16-byte aligned
  *        bases, row strides that are multiples of 8 elements.  Other shapes return
- *        UNSUPPORTED (the few-token kernels have no compact form).
- * Errors: INVALID_ARG as caat_rowpar_linear_fwd (null or short outputs,
- *        overlaps); UNSUPPORTED as above.
+ *        UNSUPPORTED (the few-token kernels have no compact form); with an index
+ *        list the workspace may have been written by then.
+ * Errors: INVALID_ARG as caat_rowpar_linear_fwd (null or short outputs, overlaps,
+ *        a workspace that is missing, short or misaligned); UNSUPPORTED as above.
  */
 caat_status caat_rowpar_linear_fwd_compact(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
                                            const void *X, int64_t ldx,
                                            const void *W, int64_t w_rs, int64_t w_cs,
                                            void *YS, int64_t ldys, void *const *YN, int64_t ldyn,
-                                           int64_t n_sel, caat_stream_t stream);
+                                           const int32_t *sel, int64_t n_sel,
+                                           void *workspace, size_t ws_bytes, caat_stream_t stream);
 
 /*
  * caat_rowpar_linear_bwd_compact -- gradients of caat_rowpar_linear_fwd_compact.
@@ -270,19 +278,25 @@ caat_status caat_rowpar_linear_fwd_compact(int t, int64_t N, int64_t K, int64_t 
  *      over the ranks of their gradients on S.
  * dYN: host array of t device pointers, each [N, h - n_sel], row stride lddyn:
  *      the gradient arriving at YN[r].
- * With dY_r = [dYS | dYN[r]] in channel order this writes
+ * With dY_r the [N, h] gradient that holds dYS on the channels of S and dYN[r] on
+ * the others (each in ascending channel order) this writes
  *   dX[:, shard r] = dY_r W_r^T   and   dW[shard r, :] = X_r^T dY_r,
  * which is caat_rowpar_linear_bwd in CAAT_BWD_REDUCE_DOUT mode for any dOut whose
  * S channels sum over the ranks to dYS and whose other channels are dYN[r]: the
- * reduce of the gradient has already happened, and no workspace is required.
- * workspace: optional fp32 accumulator of dW, [h, K], 256-byte aligned, of
- *      caat_rowpar_linear_bwd_workspace(t, N, K, h, dt, CAAT_BWD_NO_REDUCE) bytes;
- *      with it dW is reduced over tokens in several parts, then rounded once.
+ * reduce of the gradient has already happened.
+ * workspace: 256-byte aligned, caat_rowpar_linear_compact_workspace(..., backward
+ *      = 1) bytes.  For an index list with 0 < n_sel < h it starts with two
+ *      required parts of h*K*2 bytes each (rounded to 256): W in the S-first
+ *      order, and room to stage dW in that order before its rows return to
+ *      channel order.  Then, for any S, the optional fp32 accumulator of dW,
+ *      h*K*4 bytes rounded to 256.  With the accumulator, dW is reduced over
+ *      tokens in several parts when its tiles leave at least half of the SMs
+ *      idle; then rounded once.  With a contiguous S the workspace may be null.
  * Kernel: the tensor-core backward only: bf16, W and dW in the nn.Linear layout
  *      (w_rs == dw_rs == 1), N >= 128, h >= 256, n_sel a multiple of 64, the TMA
  *      alignment rules; else UNSUPPORTED.
  * Errors: INVALID_ARG as caat_rowpar_linear_bwd (dX, dW and the workspace must not
- *      overlap each other or an input).
+ *      overlap each other or an input; a required workspace missing or short).
  */
 caat_status caat_rowpar_linear_bwd_compact(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
                                            const void *X, int64_t ldx,
@@ -291,8 +305,15 @@ caat_status caat_rowpar_linear_bwd_compact(int t, int64_t N, int64_t K, int64_t 
                                            const void *const *dYN, int64_t lddyn,
                                            void *dX, int64_t lddx,
                                            void *dW, int64_t dw_rs, int64_t dw_cs,
-                                           int64_t n_sel, void *workspace, size_t ws_bytes,
+                                           const int32_t *sel, int64_t n_sel,
+                                           void *workspace, size_t ws_bytes,
                                            caat_stream_t stream);
+
+/* Workspace bytes of the compact calls: index_list != 0 for an index list of S
+ * with 0 < |S| < h, backward != 0 for caat_rowpar_linear_bwd_compact (whose part
+ * for the dW accumulator is included).  0 for invalid arguments. */
+size_t caat_rowpar_linear_compact_workspace(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                            int index_list, int backward);
 
 /*
  * caat_rowpar_linear_bwd_noalloc -- caat_rowpar_linear_bwd without a caller

@@ -20,7 +20,8 @@ CAAT_BWD_REDUCE_DOUT, CAAT_BWD_NO_REDUCE = 0, 1
 
 __all__ = [
     "select_channels", "partial_channel_reduce", "rowpar_linear_fwd", "rowpar_linear_bwd",
-    "rowpar_linear_bwd_workspace", "rowpar_linear_bwd_noalloc", "colpar_linear_fwd",
+    "rowpar_linear_bwd_workspace", "rowpar_linear_bwd_noalloc", "rowpar_linear_fwd_compact",
+    "rowpar_linear_bwd_compact", "rowpar_linear_compact_workspace", "colpar_linear_fwd",
     "colpar_linear_bwd", "colpar_linear_bwd_workspace", "device_status", "last_kernel", "launch_count",
     "debug_set_wait", "CAAT_INJECT_NONE", "CAAT_INJECT_SKIP_LOADS", "pcr_pack", "pcr_unpack", "rank_fold",
     "CaatError", "CAAT_S_CONTIGUOUS", "CAAT_S_RANDOM", "CAAT_BWD_REDUCE_DOUT",
@@ -252,20 +253,34 @@ def rowpar_linear_bwd(X, W, dOut, t: int, sel, mode: int = CAAT_BWD_REDUCE_DOUT,
 
 # ------------------------------------------------- compact outputs
 
-def rowpar_linear_fwd_compact(X, W, t: int, n_sel: int, YS=None, YN=None, stream=None):
-    """The fused layer with the outputs in compact form, for the contiguous
-    S = {0, ..., n_sel-1}: YS [N, n_sel] holds the S channels once (the same on
-    every rank), YN[r] [N, h - n_sel] rank r's other channels.  Returns (YS, YN)."""
+def rowpar_linear_compact_workspace(t: int, N: int, K: int, h: int, dtype_code: int, index_list: bool,
+                                    backward: bool) -> int:
+    return int(_lib.load().caat_rowpar_linear_compact_workspace(int(t), int(N), int(K), int(h), int(dtype_code),
+                                                                1 if index_list else 0, 1 if backward else 0))
+
+
+def _compact_sel(sel, h):
+    """(pointer, n_sel, whether it is an index list with 0 < |S| < h)."""
+    sp, ns = _sel_ptr(sel)
+    return sp, ns, (not isinstance(sel, (int, np.integer)) and sel is not None and 0 < ns < h)
+
+
+def rowpar_linear_fwd_compact(X, W, t: int, sel, YS=None, YN=None, workspace=None, stream=None):
+    """The fused layer with the outputs in compact form: YS [N, |S|] holds the
+    channels of S once (the same on every rank), YN[r] [N, h - |S|] rank r's other
+    channels, each in ascending channel order.  sel: an int n (S = the first n
+    channels) or a device int32 index tensor; an index list needs a workspace (W
+    in the S-first order), allocated here when None.  Returns (YS, YN)."""
     torch = _torch()
     N, K = X.shape
     h = W.shape[1]
-    n_sel = int(n_sel)
     ldx = _rowmajor(X, "X")
     w_rs, w_cs = _weight_strides(W, K, h)
     if W.dtype != X.dtype:
         raise TypeError("caat: X and W must share a dtype")
+    sp, n_sel, idx = _compact_sel(sel, h)
     if not 0 <= n_sel <= h:
-        raise ValueError("caat: n_sel must lie in [0, h]")
+        raise ValueError("caat: |S| must lie in [0, h]")
     if YS is None:
         YS = torch.empty((N, n_sel), dtype=X.dtype, device=X.device)
     if YN is None:
@@ -275,24 +290,33 @@ def rowpar_linear_fwd_compact(X, W, t: int, n_sel: int, YS=None, YN=None, stream
     _check_like(YS, (N, n_sel), X.dtype, "YS")
     ldys = _rowmajor(YS, "YS") if YS.numel() else n_sel
     ldyn = _same_layout(YN, (N, h - n_sel), "YN") if h > n_sel and N > 0 else h - n_sel
+    dt = _dtype_code(X)
+    if workspace is None and idx:
+        workspace = torch.empty(rowpar_linear_compact_workspace(t, N, K, h, dt, True, False),
+                                dtype=torch.uint8, device=X.device)
+    wp, wb = _workspace(workspace)
     st = _lib.load().caat_rowpar_linear_fwd_compact(
-        int(t), N, K, h, _dtype_code(X), ctypes.c_void_p(X.data_ptr()), ldx,
+        int(t), N, K, h, dt, ctypes.c_void_p(X.data_ptr()), ldx,
         ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
         ctypes.c_void_p(YS.data_ptr()), ldys, _lib.ptr_array([y.data_ptr() for y in YN]), ldyn,
-        n_sel, _stream_ptr(stream, X))
+        sp, n_sel, wp, wb, _stream_ptr(stream, X))
     _check(st, "caat_rowpar_linear_fwd_compact")
     return YS, YN
 
 
-def rowpar_linear_bwd_compact(X, W, dYS, dYN, t: int, dX=None, dW=None, workspace=None, stream=None):
-    """Gradients of ``rowpar_linear_fwd_compact``: dYS [N, n_sel] (the gradient at
-    YS, already summed over the ranks), dYN t tensors [N, h - n_sel].  Returns
-    (dX [N, K], dW logical [K, h] in W's layout when allocated here).  workspace:
-    optional fp32 dW accumulator (allocated here when None)."""
+def rowpar_linear_bwd_compact(X, W, dYS, dYN, t: int, sel=None, dX=None, dW=None, workspace=None, stream=None):
+    """Gradients of ``rowpar_linear_fwd_compact``: dYS [N, |S|] (the gradient at YS,
+    already summed over the ranks), dYN t tensors [N, h - |S|].  sel: as for the
+    forward (None: the first dYS.shape[1] channels).  Returns (dX [N, K], dW
+    logical [K, h] in the nn.Linear layout when allocated here).  workspace:
+    allocated here when None (W in the S-first order for an index list, and the
+    fp32 dW accumulator)."""
     torch = _torch()
     N, K = X.shape
     h = W.shape[1]
-    n_sel = int(dYS.shape[1])
+    if sel is None:
+        sel = int(dYS.shape[1])
+    sp, n_sel, idx = _compact_sel(sel, h)
     ldx = _rowmajor(X, "X")
     w_rs, w_cs = _weight_strides(W, K, h)
     if W.dtype != X.dtype or dYS.dtype != X.dtype:
@@ -312,7 +336,7 @@ def rowpar_linear_bwd_compact(X, W, dYS, dYN, t: int, dX=None, dW=None, workspac
     dw_rs, dw_cs = _weight_strides(dW, K, h)
     dt = _dtype_code(X)
     if workspace is None:
-        need = rowpar_linear_bwd_workspace(t, N, K, h, dt, CAAT_BWD_NO_REDUCE)
+        need = rowpar_linear_compact_workspace(t, N, K, h, dt, idx, True)
         if need > 0:
             workspace = torch.empty(need, dtype=torch.uint8, device=X.device)
     wp, wb = _workspace(workspace)
@@ -321,9 +345,10 @@ def rowpar_linear_bwd_compact(X, W, dYS, dYN, t: int, dX=None, dW=None, workspac
         ctypes.c_void_p(W.data_ptr()), w_rs, w_cs,
         ctypes.c_void_p(dYS.data_ptr()), lddys, _lib.ptr_array([g.data_ptr() for g in dYN]), lddyn,
         ctypes.c_void_p(dX.data_ptr()), lddx, ctypes.c_void_p(dW.data_ptr()), dw_rs, dw_cs,
-        n_sel, wp, wb, _stream_ptr(stream, X))
+        sp, n_sel, wp, wb, _stream_ptr(stream, X))
     _check(st, "caat_rowpar_linear_bwd_compact")
     return dX, dW
+
 
 # ------------------------------------------------- column-parallel layer
 

@@ -21,6 +21,7 @@ EXPORTS = (
     "caat_rowpar_linear_bwd_noalloc",
     "caat_rowpar_linear_fwd_compact",
     "caat_rowpar_linear_bwd_compact",
+    "caat_rowpar_linear_compact_workspace",
     "caat_colpar_linear_fwd",
     "caat_colpar_linear_bwd_workspace",
     "caat_colpar_linear_bwd",
@@ -72,14 +73,18 @@ def load(path: str = None) -> ctypes.CDLL:
     L.caat_rowpar_linear_bwd_noalloc.restype = ctypes.c_int
     L.caat_rowpar_linear_fwd_compact.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
                                                  _c_p, _c_i64, _c_p, _c_i64, _c_i64,
-                                                 _c_p, _c_i64, _c_pp, _c_i64, _c_i64, _c_p]
+                                                 _c_p, _c_i64, _c_pp, _c_i64, _c_p, _c_i64,
+                                                 _c_p, ctypes.c_size_t, _c_p]
     L.caat_rowpar_linear_fwd_compact.restype = ctypes.c_int
     L.caat_rowpar_linear_bwd_compact.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
                                                  _c_p, _c_i64, _c_p, _c_i64, _c_i64,
                                                  _c_p, _c_i64, _c_pp, _c_i64,
                                                  _c_p, _c_i64, _c_p, _c_i64, _c_i64,
-                                                 _c_i64, _c_p, ctypes.c_size_t, _c_p]
+                                                 _c_p, _c_i64, _c_p, ctypes.c_size_t, _c_p]
     L.caat_rowpar_linear_bwd_compact.restype = ctypes.c_int
+    L.caat_rowpar_linear_compact_workspace.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
+                                                       ctypes.c_int, ctypes.c_int]
+    L.caat_rowpar_linear_compact_workspace.restype = ctypes.c_size_t
     L.caat_colpar_linear_fwd.argtypes = [ctypes.c_int, _c_i64, _c_i64, _c_i64, ctypes.c_int,
                                          _c_pp, _c_i64, _c_p, _c_i64, _c_i64, _c_p, _c_i64, _c_p]
     L.caat_colpar_linear_fwd.restype = ctypes.c_int

@@ -502,20 +502,47 @@ extern "C" caat_status caat_rowpar_linear_bwd(int t, int64_t N, int64_t K, int64
 
 // ------------------------------------------------- compact outputs
 // The t outputs with the S channels (the same on every rank) stored once:
-// YS [N, n_sel] and YN[r] [N, h - n_sel] for the contiguous S = {0..n_sel-1}.
+// YS [N, |S|] and YN[r] [N, h - |S|], each in ascending channel order.  A
+// contiguous S runs the tile kernels directly; an index list of S runs them on a
+// copy of W whose channels are in the order "S first" (the workspace), which
+// makes S contiguous, and puts dW's rows back in channel order at the end.
+
+namespace {
+
+size_t wperm_region_bytes(int64_t K, int64_t h) { return ((size_t)K * (size_t)h * 2 + 255) / 256 * 256; }
+
+}  // namespace
+
+extern "C" size_t caat_rowpar_linear_compact_workspace(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
+                                                       int index_list, int backward)
+{
+    if (t < 1 || t > CAAT_MAX_T || N < 0 || K < 0 || h < 0 || !valid_dtype(dt)) return 0;
+    // forward: W in the S-first order; backward: that, then dW staged in the same
+    // order, then the optional fp32 accumulator of dW
+    if (!backward) return index_list ? wperm_region_bytes(K, h) : 0;
+    return (index_list ? 2 * wperm_region_bytes(K, h) : 0) + wacc_region_bytes(K, h, dt);
+}
 
 extern "C" caat_status caat_rowpar_linear_fwd_compact(int t, int64_t N, int64_t K, int64_t h, caat_dtype dt,
                                                       const void *X, int64_t ldx,
                                                       const void *W, int64_t w_rs, int64_t w_cs,
                                                       void *YS, int64_t ldys, void *const *YN, int64_t ldyn,
-                                                      int64_t n_sel, caat_stream_t stream)
+                                                      const int32_t *sel, int64_t n_sel,
+                                                      void *workspace, size_t ws_bytes, caat_stream_t stream)
 {
-    caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, nullptr, n_sel);
+    caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, sel, n_sel);
     if (st != CAAT_OK) return st;
+    if ((st = check_sel_debug(sel, n_sel, h, (cudaStream_t)stream)) != CAAT_OK) return st;
+    sel = all_channels(sel, n_sel, h);
     const int64_t h_own = h - n_sel;
     if (N > 0 && n_sel > 0 && (YS == nullptr || ldys < n_sel)) return CAAT_ERR_INVALID_ARG;
     if (N > 0 && h_own > 0 && (YN == nullptr || ldyn < h_own)) return CAAT_ERR_INVALID_ARG;
     const int64_t es = elem_size(dt);
+    // an index list of S with 0 < |S| < h needs W in the S-first order
+    const bool perm = sel != nullptr && n_sel > 0 && n_sel < h && K > 0;
+    const size_t need = perm ? wperm_region_bytes(K, h) : 0;
+    if (need > 0 && (workspace == nullptr || ws_bytes < need || ((uintptr_t)workspace & 255)))
+        return CAAT_ERR_INVALID_ARG;
     MutPtrs py{};
     if (h_own > 0)
         for (int r = 0; r < t; ++r) {
@@ -524,11 +551,14 @@ extern "C" caat_status caat_rowpar_linear_fwd_compact(int t, int64_t N, int64_t 
         }
     {
         const Span sx = span_of(X, N, K, ldx, es), sw = span_strided(W, K, h, w_rs, w_cs, es);
-        const Span ss = span_of(YS, N, n_sel, ldys, es);
-        if (overlap(ss, sx) || overlap(ss, sw)) return CAAT_ERR_INVALID_ARG;
+        const Span ss = span_of(YS, N, n_sel, ldys, es), sl = span_sel(sel, n_sel);
+        const Span sws = span_bytes(workspace, need);
+        if (overlap(ss, sx) || overlap(ss, sw) || overlap(ss, sl) || overlap(ss, sws)) return CAAT_ERR_INVALID_ARG;
+        if (overlap(sws, sx) || overlap(sws, sw) || overlap(sws, sl)) return CAAT_ERR_INVALID_ARG;
         for (int r = 0; h_own > 0 && r < t; ++r) {
             const Span so = span_of(YN[r], N, h_own, ldyn, es);
-            if (overlap(so, ss) || overlap(so, sx) || overlap(so, sw)) return CAAT_ERR_INVALID_ARG;
+            if (overlap(so, ss) || overlap(so, sx) || overlap(so, sw) || overlap(so, sl) || overlap(so, sws))
+                return CAAT_ERR_INVALID_ARG;
             for (int q = r + 1; q < t; ++q)
                 if (overlap(so, span_of(YN[q], N, h_own, ldyn, es))) return CAAT_ERR_INVALID_ARG;
         }
@@ -545,8 +575,17 @@ extern "C" caat_status caat_rowpar_linear_fwd_compact(int t, int64_t N, int64_t 
                 return CAAT_ERR_CUDA;
         return CAAT_OK;
     }
+    const void *Wk = W;
+    int64_t ldw = w_cs;
+    if (perm) {
+        // the tile kernel's shape rules first, so that nothing runs for a call it declines
+        if (N < 16 || (K / t) < 64 || (K / t) % 8 != 0) return CAAT_ERR_UNSUPPORTED;
+        if ((st = launch_permute_rows(W, w_cs, workspace, K, h, K, sel, n_sel, true, s)) != CAAT_OK) return st;
+        Wk = workspace;
+        ldw = K;
+    }
     // with no S channel the compact form is the plain one (YN[r] = Y[r])
-    return launch_rowpar_fwd_tc(t, N, K, h, X, ldx, W, w_cs, py, ldyn, nullptr, n_sel, s,
+    return launch_rowpar_fwd_tc(t, N, K, h, X, ldx, Wk, ldw, py, ldyn, nullptr, n_sel, s,
                                 n_sel > 0 ? YS : nullptr, ldys);
 }
 
@@ -557,11 +596,13 @@ extern "C" caat_status caat_rowpar_linear_bwd_compact(int t, int64_t N, int64_t 
                                                       const void *const *dYN, int64_t lddyn,
                                                       void *dX, int64_t lddx,
                                                       void *dW, int64_t dw_rs, int64_t dw_cs,
-                                                      int64_t n_sel, void *workspace, size_t ws_bytes,
-                                                      caat_stream_t stream)
+                                                      const int32_t *sel, int64_t n_sel,
+                                                      void *workspace, size_t ws_bytes, caat_stream_t stream)
 {
-    caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, nullptr, n_sel);
+    caat_status st = check_layer_args(t, N, K, h, dt, X, ldx, W, w_rs, w_cs, sel, n_sel);
     if (st != CAAT_OK) return st;
+    if ((st = check_sel_debug(sel, n_sel, h, (cudaStream_t)stream)) != CAAT_OK) return st;
+    sel = all_channels(sel, n_sel, h);
     const int64_t h_own = h - n_sel;
     if (N > 0 && n_sel > 0 && (dYS == nullptr || lddys < n_sel)) return CAAT_ERR_INVALID_ARG;
     if (N > 0 && h_own > 0 && (dYN == nullptr || lddyn < h_own)) return CAAT_ERR_INVALID_ARG;
@@ -579,19 +620,27 @@ extern "C" caat_status caat_rowpar_linear_bwd_compact(int t, int64_t N, int64_t 
             dy.p[r] = dYN[r];
         }
     const int64_t es = elem_size(dt);
+    // an index list of S: W in the S-first order and room to stage dW in that
+    // order are required (dW's rows then return to channel order); the fp32
+    // accumulator after them stays optional
+    const bool perm = sel != nullptr && n_sel > 0 && n_sel < h && K > 0 && N > 0;
+    const size_t wperm = perm ? 2 * wperm_region_bytes(K, h) : 0;
+    const size_t need = wperm;
+    if (need > 0 && (workspace == nullptr || ws_bytes < need || ((uintptr_t)workspace & 255)))
+        return CAAT_ERR_INVALID_ARG;
     float *wacc = nullptr;
-    if (workspace != nullptr && ((uintptr_t)workspace & 255) == 0 && ws_bytes >= wacc_region_bytes(K, h, dt) &&
-        wacc_region_bytes(K, h, dt) > 0)
-        wacc = (float *)workspace;
+    if (workspace != nullptr && ((uintptr_t)workspace & 255) == 0 && wacc_region_bytes(K, h, dt) > 0 &&
+        ws_bytes >= wperm + wacc_region_bytes(K, h, dt))
+        wacc = (float *)((char *)workspace + wperm);
     {
         const Span w_dx = span_of(dX, N, K, lddx, es);
         const Span w_dw = span_strided(dW, K, h, dw_rs, dw_cs, es);
-        const Span w_ws = span_bytes(workspace, wacc != nullptr ? wacc_region_bytes(K, h, dt) : 0);
+        const Span w_ws = span_bytes(workspace, wperm + (wacc != nullptr ? wacc_region_bytes(K, h, dt) : 0));
         const Span outs[3] = {w_dx, w_dw, w_ws};
         if (overlap(w_dx, w_dw) || overlap(w_dx, w_ws) || overlap(w_dw, w_ws)) return CAAT_ERR_INVALID_ARG;
         for (const Span &o : outs) {
             if (overlap(o, span_of(X, N, K, ldx, es)) || overlap(o, span_strided(W, K, h, w_rs, w_cs, es)) ||
-                overlap(o, span_of(dYS, N, n_sel, lddys, es)))
+                overlap(o, span_of(dYS, N, n_sel, lddys, es)) || overlap(o, span_sel(sel, n_sel)))
                 return CAAT_ERR_INVALID_ARG;
             for (int r = 0; h_own > 0 && r < t; ++r)
                 if (overlap(o, span_of(dYN[r], N, h_own, lddyn, es))) return CAAT_ERR_INVALID_ARG;
@@ -613,9 +662,13 @@ extern "C" caat_status caat_rowpar_linear_bwd_compact(int t, int64_t N, int64_t 
     if (!bwd_tc_supported(t, N, K, h, X, ldx, W, w_cs, dy, lddyn, dX, lddx, dW, dw_cs) ||
         (n_sel > 0 && ((uintptr_t)dYS % 16 != 0 || lddys % 8 != 0)))
         return CAAT_ERR_UNSUPPORTED;
+    // with an index list W is permuted inside, after the dW chain has forked off
+    void *dw_tmp = perm ? (char *)workspace + wperm_region_bytes(K, h) : nullptr;
     return launch_rowpar_bwd_tc(t, N, K, h, X, ldx, W, w_cs, dy, lddyn, dX, lddx, dW, dw_cs, wacc, n_sel,
-                                n_sel > 0 ? dYS : nullptr, lddys, s, true);
+                                n_sel > 0 ? dYS : nullptr, lddys, s, true, perm ? sel : nullptr, n_sel, dw_tmp,
+                                perm ? workspace : nullptr);
 }
+
 
 // ------------------------------------------------- column-parallel layer
 // The column-parallel layer is the row-parallel one seen through W = W1^T

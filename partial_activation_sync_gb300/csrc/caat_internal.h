@@ -116,6 +116,17 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
                                  void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
                                  int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s,
-                                 bool own_compact = false);
+                                 bool own_compact = false, const int32_t *row_sel = nullptr,
+                                 int64_t row_nsel = 0, void *dw_tmp = nullptr, void *w_perm = nullptr);
+
+// bf16 rows [h, K] between channel order and the order "channels of S ascending,
+// then the others" (sel: S, ascending, n_sel): to_s_first moves row c of src to
+// row s_first_pos(c) of dst, else row s_first_pos(c) of src to row c of dst.
+// row_sel in launch_rowpar_bwd_tc undoes that order on dW's rows: through the
+// fp32 accumulator when dW is split over tokens, else through dw_tmp (bf16 [h, K],
+// row stride K), which it then requires.  With w_perm (bf16 [h, K]) it first puts
+// W's rows into that order there, for dX.
+caat_status launch_permute_rows(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t h, int64_t K,
+                                const int32_t *sel, int64_t n_sel, bool to_s_first, cudaStream_t s);
 
 }  // namespace caat

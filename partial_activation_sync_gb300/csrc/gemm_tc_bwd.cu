@@ -484,23 +484,97 @@ bool use_pairs(int64_t M, int64_t n)
     return M > BM && pick_bn(n) == MAX_BN;
 }
 
-// fp32 [rows, cols] (row stride lds) -> bf16 (row stride ldd), 8 columns per thread
+// Position of channel c in the order "the channels of S ascending, then the
+// others ascending" (sel: the n_sel indices of S, ascending and unique): its rank
+// in S, or n_sel plus the number of channels outside S below it.  A list that is
+// not ascending can give a position outside [0, h): -1 then, and the callers skip
+// the row.
+__device__ __forceinline__ int64_t s_first_pos(const int32_t *__restrict__ sel, int64_t n_sel, int64_t h,
+                                               int64_t c)
+{
+    int64_t lo = 0, hi = n_sel;                       // first i with sel[i] >= c
+    while (lo < hi) {
+        const int64_t mid = (lo + hi) >> 1;
+        if ((int64_t)__ldg(sel + mid) < c) lo = mid + 1;
+        else hi = mid;
+    }
+    const int64_t pos = (lo < n_sel && (int64_t)__ldg(sel + lo) == c) ? lo : n_sel + (c - lo);
+    return (pos >= 0 && pos < h) ? pos : -1;
+}
+
+// fp32 [rows, cols] (row stride lds) -> bf16 (row stride ldd), 8 columns per
+// thread.  With sel: destination row c takes source row s_first_pos(c) (the
+// source rows in the S-first channel order, the destination in channel order).
 __global__ void __launch_bounds__(256)
 f32_rows_to_bf16_kernel(const float *__restrict__ src, int64_t rows, int64_t cols, int64_t lds,
-                        uint16_t *__restrict__ dst, int64_t ldd)
+                        uint16_t *__restrict__ dst, int64_t ldd, const int32_t *__restrict__ sel,
+                        int64_t n_sel)
 {
     const int64_t per_row = cols / 8;
     const int64_t total = rows * per_row;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t rr = i / per_row, c = (i - rr * per_row) * 8;
-        const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + rr * lds + c));
-        const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + rr * lds + c + 4));
+        const int64_t sr = sel != nullptr ? s_first_pos(sel, n_sel, rows, rr) : rr;
+        if (sr < 0) continue;
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(src + sr * lds + c));
+        const float4 b = __ldcs(reinterpret_cast<const float4 *>(src + sr * lds + c + 4));
         const uint4 w = make_uint4(pack_bf16x2(__float_as_uint(a.x), __float_as_uint(a.y)),
                                    pack_bf16x2(__float_as_uint(a.z), __float_as_uint(a.w)),
                                    pack_bf16x2(__float_as_uint(b.x), __float_as_uint(b.y)),
                                    pack_bf16x2(__float_as_uint(b.z), __float_as_uint(b.w)));
         *reinterpret_cast<uint4 *>(dst + rr * ldd + c) = w;
+    }
+}
+
+// Rows of a bf16 [h, K] matrix between channel order and the S-first order: with
+// to_s_first, dst row s_first_pos(c) = src row c; else dst row c = src row
+// s_first_pos(c).  One warp per row, 16-byte copies, four in flight per lane.
+// With room for it (dynamic shared memory of n_sel entries) S is staged in
+// shared memory first, so that each row's binary search does not wait on a
+// chain of global loads.
+__global__ void __launch_bounds__(256)
+permute_rows_kernel(const uint16_t *__restrict__ src, int64_t lds, uint16_t *__restrict__ dst, int64_t ldd,
+                    int64_t h, int64_t K, const int32_t *__restrict__ sel, int64_t n_sel, int to_s_first,
+                    int staged)
+{
+    extern __shared__ int32_t ssel[];
+    if (staged) {
+        for (int64_t i = threadIdx.x; i < n_sel; i += blockDim.x) ssel[i] = __ldg(sel + i);
+        __syncthreads();
+    }
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t n16 = K / 8;
+    for (int64_t c = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); c < h; c += warps) {
+        int64_t pos = 0;
+        if (lane == 0) {
+            if (staged) {
+                int64_t lo = 0, hi = n_sel;
+                while (lo < hi) {
+                    const int64_t mid = (lo + hi) >> 1;
+                    if ((int64_t)ssel[mid] < c) lo = mid + 1;
+                    else hi = mid;
+                }
+                pos = (lo < n_sel && (int64_t)ssel[lo] == c) ? lo : n_sel + (c - lo);
+                if (pos < 0 || pos >= h) pos = -1;
+            } else {
+                pos = s_first_pos(sel, n_sel, h, c);
+            }
+        }
+        pos = __shfl_sync(0xffffffffu, pos, 0);
+        if (pos < 0) continue;                        // the whole warp
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(src + (to_s_first ? c : pos) * lds);
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + (to_s_first ? pos : c) * ldd);
+        int64_t i = lane;
+        for (; i + 224 < n16; i += 256) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = __ldcs(s4 + i + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) d4[i + 32 * u] = v[u];
+        }
+        for (; i < n16; i += 32) d4[i] = __ldcs(s4 + i);
     }
 }
 
@@ -517,6 +591,14 @@ void set_ksplit(GemmParams &p, int k, int tiles)
 // waves-of-work over `slots` workers, per part
 void pick_ksplit(GemmParams &p, int tiles, int slots)
 {
+    // Each extra part adds an fp32 reduce-add of the whole of dW; that only pays
+    // where the unsplit tiles leave at least half of the slots idle (at the
+    // 1.1B down-projection, 192 pair tiles on 76 pairs, a 7-way split added
+    // about 320 MB of reduce traffic and cost 35 us).
+    if (2 * tiles > slots) {
+        set_ksplit(p, 1, tiles);
+        return;
+    }
     int best = 1;
     double best_cost = (double)((tiles + slots - 1) / slots);
     for (int k = 2; k <= 8 && p.nkb / k >= 8; ++k) {
@@ -586,10 +668,13 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
                                  const void *W, int64_t ldw, const ConstPtrs &dY, int64_t ld_dy,
                                  void *dX, int64_t lddx, void *dW, int64_t ld_dw, float *wacc,
                                  int64_t s_sum, const void *dsum, int64_t ld_dsum, cudaStream_t s,
-                                 bool own_compact)
+                                 bool own_compact, const int32_t *row_sel, int64_t row_nsel, void *dw_tmp,
+                                 void *w_perm)
 {
     const int64_t kt = K / t;
     if (s_sum < 0 || s_sum > h || s_sum % 64 != 0 || (s_sum > 0 && dsum == nullptr)) return CAAT_ERR_UNSUPPORTED;
+    if (row_sel != nullptr && dW != nullptr && (dw_tmp == nullptr || (uintptr_t)dw_tmp % 16 != 0 || K % 8 != 0))
+        return CAAT_ERR_UNSUPPORTED;
     const int64_t h_own = h - s_sum;           // channels read from each rank's own gradient
 
     // A-operand maps: rank r's gradient from channel s_sum on (each rank; in the
@@ -627,6 +712,14 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
     };
     // ---- dX = dY_r W_r^T: A = dY_r (K-major), B = W_r^T (MN-major)
     if (dX != nullptr) {
+        if (w_perm != nullptr) {
+            // W's rows in the S-first order (the order of dY's channels) first; the
+            // dW chain, on the side stream, does not read W and runs beside it
+            const caat_status st = launch_permute_rows(W, ldw, w_perm, K, h, K, row_sel, row_nsel, true, s);
+            if (st != CAAT_OK) return join(st);
+            W = w_perm;
+            ldw = K;
+        }
         TmapArray am;
         CUtensorMap sm;
         if (!grad_maps(am, sm, 64, BM)) return CAAT_ERR_UNSUPPORTED;
@@ -676,16 +769,22 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         if (wacc != nullptr) pick_ksplit(p, tiles, pair ? num_sms() / 2 : num_sms());
         else set_ksplit(p, 1, tiles);
         if (p.ksplit == 1) {
+            // straight to dW; with row_sel to dw_tmp [h, K] in the S-first row
+            // order, then rows back to channel order
+            void *dst = row_sel != nullptr ? dw_tmp : dW;
+            const int64_t ldd = row_sel != nullptr ? K : ld_dw;
             CUtensorMap cm;
             const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
-            const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)ld_dw * 2};
+            const uint64_t cstr[2] = {(uint64_t)kt * 2, (uint64_t)ldd * 2};
             const uint32_t cbox[3] = {64, 1, 32};
-            if (!encode_tmap(&cm, dW, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
-            return pair ? launch_grouped<true, false, true>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc")
-                        : launch_grouped<true, false, false>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc");
+            if (!encode_tmap(&cm, dst, 3, cdims, cstr, cbox)) return CAAT_ERR_UNSUPPORTED;
+            caat_status st = pair ? launch_grouped<true, false, true>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc")
+                                  : launch_grouped<true, false, false>(am, sm, bm, cm, p, sw, "rowpar_bwd_dw_tc");
+            if (st != CAAT_OK || row_sel == nullptr) return st;
+            return launch_permute_rows((const uint16_t *)dw_tmp, K, dW, ld_dw, h, K, row_sel, row_nsel, false, sw);
         }
         // split over tokens: fp32 partials reduce-added into wacc [h, K], then one
-        // rounding to bf16 into dW
+        // rounding to bf16 into dW (with row_sel: rows back in channel order)
         CUtensorMap cm;
         const uint64_t cdims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)h};
         const uint64_t cstr[2] = {(uint64_t)kt * 4, (uint64_t)K * 4};
@@ -698,11 +797,28 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const int64_t total = h * (K / 8);
         int64_t blocks = (total + 255) / 256;
         if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
-        f32_rows_to_bf16_kernel<<<(unsigned)blocks, 256, 0, sw>>>(wacc, h, K, K, (uint16_t *)dW, ld_dw);
+        f32_rows_to_bf16_kernel<<<(unsigned)blocks, 256, 0, sw>>>(wacc, h, K, K, (uint16_t *)dW, ld_dw, row_sel,
+                                                                  row_nsel);
         note_launch("rowpar_bwd_dw_tc", 1);
         return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
     };
     return join(dw_chain());
+}
+
+caat_status launch_permute_rows(const void *src, int64_t lds, void *dst, int64_t ldd, int64_t h, int64_t K,
+                                const int32_t *sel, int64_t n_sel, bool to_s_first, cudaStream_t s)
+{
+    if (h == 0 || K == 0) return CAAT_OK;
+    if (K % 8 != 0 || lds % 8 != 0 || ldd % 8 != 0 || (uintptr_t)src % 16 != 0 || (uintptr_t)dst % 16 != 0)
+        return CAAT_ERR_UNSUPPORTED;
+    int64_t blocks = (h + 7) / 8;                     // 8 warps per CTA, one row per warp
+    if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
+    const bool staged = n_sel <= 8192;                // up to 32 KB of shared memory
+    const size_t smem = staged ? (size_t)n_sel * 4 : 0;
+    permute_rows_kernel<<<(unsigned)blocks, 256, smem, s>>>((const uint16_t *)src, lds, (uint16_t *)dst, ldd, h, K,
+                                                             sel, n_sel, to_s_first ? 1 : 0, staged ? 1 : 0);
+    note_launch("permute_rows", 1);
+    return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }
 
 }  // namespace caat

@@ -151,32 +151,55 @@ def test_compact_layer_rejects_bad_args_without_launch(lib):
     # compact outputs: YS [4, n_sel] and YN[r] [4, 8 - n_sel]; fake device pointers,
     # every case returns before anything touches the device
     X, W, YS, Y0, Y1 = 1 << 20, 2 << 20, 3 << 20, 4 << 20, 5 << 20
+    sel, ws = ctypes.c_void_p(9 << 20), 10 << 20
     f = lib.caat_rowpar_linear_fwd_compact
-    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, 2, None) == 2   # n_sel % 64
-    assert f(2, 4, 8, 8, 0, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, 2, None) == 2   # fp32
-    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 1, _ptrs([Y0, Y1]), 6, 2, None) == 1   # ldys < n_sel
-    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 5, 2, None) == 1   # ldyn < h - n_sel
-    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, None, 2, _ptrs([Y0, Y1]), 6, 2, None) == 1  # no YS
-    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, YS + 8]), 6, 2, None) == 1   # YN over YS
-    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y0 + 4]), 6, 2, None) == 1   # YN overlap
-    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, X + 2, 2, _ptrs([Y0, Y1]), 6, 2, None) == 1    # YS over X
-    assert f(2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, 9, None) == 1       # n_sel > h
+    ok = [2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, None, 2, None, 0, None]
+
+    def fc(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert fc() == 2                                      # n_sel % 64
+    assert fc(a4=0) == 2                                  # fp32
+    assert fc(a11=1) == 1                                 # ldys < n_sel
+    assert fc(a13=5) == 1                                 # ldyn < h - n_sel
+    assert fc(a10=None) == 1                              # no YS
+    assert fc(a12=_ptrs([Y0, YS + 8])) == 1               # YN over YS
+    assert fc(a12=_ptrs([Y0, Y0 + 4])) == 1               # YN overlap
+    assert fc(a10=X + 2) == 1                             # YS over X
+    assert fc(a15=9) == 1                                 # n_sel > h
+    assert fc(a14=sel) == 1                               # an index list needs the permuted W
+    assert fc(a14=sel, a16=ws, a17=64) == 1               # ... of h*K*2 = 128 bytes (256 rounded)
+    assert fc(a14=sel, a16=ws + 16, a17=256) == 1         # ... 256-byte aligned
+    assert fc(a14=sel, a16=YS, a17=256) == 1              # ... not over an output
+    assert fc(a14=sel, a16=ws, a17=256) == 2              # valid, but n_sel % 64
     g = lib.caat_rowpar_linear_bwd_compact
     dX, dW = 6 << 20, 7 << 20
-    ok = (2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, dX, 8, dW, 1, 8, 2, None, 0, None)
-    assert g(*ok) == 2                                                             # n_sel % 64
-    bad = list(ok); bad[11] = 1
-    assert g(*bad) == 1                                                            # lddys < n_sel
-    bad = list(ok); bad[13] = 5
-    assert g(*bad) == 1                                                            # lddyn < h - n_sel
-    bad = list(ok); bad[14] = YS + 4
-    assert g(*bad) == 1                                                            # dX over dYS
-    bad = list(ok); bad[16] = Y1 + 8
-    assert g(*bad) == 1                                                            # dW over a dYN
-    bad = list(ok); bad[16] = dX + 16
-    assert g(*bad) == 1                                                            # dX and dW overlap
-    bad = list(ok); bad[12] = None
-    assert g(*bad) == 1                                                            # no dYN
+    okb = [2, 4, 8, 8, 1, X, 8, W, 1, 8, YS, 2, _ptrs([Y0, Y1]), 6, dX, 8, dW, 1, 8, None, 2, None, 0, None]
+
+    def gc(**kw):
+        a = list(okb)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return g(*a)
+    assert gc() == 2                                      # n_sel % 64
+    assert gc(a11=1) == 1                                 # lddys < n_sel
+    assert gc(a13=5) == 1                                 # lddyn < h - n_sel
+    assert gc(a14=YS + 4) == 1                            # dX over dYS
+    assert gc(a16=Y1 + 8) == 1                            # dW over a dYN
+    assert gc(a16=dX + 16) == 1                           # dX and dW overlap
+    assert gc(a12=None) == 1                              # no dYN
+    assert gc(a19=sel) == 1                               # index list: W copy + dW staging required
+    assert gc(a19=sel, a21=ws, a22=256) == 1              # 256 + 256 bytes needed
+    assert gc(a19=sel, a21=ws, a22=512) == 2              # valid, but n_sel % 64
+    w = lib.caat_rowpar_linear_compact_workspace
+    assert w(2, 4, 8, 8, 1, 0, 0) == 0
+    assert w(2, 4, 8, 8, 1, 1, 0) == 256                  # W [8, 8] bf16, rounded up
+    assert w(2, 4, 8, 8, 1, 0, 1) == 256                  # fp32 accumulator [8, 8]
+    assert w(2, 4, 8, 8, 1, 1, 1) == 768                  # W, dW staging, accumulator
+    assert w(0, 4, 8, 8, 1, 1, 1) == 0
+
 
 def test_colpar_rejects_bad_args_without_launch(lib):
     A0, A1, W1, Z = 1 << 20, 2 << 20, 3 << 20, 4 << 20

@@ -201,3 +201,88 @@ def test_compact_full_size_matches_plain_form(caat, wname, li):
     T.cuda.synchronize()
     assert caat.device_status() == 0
     assert T.equal(dX, pX) and T.equal(dW, pW)
+
+
+# (t, N, k_t, h, p, note): a seeded random S of |S| = p h channels (a multiple of 64)
+RANDOM_SHAPES = [
+    (8, 300, 96, 768, 0.5, "130M-like, 192-wide tiles"),
+    (4, 512, 512, 1024, 0.5, "CTA pairs"),
+    (2, 256, 256, 512, 0.25, "p = 1/4"),
+]
+
+
+@pytest.mark.parametrize("t,N,kt,h,p,note", RANDOM_SHAPES)
+def test_random_set_compact_parity(caat, t, N, kt, h, p, note):
+    """An index list of S: YS holds S's channels in ascending order and YN[r] the
+    other channels of rank r.  Against the oracle, and bit for bit against the
+    contiguous compact call on W with its channels renamed S-first (what the
+    index-list call runs internally); the backward likewise (dX bit for bit, dW
+    through the accumulator, whose rows return to channel order)."""
+    from tests.gpu_helpers import sel_dev
+    T = torch()
+    K = kt * t
+    seed = 17 * t + N + h
+    S = caat.select_channels(h, p, caat.CAAT_S_RANDOM, 4000 + seed)
+    assert 0 < S.size < h and S.size % 64 == 0
+    U = np.setdiff1d(np.arange(h), S)
+    perm = np.concatenate([S, U])
+    X = ci.normal(1000 + seed, (N, K))
+    Wl = ci.normal(2000 + seed, (K, h), std=0.02)
+    Xd, Wd = dev(X, "bf16"), _w_nn(Wl)
+    Xv, Wv = host_values(X, "bf16"), host_values(Wl, "bf16")
+    YS, YN = caat.rowpar_linear_fwd_compact(Xd, Wd, t, sel_dev(S))
+    T.cuda.synchronize()
+    assert caat.device_status() == 0
+    want, _ = orc.rowpar_fwd(Xv, Wv, t, S)
+    check(to_f64(YS), want[0][:, S], "bf16", what=("YS", note))
+    for r in range(t):
+        check(to_f64(YN[r]), want[r][:, U], "bf16", what=("YN", r, note))
+    Wp = _w_nn(Wl[:, perm])
+    cS, cN = caat.rowpar_linear_fwd_compact(Xd, Wp, t, int(S.size))
+    T.cuda.synchronize()
+    assert T.equal(YS, cS) and all(T.equal(a, b) for a, b in zip(YN, cN)), note
+    # backward
+    GS = ci.normal(3100 + seed, (N, S.size))
+    GN = ci.normal(3200 + seed, (t, N, U.size))
+    dYS = dev(GS, "bf16")
+    dYN = [dev(GN[r], "bf16") for r in range(t)]
+    G = np.zeros((t, N, h))
+    G[0][:, S] = host_values(GS, "bf16")
+    for r in range(t):
+        G[r][:, U] = host_values(GN[r], "bf16")
+    wX, wW = orc.rowpar_bwd(Xv, Wv, G, t, S, orc.REDUCE_DOUT)
+    pX, pW = caat.rowpar_linear_bwd_compact(Xd, Wp, dYS, dYN, t,
+                                            workspace=T.empty(0, dtype=T.uint8, device="cuda"))
+    full = caat.rowpar_linear_compact_workspace(t, N, K, h, caat.CAAT_BF16, True, True)
+    required = full - caat.rowpar_linear_compact_workspace(t, N, K, h, caat.CAAT_BF16, False, True)
+    # with the fp32 accumulator (dW may be split over tokens: rows back to channel
+    # order as it is rounded), and with only the required part (dW staged in the
+    # S-first order, then its rows moved back)
+    for ws_bytes in (full, required):
+        ws = T.empty(ws_bytes, dtype=T.uint8, device="cuda")
+        dX, dW = caat.rowpar_linear_bwd_compact(Xd, Wd, dYS, dYN, t, sel=sel_dev(S), workspace=ws)
+        T.cuda.synchronize()
+        assert caat.device_status() == 0
+        check(to_f64(dX), wX, "bf16", bwd=True, what=("dX", note, ws_bytes))
+        check(to_f64(dW), wW, "bf16", bwd=True, what=("dW", note, ws_bytes))
+        assert T.equal(dX, pX), note
+        if ws_bytes == required:
+            # one pass over the tokens on the renamed W, rows moved back: the same bits
+            assert T.equal(dW.t()[T.from_numpy(perm).cuda()], pW.t()), note
+
+
+def test_random_set_compact_declines_short_workspace(caat):
+    """An index list without room for the permuted W: INVALID_ARG, nothing launched."""
+    from tests.gpu_helpers import sel_dev
+    T = torch()
+    t, N, K, h = 4, 256, 256, 512
+    S = caat.select_channels(h, 0.5, caat.CAAT_S_RANDOM, 3)
+    X = dev(ci.normal(5, (N, K)), "bf16")
+    Wd = _w_nn(ci.normal(6, (K, h), std=0.02))
+    small = T.empty(1024, dtype=T.uint8, device="cuda")
+    n0 = caat.launch_count()
+    with pytest.raises(caat.CaatError) as e:
+        caat.rowpar_linear_fwd_compact(X, Wd, t, sel_dev(S), workspace=small)
+    assert e.value.status == 1
+    T.cuda.synchronize()
+    assert caat.launch_count() == n0
