@@ -48,15 +48,17 @@ STEP_SPIN_CYCLES = 400000
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # dominant forward kernel, from an ncu capture of the same workload with the
-# kernels as they are now (7B prefill: the full capture of one step; 130M: the
-# one-pass launch list, averaged over its steps); a workload or layer without a
-# capture reports null.  Output lines still dirty in L2 when the kernel ends are
-# not in the count.
+# kernels as they are now (7B prefill: the full capture of one step, plain and
+# compact outputs; 130M: the one-pass launch list, averaged over its steps); a
+# workload or layer without a capture reports null.  Output lines still dirty in
+# L2 when the kernel ends are not in the count.
 DRAM_TRAFFIC = {
-    ("7b_prefill", "out_proj"): 117.97e6 + 208.75e6,
-    ("7b_prefill", "down_proj"): 421.03e6 + 222.59e6,
-    ("130m", "out_proj"): 13.85e6 + 36.34e6,
-    ("130m", "down_proj"): 56.79e6 + 38.50e6,
+    ("7b_prefill", "out_proj"): 118.12e6 + 208.16e6,
+    ("7b_prefill", "down_proj"): 419.78e6 + 221.32e6,
+    ("7b_prefill_compact", "out_proj"): 83.42e6 + 101.20e6,
+    ("7b_prefill_compact", "down_proj"): 404.95e6 + 114.63e6,
+    ("130m", "out_proj"): 13.85e6 + 36.33e6,
+    ("130m", "down_proj"): 57.29e6 + 38.87e6,
 }
 
 
@@ -412,8 +414,8 @@ def roofline_of(ls, per_call, steps, peaks, kernel_name):
         roof["peak_kind"] = "copy bandwidth (read + write)"
     roof["peak_source"] = "of measured (MEASURED_PEAKS.json)" if peaks["source"] == "measured" else "of fallback"
     # DRAM counters exist for the one-GPU launch configuration only
-    roof["traffic"] = (DRAM_TRAFFIC.get((w.name, Ld.name))
-                       if isinstance(ls, LayerStep) and not ls.compact else None)
+    roof["traffic"] = (DRAM_TRAFFIC.get((w.name + ("_compact" if ls.compact else ""), Ld.name))
+                       if isinstance(ls, LayerStep) else None)
     roof["algorithmic_per_launch"] = {"flops": Ld.flops_fwd, "bytes": Ld.bytes_fwd}
     roof["us_per_launch"] = round(t_dom * 1e6, 2)
     return roof

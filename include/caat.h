@@ -290,8 +290,8 @@ caat_status caat_rowpar_linear_fwd_compact(int t, int64_t N, int64_t K, int64_t 
  *      order, and room to stage dW in that order before its rows return to
  *      channel order.  Then, for any S, the optional fp32 accumulator of dW,
  *      h*K*4 bytes rounded to 256.  With the accumulator, dW is reduced over
- *      tokens in several parts when its tiles leave at least half of the SMs
- *      idle; then rounded once.  With a contiguous S the workspace may be null.
+ *      tokens in several parts when its tiles do not fill the SMs; then rounded
+ *      once.  With a contiguous S the workspace may be null.
  * Kernel: the tensor-core backward only: bf16, W and dW in the nn.Linear layout
  *      (w_rs == dw_rs == 1), N >= 128, h >= 256, n_sel a multiple of 64, the TMA
  *      alignment rules; else UNSUPPORTED.

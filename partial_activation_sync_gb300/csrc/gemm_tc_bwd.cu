@@ -592,10 +592,11 @@ void set_ksplit(GemmParams &p, int k, int tiles)
 void pick_ksplit(GemmParams &p, int tiles, int slots)
 {
     // Each extra part adds an fp32 reduce-add of the whole of dW; that only pays
-    // where the unsplit tiles leave at least half of the slots idle (at the
-    // 1.1B down-projection, 192 pair tiles on 76 pairs, a 7-way split added
-    // about 320 MB of reduce traffic and cost 35 us).
-    if (2 * tiles > slots) {
+    // where the unsplit tiles do not fill one round of the slots (at the 1.1B
+    // down-projection, 192 pair tiles on 76 pairs, a 7-way split added about
+    // 320 MB of reduce traffic and cost 35 us; at the 130M down-projection, 96
+    // tiles on 152 SMs, a 3-way split saves 3.5 us).
+    if (tiles >= slots) {
         set_ksplit(p, 1, tiles);
         return;
     }
