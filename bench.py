@@ -57,8 +57,8 @@ DRAM_TRAFFIC = {
     ("7b_prefill", "down_proj"): 419.78e6 + 221.32e6,
     ("7b_prefill_compact", "out_proj"): 83.42e6 + 101.20e6,
     ("7b_prefill_compact", "down_proj"): 404.95e6 + 114.63e6,
-    ("130m", "out_proj"): 13.85e6 + 36.33e6,
-    ("130m", "down_proj"): 57.29e6 + 38.87e6,
+    ("130m", "out_proj"): 13.85e6 + 36.27e6,
+    ("130m", "down_proj"): 57.34e6 + 38.90e6,
 }
 
 
