@@ -43,8 +43,10 @@ METRIC = "fused rowpar-GEMM+partial-reduce TFLOP/s & reduce GB/s (% of GB300 pea
 L2_BYTES = 129 * 2**20
 
 
-# untimed spin before each timed step (clock cycles, about 200 us)
-STEP_SPIN_CYCLES = 400000
+# untimed spin before each timed step (clock cycles, about 0.5 ms): the host needs
+# 140 - 330 us to queue a training step of four calls, and the spin keeps it ahead of
+# the GPU so that no host gap falls inside a timed call
+STEP_SPIN_CYCLES = 1000000
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # dominant forward kernel, from an ncu capture of the same workload with the
@@ -654,17 +656,17 @@ def run_e2e_tp(torch, ls, args, device, dist):
             "overlap": "none: copies in, step, copies out on one stream (per process)"}
 
 
-def _time_call(torch, fn, reps, flush=None):
+def _time_call(torch, fn, reps, flush=None, spin=100000):
     """Median device time of fn() (CUDA events on the current stream).  Before each
-    timed call the GPU gets an untimed head start (a spin kernel of ~50 us) so that
-    the host's launch work of a short call does not leave the GPU idle inside the
-    timed region."""
+    timed call the GPU gets an untimed head start (a spin kernel of `spin` cycles,
+    ~50 us by default; a step of several calls takes STEP_SPIN_CYCLES) so that the
+    host's launch work does not leave the GPU idle inside the timed region."""
     stream = torch.cuda.current_stream()
     ts = []
     for _ in range(reps):
         if flush is not None:
             flush.sum()
-        torch.cuda._sleep(100000)
+        torch.cuda._sleep(spin)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -707,7 +709,7 @@ def _compact_step(torch, caat, w, device, flush, peaks, random_s):
             caat.rowpar_linear_bwd_compact(d["X"], d["W"], d["dYS"], d["dYN"], w.t, sel=sel, dX=d["dX"],
                                            dW=d["dW"], workspace=d["wsb"])
     step()
-    sec = _time_call(torch, step, 10, flush)
+    sec = _time_call(torch, step, 10, flush, spin=STEP_SPIN_CYCLES)
     fl = sum(6.0 * w.N * L.K * w.h for L in w.layers)
     del lay
     torch.cuda.empty_cache()

@@ -941,7 +941,12 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         // keeps every tile whole; CAAT_FWD_SCHED=first runs the whole tiles first)
         p.balanced = 0;
         p.n_whole = p.num_n;
-        p.wgt = t;
+        // A whole tile of S costs about t pieces when it writes t copies.  With the
+        // compact outputs it writes one, so it is worth fewer pieces the shorter
+        // the shards: measured best near k-blocks / 2 + 2 (130M out-proj 35.3 ->
+        // 29.2 us, 1.1B 72.4 -> 66.0, 7B 104.1 -> 98.4; t for the long shards of
+        // the down-projections).
+        p.wgt = compact ? (p.nkb / 2 + 2 < t ? p.nkb / 2 + 2 : t) : t;
         if (const char *e = std::getenv("CAAT_FWD_WGT")) {
             const int v = std::atoi(e);
             if (v >= 1 && v <= t) p.wgt = v;
@@ -981,10 +986,15 @@ caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
                        BK, 1, wrows))
             return CAAT_ERR_UNSUPPORTED;
         caat_status st;
-        if (bn == 192)
+        if (bn == 192) {
+            // the deeper ring (5 stages, one staging buffer per warp) for shards of
+            // 4 or more k-blocks (override: CAAT_FWD_DEEP=0|1)
+            bool deep = p.nkb >= 4;
+            if (const char *e = std::getenv("CAAT_FWD_DEEP")) deep = e[0] == '1';
             st = cln == 2 ? launch_fwd<2, 192>(tmX, tmW, ym, p, s, compact)
-               : (p.nkb >= 4 ? launch_fwd<1, 192, true>(tmX, tmW, ym, p, s, compact)
-                             : launch_fwd<1, 192>(tmX, tmW, ym, p, s, compact));
+               : (deep ? launch_fwd<1, 192, true>(tmX, tmW, ym, p, s, compact)
+                       : launch_fwd<1, 192>(tmX, tmW, ym, p, s, compact));
+        }
         else {
             // two staging buffers where the bitmap leaves room (CAAT_FWD_STG=1: one)
             const char *stg_env = std::getenv("CAAT_FWD_STG");

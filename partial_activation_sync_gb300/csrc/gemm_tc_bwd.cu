@@ -591,11 +591,14 @@ void set_ksplit(GemmParams &p, int k, int tiles)
 // waves-of-work over `slots` workers, per part
 void pick_ksplit(GemmParams &p, int tiles, int slots)
 {
-    // Each extra part adds an fp32 reduce-add of the whole of dW; that only pays
-    // where the unsplit tiles do not fill one round of the slots (at the 1.1B
+    // Each extra part adds an fp32 reduce-add of the whole of dW.  Only tiles
+    // that do not fill one round of the slots are split (at the 1.1B
     // down-projection, 192 pair tiles on 76 pairs, a 7-way split added about
-    // 320 MB of reduce traffic and cost 35 us; at the 130M down-projection, 96
-    // tiles on 152 SMs, a 3-way split saves 3.5 us).
+    // 320 MB of reduce traffic and cost 35 us), and each extra part is charged
+    // 0.05 rounds: the 130M down-projection (96 tiles on 152 SMs) still splits
+    // three ways (2 rounds / 3 + 0.1 < 1; 3.5 us faster), the 1.1B out-projection
+    // (64 pair tiles on 76 pairs) no longer seven ways (6 rounds / 7 + 0.3 > 1;
+    // that split cost 15 us).
     if (tiles >= slots) {
         set_ksplit(p, 1, tiles);
         return;
@@ -603,7 +606,7 @@ void pick_ksplit(GemmParams &p, int tiles, int slots)
     int best = 1;
     double best_cost = (double)((tiles + slots - 1) / slots);
     for (int k = 2; k <= 8 && p.nkb / k >= 8; ++k) {
-        const double cost = (double)((tiles * k + slots - 1) / slots) / k;
+        const double cost = (double)((tiles * k + slots - 1) / slots) / k + 0.05 * (k - 1);
         if (cost < best_cost - 1e-9) { best = k; best_cost = cost; }
     }
     set_ksplit(p, best, tiles);
