@@ -31,7 +31,11 @@
  *    load; or the whole tiles first and the pieces after them, instead of the
  *    pieces in runs around each worker's whole tiles),
  *    CAAT_FWD_STG=1 (one staging buffer per epilogue warp in the 256-wide tiles
- *    instead of two where shared memory allows),
+ *    instead of two where shared memory allows), CAAT_FWD_DEEP=0|1 (the 192-wide
+ *    single-CTA tiles with 4 ring stages and two staging buffers, or 5 stages and
+ *    one; by default 5 for shards of 4 or more k-blocks), CAAT_FWD_WGT=1..t (the
+ *    pieces a whole tile's time is worth in the balanced schedule; by default t,
+ *    and for the compact outputs min(t, k-blocks per shard / 2 + 2)),
  *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
  *    (backward on `stream` only), CAAT_BWD_RING=4 (the backward GEMMs' ring at 4
  *    stages whatever the tile width; single CTAs only), CAAT_BWD_PAIR=0 (the
