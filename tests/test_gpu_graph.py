@@ -1,6 +1,7 @@
 """The library's calls inside a captured CUDA graph: the forward (tile and few-token
 kernels), the backward in both placements (its dW chain forks onto a side stream
-and joins back through events), and the column-parallel backward.  A replay must
+and joins back through events), the column-parallel backward, and the compact
+forward and backward (contiguous S and an index list).  A replay must
 give the results of the same calls run eagerly: bit for bit where the kernels fix
 the summation order, and within 1e-3 relative Frobenius for dW, whose token-split
 parts are added in whatever order they finish."""
@@ -90,6 +91,49 @@ def test_colpar_backward_replays_from_a_graph(caat):
     assert caat.device_status() == 0
     assert bool((dA.view(T.int16) == rA.view(T.int16)).all())
     assert rel_fro(to_f64(dW1), to_f64(rW)) <= 1e-3
+
+
+@pytest.mark.parametrize("layout", ["contiguous", "random"])
+def test_compact_calls_replay_from_a_graph(caat, layout):
+    """The compact forward and backward in a graph: with an index list of S they
+    also permute W's rows (and dW's) through the workspace, and the backward's dW
+    chain forks onto the side stream before that permute."""
+    T = torch()
+    from tests.gpu_helpers import sel_dev
+    t, N, kt, h = 8, 256, 96, 768
+    K = t * kt
+    S = caat.select_channels(h, 0.5, caat.CAAT_S_RANDOM if layout == "random" else caat.CAAT_S_CONTIGUOUS, 1701)
+    sel = sel_dev(S) if layout == "random" else int(S.size)
+    ns = int(S.size)
+    X = dev(ci.normal(1702, (N, K)), "bf16")
+    W = dev(np.ascontiguousarray(ci.normal(1703, (K, h), std=0.02).T), "bf16").t()
+    dYS = dev(ci.normal(1704, (N, ns)), "bf16")
+    dYN = [dev(ci.normal(1705 + r, (N, h - ns)), "bf16") for r in range(t)]
+    YS = T.empty((N, ns), dtype=T.bfloat16, device="cuda")
+    YN = [T.empty((N, h - ns), dtype=T.bfloat16, device="cuda") for _ in range(t)]
+    dX = T.empty((N, K), dtype=T.bfloat16, device="cuda")
+    dW = T.empty((h, K), dtype=T.bfloat16, device="cuda").t()
+    idx = layout == "random"
+    wsf = T.empty(max(caat.rowpar_linear_compact_workspace(t, N, K, h, 1, idx, False), 1), dtype=T.uint8,
+                  device="cuda")
+    wsb = T.empty(caat.rowpar_linear_compact_workspace(t, N, K, h, 1, idx, True), dtype=T.uint8, device="cuda")
+
+    def calls():
+        caat.rowpar_linear_fwd_compact(X, W, t, sel, YS=YS, YN=YN, workspace=wsf)
+        caat.rowpar_linear_bwd_compact(X, W, dYS, dYN, t, sel=sel, dX=dX, dW=dW, workspace=wsb)
+
+    calls()
+    T.cuda.synchronize()
+    ref = [YS.clone()] + [y.clone() for y in YN] + [dX.clone(), dW.clone()]
+    g = _capture(T, calls)
+    for buf in [YS] + YN + [dX, dW]:
+        buf.zero_()
+    g.replay()
+    T.cuda.synchronize()
+    assert caat.device_status() == 0
+    for a, b in zip([YS] + YN + [dX], ref[:-1]):
+        assert bool((a.view(T.int16) == b.view(T.int16)).all())
+    assert rel_fro(to_f64(dW), to_f64(ref[-1])) <= 1e-3
 
 
 @pytest.mark.parametrize("N", [1, 8, 64])
