@@ -180,7 +180,11 @@ caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, caat_dtype 
  *      every rank's reduced gradient.  An index list of all h channels can only be
  *      {0, ..., h-1} and takes the contiguous paths.
  * Precision: bf16 in, fp32 accumulate, one rounding to bf16; or fp32 throughout
- * (fp32 FMA, no TF32).
+ * (fp32 FMA, no TF32).  One exception: with an index list of S (0 < n_sel < h)
+ * the tile kernel (N > 128) writes every rank's whole partial first and the S
+ * channels then sum those bf16 partials in rank order (fp32 fold, one more
+ * rounding), so they may differ from the one-rounding sum by up to half an ulp of
+ * each partial.
  * Errors: INVALID_ARG for t outside 1..64, K % t != 0, negative sizes, a stride
  *         or leading dimension smaller than the row it spans, null pointers.
  *         UNSUPPORTED when no kernel takes the layout and alignment given (for

@@ -280,7 +280,7 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
         // CAAT_FWD_SKINNY=0 turns the first one off (for comparisons).
         const char *skinny_env = std::getenv("CAAT_FWD_SKINNY");
         const bool skinny_on = skinny_env == nullptr || std::strcmp(skinny_env, "0") != 0;
-        if (N <= 64 && skinny_on) {
+        if (N <= 128 && skinny_on) {
             st = launch_rowpar_fwd_skinny(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
             if (st != CAAT_ERR_UNSUPPORTED) return st;
         }

@@ -1,4 +1,4 @@
-// Row-parallel forward + partial channel-reduce for few tokens (N <= 64, decode
+// Row-parallel forward + partial channel-reduce for few tokens (N <= 128, decode
 // and small batches) on the tensor cores, operands swapped.
 //
 // "Tensor-Parallelism with Partially Synchronized Activations" (Introduction,
@@ -8,7 +8,7 @@
 //
 //   * one CTA per (128-channel block, shard r): it streams W_r[128 channels, k_t]
 //     and the few token rows of X_r through a TMA ring and accumulates
-//     D[channel, token] = W_r X_r^T in TMEM (tcgen05, M = 128 channels, N = 16..64
+//     D[channel, token] = W_r X_r^T in TMEM (tcgen05, M = 128 channels, N = 16..128
 //     tokens: the token count is the MMA's narrow side);
 //   * the t shard-CTAs of a channel block form one thread-block cluster: a channel
 //     outside S is final in its own CTA (rank r's partial goes to Y[r]); for the
@@ -53,9 +53,9 @@ constexpr int BK = 64;                       // k per stage (one 128-byte swizzl
 constexpr int MAX_STAGES = 6;
 // Ring depth by token tile: as deep as lets two CTAs share an SM (the 7B layers
 // launch 256 CTAs on 152 SMs): 6 stages of 18 KB at NT = 16, 5 of 20 KB at 32,
-// 4 of 24 KB at 64.
+// 4 of 24 KB at 64, 3 of 32 KB at 128.
 template <int NT>
-__host__ __device__ constexpr int stages() { return NT <= 16 ? 6 : (NT <= 32 ? 5 : 4); }
+__host__ __device__ constexpr int stages() { return NT <= 16 ? 6 : (NT <= 32 ? 5 : (NT <= 64 ? 4 : 3)); }
 constexpr int NUM_THREADS = 192;
 constexpr int W_BYTES = CH * BK * 2;         // 16 KB
 constexpr int MAX_T_SKINNY = 8;              // portable cluster size
@@ -153,7 +153,7 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     uint8_t *smW = base;
     uint8_t *smX = base + STAGES * W_BYTES;
     SkinnyCtl *ctl = (SkinnyCtl *)(base + STAGES * (W_BYTES + XB));
-    float *part = (float *)base;     // [NT][CH] fp32 partials, reusing the ring after the last MMA
+    float *part = (float *)base;     // [NT][CH] fp32 partials, reusing the ring (W and X stages) after the last MMA
     volatile int *abort = &ctl->abort;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -394,7 +394,7 @@ caat_status launch_nt(const CUtensorMap &tmX, const CUtensorMap &tmW, const Skin
     auto kern = rowpar_fwd_skinny_kernel<NT>;
     constexpr size_t smem = skinny_smem<NT>();
     static_assert(2 * (smem + 1024) <= 228 * 1024, "two CTAs per SM (1 KB reserved each)");
-    static_assert((size_t)NT * CH * 4 <= (size_t)stages<NT>() * W_BYTES, "partials fit in the ring");
+    static_assert((size_t)NT * CH * 4 <= (size_t)stages<NT>() * (W_BYTES + x_bytes<NT>()), "partials fit in the ring");
     if (prepare_kernel_smem((const void *)kern, (int)smem) != CAAT_OK) return CAAT_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -430,11 +430,11 @@ caat_status launch_rowpar_fwd_skinny(int t, int64_t N, int64_t K, int64_t h, con
                                      const int32_t *sel, int64_t n_sel, cudaStream_t s)
 {
     const int64_t kt = K / t;
-    if (t < 1 || t > MAX_T_SKINNY || N < 1 || N > 64 || kt < BK || kt % 8 != 0) return CAAT_ERR_UNSUPPORTED;
+    if (t < 1 || t > MAX_T_SKINNY || N < 1 || N > 128 || kt < BK || kt % 8 != 0) return CAAT_ERR_UNSUPPORTED;
     if (ldx % 8 != 0 || ldw % 8 != 0 || h < 1 || h > (int64_t)INT32_MAX / 2) return CAAT_ERR_UNSUPPORTED;
     if ((uintptr_t)X % 16 != 0 || (uintptr_t)W % 16 != 0) return CAAT_ERR_UNSUPPORTED;
     if (kt > (int64_t)INT32_MAX / 2 || N * ldy > (int64_t)INT32_MAX) return CAAT_ERR_UNSUPPORTED;
-    const int nt = N <= 16 ? 16 : (N <= 32 ? 32 : 64);
+    const int nt = N <= 16 ? 16 : (N <= 32 ? 32 : (N <= 64 ? 64 : 128));
     CUtensorMap tmX, tmW;
     {
         const uint64_t dims[3] = {(uint64_t)kt, (uint64_t)t, (uint64_t)N};
@@ -469,7 +469,8 @@ caat_status launch_rowpar_fwd_skinny(int t, int64_t N, int64_t K, int64_t h, con
     switch (nt) {
     case 16: return launch_nt<16>(tmX, tmW, p, (int)num_cb, s);
     case 32: return launch_nt<32>(tmX, tmW, p, (int)num_cb, s);
-    default: return launch_nt<64>(tmX, tmW, p, (int)num_cb, s);
+    case 64: return launch_nt<64>(tmX, tmW, p, (int)num_cb, s);
+    default: return launch_nt<128>(tmX, tmW, p, (int)num_cb, s);
     }
 }
 

@@ -178,7 +178,9 @@ def fwd_mode(request, monkeypatch):
 
 
 @pytest.mark.parametrize("t,N,kt,h", TC_FWD_SHAPES)
-def test_fwd_tc_parity(caat, t, N, kt, h, fwd_mode):
+def test_fwd_tc_parity(caat, t, N, kt, h, fwd_mode, monkeypatch):
+    # the tile kernel, also at N <= 128 where the few-token kernel would run
+    monkeypatch.setenv("CAAT_FWD_SKINNY", "0")
     # p = 1/h and 1 - 1/h: a single channel in S, a single channel outside it
     for p in (0.0, 1.0 / h, 0.25, 0.5, 0.75, 1.0 - 1.0 / h, 1.0):
         # contiguous S by size (balanced schedule) and as an index list; random S
@@ -290,7 +292,7 @@ def test_fwd_full_size_sampled_rows(caat, wname, li):
             del outs
 
 
-@pytest.mark.parametrize("Nd", [1, 8, 64])
+@pytest.mark.parametrize("Nd", [1, 8, 64, 128])
 @pytest.mark.parametrize("li", [0, 1])
 def test_fwd_7b_decode(caat, Nd, li):
     w = ci.WORKLOADS["7b_prefill"]
@@ -557,9 +559,9 @@ def test_bwd_contiguous_reduce_once_wide(caat, s):
 
 
 @pytest.mark.parametrize("t", [1, 2, 3, 4, 5, 7, 8])
-@pytest.mark.parametrize("N", [1, 3, 8, 15, 16, 17, 33, 48, 64])
+@pytest.mark.parametrize("N", [1, 3, 8, 15, 16, 17, 33, 48, 64, 65, 100, 128])
 def test_fwd_skinny_parity(caat, t, N):
-    """Few tokens (N <= 64, t <= 8): the swapped-operand tensor-core kernel, one
+    """Few tokens (N <= 128, t <= 8): the swapped-operand tensor-core kernel, one
     cluster of t shard-CTAs per 128-channel block; ragged channel blocks (h = 1000)
     and ragged shards (k_t = 136: the last 64-wide k block is part zero fill).
     t = 3, 5, 7 give the CTAs channel slices of the S sum (128 / t channels)
@@ -585,7 +587,7 @@ def test_fwd_skinny_declines_to_other_kernels(caat):
             check(got[r], want[r], "bf16", spread=spread)
 
 
-@pytest.mark.parametrize("N", [5, 40])
+@pytest.mark.parametrize("N", [5, 40, 100])
 def test_fwd_skinny_output_guard(caat, N):
     # rank outputs with a row stride wider than h and a ragged last channel block
     # (h = 200): the padding columns must stay untouched
