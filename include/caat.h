@@ -40,10 +40,10 @@
  *    (backward on `stream` only), CAAT_BWD_RING=4 (the backward GEMMs' ring at 4
  *    stages whatever the tile width; single CTAs only), CAAT_BWD_PAIR=0 (the
  *    backward GEMMs on single CTAs instead of CTA pairs), CAAT_PDL=0 (the
- *    few-token forward and the standalone reduce launched plainly instead of as
- *    programmatic dependents of the previous launch in the stream, whose blocks
- *    may then start while that launch finishes; they wait for it before they
- *    touch memory).
+ *    forward kernels, the backward GEMMs, the sum of the gradient's S channels
+ *    and the standalone reduce launched plainly instead of as programmatic
+ *    dependents of the previous launch in the stream, whose blocks may then start
+ *    while that launch finishes; they wait for it before they touch memory).
  *  - CAAT_CHECK_SEL=1 (a debug switch) checks every index list of S: the list is
  *    copied to the host on the call's stream, which is synchronised, and must be
  *    ascending, unique and inside [0, h), else the call returns INVALID_ARG

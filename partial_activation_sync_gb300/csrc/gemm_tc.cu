@@ -42,6 +42,7 @@
 
 #include <atomic>
 #include <cstdlib>
+#include <cstring>
 
 #include "caat_internal.h"
 #include "tc_ptx.cuh"
@@ -421,6 +422,12 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
+    // Launched as a programmatic dependent, this grid may have started while the
+    // previous one in the stream was still running: nothing above touched global
+    // memory (the tensor maps are launch parameters).  Wait for it before the
+    // first global read or write, then let the next grid start its own setup.
+    griddep_wait();
+    griddep_launch_dependents();
     if (warp != 0) {
         // The channel bitmap of S, built by the MMA and epilogue warps while the
         // producer already streams the first stages (it needs no bitmap): every
@@ -825,6 +832,16 @@ caat_status launch_fwd_v(const CUtensorMap &tmX, const CUtensorMap &tmW, const Y
     }
     if (groups > num_units) groups = num_units;
     cfg.gridDim = dim3(groups * per);
+    // a programmatic dependent of the previous launch in the stream (CAAT_PDL=0: a
+    // plain launch); the kernel waits for that grid before touching memory
+    cudaLaunchAttribute attr2[2] = {attr[0], {}};
+    const char *pdl_env = std::getenv("CAAT_PDL");
+    if (pdl_env == nullptr || std::strcmp(pdl_env, "0") != 0) {
+        attr2[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr2[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr2;
+        cfg.numAttrs = 2;
+    }
     if (cudaLaunchKernelEx(&cfg, kern, tmX, tmW, ym, p) != cudaSuccess) return CAAT_ERR_CUDA;
     note_launch("rowpar_fwd_tc");
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;

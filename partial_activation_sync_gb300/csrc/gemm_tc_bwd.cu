@@ -202,6 +202,10 @@ grouped_gemm_tc_kernel(const __grid_constant__ TmapArray amaps, const __grid_con
     __syncthreads();
     fence_after_sync();
     const uint32_t tmem = ctl->tmem_base;
+    // a programmatic dependent of the previous launch in the stream: wait for it
+    // before the first global read or write, then let the next grid set up
+    griddep_wait();
+    griddep_launch_dependents();
     // units are dealt round-robin to the workers (CTAs, or CTA pairs)
     const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
     const int nworkers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
@@ -434,20 +438,22 @@ caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &smap, cons
     const size_t smem = ring_smem(g);
     if (smem > SMEM_LIMIT || p.stages > MAX_STAGES) return CAAT_ERR_UNSUPPORTED;
     if (prepare_kernel_smem((const void *)kern, (int)SMEM_LIMIT) != CAAT_OK) return CAAT_ERR_CUDA;
-    if (!PAIR) {
-        const int grid = p.units < num_sms() ? p.units : num_sms();
-        kern<<<grid, NUM_THREADS, smem, s>>>(amaps, smap, bmap, cmap, p);
-    } else {
-        cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+    // a programmatic dependent of the previous launch in the stream (CAAT_PDL=0: a
+    // plain launch); the kernel waits for that grid before touching memory
+    const char *pdl_env = std::getenv("CAAT_PDL");
+    const bool pdl = pdl_env == nullptr || std::strcmp(pdl_env, "0") != 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    if (PAIR) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(NUM_THREADS);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = s;
-        cfg.attrs = attr;
         cfg.numAttrs = 1;
         int pairs = num_sms() / 2;
         cfg.gridDim = dim3(2 * pairs);
@@ -456,8 +462,15 @@ caat_status launch_grouped(const TmapArray &amaps, const CUtensorMap &smap, cons
         if (active < pairs) pairs = active;
         if (pairs > p.units) pairs = p.units;
         cfg.gridDim = dim3(2 * pairs);
-        if (cudaLaunchKernelEx(&cfg, kern, amaps, smap, bmap, cmap, p) != cudaSuccess) return CAAT_ERR_CUDA;
+    } else {
+        cfg.gridDim = dim3(p.units < num_sms() ? p.units : num_sms());
     }
+    if (pdl) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
+    }
+    if (cudaLaunchKernelEx(&cfg, kern, amaps, smap, bmap, cmap, p) != cudaSuccess) return CAAT_ERR_CUDA;
     note_launch(name);
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }

@@ -241,6 +241,10 @@ pcr_colsum_kernel(int t, int64_t N, int64_t s, ConstPtrs in, int64_t ld_in, uint
 {
     const int T = TT > 0 ? TT : t;
     const int64_t cpr = s / 8;
+    // a programmatic dependent of the previous launch: wait for it before reading
+    // its outputs, then let the next grid start its setup
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int64_t n = (int64_t)blockIdx.y * blockDim.y + threadIdx.y; n < N; n += (int64_t)gridDim.y * blockDim.y) {
         for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < cpr;
              j += (int64_t)gridDim.x * blockDim.x) {
@@ -331,10 +335,10 @@ caat_status launch_pcr_colsum(int t, int64_t N, int64_t s, const ConstPtrs &in, 
     const dim3 grid((unsigned)gx, (unsigned)gy), bx2((unsigned)bx, (unsigned)by);
     uint16_t *o = (uint16_t *)out;
     switch (t) {
-    case 2: pcr_colsum_kernel<2><<<grid, bx2, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
-    case 4: pcr_colsum_kernel<4><<<grid, bx2, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
-    case 8: pcr_colsum_kernel<8><<<grid, bx2, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
-    default: pcr_colsum_kernel<0><<<grid, bx2, 0, st>>>(t, N, s, in, ld_in, o, ld_out); break;
+    case 2: launch_dependent(pcr_colsum_kernel<2>, grid, bx2, 0, st, t, N, s, in, ld_in, o, ld_out); break;
+    case 4: launch_dependent(pcr_colsum_kernel<4>, grid, bx2, 0, st, t, N, s, in, ld_in, o, ld_out); break;
+    case 8: launch_dependent(pcr_colsum_kernel<8>, grid, bx2, 0, st, t, N, s, in, ld_in, o, ld_out); break;
+    default: launch_dependent(pcr_colsum_kernel<0>, grid, bx2, 0, st, t, N, s, in, ld_in, o, ld_out); break;
     }
     note_launch("pcr_colsum");
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;

@@ -234,3 +234,56 @@ def test_reduce_chain_with_programmatic_launch(caat, dtype, graph, monkeypatch):
         for r in range(t):
             np.testing.assert_array_equal(pdl[j][r], plain[j][r], err_msg="buffer %d rank %d" % (j, r))
     assert caat.device_status() == 0
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_layer_chain_with_programmatic_launch(caat, graph, monkeypatch):
+    """The tile forward, the backward GEMMs and the sum of the gradient's S
+    channels are launched as programmatic dependents of the previous launch: each
+    waits for it before touching memory.  A chain where every call reads what the
+    call before it wrote -- forward into the next forward's X, its outputs as the
+    backward's gradient, the backward's dX as the next forward's X -- must give the
+    same bits with and without that launch mode, in a stream and from a graph.  dW
+    is computed in one pass (no accumulator), so it is deterministic too."""
+    T = torch()
+    t, N, h = 8, 256, 768
+    K = h
+    depth = 3
+    Ws = [dev(np.ascontiguousarray(ci.normal(1800 + i, (K, h), std=0.05).T), "bf16").t() for i in range(depth)]
+    X0 = dev(ci.normal(1799, (N, K)), "bf16")
+    outs = [[T.empty((N, h), dtype=T.bfloat16, device="cuda") for _ in range(t)] for _ in range(depth)]
+    dXs = [T.empty((N, K), dtype=T.bfloat16, device="cuda") for _ in range(depth)]
+    dWs = [T.empty((h, K), dtype=T.bfloat16, device="cuda").t() for _ in range(depth)]
+    req = (caat.rowpar_linear_bwd_workspace(t, N, K, h, 1, caat.CAAT_BWD_REDUCE_DOUT)
+           - caat.rowpar_linear_bwd_workspace(t, N, K, h, 1, caat.CAAT_BWD_NO_REDUCE))
+    ws = T.empty(req, dtype=T.uint8, device="cuda")
+
+    def chain():
+        x = X0
+        for i in range(depth):
+            caat.rowpar_linear_fwd(x, Ws[i], t, h // 2, outs=outs[i])
+            caat.rowpar_linear_bwd(outs[i][1], Ws[i], outs[i], t, h // 2, caat.CAAT_BWD_REDUCE_DOUT,
+                                   dX=dXs[i], dW=dWs[i], workspace=ws)
+            x = dXs[i]
+
+    def run():
+        bufs = [y for o in outs for y in o] + dXs + dWs
+        for b in bufs:
+            b.fill_(float("nan"))
+        if graph:
+            g = _capture(T, chain)
+            for b in bufs:
+                b.fill_(float("nan"))
+            g.replay()
+        else:
+            chain()
+        T.cuda.synchronize()
+        return [b.contiguous().view(T.int16).cpu().numpy().copy() for b in bufs]
+
+    monkeypatch.setenv("CAAT_PDL", "0")
+    plain = run()
+    monkeypatch.setenv("CAAT_PDL", "1")
+    pdl = run()
+    assert caat.device_status() == 0
+    for i, (a, b) in enumerate(zip(pdl, plain)):
+        np.testing.assert_array_equal(a, b, err_msg="buffer %d" % i)
