@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -72,6 +74,30 @@ caat_status launch_rowpar_fwd_skinny(int t, int64_t N, int64_t K, int64_t h, con
 // YS == nullptr: the t outputs Y [N, h].  Otherwise the compact outputs (a
 // contiguous S, sel == nullptr, n_sel a multiple of 64): YS [N, n_sel] (row
 // stride ldys) once and Y = YN, t outputs [N, h - n_sel] (row stride ldy).
+// A launch as a programmatic dependent of the previous launch in the stream
+// (CAAT_PDL=0: a plain launch).  The kernel waits for that launch
+// (griddepcontrol.wait) before it touches memory, so only its start-up overlaps
+// the previous grid's end.  Launch errors are read by the caller.
+template <typename... Params, typename... Args>
+void launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                      Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    const char *env = std::getenv("CAAT_PDL");
+    if (env == nullptr || std::strcmp(env, "0") != 0) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    (void)cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 caat_status launch_rowpar_fwd_tc(int t, int64_t N, int64_t K, int64_t h,
                                  const void *X, int64_t ldx, const void *W, int64_t ldw,
                                  const MutPtrs &Y, int64_t ldy,

@@ -525,6 +525,8 @@ f32_rows_to_bf16_kernel(const float *__restrict__ src, int64_t rows, int64_t col
 {
     const int64_t per_row = cols / 8;
     const int64_t total = rows * per_row;
+    griddep_wait();                  // a programmatic dependent of the accumulating GEMM
+    griddep_launch_dependents();
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t rr = i / per_row, c = (i - rr * per_row) * 8;
@@ -552,6 +554,11 @@ permute_rows_kernel(const uint16_t *__restrict__ src, int64_t lds, uint16_t *__r
                     int staged)
 {
     extern __shared__ int32_t ssel[];
+    // A programmatic dependent of the previous launch.  It does not let its own
+    // dependent start early: that is the dX GEMM, whose persistent CTAs would sit
+    // on every SM waiting for this short kernel and keep the dW GEMM (on the side
+    // stream, which needs no permuted W) from running beside it.
+    griddep_wait();
     if (staged) {
         for (int64_t i = threadIdx.x; i < n_sel; i += blockDim.x) ssel[i] = __ldg(sel + i);
         __syncthreads();
@@ -814,8 +821,8 @@ caat_status launch_rowpar_bwd_tc(int t, int64_t N, int64_t K, int64_t h, const v
         const int64_t total = h * (K / 8);
         int64_t blocks = (total + 255) / 256;
         if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
-        f32_rows_to_bf16_kernel<<<(unsigned)blocks, 256, 0, sw>>>(wacc, h, K, K, (uint16_t *)dW, ld_dw, row_sel,
-                                                                  row_nsel);
+        launch_dependent(f32_rows_to_bf16_kernel, dim3((unsigned)blocks), dim3(256), 0, sw, (const float *)wacc, h,
+                         K, K, (uint16_t *)dW, ld_dw, row_sel, row_nsel);
         note_launch("rowpar_bwd_dw_tc", 1);
         return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
     };
@@ -832,8 +839,8 @@ caat_status launch_permute_rows(const void *src, int64_t lds, void *dst, int64_t
     if (blocks > (int64_t)num_sms() * 8) blocks = (int64_t)num_sms() * 8;
     const bool staged = n_sel <= 8192;                // up to 32 KB of shared memory
     const size_t smem = staged ? (size_t)n_sel * 4 : 0;
-    permute_rows_kernel<<<(unsigned)blocks, 256, smem, s>>>((const uint16_t *)src, lds, (uint16_t *)dst, ldd, h, K,
-                                                             sel, n_sel, to_s_first ? 1 : 0, staged ? 1 : 0);
+    launch_dependent(permute_rows_kernel, dim3((unsigned)blocks), dim3(256), smem, s, (const uint16_t *)src, lds,
+                     (uint16_t *)dst, ldd, h, K, sel, n_sel, to_s_first ? 1 : 0, staged ? 1 : 0);
     note_launch("permute_rows", 1);
     return cudaGetLastError() == cudaSuccess ? CAAT_OK : CAAT_ERR_CUDA;
 }

@@ -266,28 +266,6 @@ pcr_colsum_kernel(int t, int64_t N, int64_t s, ConstPtrs in, int64_t ld_in, uint
     }
 }
 
-// A launch as a programmatic dependent of the previous launch in the stream
-// (CAAT_PDL=0: a plain launch).  The kernel waits for that launch before it
-// touches memory, so only its start-up overlaps the previous grid's end.
-template <typename... Params, typename... Args>
-void launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                      Args... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    const char *env = std::getenv("CAAT_PDL");
-    if (env == nullptr || std::strcmp(env, "0") != 0) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    (void)cudaLaunchKernelEx(&cfg, kern, args...);   // errors are read by the caller
-}
 
 template <int TT, bool BF16, bool INPLACE>
 void launch_vec(dim3 grid, dim3 block, size_t smem, cudaStream_t s, int t, int64_t N, int64_t h,
