@@ -464,9 +464,6 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
         if (lane == 0 && p.inject != CAAT_INJECT_SKIP_LOADS) {
             int stage = 0;
             uint32_t ph = 0;
-#ifdef EXP_LOAD_HINT
-            const uint64_t pol_in = policy_evict_last();
-#endif
             Cursor cur;
             cursor_init(cur, p, worker, nworkers, num_mg);
             Work wk;
@@ -484,15 +481,9 @@ rowpar_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
                             // both CTAs' halves land on the pair leader's barrier
                             const uint32_t fl = map_to_cta(fb, leader);
                             if (is_leader) mbar_arrive_expect_tx(fb, C::TX_BYTES);
-#ifdef EXP_LOAD_HINT
-                            tma_load_3d_pair_hint(smem_u32(smA + stage * A_BYTES), &tmX, fl, kb * BK, r, mb * BM, pol_in);
-                            tma_load_3d_pair_hint(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
-                                             nb * BNT + (int)crank * C::B_ROWS, pol_in);
-#else
                             tma_load_3d_pair(smem_u32(smA + stage * A_BYTES), &tmX, fl, kb * BK, r, mb * BM);
                             tma_load_3d_pair(smem_u32(smB + stage * C::B_BYTES), &tmW, fl, kb * BK, r,
                                              nb * BNT + (int)crank * C::B_ROWS);
-#endif
                         } else {
                             mbar_arrive_expect_tx(fb, C::TX_BYTES);
                             tma_load_3d(smem_u32(smA + stage * A_BYTES), &tmX, fb, kb * BK, r, mb * BM);

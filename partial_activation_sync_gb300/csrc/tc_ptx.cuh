@@ -197,51 +197,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr)
                  : "memory");
 }
 
-// L2 eviction-priority policies for the cache_hint forms below
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const void *tmap, uint32_t bar, int c0,
-                                                 int c1, int c2, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void *tmap, uint32_t bar, int c0,
-                                                      int c1, int c2, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-        "l"(tmap), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_store_2d_hint(const void *tmap, uint32_t src, int c0, int c1,
-                                                  uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;" ::"l"(
-            tmap),
-        "r"(src), "r"(c0), "r"(c1), "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
     uint32_t r;
