@@ -55,12 +55,12 @@ STEP_SPIN_CYCLES = 1000000
 # workload or layer without a capture reports null.  Output lines still dirty in
 # L2 when the kernel ends are not in the count.
 DRAM_TRAFFIC = {
-    ("7b_prefill", "out_proj"): 118.12e6 + 208.16e6,
-    ("7b_prefill", "down_proj"): 419.78e6 + 221.32e6,
-    ("7b_prefill_compact", "out_proj"): 83.42e6 + 101.20e6,
-    ("7b_prefill_compact", "down_proj"): 404.95e6 + 114.63e6,
-    ("130m", "out_proj"): 13.85e6 + 36.27e6,
-    ("130m", "down_proj"): 57.34e6 + 38.90e6,
+    ("7b_prefill", "out_proj"): 118.40e6 + 208.71e6,
+    ("7b_prefill", "down_proj"): 419.26e6 + 221.02e6,
+    ("7b_prefill_compact", "out_proj"): 80.22e6 + 100.05e6,
+    ("7b_prefill_compact", "down_proj"): 404.57e6 + 115.12e6,
+    ("130m", "out_proj"): 13.85e6 + 36.30e6,
+    ("130m", "down_proj"): 57.29e6 + 38.94e6,
 }
 
 
