@@ -544,7 +544,7 @@ f32_rows_to_bf16_kernel(const float *__restrict__ src, int64_t rows, int64_t col
 
 // Rows of a bf16 [h, K] matrix between channel order and the S-first order: with
 // to_s_first, dst row s_first_pos(c) = src row c; else dst row c = src row
-// s_first_pos(c).  One warp per row, 16-byte copies, four in flight per lane.
+// s_first_pos(c).  One warp per row, 16-byte copies, eight in flight per lane.
 // With room for it (dynamic shared memory of n_sel entries) S is staged in
 // shared memory first, so that each row's binary search does not wait on a
 // chain of global loads.
