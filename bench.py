@@ -875,6 +875,37 @@ def run_extras(torch, caat, device, peaks, args):
                         "graph_static_weights_frac_hbm": round(byt / sec_w / 1e9 / peaks["hbm"], 4)})
             out["7b_decode_N%d_%s" % (Nd, L.name)] = rec
             del X, Ys, graph, graph_w
+        # a short prefill, 256 tokens, S by its size: the few-token kernel in two
+        # chunks of 128 tokens against the tile kernel (CAAT_FWD_SKINNY=0), per call
+        # in the graph
+        Np = 256
+        n_sel = int(sel.numel())
+        X = torch.randn((Np, L.K), device=device).to(torch.bfloat16)
+        Ys = [torch.empty((Np, w.h), dtype=torch.bfloat16, device=device) for _ in range(w.t)]
+        rec = {}
+        for key, env in (("", None), ("tile_kernel_", "0")):
+            prev = os.environ.get("CAAT_FWD_SKINNY")
+            if env is not None:
+                os.environ["CAAT_FWD_SKINNY"] = env
+            try:
+                caat.rowpar_linear_fwd(X, Wst.t(), w.t, n_sel, outs=Ys)
+                kern = caat.last_kernel()
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph):
+                    for Wk in Wsets:
+                        caat.rowpar_linear_fwd(X, Wk.t(), w.t, n_sel, outs=Ys)
+            finally:
+                if prev is None:
+                    os.environ.pop("CAAT_FWD_SKINNY", None)
+                else:
+                    os.environ["CAAT_FWD_SKINNY"] = prev
+            graph.replay()
+            sec_g = _time_call(torch, graph.replay, 10, flush) / nsets
+            rec.update({key + "kernel": kern, key + "graph_us": round(sec_g * 1e6, 2),
+                        key + "graph_TFLOP/s": round(2.0 * Np * L.K * w.h / sec_g / 1e12, 1)})
+            del graph
+        out["7b_prefill_N%d_%s" % (Np, L.name)] = rec
+        del X, Ys
         del Wsets, Wst
     # column-parallel layer at the 130M MLP up-projection (N = 8192, h = 768,
     # FFN 3072, t = 8, p = 0.5): forward, and the backward with the partial reduce

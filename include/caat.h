@@ -36,7 +36,10 @@
  *    one; by default 5 for shards of 4 or more k-blocks), CAAT_FWD_WGT=1..t (the
  *    pieces a whole tile's time is worth in the balanced schedule; by default t,
  *    and for the compact outputs min(t, k-blocks per shard / 2 + 2)),
- *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_BWD_SIDE_STREAM=0
+ *    CAAT_FWD_SKINNY=0 (no few-token tensor-core kernel), CAAT_FWD_SKINNY_MAX=n
+ *    (the most tokens it takes: by default 256 for a contiguous S given by its
+ *    size, 128 for an index list; above 128 it runs chunks of 128 tokens and
+ *    declines a grid of more than four CTAs per SM), CAAT_BWD_SIDE_STREAM=0
  *    (backward on `stream` only), CAAT_BWD_RING=4 (the backward GEMMs' ring at 4
  *    stages whatever the tile width; single CTAs only), CAAT_BWD_PAIR=0 (the
  *    backward GEMMs on single CTAs instead of CTA pairs), CAAT_PDL=0 (the
@@ -181,10 +184,10 @@ caat_status caat_partial_channel_reduce(int t, int64_t N, int64_t h, caat_dtype 
  *      {0, ..., h-1} and takes the contiguous paths.
  * Precision: bf16 in, fp32 accumulate, one rounding to bf16; or fp32 throughout
  * (fp32 FMA, no TF32).  One exception: with an index list of S (0 < n_sel < h)
- * the tile kernel (N > 128) writes every rank's whole partial first and the S
- * channels then sum those bf16 partials in rank order (fp32 fold, one more
- * rounding), so they may differ from the one-rounding sum by up to half an ulp of
- * each partial.
+ * the tile kernel (the calls the few-token kernel does not take) writes every
+ * rank's whole partial first and the S channels then sum those bf16 partials in
+ * rank order (fp32 fold, one more rounding), so they may differ from the
+ * one-rounding sum by up to half an ulp of each partial.
  * Errors: INVALID_ARG for t outside 1..64, K % t != 0, negative sizes, a stride
  *         or leading dimension smaller than the row it spans, null pointers.
  *         UNSUPPORTED when no kernel takes the layout and alignment given (for

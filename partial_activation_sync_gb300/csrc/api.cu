@@ -277,10 +277,20 @@ extern "C" caat_status caat_rowpar_linear_fwd(int t, int64_t N, int64_t K, int64
         // a few tokens: the swapped-operand tensor-core kernel (one cluster of
         // shard-CTAs per channel block), else weight streaming on the CUDA cores;
         // otherwise the tile kernel (decode kernel again if that one declines).
-        // CAAT_FWD_SKINNY=0 turns the first one off (for comparisons).
+        // CAAT_FWD_SKINNY=0 turns the first one off (for comparisons);
+        // CAAT_FWD_SKINNY_MAX=n moves its token bound (chunks of 128 tokens above 128).
         const char *skinny_env = std::getenv("CAAT_FWD_SKINNY");
         const bool skinny_on = skinny_env == nullptr || std::strcmp(skinny_env, "0") != 0;
-        if (N <= 128 && skinny_on) {
+        // A contiguous S given by its size, up to 256 tokens: at the 7B shapes two
+        // chunks (512 CTAs, two per SM) beat the tile kernel, whose whole tiles of S
+        // run all t shards on one CTA (out-proj 33.9 -> 28.2 us at 160 tokens, 34.1
+        // -> 32.1 at 256; down-proj 66.1 -> 44.8 and 66.9 -> 48.8); from three chunks
+        // on the extra waves lose.  With an index list the tile kernel cuts every
+        // tile into per-shard pieces (the S sums then fold rounded partials) and is
+        // the faster one above 128 tokens (256 tokens: 23.9 / 35.4 us).
+        int64_t skinny_max = sel == nullptr ? 256 : 128;
+        if (const char *e = std::getenv("CAAT_FWD_SKINNY_MAX")) skinny_max = std::atoll(e);
+        if (N <= skinny_max && skinny_on) {
             st = launch_rowpar_fwd_skinny(t, N, K, h, X, ldx, W, w_cs, py, ldy, sel, n_sel, s);
             if (st != CAAT_ERR_UNSUPPORTED) return st;
         }

@@ -65,8 +65,10 @@ caat_status launch_batched_gemm_simt(const BatchedGemm &g, cudaStream_t s);
 // ---- tcgen05 tensor-core paths (gemm_tc.cu)
 // Returns CAAT_ERR_UNSUPPORTED (without launching) when the shape/layout is not
 // one the tensor-core kernel takes; the caller then picks another kernel.
-// few tokens (1 <= N <= 128, t <= 8): tensor cores with the operands swapped, one
-// cluster of t shard-CTAs per 128-channel block
+// few tokens (1 <= N <= 8192, t <= 8): tensor cores with the operands swapped, one
+// cluster of t shard-CTAs per (128-channel block, chunk of up to 128 tokens).
+// Above 128 tokens it declines (CAAT_ERR_UNSUPPORTED) a grid of more than four
+// CTAs per SM, where the tile kernel is the faster one.
 caat_status launch_rowpar_fwd_skinny(int t, int64_t N, int64_t K, int64_t h, const void *X, int64_t ldx,
                                      const void *W, int64_t ldw, const MutPtrs &Y, int64_t ldy,
                                      const int32_t *sel, int64_t n_sel, cudaStream_t s);

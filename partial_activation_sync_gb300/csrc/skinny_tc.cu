@@ -1,5 +1,5 @@
-// Row-parallel forward + partial channel-reduce for few tokens (N <= 128, decode
-// and small batches) on the tensor cores, operands swapped.
+// Row-parallel forward + partial channel-reduce for few tokens (decode and small
+// batches, up to a few hundred tokens) on the tensor cores, operands swapped.
 //
 // "Tensor-Parallelism with Partially Synchronized Activations" (Introduction,
 // partial channel-reduce; inference with the partial reduce in place of the
@@ -14,7 +14,10 @@
 //     outside S is final in its own CTA (rank r's partial goes to Y[r]); for the
 //     channels of S every CTA puts its fp32 partial tile in shared memory, and CTA
 //     q sums a 1/t slice of the channels over the cluster (distributed shared
-//     memory, rank order 0..t-1) and writes the sum to all t outputs.
+//     memory, rank order 0..t-1) and writes the sum to all t outputs;
+//   * above 128 tokens the tokens are cut into chunks of 128, one cluster per
+//     (channel block, chunk): the chunks of a block read the same weight tiles,
+//     the first from HBM and the others mostly from L2.
 //
 // Warp roles: warp 0 issues the TMA loads, warp 1 owns TMEM and issues the MMAs,
 // warps 2..5 read the accumulator back (warp w reads TMEM lanes 32*(w%4)..).
@@ -59,6 +62,7 @@ __host__ __device__ constexpr int stages() { return NT <= 16 ? 6 : (NT <= 32 ? 5
 constexpr int NUM_THREADS = 192;
 constexpr int W_BYTES = CH * BK * 2;         // 16 KB
 constexpr int MAX_T_SKINNY = 8;              // portable cluster size
+constexpr int64_t SKINNY_MAX_N = 8192;       // token rows (chunks of 128 above 128 tokens)
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;
 
 struct SkinnyCtl {
@@ -79,6 +83,7 @@ struct SkinnyParams {
     const int32_t *sel;
     int64_t n_sel;
     int prefetch_w;                          // weight tiles of the first stages before the wait
+    int nchunks;                             // token chunks of NT rows (clusters per channel block)
 };
 
 template <int NT>
@@ -159,8 +164,14 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int t = p.t;
     const int r = t > 1 ? (int)cluster_ctarank() : 0;
-    const int cb = (int)(blockIdx.x / (unsigned)t);
+    // cluster index -> (channel block, token chunk), the chunks of a channel block
+    // adjacent so that they read its weight tiles at about the same time (from L2
+    // after the first)
+    const int ci = (int)(blockIdx.x / (unsigned)t);
+    const int cb = ci / p.nchunks;
     const int64_t c0 = (int64_t)cb * CH;
+    const int64_t tok0 = (int64_t)(ci % p.nchunks) * NT;
+    const int ntok = p.N - tok0 < NT ? (int)(p.N - tok0) : NT;   // token rows of this chunk (>= 1)
 
     if (tid < CH / 32) ctl->smask[tid] = 0u;
     if (tid == 0) {
@@ -209,7 +220,7 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 }
                 griddep_wait();
                 for (int kb = 0; kb < pre; ++kb)
-                    tma_load_3d(smem_u32(smX + kb * XB), &tmX, smem_u32(&ctl->full[kb]), kb * BK, r, 0);
+                    tma_load_3d(smem_u32(smX + kb * XB), &tmX, smem_u32(&ctl->full[kb]), kb * BK, r, (int)tok0);
                 kb0 = pre;
                 stage = pre % STAGES;
                 ph = pre == STAGES ? 1u : 0u;
@@ -222,7 +233,7 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 const uint32_t fb = smem_u32(&ctl->full[stage]);
                 mbar_arrive_expect_tx(fb, TX);
                 tma_load_3d(smem_u32(smW + stage * W_BYTES), &tmW, fb, kb * BK, r, (int)c0);
-                tma_load_3d(smem_u32(smX + stage * XB), &tmX, fb, kb * BK, r, 0);
+                tma_load_3d(smem_u32(smX + stage * XB), &tmX, fb, kb * BK, r, (int)tok0);
                 if (++stage == STAGES) { stage = 0; ph ^= 1u; }
             }
         }
@@ -302,7 +313,6 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
 #pragma unroll
             for (int qq = 0; qq < MAX_T_SKINNY; ++qq)
                 if (qq == r) yr = (uint16_t *)p.Y[qq];
-            const int ntok = p.N < NT ? (int)p.N : NT;
             for (int it = e; it < ntok * (CH / 8); it += 128) {
                 const int tok = it / (CH / 8), cl0 = 8 * (it % (CH / 8));
                 const int64_t ch0 = c0 + cl0;
@@ -312,7 +322,7 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 const float4 a = *reinterpret_cast<const float4 *>(part + tok * CH + cl0);
                 const float4 b = *reinterpret_cast<const float4 *>(part + tok * CH + cl0 + 4);
                 const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-                store8(yr + tok * p.ldy, ch0, p.h, ~sbits & 0xffu, p.vec != 0, v);
+                store8(yr + (tok0 + tok) * p.ldy, ch0, p.h, ~sbits & 0xffu, p.vec != 0, v);
             }
         }
     }
@@ -327,7 +337,6 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
             // channels are loaded before they are added in rank order 0..t-1
             const int e = tid - 64;
             const int lo = (r * CH) / t, hi = ((r + 1) * CH) / t;
-            const int ntok = p.N < NT ? (int)p.N : NT;
             const uint32_t my_part = smem_u32(part);
             const int g0 = lo / 8, g1 = (hi + 7) / 8;        // 8-channel groups touching [lo, hi)
             const int ng = g1 - g0;
@@ -363,7 +372,7 @@ rowpar_fwd_skinny_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_c
                 }
 #pragma unroll
                 for (int qq = 0; qq < MAX_T_SKINNY; ++qq)
-                    if (qq < t) store8((uint16_t *)p.Y[qq] + tok * p.ldy, ch0, p.h, want, p.vec != 0, v);
+                    if (qq < t) store8((uint16_t *)p.Y[qq] + (tok0 + tok) * p.ldy, ch0, p.h, want, p.vec != 0, v);
             }
         }
         cluster_sync();              // no CTA leaves while another reads its tile
@@ -402,7 +411,7 @@ caat_status launch_nt(const CUtensorMap &tmX, const CUtensorMap &tmW, const Skin
     attr[0].val.clusterDim.x = (unsigned)p.t;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3((unsigned)(p.t * num_cb));
+    cfg.gridDim = dim3((unsigned)(p.t * num_cb * p.nchunks));
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -430,7 +439,7 @@ caat_status launch_rowpar_fwd_skinny(int t, int64_t N, int64_t K, int64_t h, con
                                      const int32_t *sel, int64_t n_sel, cudaStream_t s)
 {
     const int64_t kt = K / t;
-    if (t < 1 || t > MAX_T_SKINNY || N < 1 || N > 128 || kt < BK || kt % 8 != 0) return CAAT_ERR_UNSUPPORTED;
+    if (t < 1 || t > MAX_T_SKINNY || N < 1 || N > SKINNY_MAX_N || kt < BK || kt % 8 != 0) return CAAT_ERR_UNSUPPORTED;
     if (ldx % 8 != 0 || ldw % 8 != 0 || h < 1 || h > (int64_t)INT32_MAX / 2) return CAAT_ERR_UNSUPPORTED;
     if ((uintptr_t)X % 16 != 0 || (uintptr_t)W % 16 != 0) return CAAT_ERR_UNSUPPORTED;
     if (kt > (int64_t)INT32_MAX / 2 || N * ldy > (int64_t)INT32_MAX) return CAAT_ERR_UNSUPPORTED;
@@ -464,8 +473,13 @@ caat_status launch_rowpar_fwd_skinny(int t, int64_t N, int64_t K, int64_t h, con
     p.n_sel = n_sel;
     const char *pw_env = std::getenv("CAAT_PDL_WEIGHTS");
     p.prefetch_w = pw_env != nullptr && std::strcmp(pw_env, "1") == 0;
+    p.nchunks = (int)((N + nt - 1) / nt);
     const int64_t num_cb = (h + CH - 1) / CH;
-    if (num_cb * t > INT32_MAX) return CAAT_ERR_UNSUPPORTED;
+    if (num_cb * t * p.nchunks > INT32_MAX) return CAAT_ERR_UNSUPPORTED;
+    // Token chunks re-read each weight tile from L2, and more than two CTAs per SM
+    // run in several waves: at the 7B shapes (256 CTAs a chunk) two chunks are
+    // faster than the tile kernel, three are slower.
+    if (p.nchunks > 1 && num_cb * t * p.nchunks > 4 * (int64_t)num_sms()) return CAAT_ERR_UNSUPPORTED;
     switch (nt) {
     case 16: return launch_nt<16>(tmX, tmW, p, (int)num_cb, s);
     case 32: return launch_nt<32>(tmX, tmW, p, (int)num_cb, s);

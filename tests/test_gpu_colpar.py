@@ -90,7 +90,7 @@ def test_colpar_tensor_core_shapes(caat, t, N, h, K, p, layout):
     _check(got, want, S, t, "bf16")
     # the tensor-core kernels ran (no fallback to the CUDA-core GEMMs)
     assert kernels[0] == "rowpar_bwd_dx_tc"
-    assert kernels[1] == "rowpar_fwd_tc"
+    assert kernels[1] in ("rowpar_fwd_tc", "rowpar_fwd_skinny_tc")
 
 
 def test_colpar_contiguous_set_by_size(caat):

@@ -27,6 +27,7 @@ def caat():
 def test_forward_wait_timeout_reported_then_context_usable(caat, cluster, kt, monkeypatch):
     T = torch()
     monkeypatch.setenv("CAAT_FWD_CLUSTER", cluster)
+    monkeypatch.setenv("CAAT_FWD_SKINNY", "0")      # the tile kernel (the few-token one takes N <= 256)
     t, N, h = 2, 256, 256
     X = ci.normal(1901, (N, kt * t))
     Wl = ci.normal(1902, (kt * t, h), std=0.02)

@@ -136,7 +136,7 @@ def test_compact_calls_replay_from_a_graph(caat, layout):
     assert rel_fro(to_f64(dW), to_f64(ref[-1])) <= 1e-3
 
 
-@pytest.mark.parametrize("N", [1, 8, 64])
+@pytest.mark.parametrize("N", [1, 8, 64, 200])
 @pytest.mark.parametrize("graph", [False, True])
 def test_few_token_chain_with_programmatic_launch(caat, N, graph, monkeypatch):
     """The few-token kernel is launched as a programmatic dependent of the

@@ -170,6 +170,7 @@ def fwd_mode(request, monkeypatch):
     # per-shard pieces of NO_S tiles); ":f": whole tiles first, pieces after
     mode, _, opt = request.param.partition(":")
     cl, _, bn = mode.partition("/")
+    monkeypatch.setenv("CAAT_FWD_SKINNY", "0")      # the tile kernel at any token count
     monkeypatch.setenv("CAAT_FWD_CLUSTER", cl)
     monkeypatch.setenv("CAAT_FWD_BN", bn or "256")
     monkeypatch.setenv("CAAT_FWD_ORDER", "m" if opt == "m" else "n")
@@ -179,7 +180,7 @@ def fwd_mode(request, monkeypatch):
 
 @pytest.mark.parametrize("t,N,kt,h", TC_FWD_SHAPES)
 def test_fwd_tc_parity(caat, t, N, kt, h, fwd_mode, monkeypatch):
-    # the tile kernel, also at N <= 128 where the few-token kernel would run
+    # the tile kernel, also at N <= 256 where the few-token kernel would run
     monkeypatch.setenv("CAAT_FWD_SKINNY", "0")
     # p = 1/h and 1 - 1/h: a single channel in S, a single channel outside it
     for p in (0.0, 1.0 / h, 0.25, 0.5, 0.75, 1.0 - 1.0 / h, 1.0):
@@ -575,6 +576,45 @@ def test_fwd_skinny_parity(caat, t, N):
                     check(got[r], want[r], "bf16", what=(h, r, p, layout), spread=spread)
                 for r in range(1, t):
                     assert np.array_equal(got[r][:, S], got[0][:, S])
+
+
+@pytest.mark.parametrize("t", [1, 3, 8])
+@pytest.mark.parametrize("N", [129, 200, 256, 385])
+def test_fwd_skinny_token_chunks(caat, t, N, monkeypatch):
+    """Above 128 tokens the swapped-operand kernel runs one cluster per
+    (128-channel block, chunk of 128 tokens), taken here by raising its token
+    bound: every chunk's rows land in their own output rows, the last chunk
+    ragged (N = 129 leaves one row in it), and the S sums agree across ranks."""
+    monkeypatch.setenv("CAAT_FWD_SKINNY_MAX", "8192")
+    for h, kt in ((1000, 136), (512, 64)):
+        for p, layout in ((0.5, 0), (0.5, 1), (1.0, 0)):
+            got, want, S, spread = _fwd_case(caat, t, N, kt * t, h, p, layout, "bf16", "nn", seed=7 * t + N + h)
+            assert caat.last_kernel() == "rowpar_fwd_skinny_tc"
+            for r in range(t):
+                check(got[r], want[r], "bf16", what=(h, r, p, layout), spread=spread)
+            for r in range(1, t):
+                assert np.array_equal(got[r][:, S], got[0][:, S])
+
+
+def test_fwd_skinny_token_chunks_guard(caat, monkeypatch):
+    # token chunks into rank outputs with a row stride wider than h: the padding
+    # columns and the row after the last stay untouched
+    monkeypatch.setenv("CAAT_FWD_SKINNY_MAX", "8192")
+    T = torch()
+    t, N, kt, h, ld = 4, 300, 64, 200, 264
+    X = ci.normal(907, (N, kt * t))
+    Wl = ci.normal(908, (kt * t, h), std=0.02)
+    S = caat.select_channels(h, 0.5, 1, 6)
+    bufs = [T.full((N + 1, ld), 7.0, dtype=T.bfloat16, device="cuda") for _ in range(t)]
+    outs = [b[:N, :h] for b in bufs]
+    caat.rowpar_linear_fwd(dev(X, "bf16"), _weight(Wl, "bf16", "nn"), t, sel_dev(S), outs=outs)
+    T.cuda.synchronize()
+    assert caat.last_kernel() == "rowpar_fwd_skinny_tc"
+    for b in bufs:
+        assert bool((b[:, h:] == 7.0).all()) and bool((b[N] == 7.0).all())
+    want, _ = orc.rowpar_fwd(host_values(X, "bf16"), host_values(Wl, "bf16"), t, S)
+    for r in range(t):
+        check(to_f64(outs[r]), want[r], "bf16")
 
 
 def test_fwd_skinny_declines_to_other_kernels(caat):
