@@ -10,7 +10,7 @@ of the upstream gradient, dX, dW).  Metric: algorithmic TFLOP/s (2NKh forward,
 4NKh backward per layer, independent of p).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl caat|reference]
-                  [--workload 7b_prefill|130m|1.1b|7b_decode8|130m_stack]
+                  [--workload 7b_prefill|130m|1.1b|7b_decode8|7b_prefill256|130m_stack]
                   [--layout contiguous|random] [--p P] [--t T] [--placement reduce_dout|column]
                   [--no-extras] [--no-stack]
 
@@ -51,7 +51,8 @@ STEP_SPIN_CYCLES = 1000000
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the
 # dominant forward kernel, from an ncu capture of the same workload with the
 # kernels as they are now (7B prefill: the full capture of one step, plain and
-# compact outputs; 130M: the one-pass launch list, averaged over its steps); a
+# compact outputs, and at 256 tokens; 130M: the one-pass launch list, averaged
+# over its steps); a
 # workload or layer without a capture reports null.  Output lines still dirty in
 # L2 when the kernel ends are not in the count.
 DRAM_TRAFFIC = {
@@ -61,6 +62,8 @@ DRAM_TRAFFIC = {
     ("7b_prefill_compact", "down_proj"): 404.57e6 + 115.12e6,
     ("130m", "out_proj"): 13.85e6 + 36.30e6,
     ("130m", "down_proj"): 57.29e6 + 38.94e6,
+    ("7b_prefill256", "out_proj"): 35.69e6 + 0.06e6,
+    ("7b_prefill256", "down_proj"): 95.91e6 + 3.93e6,
 }
 
 
@@ -440,8 +443,11 @@ def run_gpu(args, w):
     total_ms, tflops = job_rate(dist, device, float(per_call.sum()), ls.flops, args.steps)
     ms_step = total_ms / args.steps
     breakdown = {n: round(float(v) / args.steps, 4) for n, v in zip(ls.names, per_call)}
+    # a forward-only step ends with its dominant call (the down-proj), so the last
+    # kernel is that call's; a training step ends with a backward kernel, and its
+    # forward calls (thousands of tokens) run on the tile kernel
     roof = roofline_of(ls, per_call, args.steps, peaks,
-                       ("rowpar_fwd_tc" if w.N > 64 else kernel_name) + ("" if world == 1 else " + exchange"))
+                       (kernel_name if not w.backward else "rowpar_fwd_tc") + ("" if world == 1 else " + exchange"))
 
     result = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world,
@@ -1195,7 +1201,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["caat", "reference"], default="caat")
     ap.add_argument("--workload", default="7b_prefill",
-                    choices=["7b_prefill", "130m", "1.1b", "7b_decode8", "130m_stack"] + list(PCR_WORKLOADS))
+                    choices=["7b_prefill", "130m", "1.1b", "7b_decode8", "7b_prefill256", "130m_stack"]
+                    + list(PCR_WORKLOADS))
     ap.add_argument("--layout", choices=["contiguous", "random"], default=None,
                     help="channel-set layout (default: the workload's own)")
     ap.add_argument("--p", type=float, default=None, help="synchronized fraction (default: workload's)")

@@ -81,6 +81,10 @@ WORKLOADS = {
     "7b_decode8": Workload("7b_decode8", 4, t=8, N=8, h=4096,
                            layers=[Layer("out_proj", 4096), Layer("down_proj", 11008)],
                            backward=False),
+    # Llama2-7B short prefill, 256 tokens (the few-token kernel in two token chunks)
+    "7b_prefill256": Workload("7b_prefill256", 4, t=8, N=256, h=4096,
+                              layers=[Layer("out_proj", 4096), Layer("down_proj", 11008)],
+                              backward=False),
 }
 
 
