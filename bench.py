@@ -443,11 +443,12 @@ def run_gpu(args, w):
     total_ms, tflops = job_rate(dist, device, float(per_call.sum()), ls.flops, args.steps)
     ms_step = total_ms / args.steps
     breakdown = {n: round(float(v) / args.steps, 4) for n, v in zip(ls.names, per_call)}
-    # a forward-only step ends with its dominant call (the down-proj), so the last
-    # kernel is that call's; a training step ends with a backward kernel, and its
-    # forward calls (thousands of tokens) run on the tile kernel
-    roof = roofline_of(ls, per_call, args.steps, peaks,
-                       (kernel_name if not w.backward else "rowpar_fwd_tc") + ("" if world == 1 else " + exchange"))
+    # a forward-only step on one GPU ends with its dominant call (the down-proj), so
+    # the last kernel is that call's; a training step ends with a backward kernel
+    # and the split step with the exchange, and their forward calls (thousands of
+    # tokens) run on the tile kernel
+    fwd_kernel = kernel_name if (not w.backward and world == 1) else "rowpar_fwd_tc"
+    roof = roofline_of(ls, per_call, args.steps, peaks, fwd_kernel + ("" if world == 1 else " + exchange"))
 
     result = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world,
